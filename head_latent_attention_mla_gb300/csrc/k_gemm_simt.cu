@@ -1,0 +1,211 @@
+// FP8 block-scaled projections on the CUDA cores: a weight-streaming GEMV for a few tokens
+// and a tiled fallback for larger token counts.
+//
+// Y[m, n] = sum_k X[m, k] * e4m3(W[n, k]) * S[n/128][k/128]  ("linear" excerpt of the
+// "Key-value latent" page: fmt e4m3, weight_block_size [128, 128]; nn.Linear without bias).
+// Every 128-wide k block is summed in float32 with the raw e4m3 values and then multiplied by
+// its block scale once, so the dequantised weight is never rounded.
+#include "mla_internal.h"
+
+namespace mla {
+
+namespace {
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Four e4m3 bytes of one 32-bit word -> four floats (exact).
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float* f) {
+  __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFF), __NV_E4M3);
+  __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+  float2 a = __half22float2(*reinterpret_cast<__half2*>(&lo));
+  float2 b = __half22float2(*reinterpret_cast<__half2*>(&hi));
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(uint4 v, float* f) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(u[i] << 16);
+    f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+
+struct ProjSet {
+  Proj p[2];
+  int np;
+  int rows0;  // rows of p[0]
+};
+
+// One warp per output row n; lanes stride over k in 16-byte (16 weight) chunks.
+template <int M>
+__global__ void __launch_bounds__(256) gemv_f8w_kernel(const __nv_bfloat16* __restrict__ X,
+                                                       int ldx, int K, ProjSet ps) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int total = ps.p[0].N + (ps.np > 1 ? ps.p[1].N : 0);
+  if (warp >= total) return;
+  const Proj& P = (warp < ps.rows0) ? ps.p[0] : ps.p[1];
+  const int n = (warp < ps.rows0) ? warp : warp - ps.rows0;
+  const uint8_t* wrow = P.W + (size_t)n * K;
+  const float* srow = P.S + (size_t)(n / BLK) * (K / BLK);
+
+  float acc[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) acc[m] = 0.f;
+
+  constexpr int U = 4;
+  for (int base = 0; base < K; base += 512 * U) {
+    uint4 w[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int k = base + u * 512 + lane * 16;
+      w[u] = (k < K) ? ld_stream(wrow + k) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int k = base + u * 512 + lane * 16;
+      if (k < K) {
+        float wf[16];
+        e4m3x4_to_f32(w[u].x, wf);
+        e4m3x4_to_f32(w[u].y, wf + 4);
+        e4m3x4_to_f32(w[u].z, wf + 8);
+        e4m3x4_to_f32(w[u].w, wf + 12);
+        const float sc = __ldg(srow + k / BLK);
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const uint4* xp = reinterpret_cast<const uint4*>(X + (size_t)m * ldx + k);
+          float xf[16];
+          bf16x8_to_f32(__ldg(xp), xf);
+          bf16x8_to_f32(__ldg(xp + 1), xf + 8);
+          float part = 0.f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) part = fmaf(wf[i], xf[i], part);
+          acc[m] = fmaf(sc, part, acc[m]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    float v = acc[m];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) {
+      if (P.y_fp32)
+        reinterpret_cast<float*>(P.Y)[(size_t)m * P.ldy + n] = v;
+      else
+        reinterpret_cast<__nv_bfloat16*>(P.Y)[(size_t)m * P.ldy + n] = __float2bfloat16_rn(v);
+    }
+  }
+}
+
+// Tiled fallback: 64 (m) x 64 (n) per CTA, 4x4 outputs per thread, k steps of 32.
+// n tiles never straddle a 128-row scale block because 64 divides 128.
+__global__ void __launch_bounds__(256) gemm_f8w_tiled_kernel(const __nv_bfloat16* __restrict__ X,
+                                                             int ldx, int M, int K, ProjSet ps) {
+  __shared__ float As[32][64 + 4];
+  __shared__ float Bs[32][64 + 4];
+  const int tiles0 = ps.p[0].N / 64;
+  int nt = blockIdx.x;
+  const Proj& P = (nt < tiles0) ? ps.p[0] : ps.p[1];
+  if (nt >= tiles0) nt -= tiles0;
+  const int n0 = nt * 64, m0 = blockIdx.y * 64;
+  const int tid = threadIdx.x, tm = tid >> 4, tn = tid & 15;
+  const float* srow = P.S + (size_t)(n0 / BLK) * (K / BLK);
+
+  float acc[4][4] = {}, blk[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += 32) {
+    {  // X tile: 64 rows x 32 k, 8 bf16 per thread
+      const int r = tid >> 2, c = (tid & 3) * 8;
+      float xf[8];
+      if (m0 + r < M) {
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(X + (size_t)(m0 + r) * ldx + k0 + c), xf);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xf[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) As[c + i][r] = xf[i];
+    }
+    {  // W tile: 64 rows x 32 k, 8 e4m3 per thread
+      const int r = tid >> 2, c = (tid & 3) * 8;
+      const uint2 wv = *reinterpret_cast<const uint2*>(P.W + (size_t)(n0 + r) * K + k0 + c);
+      float wf[8];
+      e4m3x4_to_f32(wv.x, wf);
+      e4m3x4_to_f32(wv.y, wf + 4);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) Bs[c + i][r] = wf[i];
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < 32; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { a[i] = As[kk][tm * 4 + i]; b[i] = Bs[kk][tn * 4 + i]; }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) blk[i][j] = fmaf(a[i], b[j], blk[i][j]);
+    }
+    __syncthreads();
+    if (((k0 + 32) % BLK) == 0) {
+      const float sc = srow[k0 / BLK];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) { acc[i][j] = fmaf(sc, blk[i][j], acc[i][j]); blk[i][j] = 0.f; }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + tm * 4 + i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tn * 4 + j;
+      if (P.y_fp32)
+        reinterpret_cast<float*>(P.Y)[(size_t)m * P.ldy + n] = acc[i][j];
+      else
+        reinterpret_cast<__nv_bfloat16*>(P.Y)[(size_t)m * P.ldy + n] = __float2bfloat16_rn(acc[i][j]);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
+                        cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  ProjSet ps{};
+  ps.np = np;
+  ps.p[0] = p[0];
+  if (np > 1) ps.p[1] = p[1];
+  ps.rows0 = p[0].N;
+  const int rows = p[0].N + (np > 1 ? p[1].N : 0);
+  if (M <= 8) {
+    const dim3 grid((rows + 7) / 8), block(256);
+    switch (M) {
+      case 1: gemv_f8w_kernel<1><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
+      case 2: gemv_f8w_kernel<2><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
+      case 3: gemv_f8w_kernel<3><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
+      case 4: gemv_f8w_kernel<4><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
+      case 5: gemv_f8w_kernel<5><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
+      case 6: gemv_f8w_kernel<6><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
+      case 7: gemv_f8w_kernel<7><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
+      default: gemv_f8w_kernel<8><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
+    }
+  } else {
+    const dim3 grid(rows / 64, (M + 63) / 64), block(256);
+    gemm_f8w_tiled_kernel<<<grid, block, 0, st>>>(X, ldx, M, K, ps);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,279 @@
+// Elementwise and small kernels of the MLA layer: latent RMSNorms with RoPE and the cache
+// store, query RoPE, decode-side W_UK / W_UV absorption, length bookkeeping and the FP8
+// dequantisation export.
+#include "mla_internal.h"
+
+namespace mla {
+
+namespace {
+
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint8_t v) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)v, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// Block-wide sum of two values (256 threads).
+__device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, off);
+    b += __shfl_xor_sync(0xffffffffu, b, off);
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = make_float2(a, b);
+  __syncthreads();
+  float2 t = make_float2(0.f, 0.f);
+  if (threadIdx.x < 32) {
+    t = (l < (int)(blockDim.x >> 5)) ? red[l] : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      t.x += __shfl_xor_sync(0xffffffffu, t.x, off);
+      t.y += __shfl_xor_sync(0xffffffffu, t.y, off);
+    }
+    if (l == 0) red[8] = t;
+  }
+  __syncthreads();
+  return red[8];
+}
+
+// RoPE of one pair (a, b) by the table entry (cos, sin): (a c - b s, b c + a s).
+__device__ __forceinline__ float2 rotate(float a, float b, float2 cs) {
+  return make_float2(a * cs.x - b * cs.y, b * cs.x + a * cs.y);
+}
+
+// Element indices of pair j in a 64-wide rotary slice.
+__device__ __forceinline__ int2 pair_idx(int j, int pairing) {
+  return pairing == 0 ? make_int2(2 * j, 2 * j + 1) : make_int2(j, j + ROPE / 2);
+}
+
+// One CTA (256 threads) per token.
+// RMSNorm ("rmsnorm" excerpt): y = g * bf16(x * rsqrt(mean(x^2) + eps)), rounded to bf16,
+// for the q latent (1536) and the kv latent (512); the kv latent and the rotated shared
+// rotary key form the token's cache row [c_hat (512) | RoPE(k_pe) (64)].
+__global__ void __launch_bounds__(256) norm_rope_cache_kernel(
+    const float* __restrict__ g1, int T, const __nv_bfloat16* __restrict__ gq,
+    const __nv_bfloat16* __restrict__ gkv, float eps, const float2* __restrict__ rope_tab,
+    int pairing, const int* __restrict__ seq_lens, __nv_bfloat16* __restrict__ cache, int cap,
+    int limit, __nv_bfloat16* __restrict__ cq_out, __nv_bfloat16* __restrict__ ckv_out, int* err) {
+  __shared__ float2 red[9];
+  __shared__ __align__(16) __nv_bfloat16 row[LAT];
+  const int token = blockIdx.x, b = token / T, t = token % T;
+  const int tid = threadIdx.x;
+  const float* in = g1 + (size_t)token * G1_N;
+  const bool do_q = cq_out != nullptr;
+
+  float xq[Q_LORA / 256], xk[KV_LORA / 256];
+  float sq = 0.f, sk = 0.f;
+#pragma unroll
+  for (int i = 0; i < Q_LORA / 256; ++i) {
+    xq[i] = do_q ? in[tid + 256 * i] : 0.f;
+    sq += xq[i] * xq[i];
+  }
+#pragma unroll
+  for (int i = 0; i < KV_LORA / 256; ++i) {
+    xk[i] = in[Q_LORA + tid + 256 * i];
+    sk += xk[i] * xk[i];
+  }
+  const float2 ss = block_sum2(sq, sk, red);
+  const float rq = rsqrtf(ss.x / Q_LORA + eps);
+  const float rk = rsqrtf(ss.y / KV_LORA + eps);
+  if (do_q) {
+#pragma unroll
+    for (int i = 0; i < Q_LORA / 256; ++i) {
+      const int c = tid + 256 * i;
+      cq_out[(size_t)token * Q_LORA + c] =
+          __float2bfloat16_rn(__bfloat162float(gq[c]) * bf16_round(xq[i] * rq));
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < KV_LORA / 256; ++i) {
+    const int c = tid + 256 * i;
+    row[c] = __float2bfloat16_rn(__bfloat162float(gkv[c]) * bf16_round(xk[i] * rk));
+    if (ckv_out) ckv_out[(size_t)token * KV_LORA + c] = row[c];
+  }
+  const int pos = seq_lens[b] + t;
+  if (pos < 0 || pos >= limit) {  // device lengths past the cache or the RoPE table
+    if (tid == 0) atomicExch(err, DEV_ERR_RANGE);
+    return;
+  }
+  if (tid < ROPE / 2) {
+    const int2 ij = pair_idx(tid, pairing);
+    const float* kr = in + Q_LORA + KV_LORA;
+    const float2 r = rotate(kr[ij.x], kr[ij.y], rope_tab[(size_t)pos * (ROPE / 2) + tid]);
+    row[KV_LORA + ij.x] = __float2bfloat16_rn(r.x);
+    row[KV_LORA + ij.y] = __float2bfloat16_rn(r.y);
+  }
+  __syncthreads();
+  if (tid < LAT / 8) {
+    uint4* dst = reinterpret_cast<uint4*>(cache + ((size_t)b * cap + pos) * LAT);
+    dst[tid] = reinterpret_cast<const uint4*>(row)[tid];
+  }
+}
+
+// In-place RoPE of q's rotary slices: one CTA per token, 64 heads x 32 pairs.
+__global__ void __launch_bounds__(256) rope_q_kernel(__nv_bfloat16* __restrict__ q, int T,
+                                                     const float2* __restrict__ rope_tab,
+                                                     int pairing, const int* __restrict__ seq_lens,
+                                                     int limit) {
+  const int token = blockIdx.x, b = token / T, t = token % T;
+  const int pos = seq_lens[b] + t;
+  if (pos < 0 || pos >= limit) return;
+  for (int i = threadIdx.x; i < HEADS * (ROPE / 2); i += blockDim.x) {
+    const int h = i / (ROPE / 2), j = i % (ROPE / 2);
+    const int2 ij = pair_idx(j, pairing);
+    __nv_bfloat16* qp = q + ((size_t)token * HEADS + h) * QHEAD + NOPE;
+    const float2 r = rotate(__bfloat162float(qp[ij.x]), __bfloat162float(qp[ij.y]),
+                            rope_tab[(size_t)pos * (ROPE / 2) + j]);
+    qp[ij.x] = __float2bfloat16_rn(r.x);
+    qp[ij.y] = __float2bfloat16_rn(r.y);
+  }
+}
+
+// Decode query absorption.  CTA (h, cb): head h, latent columns [128 cb, 128 cb + 128).
+// qfull[b, h, c] = bf16( s[2h][cb] * sum_i q_nope[b, h, i] * e4m3(W_kvb[256 h + i, c]) ),
+// i.e. W_UK,h^T q_nope with W_UK,h = rows 0..127 of head h's 256 ("Key content
+// up-projection" page, Explanation).  The cb == 0 CTA also writes RoPE(q_pe) to [512, 576).
+constexpr int ABS_BCHUNK = 16;
+__global__ void __launch_bounds__(128) absorb_q_kernel(
+    const __nv_bfloat16* __restrict__ q, int B, const uint8_t* __restrict__ Wkvb,
+    const float* __restrict__ Skvb, const float2* __restrict__ rope_tab, int pairing,
+    const int* __restrict__ seq_lens, int limit, __nv_bfloat16* __restrict__ qfull) {
+  __shared__ float qn[ABS_BCHUNK][NOPE];
+  __shared__ float wt[NOPE][BLK + 1];
+  const int h = blockIdx.x, cb = blockIdx.y, c = threadIdx.x;
+  const float sc = Skvb[(size_t)(2 * h) * (KV_LORA / BLK) + cb];
+  for (int i = 0; i < NOPE; ++i)
+    wt[i][c] = e4m3_to_f32(Wkvb[(size_t)(h * KVB_PER_HEAD + i) * KV_LORA + cb * BLK + c]);
+  for (int b0 = 0; b0 < B; b0 += ABS_BCHUNK) {
+    const int nb = min(ABS_BCHUNK, B - b0);
+    __syncthreads();
+    for (int e = threadIdx.x; e < nb * NOPE; e += blockDim.x) {
+      const int bb = e / NOPE, i = e % NOPE;
+      qn[bb][i] = __bfloat162float(q[((size_t)(b0 + bb) * HEADS + h) * QHEAD + i]);
+    }
+    __syncthreads();
+    for (int bb = 0; bb < nb; ++bb) {
+      float acc = 0.f;
+#pragma unroll 8
+      for (int i = 0; i < NOPE; ++i) acc = fmaf(qn[bb][i], wt[i][c], acc);
+      qfull[((size_t)(b0 + bb) * HEADS + h) * LAT + cb * BLK + c] = __float2bfloat16_rn(sc * acc);
+    }
+  }
+  if (cb == 0) {
+    for (int e = threadIdx.x; e < B * (ROPE / 2); e += blockDim.x) {
+      const int bb = e / (ROPE / 2), j = e % (ROPE / 2);
+      const int pos = seq_lens[bb];
+      if (pos < 0 || pos >= limit) continue;
+      const int2 ij = pair_idx(j, pairing);
+      const __nv_bfloat16* qp = q + ((size_t)bb * HEADS + h) * QHEAD + NOPE;
+      const float2 r = rotate(__bfloat162float(qp[ij.x]), __bfloat162float(qp[ij.y]),
+                              rope_tab[(size_t)pos * (ROPE / 2) + j]);
+      __nv_bfloat16* dst = qfull + ((size_t)bb * HEADS + h) * LAT + KV_LORA;
+      dst[ij.x] = __float2bfloat16_rn(r.x);
+      dst[ij.y] = __float2bfloat16_rn(r.y);
+    }
+  }
+}
+
+// Decode output absorption.  CTA h, thread v: out[b, h*128 + v] =
+// bf16( sum_cb s[2h+1][cb] * sum_{c in cb} e4m3(W_kvb[256 h + 128 + v, c]) * o_lat[b, h, c] ).
+__global__ void __launch_bounds__(128) absorb_out_kernel(
+    const __nv_bfloat16* __restrict__ o_lat, int B, const uint8_t* __restrict__ Wkvb,
+    const float* __restrict__ Skvb, __nv_bfloat16* __restrict__ out) {
+  __shared__ float ol[4][KV_LORA];
+  const int h = blockIdx.x, v = threadIdx.x;
+  const uint8_t* wrow = Wkvb + (size_t)(h * KVB_PER_HEAD + NOPE + v) * KV_LORA;
+  const float* srow = Skvb + (size_t)(2 * h + 1) * (KV_LORA / BLK);
+  for (int b0 = 0; b0 < B; b0 += 4) {
+    const int nb = min(4, B - b0);
+    __syncthreads();
+    for (int e = threadIdx.x; e < nb * KV_LORA; e += blockDim.x) {
+      const int bb = e / KV_LORA, c = e % KV_LORA;
+      ol[bb][c] = __bfloat162float(o_lat[((size_t)(b0 + bb) * HEADS + h) * KV_LORA + c]);
+    }
+    __syncthreads();
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int cb = 0; cb < KV_LORA / BLK; ++cb) {
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int c = cb * BLK; c < (cb + 1) * BLK; ++c) {
+        const float w = e4m3_to_f32(wrow[c]);
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) part[bb] = fmaf(w, ol[bb][c], part[bb]);
+      }
+      const float sc = srow[cb];
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) acc[bb] = fmaf(sc, part[bb], acc[bb]);
+    }
+    for (int bb = 0; bb < nb; ++bb)
+      out[(size_t)(b0 + bb) * O_IN + h * VDIM + v] = __float2bfloat16_rn(acc[bb]);
+  }
+}
+
+__global__ void advance_lens_kernel(int* seq_lens, int B, int T) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) seq_lens[b] += T;
+}
+
+__global__ void dequant_kernel(const uint8_t* __restrict__ W, const float* __restrict__ S,
+                               int rows, int cols, float* __restrict__ out) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (size_t)rows * cols) return;
+  const int r = (int)(i / cols), c = (int)(i % cols);
+  const int kb = (cols + BLK - 1) / BLK;
+  out[i] = __fmul_rn(e4m3_to_f32(W[i]), S[(size_t)(r / BLK) * kb + c / BLK]);
+}
+
+}  // namespace
+
+cudaError_t launch_norm_rope_cache(const float* g1, int B, int T, const __nv_bfloat16* gq,
+                                   const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
+                                   int rope_pairing, const int* seq_lens, __nv_bfloat16* cache,
+                                   int cap, int limit, __nv_bfloat16* cq_out,
+                                   __nv_bfloat16* ckv_out, int* err, cudaStream_t st) {
+  if (B * T == 0) return cudaSuccess;
+  norm_rope_cache_kernel<<<B * T, 256, 0, st>>>(g1, T, gq, gkv, eps, rope_tab, rope_pairing,
+                                                seq_lens, cache, cap, limit, cq_out, ckv_out, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_q(__nv_bfloat16* q, int B, int T, const float2* rope_tab,
+                          int rope_pairing, const int* seq_lens, int limit, cudaStream_t st) {
+  if (B * T == 0) return cudaSuccess;
+  rope_q_kernel<<<B * T, 256, 0, st>>>(q, T, rope_tab, rope_pairing, seq_lens, limit);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_absorb_q(const __nv_bfloat16* q, int B, const uint8_t* Wkvb,
+                            const float* Skvb, const float2* rope_tab, int rope_pairing,
+                            const int* seq_lens, int limit, __nv_bfloat16* qfull,
+                            cudaStream_t st) {
+  absorb_q_kernel<<<dim3(HEADS, KV_LORA / BLK), 128, 0, st>>>(q, B, Wkvb, Skvb, rope_tab,
+                                                             rope_pairing, seq_lens, limit, qfull);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* Wkvb,
+                              const float* Skvb, __nv_bfloat16* out, cudaStream_t st) {
+  absorb_out_kernel<<<HEADS, VDIM, 0, st>>>(o_lat, B, Wkvb, Skvb, out);
+  return cudaGetLastError();
+}
+
+cudaError_t init_kernels() { return init_attention_kernels(); }
+
+cudaError_t launch_advance_lens(int* seq_lens, int B, int T, cudaStream_t st) {
+  advance_lens_kernel<<<(B + 255) / 256, 256, 0, st>>>(seq_lens, B, T);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const uint8_t* W, const float* S, int rows, int cols, float* out,
+                           cudaStream_t st) {
+  const size_t n = (size_t)rows * cols;
+  dequant_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(W, S, rows, cols, out);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,399 @@
+// C ABI of libmla (declared in include/mla.h): argument checks, workspace layout and the
+// launch sequence of each call.  Every step of the layer runs in this library's kernels.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/mla.h"
+#include "mla_internal.h"
+
+using namespace mla;
+
+struct mla_ctx {
+  mla_config cfg;
+  int device = 0;
+  int num_sms = 0;
+  const uint8_t* W[5] = {};
+  const float* S[5] = {};
+  const __nv_bfloat16* gain[2] = {};
+  float2* rope_tab = nullptr;  // [max_positions][32] (cos, sin)
+  int* d_err = nullptr;
+  // Launch log of the most recent token call (names, and device timings when profiling).
+  static constexpr int kMaxLaunch = 32;
+  bool profiling = false;
+  bool last_profiled = false;
+  int n_launch = 0;
+  const char* names[kMaxLaunch] = {};
+  cudaEvent_t ev[2 * kMaxLaunch] = {};
+};
+
+namespace {
+
+const int kRows[5] = {Q_LORA, QB_N, KVA_N, KVB_N, HIDDEN};
+const int kCols[5] = {HIDDEN, Q_LORA, HIDDEN, KV_LORA, O_IN};
+const int kNorm[2] = {Q_LORA, KV_LORA};
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool ready(const mla_ctx* c) {
+  for (int i = 0; i < 5; ++i)
+    if (!c->W[i] || !c->S[i]) return false;
+  return c->gain[0] && c->gain[1];
+}
+
+// Workspace regions (byte offsets into the caller's buffer).
+struct Layout {
+  size_t g1 = 0, cq = 0, ckv = 0, q = 0, kv = 0, attn = 0, qfull = 0, opart = 0, ml = 0,
+         olat = 0, total = 0;
+};
+
+int items_max(const mla_ctx* c, int B) { return 2 * c->num_sms + B; }
+
+Layout prefill_layout(long M) {
+  Layout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off += up256(bytes); return o; };
+  L.g1 = take((size_t)M * G1_N * 4);
+  L.cq = take((size_t)M * Q_LORA * 2);
+  L.ckv = take((size_t)M * KV_LORA * 2);
+  L.q = take((size_t)M * QB_N * 2);
+  L.kv = take((size_t)M * KVB_N * 2);
+  L.attn = take((size_t)M * O_IN * 2);
+  L.total = off;
+  return L;
+}
+
+Layout decode_layout(const mla_ctx* c, int B) {
+  Layout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off += up256(bytes); return o; };
+  const size_t items = (size_t)items_max(c, B);
+  L.g1 = take((size_t)B * G1_N * 4);
+  L.cq = take((size_t)B * Q_LORA * 2);
+  L.q = take((size_t)B * QB_N * 2);
+  L.qfull = take((size_t)B * HEADS * LAT * 2);
+  L.opart = take(items * HEADS * KV_LORA * 4);
+  L.ml = take(items * HEADS * 2 * 4);
+  L.olat = take((size_t)B * HEADS * KV_LORA * 2);
+  L.attn = take((size_t)B * O_IN * 2);
+  L.total = off;
+  return L;
+}
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+void log_reset(mla_ctx* c) {
+  c->n_launch = 0;
+  c->last_profiled = c->profiling;
+}
+
+// Records one kernel launch of the current call; with profiling on, brackets it with events
+// recorded on the launching stream.
+#define MLA_LAUNCH(name, expr)                                                          \
+  do {                                                                                  \
+    const int _k = c->n_launch < mla_ctx::kMaxLaunch ? c->n_launch : mla_ctx::kMaxLaunch - 1; \
+    if (c->profiling && cudaEventRecord(c->ev[2 * _k], s) != cudaSuccess) return MLA_ERR_CUDA; \
+    cudaError_t _e = (expr);                                                            \
+    if (_e != cudaSuccess) return MLA_ERR_CUDA;                                         \
+    if (c->profiling && cudaEventRecord(c->ev[2 * _k + 1], s) != cudaSuccess) return MLA_ERR_CUDA; \
+    c->names[_k] = name;                                                                \
+    if (c->n_launch < mla_ctx::kMaxLaunch) ++c->n_launch;                               \
+  } while (0)
+
+// Common checks of the token calls.  Lengths come from the host copy.
+mla_status check_tokens(const mla_ctx* c, const void* x, int B, int T, const void* cache, int cap,
+                        const int* lens_dev, const int* lens_host, void* ws, size_t ws_bytes,
+                        size_t need) {
+  if (!c) return MLA_ERR_INVALID_ARG;
+  if (B < 0 || T < 0 || cap < 0) return MLA_ERR_INVALID_ARG;
+  if (B == 0 || T == 0) return MLA_OK;
+  if (!x || !cache || !lens_dev || !lens_host || !ws) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(cache) || !aligned16(ws)) return MLA_ERR_INVALID_ARG;
+  if (!ready(c)) return MLA_ERR_STATE;
+  if (ws_bytes < need) return MLA_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b) {
+    if (lens_host[b] < 0) return MLA_ERR_INVALID_ARG;
+    if ((long)lens_host[b] + T > cap || (long)lens_host[b] + T > c->cfg.max_positions)
+      return MLA_ERR_CAPACITY;
+  }
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void mla_default_config(mla_config* cfg) {
+  if (!cfg) return;
+  cfg->hidden = HIDDEN;
+  cfg->q_lora = Q_LORA;
+  cfg->kv_lora = KV_LORA;
+  cfg->heads = HEADS;
+  cfg->nope = NOPE;
+  cfg->rope = ROPE;
+  cfg->vdim = VDIM;
+  cfg->eps = 1e-6f;
+  cfg->rope_theta = 50000.0f;
+  cfg->softmax_scale = (float)(1.0 / std::sqrt((double)(NOPE + ROPE)));
+  cfg->max_positions = 131073;
+  cfg->rope_pairing = MLA_ROPE_ADJACENT;
+}
+
+mla_status mla_create(const mla_config* cfg, mla_ctx** out) {
+  if (!cfg || !out) return MLA_ERR_INVALID_ARG;
+  if (cfg->hidden != HIDDEN || cfg->q_lora != Q_LORA || cfg->kv_lora != KV_LORA ||
+      cfg->heads != HEADS || cfg->nope != NOPE || cfg->rope != ROPE || cfg->vdim != VDIM)
+    return MLA_ERR_UNSUPPORTED;
+  if (cfg->rope_pairing != MLA_ROPE_ADJACENT && cfg->rope_pairing != MLA_ROPE_HALF)
+    return MLA_ERR_INVALID_ARG;
+  if (cfg->max_positions <= 0 || !(cfg->eps >= 0.f) || !(cfg->rope_theta > 0.f) ||
+      !(cfg->softmax_scale > 0.f))
+    return MLA_ERR_INVALID_ARG;
+  mla_ctx* c = new (std::nothrow) mla_ctx();
+  if (!c) return MLA_ERR_INVALID_ARG;
+  c->cfg = *cfg;
+  if (init_kernels() != cudaSuccess || cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    delete c;
+    return MLA_ERR_CUDA;
+  }
+  // RoPE table in double precision: angle = pos * theta^(-2j/64), stored as float (cos, sin).
+  const size_t n = (size_t)cfg->max_positions * (ROPE / 2);
+  std::vector<float2> tab(n);
+  for (int j = 0; j < ROPE / 2; ++j) {
+    const double inv = std::pow((double)cfg->rope_theta, -2.0 * j / ROPE);
+    for (int p = 0; p < cfg->max_positions; ++p) {
+      const double a = (double)p * inv;
+      tab[(size_t)p * (ROPE / 2) + j] = make_float2((float)std::cos(a), (float)std::sin(a));
+    }
+  }
+  if (cudaMalloc(&c->rope_tab, n * sizeof(float2)) != cudaSuccess) {
+    delete c;
+    return MLA_ERR_CUDA;
+  }
+  if (cudaMalloc(&c->d_err, sizeof(int)) != cudaSuccess ||
+      cudaMemcpy(c->rope_tab, tab.data(), n * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess) {
+    cudaFree(c->rope_tab);
+    if (c->d_err) cudaFree(c->d_err);
+    delete c;
+    return MLA_ERR_CUDA;
+  }
+  *out = c;
+  return MLA_OK;
+}
+
+void mla_destroy(mla_ctx* c) {
+  if (!c) return;
+  cudaDeviceSynchronize();
+  cudaFree(c->rope_tab);
+  cudaFree(c->d_err);
+  for (cudaEvent_t e : c->ev)
+    if (e) cudaEventDestroy(e);
+  delete c;
+}
+
+mla_status mla_set_profiling(mla_ctx* c, int on) {
+  if (!c) return MLA_ERR_INVALID_ARG;
+  if (on && !c->ev[0]) {
+    for (cudaEvent_t& e : c->ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  c->profiling = on != 0;
+  return MLA_OK;
+}
+
+int mla_last_launches(mla_ctx* c, int max, const char** names, float* ms) {
+  if (!c) return -1;
+  const int n = c->n_launch;
+  for (int k = 0; k < n && k < max; ++k) {
+    if (names) names[k] = c->names[k];
+    if (ms) {
+      ms[k] = -1.f;
+      if (c->last_profiled && cudaEventSynchronize(c->ev[2 * k + 1]) == cudaSuccess)
+        cudaEventElapsedTime(&ms[k], c->ev[2 * k], c->ev[2 * k + 1]);
+    }
+  }
+  return n;
+}
+
+mla_status mla_upload_weights(mla_ctx* c, int which, const void* q, const float* s, int rows,
+                              int cols) {
+  if (!c || which < 0 || which > 4 || !q || !s) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(s) & 3u)) return MLA_ERR_INVALID_ARG;
+  if (rows != kRows[which] || cols != kCols[which]) return MLA_ERR_SHAPE;
+  c->W[which] = static_cast<const uint8_t*>(q);
+  c->S[which] = s;
+  return MLA_OK;
+}
+
+mla_status mla_upload_norm(mla_ctx* c, int which, const void* g, int n) {
+  if (!c || which < 0 || which > 1 || !g || !aligned16(g)) return MLA_ERR_INVALID_ARG;
+  if (n != kNorm[which]) return MLA_ERR_SHAPE;
+  c->gain[which] = static_cast<const __nv_bfloat16*>(g);
+  return MLA_OK;
+}
+
+size_t mla_workspace_bytes(const mla_ctx* c, int B, int T) {
+  if (!c || B < 0 || T < 0) return 0;
+  const size_t p = prefill_layout((long)B * T).total;
+  const size_t d = decode_layout(c, B).total;
+  return p > d ? p : d;
+}
+
+mla_status mla_cache_append(mla_ctx* c, const void* x, int B, int T, void* cache, int cap,
+                            int* lens_dev, const int* lens_host, void* ws, size_t ws_bytes,
+                            void* stream) {
+  const Layout L = prefill_layout((long)B * T);
+  mla_status st = check_tokens(c, x, B, T, cache, cap, lens_dev, lens_host, ws, ws_bytes, L.total);
+  if (st != MLA_OK || B == 0 || T == 0) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  log_reset(c);
+  const int M = B * T, limit = cap < c->cfg.max_positions ? cap : c->cfg.max_positions;
+  float* g1 = at<float>(ws, L.g1);
+  Proj p{c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1};
+  MLA_LAUNCH("gemm_kv_a", launch_gemm(static_cast<const __nv_bfloat16*>(x), HIDDEN, M, HIDDEN, &p, 1, s));
+  MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
+                                    c->cfg.rope_pairing, lens_dev,
+                                    static_cast<__nv_bfloat16*>(cache), cap, limit, nullptr,
+                                    nullptr, c->d_err, s));
+  MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, T, s));
+  return MLA_OK;
+}
+
+mla_status mla_prefill(mla_ctx* c, const void* x, int B, int T, void* cache, int cap,
+                       int* lens_dev, const int* lens_host, void* out, void* ws,
+                       size_t ws_bytes, void* stream) {
+  const Layout L = prefill_layout((long)B * T);
+  mla_status st = check_tokens(c, x, B, T, cache, cap, lens_dev, lens_host, ws, ws_bytes, L.total);
+  if (st != MLA_OK || B == 0 || T == 0) return st;
+  if (!out || !aligned16(out) || out == x) return MLA_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b)
+    if (lens_host[b] != 0) return MLA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  log_reset(c);
+  const int M = B * T, limit = cap < c->cfg.max_positions ? cap : c->cfg.max_positions;
+  const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(x);
+  __nv_bfloat16* C = static_cast<__nv_bfloat16*>(cache);
+  float* g1 = at<float>(ws, L.g1);
+  __nv_bfloat16* cq = at<__nv_bfloat16>(ws, L.cq);
+  __nv_bfloat16* ckv = at<__nv_bfloat16>(ws, L.ckv);
+  __nv_bfloat16* q = at<__nv_bfloat16>(ws, L.q);
+  __nv_bfloat16* kv = at<__nv_bfloat16>(ws, L.kv);
+  __nv_bfloat16* attn = at<__nv_bfloat16>(ws, L.attn);
+
+  Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
+                {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
+  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, M, HIDDEN, p1, 2, s));
+  MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
+                                    c->cfg.rope_pairing, lens_dev, C, cap, limit, cq, ckv,
+                                    c->d_err, s));
+  Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
+  MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, s));
+  MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
+  Proj p3{c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], KVB_N, kv, KVB_N, 0};
+  MLA_LAUNCH("gemm_kv_b", launch_gemm(ckv, KV_LORA, M, KV_LORA, &p3, 1, s));
+  MLA_LAUNCH("prefill_attention", launch_prefill_attention(q, kv, C, cap, B, T, c->cfg.softmax_scale, attn, s));
+  Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
+  MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, s));
+  MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, T, s));
+  return MLA_OK;
+}
+
+mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, int* lens_dev,
+                      const int* lens_host, void* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!c) return MLA_ERR_INVALID_ARG;
+  const Layout L = decode_layout(c, B < 0 ? 0 : B);
+  mla_status st = check_tokens(c, x, B, 1, cache, cap, lens_dev, lens_host, ws, ws_bytes, L.total);
+  if (st != MLA_OK || B == 0) return st;
+  if (!out || !aligned16(out) || out == x) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  log_reset(c);
+  const int limit = cap < c->cfg.max_positions ? cap : c->cfg.max_positions;
+  const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(x);
+  __nv_bfloat16* C = static_cast<__nv_bfloat16*>(cache);
+
+  // Split-KV schedule: about two work items per SM, each a run of `chunk` positions.
+  long total = 0;
+  for (int b = 0; b < B; ++b) total += (long)lens_host[b] + 1;
+  const long target = 2L * c->num_sms;
+  long chunk = (total + target - 1) / target;
+  chunk = ((chunk + 63) / 64) * 64;
+  if (chunk < 64) chunk = 64;
+  long items = 0;
+  for (int b = 0; b < B; ++b) items += ((long)lens_host[b] + 1 + chunk - 1) / chunk;
+  if (items > items_max(c, B)) return MLA_ERR_STATE;
+  DecodePlan plan{B, (int)chunk, (int)items};
+
+  float* g1 = at<float>(ws, L.g1);
+  __nv_bfloat16* cq = at<__nv_bfloat16>(ws, L.cq);
+  __nv_bfloat16* q = at<__nv_bfloat16>(ws, L.q);
+  __nv_bfloat16* qfull = at<__nv_bfloat16>(ws, L.qfull);
+  float* opart = at<float>(ws, L.opart);
+  float* ml = at<float>(ws, L.ml);
+  __nv_bfloat16* olat = at<__nv_bfloat16>(ws, L.olat);
+  __nv_bfloat16* attn = at<__nv_bfloat16>(ws, L.attn);
+
+  Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
+                {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
+  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, s));
+  MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, 1, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
+                                    c->cfg.rope_pairing, lens_dev, C, cap, limit, cq, nullptr,
+                                    c->d_err, s));
+  Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
+  MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, B, Q_LORA, &p2, 1, s));
+  MLA_LAUNCH("absorb_q", launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
+                             c->cfg.rope_pairing, lens_dev, limit, qfull, s));
+  MLA_LAUNCH("decode_attention", launch_decode_attention(qfull, C, cap, lens_dev, plan,
+                                                         c->cfg.softmax_scale, opart, ml,
+                                                         c->d_err, s));
+  MLA_LAUNCH("decode_combine", launch_decode_combine(lens_dev, plan, opart, ml, olat, c->d_err, s));
+  MLA_LAUNCH("absorb_out", launch_absorb_out(olat, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], attn, s));
+  Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
+  MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, s));
+  MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, 1, s));
+  return MLA_OK;
+}
+
+mla_status mla_dequant_weight(mla_ctx* c, int which, float* out, void* stream) {
+  if (!c || which < 0 || which > 4 || !out) return MLA_ERR_INVALID_ARG;
+  if (!c->W[which]) return MLA_ERR_STATE;
+  return cuda_status(launch_dequant(c->W[which], c->S[which], kRows[which], kCols[which], out,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+mla_status mla_get_device_status(mla_ctx* c, void* stream) {
+  if (!c) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int h = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaMemcpy(&h, c->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess) return MLA_ERR_CUDA;
+  if (h == DEV_ERR_NONE) return MLA_OK;
+  return h == DEV_ERR_TIMEOUT ? MLA_ERR_TIMEOUT : MLA_ERR_STATE;
+}
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_SHAPE: return "MLA_ERR_SHAPE";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_CAPACITY: return "MLA_ERR_CAPACITY";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    case MLA_ERR_STATE: return "MLA_ERR_STATE";
+  }
+  return "MLA_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,110 @@
+// Internal declarations shared by the libmla translation units (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mla {
+
+// Kimi-K2 MLA dimensions (config.json on the "KV cache" page).
+constexpr int HIDDEN = 7168;
+constexpr int Q_LORA = 1536;
+constexpr int KV_LORA = 512;
+constexpr int HEADS = 64;
+constexpr int NOPE = 128;
+constexpr int ROPE = 64;
+constexpr int VDIM = 128;
+constexpr int QHEAD = NOPE + ROPE;         // 192
+constexpr int LAT = KV_LORA + ROPE;        // 576 values per cached position
+constexpr int KVA_N = KV_LORA + ROPE;      // 576 rows of kv_a_proj_with_mqa
+constexpr int QB_N = HEADS * QHEAD;        // 12288
+constexpr int KVB_PER_HEAD = NOPE + VDIM;  // 256
+constexpr int KVB_N = HEADS * KVB_PER_HEAD;  // 16384
+constexpr int O_IN = HEADS * VDIM;         // 8192
+constexpr int G1_N = Q_LORA + KVA_N;       // 2112: q_a and kv_a outputs side by side
+constexpr int BLK = 128;                   // FP8 weight block (weight_block_size)
+
+// Device error word values (read back by mla_get_device_status).
+constexpr int DEV_ERR_NONE = 0;
+constexpr int DEV_ERR_RANGE = 1;    // a cache position outside [0, cap) was skipped
+constexpr int DEV_ERR_TIMEOUT = 2;  // a bounded wait gave up
+constexpr int DEV_ERR_PLAN = 3;     // device lengths disagree with the host schedule
+
+// One FP8 block-scaled projection: Y[m, n] = sum_k X[m, k] * W[n, k] * S[n/128][k/128].
+struct Proj {
+  const uint8_t* W;  // e4m3 [N, K]
+  const float* S;    // [ceil(N/128), K/128]
+  int N;
+  void* Y;           // fp32 or bf16 output, row stride ldy elements
+  int ldy;
+  int y_fp32;        // 1: float32 output, 0: bf16 output
+};
+
+// ---- launchers (each returns the launch's cudaError_t) ----------------------------------
+
+// Y = X W^T for up to two projections sharing X [M, K] (row stride ldx elements).
+cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
+                        cudaStream_t st);
+
+// RMSNorm of the q latent and kv latent, RoPE of k_pe, cache row store.  Positions at or
+// past `limit` (min of cache capacity and RoPE table rows) are skipped and flagged in *err.
+//   g1: fp32 [M, G1_N] (q_a | kv_a outputs), token m = b*T + t at position seq_lens[b] + t.
+//   cq_out: bf16 [M, Q_LORA] normalised q latent (skipped if null).
+//   ckv_out: bf16 [M, KV_LORA] normalised kv latent, the same values as the cache rows
+//   (skipped if null).
+cudaError_t launch_norm_rope_cache(const float* g1, int B, int T, const __nv_bfloat16* gq,
+                                   const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
+                                   int rope_pairing, const int* seq_lens, __nv_bfloat16* cache,
+                                   int cap, int limit, __nv_bfloat16* cq_out,
+                                   __nv_bfloat16* ckv_out, int* err, cudaStream_t st);
+
+// In-place RoPE of the rotary slice of q [M, HEADS, QHEAD] (prefill).
+cudaError_t launch_rope_q(__nv_bfloat16* q, int B, int T, const float2* rope_tab,
+                          int rope_pairing, const int* seq_lens, int limit, cudaStream_t st);
+
+// Decode query absorption: qfull[b, h] = [W_UK,h^T q_nope | RoPE(q_pe)] as bf16 [B, HEADS, LAT].
+cudaError_t launch_absorb_q(const __nv_bfloat16* q, int B, const uint8_t* Wkvb,
+                            const float* Skvb, const float2* rope_tab, int rope_pairing,
+                            const int* seq_lens, int limit, __nv_bfloat16* qfull,
+                            cudaStream_t st);
+
+// Split-KV decode attention over the latent cache, then the log-sum-exp combine.
+struct DecodePlan {
+  int B;
+  int chunk;        // positions per work item
+  int items;        // total work items (sum over b of ceil((len_b + 1) / chunk))
+};
+cudaError_t launch_decode_attention(const __nv_bfloat16* qfull, const __nv_bfloat16* cache,
+                                    int cap, const int* seq_lens, DecodePlan plan,
+                                    float scale, float* o_part, float* ml_part, int* err,
+                                    cudaStream_t st);
+cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const float* o_part,
+                                  const float* ml_part, __nv_bfloat16* o_lat, int* err,
+                                  cudaStream_t st);
+
+// One-time kernel attributes (dynamic shared memory opt-in); called by mla_create so that
+// later calls only enqueue work and can be captured into CUDA graphs.
+cudaError_t init_kernels();
+cudaError_t init_attention_kernels();
+
+// Decode output absorption: out[b, h*VDIM + v] = sum_c W_UV,h[v, c] o_lat[b, h, c].
+cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* Wkvb,
+                              const float* Skvb, __nv_bfloat16* out, cudaStream_t st);
+
+// Causal prefill attention: q [M, HEADS, QHEAD] (rotated), kv [M, HEADS, 256] (k_nope | v),
+// rotated k_pe from cache rows; writes attn_out [M, HEADS*VDIM] bf16.
+cudaError_t launch_prefill_attention(const __nv_bfloat16* q, const __nv_bfloat16* kv,
+                                     const __nv_bfloat16* cache, int cap, int B, int T,
+                                     float scale, __nv_bfloat16* attn_out, cudaStream_t st);
+
+// seq_lens[b] += T.
+cudaError_t launch_advance_lens(int* seq_lens, int B, int T, cudaStream_t st);
+
+// out[r][c] = float(e4m3(W[r][c])) * S[r/128][c/128].
+cudaError_t launch_dequant(const uint8_t* W, const float* S, int rows, int cols, float* out,
+                           cudaStream_t st);
+
+}  // namespace mla

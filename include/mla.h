@@ -1,0 +1,162 @@
+/*
+ * mla.h -- C ABI of libmla: the forward pass of one Kimi-K2 multi-head latent attention
+ * (MLA) layer on one NVIDIA GB300 (sm_103a), in prefill over an empty cache and in decode
+ * against a latent KV cache.
+ *
+ * What the layer computes (Kimi K2 model-atlas pages):
+ *   q      = q_b_proj(RMSNorm_q(q_a_proj(x)))                 per head [nope 128 | rope 64]
+ *   c, k_r = split(kv_a_proj_with_mqa(x), [512, 64]);  c_hat = RMSNorm_kv(c)
+ *   k_h    = [W_UK,h c_hat | RoPE(k_r)],  v_h = W_UV,h c_hat   (kv_b_proj rows per head)
+ *   o_h    = softmax_fp32(q_h . k_h / sqrt(192) + causal mask) . v_h
+ *   y      = o_proj(concat_h o_h)
+ * ("Key-value latent" page: mla-init, mla-kv and rmsnorm excerpts; "Key content
+ *  up-projection" page: the k^C = c^KV W_UK equation and the mla-prefill excerpt;
+ *  "Latent attention (dense block, prefill)" page: the in/out signature and mla-output.)
+ *
+ * Conventions for every call:
+ *   - Device pointers are CUDA global-memory addresses on the current device; host pointers
+ *     are ordinary process memory.  The caller allocates and owns every buffer it passes and
+ *     must keep weights, gains and caches alive for as long as the context uses them.
+ *   - bf16 means IEEE bfloat16; e4m3 means OCP FP8 E4M3 ("fn": no infinities).
+ *   - All layouts are row-major and densely packed unless a stride argument says otherwise.
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default stream.  Work is
+ *     enqueued asynchronously; the call returns once the work is enqueued.
+ *   - Every call checks its arguments on the host before enqueuing anything.  On any error
+ *     nothing is enqueued and no caller buffer is written.  Calls never throw.
+ *   - The context is not thread-safe; one host thread drives one context at a time.
+ */
+#ifndef MLA_H
+#define MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad enum, negative size            */
+  MLA_ERR_SHAPE = 2,       /* a size disagrees with the layer (the pages raise ValueError) */
+  MLA_ERR_UNSUPPORTED = 3, /* dimensions other than Kimi-K2's, or a mode not provided      */
+  MLA_ERR_CAPACITY = 4,    /* cache length + new tokens exceeds the cache or RoPE table    */
+  MLA_ERR_CUDA = 5,        /* a CUDA runtime call failed                                    */
+  MLA_ERR_TIMEOUT = 6,     /* a device-side bounded wait gave up (read via device status)   */
+  MLA_ERR_STATE = 7        /* weights or gains missing, or a device-side check failed       */
+} mla_status;
+
+typedef struct mla_ctx mla_ctx; /* opaque, host-side */
+
+/* Projection ids for mla_upload_weights (names of the pages' nn.Linear modules). */
+enum { MLA_W_Q_A = 0, MLA_W_Q_B = 1, MLA_W_KV_A = 2, MLA_W_KV_B = 3, MLA_W_O = 4 };
+/* RMSNorm gain ids for mla_upload_norm: q_a_layernorm and kv_a_layernorm. */
+enum { MLA_NORM_Q = 0, MLA_NORM_KV = 1 };
+/* RoPE pairing of the 64-wide rotary slice: pair j = (2j, 2j+1) or (j, j+32). */
+enum { MLA_ROPE_ADJACENT = 0, MLA_ROPE_HALF = 1 };
+
+typedef struct {
+  int hidden, q_lora, kv_lora, heads, nope, rope, vdim; /* must be 7168,1536,512,64,128,64,128 */
+  float eps;           /* RMSNorm epsilon (rms_norm_eps, 1e-6)                          */
+  float rope_theta;    /* RoPE base (rope_theta, 50000)                                 */
+  float softmax_scale; /* score scale; 1/sqrt(nope+rope) by default                     */
+  int max_positions;   /* RoPE table rows: positions 0 .. max_positions-1 are allowed   */
+  int rope_pairing;    /* MLA_ROPE_ADJACENT (default) or MLA_ROPE_HALF                  */
+} mla_config;
+
+/* Fills *cfg with Kimi-K2's dimensions (config.json on the "KV cache" page), eps 1e-6,
+ * theta 50000, scale 1/sqrt(192), max_positions 131073 (max_position_embeddings 131072 is
+ * not enforced by the pages' code, so position 131072 itself is allowed), adjacent pairs. */
+void mla_default_config(mla_config* cfg);
+
+/* Creates a context on the current CUDA device.  Checks the dimensions (anything but
+ * Kimi-K2's gives MLA_ERR_UNSUPPORTED), builds the RoPE cos/sin table on the host in double
+ * precision (angle = pos * theta^(-2j/64), j = 0..31) and uploads it as float32.  That table
+ * and a 4-byte device error word are the only device memory the context allocates;
+ * mla_destroy frees them.  *out is set only on success. */
+mla_status mla_create(const mla_config* cfg, mla_ctx** out);
+void mla_destroy(mla_ctx* ctx); /* NULL is ignored; synchronises the device before freeing */
+
+/* Registers one projection's FP8 weight ("linear" excerpt of the "Key-value latent" page:
+ * fmt e4m3, weight_block_size [128, 128]).  e4m3_dev: device, [rows, cols] = [out, in],
+ * 16-byte aligned; scale_dev: device float32 [ceil(rows/128), ceil(cols/128)], one scale per
+ * 128x128 block, W[o,i] = e4m3(q[o,i]) * s[o/128][i/128].  rows/cols must equal the layer's
+ * shape for `which` (q_a 1536x7168, q_b 12288x1536, kv_a 576x7168, kv_b 16384x512,
+ * o 7168x8192), else MLA_ERR_SHAPE.  Only the pointers are recorded: nothing is copied. */
+mla_status mla_upload_weights(mla_ctx* ctx, int which, const void* e4m3_dev,
+                              const float* scale_dev, int rows, int cols);
+
+/* Registers an RMSNorm gain ("rmsnorm" excerpt): bf16 device vector of n = 1536 (MLA_NORM_Q)
+ * or 512 (MLA_NORM_KV) values, 16-byte aligned.  Only the pointer is recorded. */
+mla_status mla_upload_norm(mla_ctx* ctx, int which, const void* bf16_gain_dev, int n);
+
+/* Bytes of caller-provided device workspace that mla_prefill / mla_decode /
+ * mla_cache_append need for B sequences of T new tokens each.  The same workspace may be
+ * reused by consecutive calls on one stream; calls that overlap on the GPU need their own. */
+size_t mla_workspace_bytes(const mla_ctx* ctx, int B, int T);
+
+/* Appends T tokens per sequence to the latent cache without computing attention: for each
+ * token, the normalised latent (512) and the rotated shared rotary key (64) ("mla-kv"
+ * excerpt, RoPE as for keys) are stored as one bf16 row of 576 values at position
+ * seq_lens[b] + t, then seq_lens[b] += T on the device.
+ *   x_bf16       device [B, T, 7168] hidden states
+ *   cache_bf16   device [B, cap, 576]; row r of sequence b is at (b*cap + r)*576
+ *   seq_lens_dev device int32 [B], current lengths, advanced by T
+ *   seq_lens_host host int32 [B], the same lengths, used only to check capacity
+ *   ws/ws_bytes  device workspace of at least mla_workspace_bytes(ctx, B, T) bytes
+ * Errors: MLA_ERR_CAPACITY if seq_lens_host[b] + T > cap or > max_positions. */
+mla_status mla_cache_append(mla_ctx* ctx, const void* x_bf16, int B, int T, void* cache_bf16,
+                            int cap, int* seq_lens_dev, const int* seq_lens_host, void* ws,
+                            size_t ws_bytes, void* stream);
+
+/* Prefill over an empty cache ("Latent attention (dense block, prefill)" page: in
+ * [B, T, 7168], out [B, T, 7168], the cache holds positions 0..T-1 afterwards).  Token t
+ * attends to positions 0..t (causal mask), all 64 heads, scores scaled by softmax_scale,
+ * softmax in float32.  Writes out_bf16 [B, T, 7168], fills cache rows 0..T-1 and sets
+ * seq_lens_dev[b] = T.  seq_lens_host (host, [B]) must be all zero: a non-empty cache gives
+ * MLA_ERR_UNSUPPORTED (chunked prefill is not provided).  out must not alias x. */
+mla_status mla_prefill(mla_ctx* ctx, const void* x_bf16, int B, int T, void* cache_bf16,
+                       int cap, int* seq_lens_dev, const int* seq_lens_host, void* out_bf16,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* One decode step for B sequences ("KV cache" page at p = seq_lens[b]): the new token of
+ * sequence b, x_bf16[b] (device [B, 7168]), is placed at position seq_lens[b], its cache
+ * row is appended, and it attends to all seq_lens[b] + 1 positions of its own cache.  The
+ * attention runs in the absorbed form over the latent cache (W_UK folded into the query,
+ * W_UV applied to the latent output), which equals the pages' explicit form in exact
+ * arithmetic.  Writes out_bf16 [B, 7168] and advances seq_lens_dev by 1.  seq_lens_host
+ * (host, [B]) must equal the device lengths; it sizes the split-KV schedule and is checked
+ * against cap and max_positions (MLA_ERR_CAPACITY). */
+mla_status mla_decode(mla_ctx* ctx, const void* x_bf16, int B, void* cache_bf16, int cap,
+                      int* seq_lens_dev, const int* seq_lens_host, void* out_bf16, void* ws,
+                      size_t ws_bytes, void* stream);
+
+/* Verification helper: writes the float32 dequantisation of a registered weight,
+ * out[o][i] = float(e4m3(q[o][i])) * s[o/128][i/128] (one rounded multiply), to the
+ * caller's device buffer of rows*cols floats. */
+mla_status mla_dequant_weight(mla_ctx* ctx, int which, float* out_dev, void* stream);
+
+/* Synchronises `stream` and reads the context's device error word, which device-side checks
+ * set instead of trapping (a bounded wait that gave up, a cache row out of range).  Returns
+ * MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_STATE and clears the word. */
+mla_status mla_get_device_status(mla_ctx* ctx, void* stream);
+
+/* Observability.  With profiling on, every kernel a later token call launches is bracketed
+ * by CUDA events recorded on the call's stream (also inside a CUDA-graph capture, where they
+ * become event nodes).  Creates the context's event pool on first use. */
+mla_status mla_set_profiling(mla_ctx* ctx, int on);
+
+/* Kernels launched by the most recent mla_cache_append / mla_prefill / mla_decode call:
+ * returns their count (or -1 for a NULL ctx) and fills up to `max` entries of names (static
+ * strings, may be NULL) and ms (device milliseconds of each launch when that call ran with
+ * profiling on, else -1; waits for the launch to finish; may be NULL). */
+int mla_last_launches(mla_ctx* ctx, int max, const char** names, float* ms);
+
+/* Static, human-readable name of a status code. */
+const char* mla_status_string(mla_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H */

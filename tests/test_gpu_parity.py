@@ -1,0 +1,142 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle on identical seeded inputs.
+
+Bar: FP8 dequantisation bit-exact; layer outputs within relative Frobenius error 1e-2 and
+max-abs error 5e-2.  Small cases compare every element; the full-size workloads compare
+sampled outputs that the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+from head_latent_attention_mla_gb300 import mla, synth
+from oracle import mla_oracle as O
+from tests.mla_cases import (assert_close, build_caches_gpu, oracle_cache, oracle_rows,
+                             oracle_weights, to_dev, weights_and_gains)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def layer():
+    wq, g = weights_and_gains(0)
+    L = mla.MlaLayer(wq, g)
+    yield L
+    L.close()
+
+
+def run_prefill(layer, seqs, T, cap=None):
+    """GPU prefill of sequences `seqs` (synth sequence ids), T tokens each."""
+    B = len(seqs)
+    xb = np.stack([synth.hidden_states(0, s, 0, T) for s in seqs])
+    x = to_dev(xb)
+    cap = cap or T
+    cache = torch.zeros(B, cap, 576, dtype=torch.bfloat16, device="cuda")
+    lens = torch.zeros(B, dtype=torch.int32, device="cuda")
+    y = layer.prefill(x, cache, lens, [0] * B)
+    torch.cuda.synchronize()
+    assert layer.status() == mla.MLA_OK
+    assert lens.tolist() == [T] * B
+    return xb, y.float().cpu().numpy(), cache.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["q_a", "q_b", "kv_a", "kv_b", "o"])
+def test_dequant_bit_exact(layer, name):
+    wq, _ = weights_and_gains(0)
+    got = layer.dequant(name).cpu().numpy()
+    ref = O.dequant_fp32(*wq[name])
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("T", [1, 16, 130])
+def test_prefill_small_every_element(layer, T):
+    """Config-1 size (T=16) and tile edge cases (T=1, T=130 = two tiles and a ragged tail)."""
+    W = oracle_weights(0)
+    xb, y, cache = run_prefill(layer, [0], T)
+    y_ref, cache_ref = O.prefill(O.bf16_to_f64(xb[0]), W)
+    assert_close(y[0], y_ref, f"prefill T={T}")
+    assert_close(cache[0, :T], cache_ref, f"cache T={T}")
+
+
+def test_prefill_batch_of_two(layer):
+    W = oracle_weights(0)
+    xb, y, _ = run_prefill(layer, [3, 4], 70, cap=96)
+    for b, s in enumerate([3, 4]):
+        y_ref, _ = O.prefill(O.bf16_to_f64(xb[b]), W)
+        assert_close(y[b], y_ref, f"batch row {b}")
+
+
+def test_decode_config2_p1000(layer):
+    """Decode at position 1000 over a cache built by a causal prefill of 1000 tokens."""
+    W = oracle_weights(0)
+    p = 1000
+    xb = synth.hidden_states(0, 0, 0, p + 1)
+    cache = torch.zeros(1, p + 8, 576, dtype=torch.bfloat16, device="cuda")
+    lens = torch.zeros(1, dtype=torch.int32, device="cuda")
+    layer.prefill(to_dev(xb[None, :p]), cache, lens, [0])
+    yd = layer.decode(to_dev(xb[p:p + 1]), cache, lens, [p])
+    torch.cuda.synchronize()
+    assert layer.status() == mla.MLA_OK and lens.item() == p + 1
+    xf = O.bf16_to_f64(xb)
+    cache_ref = O.cache_rows(xf[:p], np.arange(p), W)
+    y_ref, full_ref = O.decode(xf[p], cache_ref, W)
+    assert_close(yd[0].float().cpu().numpy(), y_ref, "decode p=1000")
+    assert_close(cache[0, :p + 1].float().cpu().numpy(), full_ref, "cache after decode")
+
+
+def test_decode_matches_last_prefill_row_on_gpu(layer):
+    """Decode at p equals row p of a causal prefill over p+1 tokens (both on the GPU)."""
+    p = 200
+    xb = synth.hidden_states(0, 7, 0, p + 1)
+    _, y_pre, _ = run_prefill(layer, [7], p + 1)
+    cache = torch.zeros(1, p + 1, 576, dtype=torch.bfloat16, device="cuda")
+    lens = torch.zeros(1, dtype=torch.int32, device="cuda")
+    layer.cache_append(to_dev(xb[None, :p]), cache, lens, [0])
+    yd = layer.decode(to_dev(xb[p:p + 1]), cache, lens, [p])
+    assert_close(yd[0].float().cpu().numpy(), y_pre[0, p], "decode vs prefill row")
+
+
+def test_prefill_config3_t4096_sampled(layer):
+    """Full-size prefill (T=4096): sampled rows against the oracle."""
+    W = oracle_weights(0)
+    T = 4096
+    xb, y, cache = run_prefill(layer, [0], T)
+    xf = O.bf16_to_f64(xb[0])
+    cache_ref = O.cache_rows(xf, np.arange(T), W)
+    assert_close(cache[0], cache_ref, "cache T=4096")
+    rows = np.array([0, 1, 63, 64, 65, 127, 1000, 2047, 2048, 3333, 4094, 4095])
+    assert_close(y[0, rows], oracle_rows(xf, rows, cache_ref, W), "prefill T=4096 rows")
+
+
+def test_decode_config4_ragged_b64_sampled(layer):
+    W = oracle_weights(0)
+    lengths = synth.ragged_lengths(0, 64, 512, 8192).tolist()
+    cap = max(lengths) + 1
+    cache, lens = build_caches_gpu(layer, 0, lengths, cap)
+    xb = np.stack([synth.hidden_states(0, b, lengths[b], 1)[0] for b in range(64)])
+    yd = layer.decode(to_dev(xb), cache, lens, lengths)
+    torch.cuda.synchronize()
+    assert layer.status() == mla.MLA_OK
+    assert lens.tolist() == [n + 1 for n in lengths]
+    yd = yd.float().cpu().numpy()
+    order = np.argsort(lengths)
+    for b in (int(order[0]), int(order[31]), int(order[-1])):
+        c_ref = oracle_cache(0, b, lengths[b], W)
+        y_ref, _ = O.decode(O.bf16_to_f64(xb[b]), c_ref, W)
+        assert_close(yd[b], y_ref, f"ragged decode seq {b} (len {lengths[b]})")
+
+
+def test_decode_config5_long_b8_sampled(layer):
+    W = oracle_weights(0)
+    L = 131072
+    cache, lens = build_caches_gpu(layer, 0, [L] * 8, L + 1)
+    xb = np.stack([synth.hidden_states(0, b, L, 1)[0] for b in range(8)])
+    yd = layer.decode(to_dev(xb), cache, lens, [L] * 8)
+    torch.cuda.synchronize()
+    assert layer.status() == mla.MLA_OK
+    yd = yd.float().cpu().numpy()
+    b = 5
+    c_ref = oracle_cache(0, b, L, W)
+    y_ref, full = O.decode(O.bf16_to_f64(xb[b]), c_ref, W)
+    assert_close(yd[b], y_ref, "long decode seq 5")
+    got_rows = cache[b, [0, 77777, L]].float().cpu().numpy()
+    assert_close(got_rows, full[[0, 77777, L]], "long cache rows")
