@@ -44,22 +44,25 @@ __device__ int find_item(const int* seq_lens, int B, int chunk, int item, int* l
 constexpr int DT = 32;          // cached positions per tile
 constexpr int QS = LAT + 8;     // padded smem row (bank spread)
 
-// One CTA (256 threads) per work item: positions [i*chunk, min(S_b, (i+1)*chunk)) of
+constexpr int HG = 16;           // heads per CTA (4 CTAs share each work item)
+
+// CTA (g, item): heads [16 g, 16 g + 16) over positions [i*chunk, min(S_b, (i+1)*chunk)) of
 // sequence b, S_b = seq_lens[b] + 1 (the new token's row is already stored).  Thread
-// t = 4h + q handles head h and latent columns [128q, 128q + 128).
+// t = 16 hl + u handles head 16 g + hl: scores of positions 2u, 2u+1 of each 32-position tile,
+// and output columns [32 u, 32 u + 32).
 // scores s_h(j) = qfull[b,h] . cache[b,j]  (576 = 512 latent + 64 rotary)
 // partial o_h = sum_j exp2(s_h(j)*c - m_h) cache[b, j, 0:512],  l_h = sum_j exp2(...).
-__global__ void __launch_bounds__(256, 1) decode_attn_simt_kernel(
+__global__ void __launch_bounds__(256) decode_attn_simt_kernel(
     const __nv_bfloat16* __restrict__ qfull, const __nv_bfloat16* __restrict__ cache, int cap,
     const int* __restrict__ seq_lens, int B, int chunk, float scale_log2,
     float* __restrict__ o_part, float* __restrict__ ml_part, int* err) {
   extern __shared__ __align__(16) unsigned char smem[];
   __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smem);
-  __nv_bfloat16* Cs = Qs + HEADS * QS;
+  __nv_bfloat16* Cs = Qs + HG * QS;
   float* Ps = reinterpret_cast<float*>(Cs + DT * QS);
   __shared__ int s_b, s_i;
-  const int tid = threadIdx.x, h = tid >> 2, q4 = tid & 3;
-  const int item = blockIdx.x;
+  const int tid = threadIdx.x, hl = tid >> 4, u = tid & 15;
+  const int g = blockIdx.x, item = blockIdx.y, h = g * HG + hl;
   if (tid == 0) {
     int first;
     s_b = find_item(seq_lens, B, chunk, item, &s_i, &first);
@@ -67,7 +70,6 @@ __global__ void __launch_bounds__(256, 1) decode_attn_simt_kernel(
   }
   __syncthreads();
   const int b = s_b;
-  float* op = o_part + ((size_t)item * HEADS + h) * KV_LORA + q4 * 128;
   if (b < 0) return;
   const int S = seq_lens[b] + 1;
   const int p0 = s_i * chunk, p1 = min(S, p0 + chunk);
@@ -75,15 +77,14 @@ __global__ void __launch_bounds__(256, 1) decode_attn_simt_kernel(
     if (tid == 0) atomicExch(err, DEV_ERR_RANGE);
     return;
   }
-
-  for (int e = tid; e < HEADS * (LAT / 8); e += 256) {
+  for (int e = tid; e < HG * (LAT / 8); e += 256) {
     const int r = e / (LAT / 8), c = e % (LAT / 8);
     reinterpret_cast<uint4*>(Qs + r * QS)[c] =
-        reinterpret_cast<const uint4*>(qfull + ((size_t)b * HEADS + r) * LAT)[c];
+        reinterpret_cast<const uint4*>(qfull + ((size_t)b * HEADS + g * HG + r) * LAT)[c];
   }
-  float o[128];
+  float o[32];
 #pragma unroll
-  for (int c = 0; c < 128; ++c) o[c] = 0.f;
+  for (int c = 0; c < 32; ++c) o[c] = 0.f;
   float m = -INFINITY, l = 0.f;
   const __nv_bfloat16* cb = cache + (size_t)b * cap * LAT;
 
@@ -96,58 +97,54 @@ __global__ void __launch_bounds__(256, 1) decode_attn_simt_kernel(
           r < n ? reinterpret_cast<const uint4*>(cb + (size_t)(p + r) * LAT)[c] : make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
-    float s[8];
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) s[jj] = 0.f;
+    float s0 = 0.f, s1 = 0.f;
+    const uint4* qrow = reinterpret_cast<const uint4*>(Qs + hl * QS);
+    const uint4* c0 = reinterpret_cast<const uint4*>(Cs + (2 * u) * QS);
+    const uint4* c1 = reinterpret_cast<const uint4*>(Cs + (2 * u + 1) * QS);
+#pragma unroll 4
     for (int k = 0; k < LAT / 8; ++k) {
-      const uint4 qv = reinterpret_cast<const uint4*>(Qs + h * QS)[k];
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj)
-        s[jj] = dot8_bf16(qv, reinterpret_cast<const uint4*>(Cs + (q4 * 8 + jj) * QS)[k], s[jj]);
+      const uint4 qv = qrow[k];
+      s0 = dot8_bf16(qv, c0[k], s0);
+      s1 = dot8_bf16(qv, c1[k], s1);
     }
-    float tmax = -INFINITY;
+    s0 = (2 * u < n) ? s0 * scale_log2 : -INFINITY;
+    s1 = (2 * u + 1 < n) ? s1 * scale_log2 : -INFINITY;
+    float tmax = fmaxf(s0, s1);
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      s[jj] = (q4 * 8 + jj < n) ? s[jj] * scale_log2 : -INFINITY;
-      tmax = fmaxf(tmax, s[jj]);
-    }
-    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+    for (int off = 1; off < 16; off <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
     const float m_new = fmaxf(m, tmax);
     const float alpha = exp2f(m - m_new);
-    float lsum = 0.f;
+    const float p0v = exp2f(s0 - m_new), p1v = exp2f(s1 - m_new);
+    float lsum = p0v + p1v;
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      const float pj = exp2f(s[jj] - m_new);
-      lsum += pj;
-      Ps[h * DT + q4 * 8 + jj] = pj;
-    }
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+    for (int off = 1; off < 16; off <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    Ps[hl * DT + 2 * u] = p0v;
+    Ps[hl * DT + 2 * u + 1] = p1v;
     l = l * alpha + lsum;
     m = m_new;
     __syncwarp();
 #pragma unroll
-    for (int c = 0; c < 128; ++c) o[c] *= alpha;
+    for (int c = 0; c < 32; ++c) o[c] *= alpha;
     for (int j = 0; j < n; ++j) {
-      const float pj = Ps[h * DT + j];
-      const uint4* crow = reinterpret_cast<const uint4*>(Cs + j * QS + q4 * 128);
+      const float pj = Ps[hl * DT + j];
+      const uint4* crow = reinterpret_cast<const uint4*>(Cs + j * QS + u * 32);
 #pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
+      for (int c8 = 0; c8 < 4; ++c8) {
         const uint4 v = crow[c8];
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          o[c8 * 8 + 2 * i] = fmaf(pj, __uint_as_float(u[i] << 16), o[c8 * 8 + 2 * i]);
-          o[c8 * 8 + 2 * i + 1] = fmaf(pj, __uint_as_float(u[i] & 0xFFFF0000u), o[c8 * 8 + 2 * i + 1]);
+          o[c8 * 8 + 2 * i] = fmaf(pj, __uint_as_float(w[i] << 16), o[c8 * 8 + 2 * i]);
+          o[c8 * 8 + 2 * i + 1] = fmaf(pj, __uint_as_float(w[i] & 0xFFFF0000u), o[c8 * 8 + 2 * i + 1]);
         }
       }
     }
   }
+  float* op = o_part + ((size_t)item * HEADS + h) * KV_LORA + u * 32;
 #pragma unroll
-  for (int c = 0; c < 128; c += 4)
+  for (int c = 0; c < 32; c += 4)
     *reinterpret_cast<float4*>(op + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-  if (q4 == 0) {
+  if (u == 0) {
     ml_part[((size_t)item * HEADS + h) * 2] = m;
     ml_part[((size_t)item * HEADS + h) * 2 + 1] = l;
   }
@@ -316,7 +313,7 @@ __global__ void __launch_bounds__(256) prefill_attn_simt_kernel(
 }  // namespace
 
 constexpr size_t kDecodeSmem =
-    (size_t)(HEADS + DT) * QS * sizeof(__nv_bfloat16) + HEADS * DT * sizeof(float);
+    (size_t)(HG + DT) * QS * sizeof(__nv_bfloat16) + HG * DT * sizeof(float);
 constexpr size_t kPrefillSmem =
     (size_t)PT * (2 * KS + VS) * sizeof(__nv_bfloat16) + PT * (PT + 1) * sizeof(float);
 
@@ -332,7 +329,7 @@ cudaError_t launch_decode_attention(const __nv_bfloat16* qfull, const __nv_bfloa
                                     int cap, const int* seq_lens, DecodePlan plan, float scale,
                                     float* o_part, float* ml_part, int* err, cudaStream_t st) {
   if (plan.B == 0) return cudaSuccess;
-  decode_attn_simt_kernel<<<plan.items, 256, kDecodeSmem, st>>>(
+  decode_attn_simt_kernel<<<dim3(HEADS / HG, plan.items), 256, kDecodeSmem, st>>>(
       qfull, cache, cap, seq_lens, plan.B, plan.chunk, scale * LOG2E, o_part, ml_part, err);
   return cudaGetLastError();
 }

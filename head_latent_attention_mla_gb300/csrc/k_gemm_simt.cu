@@ -43,10 +43,13 @@ struct ProjSet {
   int rows0;  // rows of p[0]
 };
 
-// One warp per output row n; lanes stride over k in 16-byte (16 weight) chunks.
-template <int M>
+// One warp per output row n.  Lane l owns the 16-byte chunks l, l+32, ... of the row; all of
+// them are loaded before any arithmetic so that a warp keeps the whole row (up to 8 KiB) in
+// flight.  NCH = K / 512 chunks per lane.
+template <int M, int NCH>
 __global__ void __launch_bounds__(256) gemv_f8w_kernel(const __nv_bfloat16* __restrict__ X,
-                                                       int ldx, int K, ProjSet ps) {
+                                                       int ldx, ProjSet ps) {
+  constexpr int K = NCH * 512;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int total = ps.p[0].N + (ps.np > 1 ? ps.p[1].N : 0);
@@ -56,40 +59,32 @@ __global__ void __launch_bounds__(256) gemv_f8w_kernel(const __nv_bfloat16* __re
   const uint8_t* wrow = P.W + (size_t)n * K;
   const float* srow = P.S + (size_t)(n / BLK) * (K / BLK);
 
+  uint4 w[NCH];
+#pragma unroll
+  for (int u = 0; u < NCH; ++u) w[u] = ld_stream(wrow + u * 512 + lane * 16);
+
   float acc[M];
 #pragma unroll
   for (int m = 0; m < M; ++m) acc[m] = 0.f;
-
-  constexpr int U = 4;
-  for (int base = 0; base < K; base += 512 * U) {
-    uint4 w[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int k = base + u * 512 + lane * 16;
-      w[u] = (k < K) ? ld_stream(wrow + k) : make_uint4(0, 0, 0, 0);
-    }
+  for (int u = 0; u < NCH; ++u) {
+    const int k = u * 512 + lane * 16;
+    float wf[16];
+    e4m3x4_to_f32(w[u].x, wf);
+    e4m3x4_to_f32(w[u].y, wf + 4);
+    e4m3x4_to_f32(w[u].z, wf + 8);
+    e4m3x4_to_f32(w[u].w, wf + 12);
+    const float sc = __ldg(srow + k / BLK);
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int k = base + u * 512 + lane * 16;
-      if (k < K) {
-        float wf[16];
-        e4m3x4_to_f32(w[u].x, wf);
-        e4m3x4_to_f32(w[u].y, wf + 4);
-        e4m3x4_to_f32(w[u].z, wf + 8);
-        e4m3x4_to_f32(w[u].w, wf + 12);
-        const float sc = __ldg(srow + k / BLK);
+    for (int m = 0; m < M; ++m) {
+      const uint4* xp = reinterpret_cast<const uint4*>(X + (size_t)m * ldx + k);
+      float xf[16];
+      bf16x8_to_f32(__ldg(xp), xf);
+      bf16x8_to_f32(__ldg(xp + 1), xf + 8);
+      float part = 0.f;
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-          const uint4* xp = reinterpret_cast<const uint4*>(X + (size_t)m * ldx + k);
-          float xf[16];
-          bf16x8_to_f32(__ldg(xp), xf);
-          bf16x8_to_f32(__ldg(xp + 1), xf + 8);
-          float part = 0.f;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) part = fmaf(wf[i], xf[i], part);
-          acc[m] = fmaf(sc, part, acc[m]);
-        }
-      }
+      for (int i = 0; i < 16; ++i) part = fmaf(wf[i], xf[i], part);
+      acc[m] = fmaf(sc, part, acc[m]);
     }
   }
 #pragma unroll
@@ -104,6 +99,20 @@ __global__ void __launch_bounds__(256) gemv_f8w_kernel(const __nv_bfloat16* __re
         reinterpret_cast<__nv_bfloat16*>(P.Y)[(size_t)m * P.ldy + n] = __float2bfloat16_rn(v);
     }
   }
+}
+
+template <int M>
+cudaError_t launch_gemv(const __nv_bfloat16* X, int ldx, int K, const ProjSet& ps, int rows,
+                        cudaStream_t st) {
+  const dim3 grid((rows + 7) / 8), block(256);
+  switch (K) {
+    case 512: gemv_f8w_kernel<M, 1><<<grid, block, 0, st>>>(X, ldx, ps); break;
+    case 1536: gemv_f8w_kernel<M, 3><<<grid, block, 0, st>>>(X, ldx, ps); break;
+    case 7168: gemv_f8w_kernel<M, 14><<<grid, block, 0, st>>>(X, ldx, ps); break;
+    case 8192: gemv_f8w_kernel<M, 16><<<grid, block, 0, st>>>(X, ldx, ps); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 // Tiled fallback: 64 (m) x 64 (n) per CTA, 4x4 outputs per thread, k steps of 32.
@@ -190,16 +199,15 @@ cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Pro
   ps.rows0 = p[0].N;
   const int rows = p[0].N + (np > 1 ? p[1].N : 0);
   if (M <= 8) {
-    const dim3 grid((rows + 7) / 8), block(256);
     switch (M) {
-      case 1: gemv_f8w_kernel<1><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
-      case 2: gemv_f8w_kernel<2><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
-      case 3: gemv_f8w_kernel<3><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
-      case 4: gemv_f8w_kernel<4><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
-      case 5: gemv_f8w_kernel<5><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
-      case 6: gemv_f8w_kernel<6><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
-      case 7: gemv_f8w_kernel<7><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
-      default: gemv_f8w_kernel<8><<<grid, block, 0, st>>>(X, ldx, K, ps); break;
+      case 1: return launch_gemv<1>(X, ldx, K, ps, rows, st);
+      case 2: return launch_gemv<2>(X, ldx, K, ps, rows, st);
+      case 3: return launch_gemv<3>(X, ldx, K, ps, rows, st);
+      case 4: return launch_gemv<4>(X, ldx, K, ps, rows, st);
+      case 5: return launch_gemv<5>(X, ldx, K, ps, rows, st);
+      case 6: return launch_gemv<6>(X, ldx, K, ps, rows, st);
+      case 7: return launch_gemv<7>(X, ldx, K, ps, rows, st);
+      default: return launch_gemv<8>(X, ldx, K, ps, rows, st);
     }
   } else {
     const dim3 grid(rows / 64, (M + 63) / 64), block(256);

@@ -133,23 +133,40 @@ __global__ void __launch_bounds__(256) rope_q_kernel(__nv_bfloat16* __restrict__
   }
 }
 
-// Decode query absorption.  CTA (h, cb): head h, latent columns [128 cb, 128 cb + 128).
-// qfull[b, h, c] = bf16( s[2h][cb] * sum_i q_nope[b, h, i] * e4m3(W_kvb[256 h + i, c]) ),
-// i.e. W_UK,h^T q_nope with W_UK,h = rows 0..127 of head h's 256 ("Key content
-// up-projection" page, Explanation).  The cb == 0 CTA also writes RoPE(q_pe) to [512, 576).
-constexpr int ABS_BCHUNK = 16;
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float* f) {
+  __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFF), __NV_E4M3);
+  __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+  float2 a = __half22float2(*reinterpret_cast<__half2*>(&lo));
+  float2 c = __half22float2(*reinterpret_cast<__half2*>(&hi));
+  f[0] = a.x; f[1] = a.y; f[2] = c.x; f[3] = c.y;
+}
+
+// Decode query absorption, q~_h = W_UK,h^T q_nope,h with W_UK,h = rows 0..127 of head h's 256
+// in kv_b_proj ("Key content up-projection" page, Explanation):
+//   qfull[b, h, c] = bf16( s[2h][c/128] * sum_i q_nope[b, h, i] * e4m3(W_kvb[256 h + i, c]) ).
+// CTA (h, cb) owns latent columns [128 cb, 128 cb + 128) (one scale); warp w sums rows
+// i in [32 w, 32 w + 32) for 4 columns per lane, and the 4 warps' partials meet in shared
+// memory.  The cb == 0 CTA also writes RoPE(q_pe) to columns [512, 576).
+constexpr int ABQ_B = 8;
 __global__ void __launch_bounds__(128) absorb_q_kernel(
     const __nv_bfloat16* __restrict__ q, int B, const uint8_t* __restrict__ Wkvb,
     const float* __restrict__ Skvb, const float2* __restrict__ rope_tab, int pairing,
     const int* __restrict__ seq_lens, int limit, __nv_bfloat16* __restrict__ qfull) {
-  __shared__ float qn[ABS_BCHUNK][NOPE];
-  __shared__ float wt[NOPE][BLK + 1];
-  const int h = blockIdx.x, cb = blockIdx.y, c = threadIdx.x;
+  __shared__ float qn[ABQ_B][NOPE];
+  __shared__ float4 part[4][ABQ_B][32];
+  const int h = blockIdx.x, cb = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float sc = Skvb[(size_t)(2 * h) * (KV_LORA / BLK) + cb];
-  for (int i = 0; i < NOPE; ++i)
-    wt[i][c] = e4m3_to_f32(Wkvb[(size_t)(h * KVB_PER_HEAD + i) * KV_LORA + cb * BLK + c]);
-  for (int b0 = 0; b0 < B; b0 += ABS_BCHUNK) {
-    const int nb = min(ABS_BCHUNK, B - b0);
+  // This lane's 32 rows x 4 columns of W_UK,h, kept in registers across the batch.
+  float w[32][4];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(
+        Wkvb + (size_t)(h * KVB_PER_HEAD + warp * 32 + r) * KV_LORA + cb * BLK + lane * 4));
+    e4m3x4_to_f32(v, w[r]);
+  }
+  for (int b0 = 0; b0 < B; b0 += ABQ_B) {
+    const int nb = min(ABQ_B, B - b0);
     __syncthreads();
     for (int e = threadIdx.x; e < nb * NOPE; e += blockDim.x) {
       const int bb = e / NOPE, i = e % NOPE;
@@ -157,10 +174,32 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(
     }
     __syncthreads();
     for (int bb = 0; bb < nb; ++bb) {
-      float acc = 0.f;
-#pragma unroll 8
-      for (int i = 0; i < NOPE; ++i) acc = fmaf(qn[bb][i], wt[i][c], acc);
-      qfull[((size_t)(b0 + bb) * HEADS + h) * LAT + cb * BLK + c] = __float2bfloat16_rn(sc * acc);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < 32; ++r) {
+        const float x = qn[bb][warp * 32 + r];
+        acc.x = fmaf(x, w[r][0], acc.x);
+        acc.y = fmaf(x, w[r][1], acc.y);
+        acc.z = fmaf(x, w[r][2], acc.z);
+        acc.w = fmaf(x, w[r][3], acc.w);
+      }
+      part[warp][bb][lane] = acc;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < nb * 32; e += blockDim.x) {
+      const int bb = e / 32, l = e % 32;
+      float4 t = part[0][bb][l];
+#pragma unroll
+      for (int ww = 1; ww < 4; ++ww) {
+        const float4 u = part[ww][bb][l];
+        t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+      }
+      __nv_bfloat162 lo = __floats2bfloat162_rn(sc * t.x, sc * t.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(sc * t.z, sc * t.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(qfull + ((size_t)(b0 + bb) * HEADS + h) * LAT + cb * BLK + l * 4) = pk;
     }
   }
   if (cb == 0) {
@@ -179,37 +218,51 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(
   }
 }
 
-// Decode output absorption.  CTA h, thread v: out[b, h*128 + v] =
-// bf16( sum_cb s[2h+1][cb] * sum_{c in cb} e4m3(W_kvb[256 h + 128 + v, c]) * o_lat[b, h, c] ).
-__global__ void __launch_bounds__(128) absorb_out_kernel(
+// Decode output absorption, one warp per output row (h, v):
+//   out[b, 128 h + v] = bf16( sum_c s[2h+1][c/128] * e4m3(W_kvb[256 h + 128 + v, c]) * o_lat[b, h, c] )
+// (W_UV,h = rows 128..255 of head h's 256).  Lane l holds columns [16 l, 16 l + 16).
+constexpr int ABO_B = 8;
+__global__ void __launch_bounds__(256) absorb_out_kernel(
     const __nv_bfloat16* __restrict__ o_lat, int B, const uint8_t* __restrict__ Wkvb,
     const float* __restrict__ Skvb, __nv_bfloat16* __restrict__ out) {
-  __shared__ float ol[4][KV_LORA];
-  const int h = blockIdx.x, v = threadIdx.x;
-  const uint8_t* wrow = Wkvb + (size_t)(h * KVB_PER_HEAD + NOPE + v) * KV_LORA;
-  const float* srow = Skvb + (size_t)(2 * h + 1) * (KV_LORA / BLK);
-  for (int b0 = 0; b0 < B; b0 += 4) {
-    const int nb = min(4, B - b0);
-    __syncthreads();
-    for (int e = threadIdx.x; e < nb * KV_LORA; e += blockDim.x) {
-      const int bb = e / KV_LORA, c = e % KV_LORA;
-      ol[bb][c] = __bfloat162float(o_lat[((size_t)(b0 + bb) * HEADS + h) * KV_LORA + c]);
-    }
-    __syncthreads();
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int cb = 0; cb < KV_LORA / BLK; ++cb) {
-      float part[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int c = cb * BLK; c < (cb + 1) * BLK; ++c) {
-        const float w = e4m3_to_f32(wrow[c]);
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;   // h * 128 + v
+  const int lane = threadIdx.x & 31;
+  if (row >= HEADS * VDIM) return;
+  const int h = row / VDIM, v = row % VDIM;
+  const uint4 wv = __ldg(reinterpret_cast<const uint4*>(
+      Wkvb + (size_t)(h * KVB_PER_HEAD + NOPE + v) * KV_LORA + lane * 16));
+  float w[16];
+  e4m3x4_to_f32(wv.x, w);
+  e4m3x4_to_f32(wv.y, w + 4);
+  e4m3x4_to_f32(wv.z, w + 8);
+  e4m3x4_to_f32(wv.w, w + 12);
+  const float sc = Skvb[(size_t)(2 * h + 1) * (KV_LORA / BLK) + lane / 8];
+  for (int b0 = 0; b0 < B; b0 += ABO_B) {
+    float acc[ABO_B];
 #pragma unroll
-        for (int bb = 0; bb < 4; ++bb) part[bb] = fmaf(w, ol[bb][c], part[bb]);
+    for (int bb = 0; bb < ABO_B; ++bb) {
+      acc[bb] = 0.f;
+      if (b0 + bb < B) {
+        const uint4* xp = reinterpret_cast<const uint4*>(
+            o_lat + ((size_t)(b0 + bb) * HEADS + h) * KV_LORA + lane * 16);
+        const uint4 x0 = __ldg(xp), x1 = __ldg(xp + 1);
+        const uint32_t u[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        float p = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          p = fmaf(w[2 * i], __uint_as_float(u[i] << 16), p);
+          p = fmaf(w[2 * i + 1], __uint_as_float(u[i] & 0xFFFF0000u), p);
+        }
+        acc[bb] = sc * p;
       }
-      const float sc = srow[cb];
-#pragma unroll
-      for (int bb = 0; bb < 4; ++bb) acc[bb] = fmaf(sc, part[bb], acc[bb]);
     }
-    for (int bb = 0; bb < nb; ++bb)
-      out[(size_t)(b0 + bb) * O_IN + h * VDIM + v] = __float2bfloat16_rn(acc[bb]);
+#pragma unroll
+    for (int bb = 0; bb < ABO_B; ++bb) {
+      float t = acc[bb];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+      if (lane == 0 && b0 + bb < B) out[(size_t)(b0 + bb) * O_IN + row] = __float2bfloat16_rn(t);
+    }
   }
 }
 
@@ -258,7 +311,7 @@ cudaError_t launch_absorb_q(const __nv_bfloat16* q, int B, const uint8_t* Wkvb,
 
 cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* Wkvb,
                               const float* Skvb, __nv_bfloat16* out, cudaStream_t st) {
-  absorb_out_kernel<<<HEADS, VDIM, 0, st>>>(o_lat, B, Wkvb, Skvb, out);
+  absorb_out_kernel<<<HEADS * VDIM / 8, 256, 0, st>>>(o_lat, B, Wkvb, Skvb, out);
   return cudaGetLastError();
 }
 

@@ -217,11 +217,16 @@ int mla_last_launches(mla_ctx* c, int max, const char** names, float* ms) {
   for (int k = 0; k < n && k < max; ++k) {
     if (names) names[k] = c->names[k];
     if (ms) {
+      // Events captured into a graph that has not been replayed yet are not recorded: they
+      // report -1.  Failed queries must not leave an error behind for the caller's next check.
       ms[k] = -1.f;
-      if (c->last_profiled && cudaEventSynchronize(c->ev[2 * k + 1]) == cudaSuccess)
-        cudaEventElapsedTime(&ms[k], c->ev[2 * k], c->ev[2 * k + 1]);
+      if (c->last_profiled && cudaEventSynchronize(c->ev[2 * k + 1]) == cudaSuccess &&
+          cudaEventQuery(c->ev[2 * k]) == cudaSuccess &&
+          cudaEventElapsedTime(&ms[k], c->ev[2 * k], c->ev[2 * k + 1]) != cudaSuccess)
+        ms[k] = -1.f;
     }
   }
+  cudaGetLastError();
   return n;
 }
 
@@ -326,8 +331,8 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
   for (int b = 0; b < B; ++b) total += (long)lens_host[b] + 1;
   const long target = 2L * c->num_sms;
   long chunk = (total + target - 1) / target;
-  chunk = ((chunk + 63) / 64) * 64;
-  if (chunk < 64) chunk = 64;
+  chunk = ((chunk + 31) / 32) * 32;
+  if (chunk < 32) chunk = 32;
   long items = 0;
   for (int b = 0; b < B; ++b) items += ((long)lens_host[b] + 1 + chunk - 1) / chunk;
   if (items > items_max(c, B)) return MLA_ERR_STATE;
