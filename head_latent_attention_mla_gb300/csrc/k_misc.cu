@@ -315,7 +315,10 @@ cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* 
   return cudaGetLastError();
 }
 
-cudaError_t init_kernels() { return init_attention_kernels(); }
+cudaError_t init_kernels() {
+  cudaError_t e = init_attention_kernels();
+  return e != cudaSuccess ? e : init_decode_tc_kernel();
+}
 
 cudaError_t launch_advance_lens(int* seq_lens, int B, int T, cudaStream_t st) {
   advance_lens_kernel<<<(B + 255) / 256, 256, 0, st>>>(seq_lens, B, T);

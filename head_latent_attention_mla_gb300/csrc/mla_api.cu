@@ -331,8 +331,8 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
   for (int b = 0; b < B; ++b) total += (long)lens_host[b] + 1;
   const long target = 2L * c->num_sms;
   long chunk = (total + target - 1) / target;
-  chunk = ((chunk + 31) / 32) * 32;
-  if (chunk < 32) chunk = 32;
+  chunk = ((chunk + 63) / 64) * 64;
+  if (chunk < 64) chunk = 64;
   long items = 0;
   for (int b = 0; b < B; ++b) items += ((long)lens_host[b] + 1 + chunk - 1) / chunk;
   if (items > items_max(c, B)) return MLA_ERR_STATE;
@@ -357,9 +357,9 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
   MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, B, Q_LORA, &p2, 1, s));
   MLA_LAUNCH("absorb_q", launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
                              c->cfg.rope_pairing, lens_dev, limit, qfull, s));
-  MLA_LAUNCH("decode_attention", launch_decode_attention(qfull, C, cap, lens_dev, plan,
-                                                         c->cfg.softmax_scale, opart, ml,
-                                                         c->d_err, s));
+  MLA_LAUNCH("decode_attention", launch_decode_attention_tc(qfull, C, cap, lens_dev, plan,
+                                                            c->cfg.softmax_scale, opart, ml,
+                                                            c->d_err, s));
   MLA_LAUNCH("decode_combine", launch_decode_combine(lens_dev, plan, opart, ml, olat, c->d_err, s));
   MLA_LAUNCH("absorb_out", launch_absorb_out(olat, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], attn, s));
   Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};

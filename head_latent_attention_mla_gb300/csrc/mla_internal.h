@@ -85,6 +85,14 @@ cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const fl
                                   const float* ml_part, __nv_bfloat16* o_lat, int* err,
                                   cudaStream_t st);
 
+// The same attention on the tcgen05 tensor cores (TMA-fed, accumulators in tensor memory);
+// writes the same partials as launch_decode_attention.
+cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bfloat16* cache,
+                                       int cap, const int* seq_lens, DecodePlan plan,
+                                       float scale, float* o_part, float* ml_part, int* err,
+                                       cudaStream_t st);
+cudaError_t init_decode_tc_kernel();
+
 // One-time kernel attributes (dynamic shared memory opt-in); called by mla_create so that
 // later calls only enqueue work and can be captured into CUDA graphs.
 cudaError_t init_kernels();

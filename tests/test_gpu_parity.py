@@ -140,3 +140,44 @@ def test_decode_config5_long_b8_sampled(layer):
     assert_close(yd[b], y_ref, "long decode seq 5")
     got_rows = cache[b, [0, 77777, L]].float().cpu().numpy()
     assert_close(got_rows, full[[0, 77777, L]], "long cache rows")
+
+
+@pytest.mark.parametrize("lengths", [[0], [1, 63, 64, 65, 127, 128, 129, 200]])
+def test_decode_tile_edges_every_sequence(layer, lengths):
+    """Empty cache (p=0) and lengths around the 64-position tile edges, all sequences checked."""
+    W = oracle_weights(0)
+    cap = max(lengths) + 3
+    cache, lens = build_caches_gpu(layer, 0, lengths, cap)
+    xb = np.stack([synth.hidden_states(0, b, lengths[b], 1)[0] for b in range(len(lengths))])
+    yd = layer.decode(to_dev(xb), cache, lens, lengths)
+    torch.cuda.synchronize()
+    assert layer.status() == mla.MLA_OK
+    yd = yd.float().cpu().numpy()
+    for b, n in enumerate(lengths):
+        c_ref = oracle_cache(0, b, n, W) if n else None
+        y_ref, _ = O.decode(O.bf16_to_f64(xb[b]), c_ref if n else np.zeros((0, 576)), W)
+        assert_close(yd[b], y_ref, f"decode len {n}")
+
+
+def test_decode_growing_scores_rescale(layer):
+    """Later tokens scaled x5: their rotary keys (not normalised by RMSNorm) grow, so the
+    running maximum of the scores jumps by far more than 2^8 in late tiles and the output
+    kept so far must be rescaled.  (Much larger scales make bf16 rounding of the keys alone
+    exceed the tolerance, in any implementation that stores the cache in bf16.)"""
+    W = oracle_weights(0)
+    n = 700
+    xb = synth.hidden_states(0, 11, 0, n + 1)
+    xf = O.bf16_to_f64(xb)
+    xf[400:] *= 5.0
+    from head_latent_attention_mla_gb300.synth import to_bf16_bits
+    xb = to_bf16_bits(xf.astype(np.float32))
+    xf = O.bf16_to_f64(xb)
+    cache = torch.zeros(1, n + 1, 576, dtype=torch.bfloat16, device="cuda")
+    lens = torch.zeros(1, dtype=torch.int32, device="cuda")
+    layer.cache_append(to_dev(xb[None, :n]), cache, lens, [0])
+    yd = layer.decode(to_dev(xb[n:n + 1]), cache, lens, [n])
+    torch.cuda.synchronize()
+    assert layer.status() == mla.MLA_OK
+    c_ref = O.cache_rows(xf[:n], np.arange(n), W)
+    y_ref, _ = O.decode(xf[n], c_ref, W)
+    assert_close(yd[0].float().cpu().numpy(), y_ref, "rescaled decode")
