@@ -457,6 +457,27 @@ def reference_arm(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def case_arm(args):
+    """One workload, small enough to profile: `decode:B:L` (B sequences with L cached positions
+    each, cache built by append) or `prefill:T` (one sequence of T tokens).  Prints a short
+    JSON line with the step time and per-kernel device times."""
+    import torch
+    from head_latent_attention_mla_gb300 import mla, synth
+    torch.cuda.set_device(0)
+    device = "cuda:0"
+    layer = mla.MlaLayer(synth.make_weights(0), synth.make_gains(0), device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    kind, *dims = args.case.split(":")
+    if kind == "decode":
+        B, L = int(dims[0]), int(dims[1])
+        r = run_decode_workload(torch, mla, synth, layer, args.case, [L] * B, "append",
+                                args.steps, args.warmup, device, flush, prof_steps=3, e2e=False)
+    else:
+        r = run_prefill_workload(torch, mla, synth, layer, int(dims[0]), args.steps,
+                                 args.warmup, device, flush)
+    return {"case": args.case, "ms_per_step": r["ms"], "per_kernel_ms": r["per_kernel_ms"]}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -465,10 +486,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="profiling case instead of the benchmark line: decode:B:L or prefill:T")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    line = reference_arm(args) if args.impl == "reference" else gpu_arm(args)
+    if args.case:
+        line = case_arm(args)
+    else:
+        line = reference_arm(args) if args.impl == "reference" else gpu_arm(args)
     if line is not None:
         print(json.dumps(line))
 

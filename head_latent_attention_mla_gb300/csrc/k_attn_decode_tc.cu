@@ -6,16 +6,21 @@
 // softmax scale, and the latent output is o_lat,h = sum_j p_h(j) c_hat_j.  Each 64-position
 // latent tile is read from HBM once and serves as both key and value.
 //
-// One CTA per work item (a run of positions of one sequence), 6 warps:
+// One CTA per work item (a run of positions of one sequence), 7 warps:
 //   warp 0      TMA producer: the query block once, then 64-position cache tiles into a
-//               two-stage ring (9 boxes of 64 rows x 64 columns, 128-byte swizzle);
-//   warp 1      allocates tensor memory and issues the MMAs from one thread:
-//                 MMA1  S[64 heads, 64 pos]   = Q[64, 576] . C[64, 576]^T    (M=64,  N=64)
-//                 MMA2  O^T[512, 64 heads]   += C[64 pos, 0:512]^T . P^T     (M=128, N=64, x4)
+//               two-stage ring (9 boxes of 64 rows x 64 columns, 128-byte swizzle).  Tiles
+//               further ahead are bulk-prefetched into L2, so that the two shared-memory
+//               stages are refilled from L2 while HBM streams the next tiles;
+//   warp 1      allocates tensor memory and issues, from one thread,
+//                 MMA1  S[64 heads, 64 pos]   = Q[64, 576] . C[64, 576]^T    (M=64,  N=64);
+//   warp 6      issues, from one thread,
+//                 MMA2  O^T[512, 64 heads]   += C[64 pos, 0:512]^T . P^T     (M=128, N=64, x4).
+//               Two issuers keep MMA2 of a tile from queueing behind the next tile's load;
 //   warps 2..5  softmax: one head per thread (rows of S), online softmax in base 2 with a
 //               lazy rescale of O^T (only when a head's running maximum grows by more than
-//               2^8), P written as bf16 to shared memory; then the epilogue writes the
-//               unnormalised partial O, the maximum m and the sum l of every head.
+//               2^8), P written as bf16 into the tile's rotary box (box 8), which MMA1 no
+//               longer needs; then the epilogue writes the unnormalised partial O, the
+//               maximum m and the sum l of every head.
 // Tensor memory: O^T in columns [0, 256) (lane = latent dim, column = head within each of the
 // four 128-dim blocks), S in [256, 320) and [320, 384) (double buffer).
 #include "tc_common.cuh"
@@ -30,16 +35,16 @@ constexpr int DA_TILE = 64;                     // positions per tile
 constexpr int DA_BOX = 64 * 128;                // one [64 rows x 64 bf16] box, bytes
 constexpr int DA_NBOX = LAT / 64;               // 9 boxes per 576-wide row block
 constexpr int DA_TILE_BYTES = DA_NBOX * DA_BOX;  // 73728
-constexpr int DA_THREADS = 192;
+constexpr int DA_THREADS = 224;
 constexpr int OFF_Q = 0;
 constexpr int OFF_C = OFF_Q + DA_TILE_BYTES;    // two stages
-constexpr int OFF_P = OFF_C + 2 * DA_TILE_BYTES;
-constexpr int OFF_BAR = OFF_P + HEADS * 128;
-constexpr int OFF_MISC = OFF_BAR + 16 * 8;
+constexpr int OFF_BAR = OFF_C + 2 * DA_TILE_BYTES;
+constexpr int OFF_MISC = OFF_BAR + 16 * 8;  // 13 barriers used
 constexpr int OFF_ALPHA = OFF_MISC + 16;
 constexpr int DA_SMEM = OFF_ALPHA + HEADS * 4 + 1024;  // + slack for 1024-byte alignment
 constexpr uint32_t TM_O = 0, TM_S = 256;
 constexpr float RESCALE_LOG2 = 8.f;             // tolerated growth of p before rescaling O
+constexpr int PF_TILES = 4;                     // tiles prefetched into L2 ahead of the ring
 
 __device__ __forceinline__ int find_item_tc(const int* seq_lens, int B, int chunk, int item,
                                             int* local) {
@@ -57,8 +62,9 @@ __device__ __forceinline__ int find_item_tc(const int* seq_lens, int B, int chun
 
 __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
     const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_c,
-    const int* __restrict__ seq_lens, int B, int cap, int chunk, float scale_log2,
-    float* __restrict__ o_part, float* __restrict__ ml_part, int* err) {
+    const __nv_bfloat16* __restrict__ cache, const int* __restrict__ seq_lens, int B, int cap,
+    int chunk, float scale_log2, float* __restrict__ o_part, float* __restrict__ ml_part,
+    int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
@@ -70,7 +76,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
   uint64_t* s_free = bars + 7;   // [2]
   uint64_t* p_full = bars + 9;
   uint64_t* o_done = bars + 10;
-  uint64_t* mma_idle = bars + 11;
+  uint64_t* mma_idle = bars + 11;  // [2]: one per MMA-issuing thread
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   int* s_item = reinterpret_cast<int*>(smem + OFF_MISC + 8);
@@ -97,7 +103,8 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
     }
     mbar_init(p_full, 128);
     mbar_init(o_done, 1);
-    mbar_init(mma_idle, 1);
+    mbar_init(&mma_idle[0], 1);
+    mbar_init(&mma_idle[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -123,9 +130,16 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
         mbar_expect_tx(q_full, DA_TILE_BYTES);
         for (int c = 0; c < DA_NBOX; ++c)
           tma_load_2d(smem + OFF_Q + c * DA_BOX, &map_q, q_full, 64 * c, HEADS * b);
+        auto prefetch = [&](int t) {
+          const int first = p0 + DA_TILE * t;
+          const int rows = min(DA_TILE, p1 - first);
+          prefetch_l2(cache + ((size_t)b * cap + first) * LAT, (uint32_t)rows * LAT * 2);
+        };
+        for (int t = 2; t < min(nt, 2 + PF_TILES); ++t) prefetch(t);
         int issued = 0;
         for (int t = 0; t < nt; ++t) {
           const int st = t & 1;
+          if (t >= 1 && t + 2 + PF_TILES - 1 < nt) prefetch(t + 2 + PF_TILES - 1);
           if (t >= 2 && !mbar_wait(&c_empty[st], ((t - 2) >> 1) & 1, err, abort_flag)) break;
           mbar_expect_tx(&c_full[st], DA_TILE_BYTES);
           const int row = b * cap + p0 + DA_TILE * t;
@@ -141,28 +155,10 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
           mbar_wait(&c_full[t & 1], (t >> 1) & 1, err, &no_abort);
       }
     } else if (warp == 1) {
-      // ---------------------------------------------------------------- MMA issuer
+      // ---------------------------------------------------------------- MMA1 issuer
       if (lane == 0) {
         constexpr uint32_t idesc_s = idesc_bf16(64, 64, false, false);
-        constexpr uint32_t idesc_o = idesc_bf16(128, 64, true, false);
         const uint32_t qb = sbase + OFF_Q;
-        auto mma2 = [&](int u) -> bool {
-          if (!mbar_wait(p_full, u & 1, err, abort_flag)) return false;
-          fence_after();
-          const uint32_t cb = sbase + OFF_C + (u & 1) * DA_TILE_BYTES;
-#pragma unroll
-          for (int d = 0; d < 4; ++d)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              // A = C^T: MN-major, 128 latent dims (2 boxes, DA_BOX apart) x 16 positions.
-              const uint64_t a = sdesc_sw128(cb + 2 * d * DA_BOX + k * 2048, DA_BOX, 1024);
-              const uint64_t bd = sdesc_sw128(sbase + OFF_P + k * 32, 16, 1024);
-              mma_bf16(tmem + TM_O + 64 * d, a, bd, idesc_o, (u > 0) || (k > 0));
-            }
-          mma_commit(o_done);
-          mma_commit(&c_empty[u & 1]);
-          return true;
-        };
         bool ok = mbar_wait(q_full, 0, err, abort_flag);
         for (int t = 0; ok && t < nt; ++t) {
           const int st = t & 1;
@@ -180,15 +176,37 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
               mma_bf16(tmem + TM_S + 64 * st, a, bd, idesc_s, (c | k) != 0);
             }
           mma_commit(&s_full[st]);
-          if (t >= 1) ok = mma2(t - 1);
         }
-        if (ok) mma2(nt - 1);
         // All issued MMAs must finish before tensor memory is released.
-        mma_commit(mma_idle);
+        mma_commit(&mma_idle[0]);
         volatile int no_abort = 0;
-        mbar_wait(mma_idle, 0, err, &no_abort);
+        mbar_wait(&mma_idle[0], 0, err, &no_abort);
       }
-    } else {
+    } else if (warp == 6) {
+      // ---------------------------------------------------------------- MMA2 issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_o = idesc_bf16(128, 64, true, false);
+        for (int u = 0; u < nt; ++u) {
+          if (!mbar_wait(p_full, u & 1, err, abort_flag)) break;
+          fence_after();
+          const uint32_t cb = sbase + OFF_C + (u & 1) * DA_TILE_BYTES;
+#pragma unroll
+          for (int d = 0; d < 4; ++d)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              // A = C^T: MN-major, 128 latent dims (2 boxes, DA_BOX apart) x 16 positions.
+              const uint64_t a = sdesc_sw128(cb + 2 * d * DA_BOX + k * 2048, DA_BOX, 1024);
+              const uint64_t bd = sdesc_sw128(cb + 8 * DA_BOX + k * 32, 16, 1024);
+              mma_bf16(tmem + TM_O + 64 * d, a, bd, idesc_o, (u > 0) || (k > 0));
+            }
+          mma_commit(o_done);
+          mma_commit(&c_empty[u & 1]);
+        }
+        mma_commit(&mma_idle[1]);
+        volatile int no_abort = 0;
+        mbar_wait(&mma_idle[1], 0, err, &no_abort);
+      }
+    } else if (warp >= 2 && warp <= 5) {
       // ---------------------------------------------------------------- softmax warps
       const int q = warp & 3;                 // tensor-memory lane quarter of this warp
       const int h = 16 * q + lane;            // head of this thread's S row (lanes 0..15)
@@ -239,6 +257,26 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
           pk[j >> 1] = *reinterpret_cast<uint32_t*>(&pr);
         }
         l += lsum;
+        // Box 8 (rotary dims) of this stage was last read by this tile's MMA1 and by MMA2 of
+        // tile u-2, both complete (the stage was refilled for tile u after the latter).
+        uint8_t* cst = smem + OFF_C + st * DA_TILE_BYTES;
+        if (own) {  // P row h: 64 bf16 = 8 chunks of 16 B, 128-byte swizzle, in box 8
+          uint8_t* prow = cst + 8 * DA_BOX + h * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) * 16)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+        if (n < DA_TILE) {  // rows past the sequence end must not reach MMA2 as NaN/Inf
+          const int chunks = (DA_TILE - n) * 8 * 8;
+          for (int e = tid; e < chunks; e += 128) {
+            const int row = n + e / 64, box = (e / 8) % 8, c16 = e % 8;
+            *reinterpret_cast<uint4*>(cst + box * DA_BOX + row * 128 + c16 * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+        // MMA2 of the previous tile must be complete before O^T may be rescaled, and every
+        // o_done phase is consumed here, in order, before this tile's MMA2 can be issued.
         if (u >= 1 && !(ok = mbar_wait(o_done, (u - 1) & 1, err, abort_flag))) break;
         if (named_bar_or(1, 128, need)) {
           fence_after();
@@ -256,22 +294,6 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
               tmem_st32(ta, o);
             }
           tmem_wait_st();
-        }
-        if (n < DA_TILE) {  // rows past the sequence end must not reach MMA2 as NaN/Inf
-          uint8_t* cst = smem + OFF_C + st * DA_TILE_BYTES;
-          const int chunks = (DA_TILE - n) * 8 * 8;
-          for (int e = tid; e < chunks; e += 128) {
-            const int row = n + e / 64, box = (e / 8) % 8, c16 = e % 8;
-            *reinterpret_cast<uint4*>(cst + box * DA_BOX + row * 128 + c16 * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-        }
-        if (own) {  // P row h: 64 bf16 = 8 chunks of 16 B, 128-byte swizzle
-          uint8_t* prow = smem + OFF_P + h * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) * 16)) =
-                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         }
         fence_proxy_async();
         fence_before();
@@ -354,8 +376,8 @@ cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bf
       !make_tmap_2d(&mc, true, cache, LAT, (uint64_t)plan.B * cap, LAT * 2, 64, 64))
     return cudaErrorInvalidValue;
   decode_attn_tc_kernel<<<plan.items, DA_THREADS, DA_SMEM, st>>>(
-      mq, mc, seq_lens, plan.B, cap, plan.chunk, scale * 1.4426950408889634f, o_part, ml_part,
-      err);
+      mq, mc, cache, seq_lens, plan.B, cap, plan.chunk, scale * 1.4426950408889634f, o_part,
+      ml_part, err);
   return cudaGetLastError();
 }
 
