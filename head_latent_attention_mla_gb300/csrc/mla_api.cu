@@ -11,24 +11,6 @@
 
 using namespace mla;
 
-struct mla_ctx {
-  mla_config cfg;
-  int device = 0;
-  int num_sms = 0;
-  const uint8_t* W[5] = {};
-  const float* S[5] = {};
-  const __nv_bfloat16* gain[2] = {};
-  float2* rope_tab = nullptr;  // [max_positions][32] (cos, sin)
-  int* d_err = nullptr;
-  // Launch log of the most recent token call (names, and device timings when profiling).
-  static constexpr int kMaxLaunch = 32;
-  bool profiling = false;
-  bool last_profiled = false;
-  int n_launch = 0;
-  const char* names[kMaxLaunch] = {};
-  cudaEvent_t ev[2 * kMaxLaunch] = {};
-};
-
 namespace {
 
 const int kRows[5] = {Q_LORA, QB_N, KVA_N, KVB_N, HIDDEN};

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/mla.h"
+
 namespace mla {
 
 // Kimi-K2 MLA dimensions (config.json on the "KV cache" page).
@@ -116,3 +118,22 @@ cudaError_t launch_dequant(const uint8_t* W, const float* S, int rows, int cols,
                            cudaStream_t st);
 
 }  // namespace mla
+
+// Host-side state of one context (the opaque mla_ctx of the C ABI).
+struct mla_ctx {
+  mla_config cfg;
+  int device = 0;
+  int num_sms = 0;
+  const uint8_t* W[5] = {};
+  const float* S[5] = {};
+  const __nv_bfloat16* gain[2] = {};
+  float2* rope_tab = nullptr;  // [max_positions][32] (cos, sin)
+  int* d_err = nullptr;
+  // Launch log of the most recent token call (names, and device timings when profiling).
+  static constexpr int kMaxLaunch = 32;
+  bool profiling = false;
+  bool last_profiled = false;
+  int n_launch = 0;
+  const char* names[kMaxLaunch] = {};
+  cudaEvent_t ev[2 * kMaxLaunch] = {};
+};

@@ -1,0 +1,154 @@
+// mla_decode_noalloc: one decode step, like mla_decode, for callers that cannot allocate GPU
+// memory.
+//
+// Some hosts of this library cannot call cudaMalloc, or any allocator, at the point where a
+// decode step runs: a serving loop that owns all device memory through a fixed arena, an
+// embedding runtime that forbids driver allocations after start-up, or a caller running
+// under a memory budget that must not move.  mla_decode asks them for a workspace; this entry
+// point needs none.  Its scratch (every intermediate of the step and the split-KV partial
+// outputs of the attention) lives in one file-scope device array of kScratchBytes, which
+// every GPU that loads the library holds until the process exits.
+//
+// Limits and rules (also stated in include/mla.h):
+//   * at most kMaxBatch sequences per call; the attention uses at most kMaxItems split work
+//     items, so long sequences get longer splits than mla_decode would give them;
+//   * every call shares the one array: calls whose work overlaps on the GPU (two streams, two
+//     threads, two contexts on one device) race with each other;
+//   * the array keeps the last call's contents; this path writes every scratch byte it reads
+//     before reading it, so nothing needs clearing between calls;
+//   * the first call on a device looks up the array's device address on that device (with
+//     that device current); make that first call before any stream capture.
+#include <mutex>
+
+#include "mla_internal.h"
+
+using namespace mla;
+
+namespace {
+
+constexpr int kMaxBatch = 8;
+constexpr int kMaxItems = 48;
+constexpr size_t kScratchBytes = size_t(8) << 20;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
+
+constexpr size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Regions {
+  size_t g1, cq, q, qfull, opart, ml, olat, attn, total;
+};
+
+constexpr Regions regions(int B) {
+  Regions r{};
+  size_t off = 0;
+  r.g1 = off;    off += up256((size_t)B * G1_N * 4);
+  r.cq = off;    off += up256((size_t)B * Q_LORA * 2);
+  r.q = off;     off += up256((size_t)B * QB_N * 2);
+  r.qfull = off; off += up256((size_t)B * HEADS * LAT * 2);
+  r.opart = off; off += up256((size_t)kMaxItems * HEADS * KV_LORA * 4);
+  r.ml = off;    off += up256((size_t)kMaxItems * HEADS * 2 * 4);
+  r.olat = off;  off += up256((size_t)B * HEADS * KV_LORA * 2);
+  r.attn = off;  off += up256((size_t)B * O_IN * 2);
+  r.total = off;
+  return r;
+}
+static_assert(regions(kMaxBatch).total <= kScratchBytes, "scratch too small for kMaxBatch");
+
+// Host code only knows a stand-in for g_decode_scratch; its device address is looked up once
+// per device, with that device current.
+std::mutex g_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" mla_status mla_decode_noalloc(mla_ctx* c, const void* x, int B, void* cache, int cap,
+                                         int* lens_dev, const int* lens_host, void* out,
+                                         void* stream) {
+  if (!c || B < 0 || cap < 0) return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (B > kMaxBatch) return MLA_ERR_CAPACITY;  // beyond the static scratch
+  if (!x || !cache || !lens_dev || !lens_host || !out || out == x) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(cache) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+  for (int i = 0; i < 5; ++i)
+    if (!c->W[i] || !c->S[i]) return MLA_ERR_STATE;
+  if (!c->gain[0] || !c->gain[1]) return MLA_ERR_STATE;
+  long total = 0;
+  for (int b = 0; b < B; ++b) {
+    if (lens_host[b] < 0) return MLA_ERR_INVALID_ARG;
+    if ((long)lens_host[b] + 1 > cap || (long)lens_host[b] + 1 > c->cfg.max_positions)
+      return MLA_ERR_CAPACITY;
+    total += (long)lens_host[b] + 1;
+  }
+  // Split-KV schedule bounded by kMaxItems: with chunk >= total / (kMaxItems - B), the sum of
+  // ceil(S_b / chunk) is at most kMaxItems.
+  long chunk = (total + (kMaxItems - B) - 1) / (kMaxItems - B);
+  chunk = ((chunk + 63) / 64) * 64;
+  if (chunk < 64) chunk = 64;
+  long items = 0;
+  for (int b = 0; b < B; ++b) items += ((long)lens_host[b] + 1 + chunk - 1) / chunk;
+  if (items > kMaxItems) return MLA_ERR_STATE;
+
+  void* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return MLA_ERR_CUDA;
+  const Regions R = regions(B);
+  char* w = static_cast<char*>(scratch);
+  float* g1 = reinterpret_cast<float*>(w + R.g1);
+  __nv_bfloat16* cq = reinterpret_cast<__nv_bfloat16*>(w + R.cq);
+  __nv_bfloat16* q = reinterpret_cast<__nv_bfloat16*>(w + R.q);
+  __nv_bfloat16* qfull = reinterpret_cast<__nv_bfloat16*>(w + R.qfull);
+  float* opart = reinterpret_cast<float*>(w + R.opart);
+  float* ml = reinterpret_cast<float*>(w + R.ml);
+  __nv_bfloat16* olat = reinterpret_cast<__nv_bfloat16*>(w + R.olat);
+  __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(w + R.attn);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  c->n_launch = 0;  // this call keeps no launch log
+  c->last_profiled = false;
+  const int limit = cap < c->cfg.max_positions ? cap : c->cfg.max_positions;
+  const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(x);
+  __nv_bfloat16* C = static_cast<__nv_bfloat16*>(cache);
+  const DecodePlan plan{B, (int)chunk, (int)items};
+
+#define NA_RUN(expr)                              \
+  do {                                            \
+    if ((expr) != cudaSuccess) return MLA_ERR_CUDA; \
+  } while (0)
+  Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
+                {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
+  NA_RUN(launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, s));
+  NA_RUN(launch_norm_rope_cache(g1, B, 1, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
+                                c->cfg.rope_pairing, lens_dev, C, cap, limit, cq, nullptr,
+                                c->d_err, s));
+  Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
+  NA_RUN(launch_gemm(cq, Q_LORA, B, Q_LORA, &p2, 1, s));
+  NA_RUN(launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
+                         c->cfg.rope_pairing, lens_dev, limit, qfull, s));
+  NA_RUN(launch_decode_attention_tc(qfull, C, cap, lens_dev, plan, c->cfg.softmax_scale, opart,
+                                    ml, c->d_err, s));
+  NA_RUN(launch_decode_combine(lens_dev, plan, opart, ml, olat, c->d_err, s));
+  NA_RUN(launch_absorb_out(olat, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], attn, s));
+  Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
+  NA_RUN(launch_gemm(attn, O_IN, B, O_IN, &p4, 1, s));
+  NA_RUN(launch_advance_lens(lens_dev, B, 1, s));
+#undef NA_RUN
+  return MLA_OK;
+}

@@ -47,6 +47,7 @@ _SIGS = {
     "mla_dequant_weight": (_I, [_P, _I, _P, _P]),
     "mla_get_device_status": (_I, [_P, _P]),
     "mla_status_string": (ctypes.c_char_p, [_I]),
+    "mla_decode_noalloc": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _P]),
     "mla_set_profiling": (_I, [_P, _I]),
     "mla_last_launches": (_I, [_P, _I, ctypes.POINTER(ctypes.c_char_p),
                                ctypes.POINTER(ctypes.c_float)]),
@@ -154,6 +155,14 @@ def mla_decode(ctx, x, cache, seq_lens_dev, seq_lens_host, out, ws, stream=None)
     _check(load().mla_decode(ctx, _ptr(x), B, _ptr(cache), cache.shape[1], _ptr(seq_lens_dev),
                              _host_i32(seq_lens_host), _ptr(out), _ptr(ws),
                              ws.numel() * ws.element_size(), _stream(stream)), "mla_decode")
+
+
+def mla_decode_noalloc(ctx, x, cache, seq_lens_dev, seq_lens_host, out, stream=None) -> None:
+    """mla_decode without a workspace: scratch comes from a static array in the library."""
+    B = x.shape[0]
+    _check(load().mla_decode_noalloc(ctx, _ptr(x), B, _ptr(cache), cache.shape[1],
+                                     _ptr(seq_lens_dev), _host_i32(seq_lens_host), _ptr(out),
+                                     _stream(stream)), "mla_decode_noalloc")
 
 
 def mla_dequant_weight(ctx: int, which: int, out: torch.Tensor, stream=None) -> None:

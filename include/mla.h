@@ -131,6 +131,23 @@ mla_status mla_decode(mla_ctx* ctx, const void* x_bf16, int B, void* cache_bf16,
                       int* seq_lens_dev, const int* seq_lens_host, void* out_bf16, void* ws,
                       size_t ws_bytes, void* stream);
 
+/* mla_decode for callers that cannot allocate device memory when they decode (an arena that
+ * owns all GPU memory, a runtime that forbids allocation after start-up): the same step and
+ * the same arguments as mla_decode without the workspace.  The paper has no counterpart; this
+ * is a deployment convenience.  Its scratch is one static 8 MiB device array inside the
+ * library, held by every GPU that loads it until the process exits.
+ *   - B must be at most 8 (else MLA_ERR_CAPACITY); the split-KV attention uses at most 48
+ *     work items, so long contexts run with fewer, longer splits than mla_decode's.
+ *   - Every call shares the array: calls that overlap on the GPU race and must be serialised
+ *     by the caller (one stream, one host thread).  The array keeps the last call's
+ *     contents; nothing in it needs clearing, since every byte read is written first.
+ *   - The first call on a device looks up the array's address on that device (the device
+ *     must be current); make that first call before capturing a stream.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
+mla_status mla_decode_noalloc(mla_ctx* ctx, const void* x_bf16, int B, void* cache_bf16, int cap,
+                              int* seq_lens_dev, const int* seq_lens_host, void* out_bf16,
+                              void* stream);
+
 /* Verification helper: writes the float32 dequantisation of a registered weight,
  * out[o][i] = float(e4m3(q[o][i])) * s[o/128][i/128] (one rounded multiply), to the
  * caller's device buffer of rows*cols floats. */
