@@ -1,5 +1,5 @@
-// FP8 block-scaled projections on the CUDA cores: a weight-streaming GEMV for a few tokens
-// and a tiled fallback for larger token counts.
+// FP8 block-scaled projections for a few tokens: a weight-streaming GEMV on the CUDA cores
+// (larger token counts go to the tensor-core kernel in k_gemm_tc.cu).
 //
 // Y[m, n] = sum_k X[m, k] * e4m3(W[n, k]) * S[n/128][k/128]  ("linear" excerpt of the
 // "Key-value latent" page: fmt e4m3, weight_block_size [128, 128]; nn.Linear without bias).
@@ -115,82 +115,10 @@ cudaError_t launch_gemv(const __nv_bfloat16* X, int ldx, int K, const ProjSet& p
   return cudaGetLastError();
 }
 
-// Tiled fallback: 64 (m) x 64 (n) per CTA, 4x4 outputs per thread, k steps of 32.
-// n tiles never straddle a 128-row scale block because 64 divides 128.
-__global__ void __launch_bounds__(256) gemm_f8w_tiled_kernel(const __nv_bfloat16* __restrict__ X,
-                                                             int ldx, int M, int K, ProjSet ps) {
-  __shared__ float As[32][64 + 4];
-  __shared__ float Bs[32][64 + 4];
-  const int tiles0 = ps.p[0].N / 64;
-  int nt = blockIdx.x;
-  const Proj& P = (nt < tiles0) ? ps.p[0] : ps.p[1];
-  if (nt >= tiles0) nt -= tiles0;
-  const int n0 = nt * 64, m0 = blockIdx.y * 64;
-  const int tid = threadIdx.x, tm = tid >> 4, tn = tid & 15;
-  const float* srow = P.S + (size_t)(n0 / BLK) * (K / BLK);
-
-  float acc[4][4] = {}, blk[4][4] = {};
-  for (int k0 = 0; k0 < K; k0 += 32) {
-    {  // X tile: 64 rows x 32 k, 8 bf16 per thread
-      const int r = tid >> 2, c = (tid & 3) * 8;
-      float xf[8];
-      if (m0 + r < M) {
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(X + (size_t)(m0 + r) * ldx + k0 + c), xf);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) xf[i] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) As[c + i][r] = xf[i];
-    }
-    {  // W tile: 64 rows x 32 k, 8 e4m3 per thread
-      const int r = tid >> 2, c = (tid & 3) * 8;
-      const uint2 wv = *reinterpret_cast<const uint2*>(P.W + (size_t)(n0 + r) * K + k0 + c);
-      float wf[8];
-      e4m3x4_to_f32(wv.x, wf);
-      e4m3x4_to_f32(wv.y, wf + 4);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) Bs[c + i][r] = wf[i];
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < 32; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) { a[i] = As[kk][tm * 4 + i]; b[i] = Bs[kk][tn * 4 + i]; }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) blk[i][j] = fmaf(a[i], b[j], blk[i][j]);
-    }
-    __syncthreads();
-    if (((k0 + 32) % BLK) == 0) {
-      const float sc = srow[k0 / BLK];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) { acc[i][j] = fmaf(sc, blk[i][j], acc[i][j]); blk[i][j] = 0.f; }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + tm * 4 + i;
-    if (m >= M) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tn * 4 + j;
-      if (P.y_fp32)
-        reinterpret_cast<float*>(P.Y)[(size_t)m * P.ldy + n] = acc[i][j];
-      else
-        reinterpret_cast<__nv_bfloat16*>(P.Y)[(size_t)m * P.ldy + n] = __float2bfloat16_rn(acc[i][j]);
-    }
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
-                        cudaStream_t st) {
+                        float* partial, int num_sms, int* err, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
   ProjSet ps{};
   ps.np = np;
@@ -209,11 +137,8 @@ cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Pro
       case 7: return launch_gemv<7>(X, ldx, K, ps, rows, st);
       default: return launch_gemv<8>(X, ldx, K, ps, rows, st);
     }
-  } else {
-    const dim3 grid(rows / 64, (M + 63) / 64), block(256);
-    gemm_f8w_tiled_kernel<<<grid, block, 0, st>>>(X, ldx, M, K, ps);
   }
-  return cudaGetLastError();
+  return launch_gemm_tc(X, ldx, M, K, p, np, partial, num_sms, err, st);
 }
 
 }  // namespace mla

@@ -317,7 +317,8 @@ cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* 
 
 cudaError_t init_kernels() {
   cudaError_t e = init_attention_kernels();
-  return e != cudaSuccess ? e : init_decode_tc_kernel();
+  if (e == cudaSuccess) e = init_decode_tc_kernel();
+  return e != cudaSuccess ? e : init_gemm_tc_kernels();
 }
 
 cudaError_t launch_advance_lens(int* seq_lens, int B, int T, cudaStream_t st) {

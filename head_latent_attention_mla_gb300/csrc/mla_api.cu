@@ -29,12 +29,23 @@ bool ready(const mla_ctx* c) {
 // Workspace regions (byte offsets into the caller's buffer).
 struct Layout {
   size_t g1 = 0, cq = 0, ckv = 0, q = 0, kv = 0, attn = 0, qfull = 0, opart = 0, ml = 0,
-         olat = 0, total = 0;
+         olat = 0, gpart = 0, total = 0;
 };
+
+// Largest split-K partial buffer of the projections of one call with M token rows.
+size_t gemm_partials(long M, int num_sms) {
+  const int m = (int)M;
+  size_t b = gemm_partial_bytes(m, Q_LORA + KVA_N, HIDDEN, num_sms);
+  const size_t o[3] = {gemm_partial_bytes(m, QB_N, Q_LORA, num_sms),
+                       gemm_partial_bytes(m, KVB_N, KV_LORA, num_sms),
+                       gemm_partial_bytes(m, HIDDEN, O_IN, num_sms)};
+  for (size_t v : o) b = v > b ? v : b;
+  return b;
+}
 
 int items_max(const mla_ctx* c, int B) { return 2 * c->num_sms + B; }
 
-Layout prefill_layout(long M) {
+Layout prefill_layout(long M, int num_sms) {
   Layout L;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off += up256(bytes); return o; };
@@ -44,6 +55,7 @@ Layout prefill_layout(long M) {
   L.q = take((size_t)M * QB_N * 2);
   L.kv = take((size_t)M * KVB_N * 2);
   L.attn = take((size_t)M * O_IN * 2);
+  L.gpart = take(gemm_partials(M, num_sms));
   L.total = off;
   return L;
 }
@@ -61,6 +73,7 @@ Layout decode_layout(const mla_ctx* c, int B) {
   L.ml = take(items * HEADS * 2 * 4);
   L.olat = take((size_t)B * HEADS * KV_LORA * 2);
   L.attn = take((size_t)B * O_IN * 2);
+  L.gpart = take(gemm_partials(B, c->num_sms));
   L.total = off;
   return L;
 }
@@ -231,7 +244,7 @@ mla_status mla_upload_norm(mla_ctx* c, int which, const void* g, int n) {
 
 size_t mla_workspace_bytes(const mla_ctx* c, int B, int T) {
   if (!c || B < 0 || T < 0) return 0;
-  const size_t p = prefill_layout((long)B * T).total;
+  const size_t p = prefill_layout((long)B * T, c ? c->num_sms : 0).total;
   const size_t d = decode_layout(c, B).total;
   return p > d ? p : d;
 }
@@ -239,7 +252,7 @@ size_t mla_workspace_bytes(const mla_ctx* c, int B, int T) {
 mla_status mla_cache_append(mla_ctx* c, const void* x, int B, int T, void* cache, int cap,
                             int* lens_dev, const int* lens_host, void* ws, size_t ws_bytes,
                             void* stream) {
-  const Layout L = prefill_layout((long)B * T);
+  const Layout L = prefill_layout((long)B * T, c ? c->num_sms : 0);
   mla_status st = check_tokens(c, x, B, T, cache, cap, lens_dev, lens_host, ws, ws_bytes, L.total);
   if (st != MLA_OK || B == 0 || T == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -247,7 +260,7 @@ mla_status mla_cache_append(mla_ctx* c, const void* x, int B, int T, void* cache
   const int M = B * T, limit = cap < c->cfg.max_positions ? cap : c->cfg.max_positions;
   float* g1 = at<float>(ws, L.g1);
   Proj p{c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1};
-  MLA_LAUNCH("gemm_kv_a", launch_gemm(static_cast<const __nv_bfloat16*>(x), HIDDEN, M, HIDDEN, &p, 1, s));
+  MLA_LAUNCH("gemm_kv_a", launch_gemm(static_cast<const __nv_bfloat16*>(x), HIDDEN, M, HIDDEN, &p, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
   MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
                                     c->cfg.rope_pairing, lens_dev,
                                     static_cast<__nv_bfloat16*>(cache), cap, limit, nullptr,
@@ -259,7 +272,7 @@ mla_status mla_cache_append(mla_ctx* c, const void* x, int B, int T, void* cache
 mla_status mla_prefill(mla_ctx* c, const void* x, int B, int T, void* cache, int cap,
                        int* lens_dev, const int* lens_host, void* out, void* ws,
                        size_t ws_bytes, void* stream) {
-  const Layout L = prefill_layout((long)B * T);
+  const Layout L = prefill_layout((long)B * T, c ? c->num_sms : 0);
   mla_status st = check_tokens(c, x, B, T, cache, cap, lens_dev, lens_host, ws, ws_bytes, L.total);
   if (st != MLA_OK || B == 0 || T == 0) return st;
   if (!out || !aligned16(out) || out == x) return MLA_ERR_INVALID_ARG;
@@ -279,18 +292,18 @@ mla_status mla_prefill(mla_ctx* c, const void* x, int B, int T, void* cache, int
 
   Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
                 {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
-  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, M, HIDDEN, p1, 2, s));
+  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, M, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
   MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
                                     c->cfg.rope_pairing, lens_dev, C, cap, limit, cq, ckv,
                                     c->d_err, s));
   Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
-  MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, s));
+  MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
   MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
   Proj p3{c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], KVB_N, kv, KVB_N, 0};
-  MLA_LAUNCH("gemm_kv_b", launch_gemm(ckv, KV_LORA, M, KV_LORA, &p3, 1, s));
+  MLA_LAUNCH("gemm_kv_b", launch_gemm(ckv, KV_LORA, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
   MLA_LAUNCH("prefill_attention", launch_prefill_attention(q, kv, C, cap, B, T, c->cfg.softmax_scale, attn, s));
   Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
-  MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, s));
+  MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
   MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, T, s));
   return MLA_OK;
 }
@@ -331,12 +344,12 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
 
   Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
                 {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
-  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, s));
+  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
   MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, 1, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
                                     c->cfg.rope_pairing, lens_dev, C, cap, limit, cq, nullptr,
                                     c->d_err, s));
   Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
-  MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, B, Q_LORA, &p2, 1, s));
+  MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, B, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
   MLA_LAUNCH("absorb_q", launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
                              c->cfg.rope_pairing, lens_dev, limit, qfull, s));
   MLA_LAUNCH("decode_attention", launch_decode_attention_tc(qfull, C, cap, lens_dev, plan,
@@ -345,7 +358,7 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
   MLA_LAUNCH("decode_combine", launch_decode_combine(lens_dev, plan, opart, ml, olat, c->d_err, s));
   MLA_LAUNCH("absorb_out", launch_absorb_out(olat, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], attn, s));
   Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
-  MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, s));
+  MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
   MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, 1, s));
   return MLA_OK;
 }

@@ -47,9 +47,15 @@ struct Proj {
 
 // ---- launchers (each returns the launch's cudaError_t) ----------------------------------
 
-// Y = X W^T for up to two projections sharing X [M, K] (row stride ldx elements).
+// Y = X W^T for up to two projections sharing X [M, K] (row stride ldx elements).  M <= 8
+// streams the weights through the CUDA cores; larger M runs on the tensor cores, split over K
+// when the grid would be small, with fp32 partials in `partial` (gemm_partial_bytes bytes).
 cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
-                        cudaStream_t st);
+                        float* partial, int num_sms, int* err, cudaStream_t st);
+cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
+                           float* partial, int num_sms, int* err, cudaStream_t st);
+size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms);
+cudaError_t init_gemm_tc_kernels();
 
 // RMSNorm of the q latent and kv latent, RoPE of k_pe, cache row store.  Positions at or
 // past `limit` (min of cache capacity and RoPE table rows) are skipped and flagged in *err.
