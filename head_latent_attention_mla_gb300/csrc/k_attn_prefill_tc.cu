@@ -1,0 +1,348 @@
+// Causal prefill attention on the tcgen05 tensor cores.
+//
+// `mla-prefill` excerpt ("Key content up-projection" page): per head, q = [q_nope | RoPE(q_pe)]
+// (192), k = [k_nope | RoPE(k_pe)] with the rotary key shared by all heads, scores q.k times the
+// softmax scale, key s visible from query t iff s <= t, fp32 softmax over keys, o = P v (128).
+// The head dimensions stay 192 / 128 (no padding of v to 192).
+//
+// One CTA per (128-query tile, head, sequence), 7 warps:
+//   warp 0      TMA producer: the query tile once (3 boxes of 64 columns), then for every
+//               128-key tile k_nope (2 boxes), the rotary key from the cache rows (1 box) and
+//               v (2 boxes) into a two-stage ring (128-byte swizzle, 3-D maps over
+//               [tokens, heads, dims]);
+//   warp 1      allocates tensor memory and issues MMA1  S = Q K^T  (M=128, N=128, K=192);
+//   warp 6      issues MMA2  O += P V  (M=128, N=128, K=128) with P read from tensor memory
+//               and v read MN-major;
+//   warps 2..5  softmax, one query row per thread: causal mask on the diagonal tile, online
+//               softmax in base 2 with a lazy rescale of O (only when the running maximum
+//               grows by more than 2^8), P written to tensor memory as packed bf16; then the
+//               epilogue normalises O and stores it as bf16.
+// Tensor memory: O in columns [0,128), S in [128,256) and [256,384), P in [384,448) and
+// [448,512).
+#include "tc_common.cuh"
+
+namespace mla {
+
+namespace {
+
+using namespace tc;
+
+constexpr int PA_TILE = 128;
+constexpr int PA_BOX = 128 * 128;                 // [128 rows x 64 bf16] box, bytes
+constexpr int PA_Q_BYTES = 3 * PA_BOX;            // q tile: 192 columns
+constexpr int PA_K_BYTES = 3 * PA_BOX;            // k tile: 128 nope + 64 rotary
+constexpr int PA_V_BYTES = 2 * PA_BOX;            // v tile: 128 columns
+constexpr int PA_STAGE = PA_K_BYTES + PA_V_BYTES;
+constexpr int PA_THREADS = 224;
+constexpr int OFF_Q = 0;
+constexpr int OFF_KV = OFF_Q + PA_Q_BYTES;
+constexpr int OFF_BAR = OFF_KV + 2 * PA_STAGE;
+constexpr int OFF_MISC = OFF_BAR + 16 * 8;
+constexpr int OFF_ALPHA_FLAG = OFF_MISC + 16;
+constexpr int PA_SMEM = OFF_ALPHA_FLAG + 16 + 1024;
+constexpr uint32_t TM_O = 0, TM_S = 128, TM_P = 384;
+constexpr float RESCALE_LOG2 = 8.f;
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// D (+)= A * B^T with A read from tensor memory (kind::f16, bf16 operands).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
+    const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
+    const __grid_constant__ CUtensorMap map_c, int T, int cap, float scale_log2,
+    __nv_bfloat16* __restrict__ attn_out, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;   // [2]
+  uint64_t* kv_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;    // [2]
+  uint64_t* s_free = bars + 7;    // [2]
+  uint64_t* p_full = bars + 9;
+  uint64_t* o_done = bars + 10;
+  uint64_t* mma_idle = bars + 11; // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nq = (T + PA_TILE - 1) / PA_TILE;
+  const int qt = nq - 1 - (int)blockIdx.x;        // heaviest (latest) query tiles first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int q0 = qt * PA_TILE;
+  const int nt = qt + 1;                           // key tiles 0..qt (causal)
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+      mbar_init(&mma_idle[i], 1);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(o_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int tok0 = b * T;
+
+  if (warp == 0) {
+    // -------------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_kv);
+      tma_prefetch_desc(&map_c);
+      mbar_expect_tx(q_full, PA_Q_BYTES);
+      for (int c = 0; c < 3; ++c)
+        tma_load_3d(smem + OFF_Q + c * PA_BOX, &map_q, q_full, 64 * c, h, tok0 + q0);
+      int issued = 0;
+      for (int j = 0; j < nt; ++j) {
+        const int st = j & 1;
+        if (j >= 2 && !mbar_wait(&kv_empty[st], ((j - 2) >> 1) & 1, err, abort_flag)) break;
+        uint8_t* stg = smem + OFF_KV + st * PA_STAGE;
+        mbar_expect_tx(&kv_full[st], PA_STAGE);
+        const int k0 = j * PA_TILE;
+        tma_load_3d(stg, &map_kv, &kv_full[st], 0, h, tok0 + k0);
+        tma_load_3d(stg + PA_BOX, &map_kv, &kv_full[st], 64, h, tok0 + k0);
+        tma_load_2d(stg + 2 * PA_BOX, &map_c, &kv_full[st], KV_LORA, b * cap + k0);
+        tma_load_3d(stg + PA_K_BYTES, &map_kv, &kv_full[st], 128, h, tok0 + k0);
+        tma_load_3d(stg + PA_K_BYTES + PA_BOX, &map_kv, &kv_full[st], 192, h, tok0 + k0);
+        issued = j + 1;
+      }
+      volatile int no_abort = 0;
+      mbar_wait(q_full, 0, err, &no_abort);
+      for (int j = max(0, issued - 2); j < issued; ++j)
+        mbar_wait(&kv_full[j & 1], (j >> 1) & 1, err, &no_abort);
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------------- MMA1 issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
+      bool ok = mbar_wait(q_full, 0, err, abort_flag);
+      for (int j = 0; ok && j < nt; ++j) {
+        const int st = j & 1;
+        ok = mbar_wait(&kv_full[st], (j >> 1) & 1, err, abort_flag);
+        if (ok && j >= 2) ok = mbar_wait(&s_free[st], ((j - 2) >> 1) & 1, err, abort_flag);
+        if (!ok) break;
+        fence_after();
+        const uint32_t kb = sbase + OFF_KV + st * PA_STAGE;
+#pragma unroll
+        for (int ks = 0; ks < 12; ++ks) {
+          const uint64_t a = sdesc_sw128(sbase + OFF_Q + (ks >> 2) * PA_BOX + (ks & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(kb + (ks >> 2) * PA_BOX + (ks & 3) * 32, 16, 1024);
+          mma_bf16(tmem + TM_S + 128 * st, a, bd, idesc, ks > 0);
+        }
+        mma_commit(&s_full[st]);
+      }
+      mma_commit(&mma_idle[0]);
+      volatile int no_abort = 0;
+      mbar_wait(&mma_idle[0], 0, err, &no_abort);
+    }
+  } else if (warp == 6) {
+    // -------------------------------------------------------------------- MMA2 issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(128, 128, false, true);
+      for (int j = 0; j < nt; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(p_full, j & 1, err, abort_flag)) break;
+        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, err, abort_flag)) break;
+        fence_after();
+        const uint32_t vb = sbase + OFF_KV + st * PA_STAGE + PA_K_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          // B = v: MN-major, 128 value dims (2 boxes, PA_BOX apart) x 16 keys.
+          const uint64_t bd = sdesc_sw128(vb + ks * 2048, PA_BOX, 1024);
+          mma_bf16_ts(tmem + TM_O, tmem + TM_P + 64 * st + 8 * ks, bd, idesc, (j > 0) || (ks > 0));
+        }
+        mma_commit(o_done);
+        mma_commit(&kv_empty[st]);
+      }
+      mma_commit(&mma_idle[1]);
+      volatile int no_abort = 0;
+      mbar_wait(&mma_idle[1], 0, err, &no_abort);
+    }
+  } else if (warp >= 2 && warp <= 5) {
+    // -------------------------------------------------------------------- softmax warps
+    const int qw = warp & 3;
+    const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
+    const int qi = q0 + 32 * qw + lane;           // query position of this thread's row
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      const int st = j & 1;
+      if (!(ok = mbar_wait(&s_full[st], (j >> 1) & 1, err, abort_flag))) break;
+      fence_after();
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + TM_S + 128 * st + 32 * c, r[c]);
+      tmem_wait_ld();
+      fence_before();
+      mbar_arrive(&s_free[st]);
+      const int kbase = j * PA_TILE;
+      const int vis = min(qi - kbase + 1, T - kbase);   // keys [kbase, kbase+vis) visible
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float s = (c < vis) ? __uint_as_float(r[c >> 5][c & 31]) * scale_log2 : -INFINITY;
+        r[c >> 5][c & 31] = __float_as_uint(s);
+        tmax = fmaxf(tmax, s);
+      }
+      float alpha = 1.f;
+      bool need = false;
+      if (tmax > m + RESCALE_LOG2) {
+        if (m != -INFINITY) {
+          alpha = exp2f(m - tmax);
+          need = true;
+        }
+        l *= alpha;
+        m = tmax;
+      }
+      const float mu = (m == -INFINITY) ? 0.f : m;   // rows past T see no key at all
+      uint32_t pk[64];
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const float a = exp2f(__uint_as_float(r[c >> 5][c & 31]) - mu);
+        const float d = exp2f(__uint_as_float(r[(c + 1) >> 5][(c + 1) & 31]) - mu);
+        __nv_bfloat162 pr = __floats2bfloat162_rn(a, d);
+        lsum += __low2float(pr) + __high2float(pr);
+        pk[c >> 1] = *reinterpret_cast<uint32_t*>(&pr);
+      }
+      l += lsum;
+      // MMA2 of the previous tile must be done before P is overwritten or O rescaled; every
+      // o_done phase is consumed here, in order, before this tile's MMA2 is issued.
+      if (j >= 1 && !(ok = mbar_wait(o_done, (j - 1) & 1, err, abort_flag))) break;
+      if (named_bar_or(1, 128, need)) {
+        fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + TM_O + 32 * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tmem + lane_off + TM_O + 32 * c, o);
+        }
+      }
+      {
+        uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
+        uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
+        tmem_st32(tmem + lane_off + TM_P + 64 * st, p0);
+        tmem_st32(tmem + lane_off + TM_P + 64 * st + 32, p1);
+      }
+      tmem_wait_st();
+      fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && mbar_wait(o_done, (nt - 1) & 1, err, abort_flag)) {
+      fence_after();
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      __nv_bfloat16* dst = attn_out + (size_t)(tok0 + qi) * O_IN + h * VDIM;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + TM_O + 32 * c, o);
+        tmem_wait_ld();
+        if (qi < T) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 v;
+            uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(o[i + 2 * e]) * inv,
+                                                        __uint_as_float(o[i + 2 * e + 1]) * inv);
+              u[e] = *reinterpret_cast<uint32_t*>(&pr);
+            }
+            *reinterpret_cast<uint4*>(dst + 32 * c + i) = v;
+          }
+        }
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+bool make_tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                  uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool make_tmap_2d(CUtensorMap* m, bool bf16, const void* base, uint64_t cols, uint64_t rows,
+                  uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows);
+
+cudaError_t init_prefill_tc_kernel() {
+  return cudaFuncSetAttribute(prefill_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              PA_SMEM);
+}
+
+cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloat16* kv,
+                                        const __nv_bfloat16* cache, int cap, int B, int T,
+                                        float scale, __nv_bfloat16* attn_out, int* err,
+                                        cudaStream_t st) {
+  if (B * T == 0) return cudaSuccess;
+  const uint64_t M = (uint64_t)B * T;
+  CUtensorMap mq, mkv, mc;
+  if (!make_tmap_3d(&mq, q, QHEAD, HEADS, M, QHEAD * 2, (uint64_t)HEADS * QHEAD * 2, 64, 1, 128) ||
+      !make_tmap_3d(&mkv, kv, KVB_PER_HEAD, HEADS, M, KVB_PER_HEAD * 2,
+                    (uint64_t)HEADS * KVB_PER_HEAD * 2, 64, 1, 128) ||
+      !make_tmap_2d(&mc, true, cache, LAT, (uint64_t)B * cap, LAT * 2, 64, 128))
+    return cudaErrorInvalidValue;
+  const dim3 grid((T + PA_TILE - 1) / PA_TILE, HEADS, B);
+  prefill_attn_tc_kernel<<<grid, PA_THREADS, PA_SMEM, st>>>(mq, mkv, mc, T, cap,
+                                                            scale * 1.4426950408889634f, attn_out,
+                                                            err);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -301,7 +301,8 @@ mla_status mla_prefill(mla_ctx* c, const void* x, int B, int T, void* cache, int
   MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
   Proj p3{c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], KVB_N, kv, KVB_N, 0};
   MLA_LAUNCH("gemm_kv_b", launch_gemm(ckv, KV_LORA, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-  MLA_LAUNCH("prefill_attention", launch_prefill_attention(q, kv, C, cap, B, T, c->cfg.softmax_scale, attn, s));
+  MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, C, cap, B, T, c->cfg.softmax_scale, attn,
+                                                            c->d_err, s));
   Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
   MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
   MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, T, s));

@@ -116,6 +116,14 @@ cudaError_t launch_prefill_attention(const __nv_bfloat16* q, const __nv_bfloat16
                                      const __nv_bfloat16* cache, int cap, int B, int T,
                                      float scale, __nv_bfloat16* attn_out, cudaStream_t st);
 
+// The same causal prefill attention on the tcgen05 tensor cores (TMA-fed, S/P/O in tensor
+// memory).
+cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloat16* kv,
+                                        const __nv_bfloat16* cache, int cap, int B, int T,
+                                        float scale, __nv_bfloat16* attn_out, int* err,
+                                        cudaStream_t st);
+cudaError_t init_prefill_tc_kernel();
+
 // seq_lens[b] += T.
 cudaError_t launch_advance_lens(int* seq_lens, int B, int T, cudaStream_t st);
 
