@@ -316,8 +316,7 @@ cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* 
 }
 
 cudaError_t init_kernels() {
-  cudaError_t e = init_attention_kernels();
-  if (e == cudaSuccess) e = init_decode_tc_kernel();
+  cudaError_t e = init_decode_tc_kernel();
   if (e == cudaSuccess) e = init_prefill_tc_kernel();
   return e != cudaSuccess ? e : init_gemm_tc_kernels();
 }

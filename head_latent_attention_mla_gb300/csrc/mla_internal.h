@@ -85,16 +85,12 @@ struct DecodePlan {
   int chunk;        // positions per work item
   int items;        // total work items (sum over b of ceil((len_b + 1) / chunk))
 };
-cudaError_t launch_decode_attention(const __nv_bfloat16* qfull, const __nv_bfloat16* cache,
-                                    int cap, const int* seq_lens, DecodePlan plan,
-                                    float scale, float* o_part, float* ml_part, int* err,
-                                    cudaStream_t st);
 cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const float* o_part,
                                   const float* ml_part, __nv_bfloat16* o_lat, int* err,
                                   cudaStream_t st);
 
-// The same attention on the tcgen05 tensor cores (TMA-fed, accumulators in tensor memory);
-// writes the same partials as launch_decode_attention.
+// Split-KV decode attention over the latent cache on the tcgen05 tensor cores (TMA-fed,
+// accumulators in tensor memory): per work item, unnormalised partial outputs and (m, l).
 cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bfloat16* cache,
                                        int cap, const int* seq_lens, DecodePlan plan,
                                        float scale, float* o_part, float* ml_part, int* err,
@@ -104,20 +100,14 @@ cudaError_t init_decode_tc_kernel();
 // One-time kernel attributes (dynamic shared memory opt-in); called by mla_create so that
 // later calls only enqueue work and can be captured into CUDA graphs.
 cudaError_t init_kernels();
-cudaError_t init_attention_kernels();
 
 // Decode output absorption: out[b, h*VDIM + v] = sum_c W_UV,h[v, c] o_lat[b, h, c].
 cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* Wkvb,
                               const float* Skvb, __nv_bfloat16* out, cudaStream_t st);
 
-// Causal prefill attention: q [M, HEADS, QHEAD] (rotated), kv [M, HEADS, 256] (k_nope | v),
-// rotated k_pe from cache rows; writes attn_out [M, HEADS*VDIM] bf16.
-cudaError_t launch_prefill_attention(const __nv_bfloat16* q, const __nv_bfloat16* kv,
-                                     const __nv_bfloat16* cache, int cap, int B, int T,
-                                     float scale, __nv_bfloat16* attn_out, cudaStream_t st);
-
-// The same causal prefill attention on the tcgen05 tensor cores (TMA-fed, S/P/O in tensor
-// memory).
+// Causal prefill attention on the tcgen05 tensor cores: q [M, HEADS, QHEAD] (rotated),
+// kv [M, HEADS, 256] (k_nope | v), rotated k_pe from the cache rows; writes attn_out
+// [M, HEADS*VDIM] bf16.
 cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloat16* kv,
                                         const __nv_bfloat16* cache, int cap, int B, int T,
                                         float scale, __nv_bfloat16* attn_out, int* err,
