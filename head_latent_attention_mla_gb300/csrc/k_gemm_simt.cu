@@ -40,19 +40,19 @@ __device__ __forceinline__ void bf16x8_to_f32(uint4 v, float* f) {
 struct ProjSet {
   Proj p[2];
   int np;
-  int rows0;  // rows of p[0]
+  int rows0;    // rows of p[0]
+  int* adv;     // optional: adv[i] += adv_by for i < adv_n, by block 0 (lengths bookkeeping)
+  int adv_n, adv_by;
 };
 
-// One warp per output row n.  Lane l owns the 16-byte chunks l, l+32, ... of the row; all of
-// them are loaded before any arithmetic so that a warp keeps the whole row (up to 8 KiB) in
-// flight.  NCH = K / 512 chunks per lane.
 template <int M, int NCH>
-__global__ void __launch_bounds__(256) gemv_f8w_kernel(const __nv_bfloat16* __restrict__ X,
+__global__ void __launch_bounds__(128) gemv_f8w_kernel(const __nv_bfloat16* __restrict__ X,
                                                        int ldx, ProjSet ps) {
   constexpr int K = NCH * 512;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int total = ps.p[0].N + (ps.np > 1 ? ps.p[1].N : 0);
+  if (ps.adv && blockIdx.x == 0 && (int)threadIdx.x < ps.adv_n) ps.adv[threadIdx.x] += ps.adv_by;
   if (warp >= total) return;
   const Proj& P = (warp < ps.rows0) ? ps.p[0] : ps.p[1];
   const int n = (warp < ps.rows0) ? warp : warp - ps.rows0;
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(256) gemv_f8w_kernel(const __nv_bfloat16* __re
 template <int M>
 cudaError_t launch_gemv(const __nv_bfloat16* X, int ldx, int K, const ProjSet& ps, int rows,
                         cudaStream_t st) {
-  const dim3 grid((rows + 7) / 8), block(256);
+  const dim3 grid((rows + 3) / 4), block(128);
   switch (K) {
     case 512: gemv_f8w_kernel<M, 1><<<grid, block, 0, st>>>(X, ldx, ps); break;
     case 1536: gemv_f8w_kernel<M, 3><<<grid, block, 0, st>>>(X, ldx, ps); break;
@@ -118,10 +118,14 @@ cudaError_t launch_gemv(const __nv_bfloat16* X, int ldx, int K, const ProjSet& p
 }  // namespace
 
 cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
-                        float* partial, int num_sms, int* err, cudaStream_t st) {
+                        float* partial, int num_sms, int* err, cudaStream_t st, int* adv,
+                        int adv_n, int adv_by) {
   if (M <= 0) return cudaSuccess;
   ProjSet ps{};
   ps.np = np;
+  ps.adv = adv;
+  ps.adv_n = adv_n;
+  ps.adv_by = adv_by;
   ps.p[0] = p[0];
   if (np > 1) ps.p[1] = p[1];
   ps.rows0 = p[0].N;
@@ -140,5 +144,7 @@ cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Pro
   }
   return launch_gemm_tc(X, ldx, M, K, p, np, partial, num_sms, err, st);
 }
+
+bool gemm_can_advance(int M) { return M > 0 && M <= 8; }
 
 }  // namespace mla

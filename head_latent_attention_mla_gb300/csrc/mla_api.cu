@@ -359,8 +359,13 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
   MLA_LAUNCH("decode_combine", launch_decode_combine(lens_dev, plan, opart, ml, olat, c->d_err, s));
   MLA_LAUNCH("absorb_out", launch_absorb_out(olat, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], attn, s));
   Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
-  MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-  MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, 1, s));
+  if (gemm_can_advance(B) && B <= 128) {  // the length update rides on the last kernel
+    MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
+                                     c->num_sms, c->d_err, s, lens_dev, B, 1));
+  } else {
+    MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+    MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, 1, s));
+  }
   return MLA_OK;
 }
 

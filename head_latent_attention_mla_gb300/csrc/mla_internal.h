@@ -50,8 +50,12 @@ struct Proj {
 // Y = X W^T for up to two projections sharing X [M, K] (row stride ldx elements).  M <= 8
 // streams the weights through the CUDA cores; larger M runs on the tensor cores, split over K
 // when the grid would be small, with fp32 partials in `partial` (gemm_partial_bytes bytes).
+// With M <= 8 (the CUDA-core path) block 0 of the launch also adds adv_by to
+// adv[0..adv_n) (the call's length bookkeeping, riding on its last kernel; adv_n <= 128).
 cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
-                        float* partial, int num_sms, int* err, cudaStream_t st);
+                        float* partial, int num_sms, int* err, cudaStream_t st,
+                        int* adv = nullptr, int adv_n = 0, int adv_by = 0);
+bool gemm_can_advance(int M);  // whether launch_gemm honours adv for this M
 cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
                            float* partial, int num_sms, int* err, cudaStream_t st);
 size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms);
