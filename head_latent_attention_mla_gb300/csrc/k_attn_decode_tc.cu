@@ -84,6 +84,8 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();  // the query and the new cache row come from earlier kernels
   if (threadIdx.x == 0) {
     int local = 0;
     const int b = find_item_tc(seq_lens, B, chunk, item, &local);
@@ -369,16 +371,15 @@ cudaError_t init_decode_tc_kernel() {
 cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bfloat16* cache,
                                        int cap, const int* seq_lens, DecodePlan plan,
                                        float scale, float* o_part, float* ml_part, int* err,
-                                       cudaStream_t st) {
+                                       cudaStream_t st, bool pdl) {
   if (plan.B == 0) return cudaSuccess;
   CUtensorMap mq, mc;
   if (!make_tmap_2d(&mq, true, qfull, LAT, (uint64_t)plan.B * HEADS, LAT * 2, 64, 64) ||
       !make_tmap_2d(&mc, true, cache, LAT, (uint64_t)plan.B * cap, LAT * 2, 64, 64))
     return cudaErrorInvalidValue;
-  decode_attn_tc_kernel<<<plan.items, DA_THREADS, DA_SMEM, st>>>(
-      mq, mc, cache, seq_lens, plan.B, cap, plan.chunk, scale * 1.4426950408889634f, o_part,
-      ml_part, err);
-  return cudaGetLastError();
+  return launch_kernel(decode_attn_tc_kernel, dim3(plan.items), dim3(DA_THREADS), DA_SMEM, st,
+                       pdl, mq, mc, cache, seq_lens, plan.B, cap, plan.chunk,
+                       scale * 1.4426950408889634f, o_part, ml_part, err);
 }
 
 }  // namespace mla

@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   __shared__ int s_first, s_n;
   __shared__ float s_w[kMaxSplits];
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ float s_red[8];
   if (tid == 0) {
     int acc = 0;
@@ -88,12 +90,10 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(
 
 cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const float* o_part,
                                   const float* ml_part, __nv_bfloat16* o_lat, int* err,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, bool pdl) {
   if (plan.B == 0) return cudaSuccess;
-  decode_combine_kernel<<<dim3(plan.B, HEADS), 128, 0, st>>>(seq_lens, plan.B, plan.chunk,
-                                                             plan.items, o_part, ml_part, o_lat,
-                                                             err);
-  return cudaGetLastError();
+  return launch_kernel(decode_combine_kernel, dim3(plan.B, HEADS), dim3(128), 0, st, pdl,
+                       seq_lens, plan.B, plan.chunk, plan.items, o_part, ml_part, o_lat, err);
 }
 
 }  // namespace mla

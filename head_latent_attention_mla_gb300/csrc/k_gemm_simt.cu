@@ -49,11 +49,17 @@ template <int M, int NCH>
 __global__ void __launch_bounds__(128) gemv_f8w_kernel(const __nv_bfloat16* __restrict__ X,
                                                        int ldx, ProjSet ps) {
   constexpr int K = NCH * 512;
+  pdl_launch_dependents();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int total = ps.p[0].N + (ps.np > 1 ? ps.p[1].N : 0);
-  if (ps.adv && blockIdx.x == 0 && (int)threadIdx.x < ps.adv_n) ps.adv[threadIdx.x] += ps.adv_by;
-  if (warp >= total) return;
+  if (warp >= total) {
+    if (ps.adv && blockIdx.x == 0 && (int)threadIdx.x < ps.adv_n) {
+      pdl_wait();
+      ps.adv[threadIdx.x] += ps.adv_by;
+    }
+    return;
+  }
   const Proj& P = (warp < ps.rows0) ? ps.p[0] : ps.p[1];
   const int n = (warp < ps.rows0) ? warp : warp - ps.rows0;
   const uint8_t* wrow = P.W + (size_t)n * K;
@@ -62,6 +68,9 @@ __global__ void __launch_bounds__(128) gemv_f8w_kernel(const __nv_bfloat16* __re
   uint4 w[NCH];
 #pragma unroll
   for (int u = 0; u < NCH; ++u) w[u] = ld_stream(wrow + u * 512 + lane * 16);
+  // The weights do not depend on earlier kernels; the activations do.
+  pdl_wait();
+  if (ps.adv && blockIdx.x == 0 && (int)threadIdx.x < ps.adv_n) ps.adv[threadIdx.x] += ps.adv_by;
 
   float acc[M];
 #pragma unroll
@@ -103,23 +112,22 @@ __global__ void __launch_bounds__(128) gemv_f8w_kernel(const __nv_bfloat16* __re
 
 template <int M>
 cudaError_t launch_gemv(const __nv_bfloat16* X, int ldx, int K, const ProjSet& ps, int rows,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool pdl) {
   const dim3 grid((rows + 3) / 4), block(128);
   switch (K) {
-    case 512: gemv_f8w_kernel<M, 1><<<grid, block, 0, st>>>(X, ldx, ps); break;
-    case 1536: gemv_f8w_kernel<M, 3><<<grid, block, 0, st>>>(X, ldx, ps); break;
-    case 7168: gemv_f8w_kernel<M, 14><<<grid, block, 0, st>>>(X, ldx, ps); break;
-    case 8192: gemv_f8w_kernel<M, 16><<<grid, block, 0, st>>>(X, ldx, ps); break;
+    case 512: return launch_kernel(gemv_f8w_kernel<M, 1>, grid, block, 0, st, pdl, X, ldx, ps);
+    case 1536: return launch_kernel(gemv_f8w_kernel<M, 3>, grid, block, 0, st, pdl, X, ldx, ps);
+    case 7168: return launch_kernel(gemv_f8w_kernel<M, 14>, grid, block, 0, st, pdl, X, ldx, ps);
+    case 8192: return launch_kernel(gemv_f8w_kernel<M, 16>, grid, block, 0, st, pdl, X, ldx, ps);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
                         float* partial, int num_sms, int* err, cudaStream_t st, int* adv,
-                        int adv_n, int adv_by) {
+                        int adv_n, int adv_by, bool pdl) {
   if (M <= 0) return cudaSuccess;
   ProjSet ps{};
   ps.np = np;
@@ -132,14 +140,14 @@ cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Pro
   const int rows = p[0].N + (np > 1 ? p[1].N : 0);
   if (M <= 8) {
     switch (M) {
-      case 1: return launch_gemv<1>(X, ldx, K, ps, rows, st);
-      case 2: return launch_gemv<2>(X, ldx, K, ps, rows, st);
-      case 3: return launch_gemv<3>(X, ldx, K, ps, rows, st);
-      case 4: return launch_gemv<4>(X, ldx, K, ps, rows, st);
-      case 5: return launch_gemv<5>(X, ldx, K, ps, rows, st);
-      case 6: return launch_gemv<6>(X, ldx, K, ps, rows, st);
-      case 7: return launch_gemv<7>(X, ldx, K, ps, rows, st);
-      default: return launch_gemv<8>(X, ldx, K, ps, rows, st);
+      case 1: return launch_gemv<1>(X, ldx, K, ps, rows, st, pdl);
+      case 2: return launch_gemv<2>(X, ldx, K, ps, rows, st, pdl);
+      case 3: return launch_gemv<3>(X, ldx, K, ps, rows, st, pdl);
+      case 4: return launch_gemv<4>(X, ldx, K, ps, rows, st, pdl);
+      case 5: return launch_gemv<5>(X, ldx, K, ps, rows, st, pdl);
+      case 6: return launch_gemv<6>(X, ldx, K, ps, rows, st, pdl);
+      case 7: return launch_gemv<7>(X, ldx, K, ps, rows, st, pdl);
+      default: return launch_gemv<8>(X, ldx, K, ps, rows, st, pdl);
     }
   }
   return launch_gemm_tc(X, ldx, M, K, p, np, partial, num_sms, err, st);

@@ -61,6 +61,8 @@ __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
     int limit, __nv_bfloat16* __restrict__ cq_out, __nv_bfloat16* __restrict__ ckv_out, int* err) {
   __shared__ float2 red[9];
   __shared__ __align__(16) __nv_bfloat16 row[LAT];
+  pdl_launch_dependents();
+  pdl_wait();
   const int token = blockIdx.x, b = token / T, t = token % T;
   const int tid = threadIdx.x;
   const float* in = g1 + (size_t)token * G1_N;
@@ -165,6 +167,8 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(
         Wkvb + (size_t)(h * KVB_PER_HEAD + warp * 32 + r) * KV_LORA + cb * BLK + lane * 4));
     e4m3x4_to_f32(v, w[r]);
   }
+  pdl_launch_dependents();
+  pdl_wait();  // the weights above do not depend on earlier kernels; q does
   for (int b0 = 0; b0 < B; b0 += ABQ_B) {
     const int nb = min(ABQ_B, B - b0);
     __syncthreads();
@@ -237,6 +241,8 @@ __global__ void __launch_bounds__(256) absorb_out_kernel(
   e4m3x4_to_f32(wv.z, w + 8);
   e4m3x4_to_f32(wv.w, w + 12);
   const float sc = Skvb[(size_t)(2 * h + 1) * (KV_LORA / BLK) + lane / 8];
+  pdl_launch_dependents();
+  pdl_wait();  // the weights above do not depend on earlier kernels; o_lat does
   for (int b0 = 0; b0 < B; b0 += ABO_B) {
     float acc[ABO_B];
 #pragma unroll
@@ -286,11 +292,11 @@ cudaError_t launch_norm_rope_cache(const float* g1, int B, int T, const __nv_bfl
                                    const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
                                    int rope_pairing, const int* seq_lens, __nv_bfloat16* cache,
                                    int cap, int limit, __nv_bfloat16* cq_out,
-                                   __nv_bfloat16* ckv_out, int* err, cudaStream_t st) {
+                                   __nv_bfloat16* ckv_out, int* err, cudaStream_t st, bool pdl) {
   if (B * T == 0) return cudaSuccess;
-  norm_rope_cache_kernel<<<B * T, 256, 0, st>>>(g1, T, gq, gkv, eps, rope_tab, rope_pairing,
-                                                seq_lens, cache, cap, limit, cq_out, ckv_out, err);
-  return cudaGetLastError();
+  return launch_kernel(norm_rope_cache_kernel, dim3(B * T), dim3(256), 0, st, pdl, g1, T, gq, gkv,
+                       eps, rope_tab, rope_pairing, seq_lens, cache, cap, limit, cq_out, ckv_out,
+                       err);
 }
 
 cudaError_t launch_rope_q(__nv_bfloat16* q, int B, int T, const float2* rope_tab,
@@ -303,16 +309,15 @@ cudaError_t launch_rope_q(__nv_bfloat16* q, int B, int T, const float2* rope_tab
 cudaError_t launch_absorb_q(const __nv_bfloat16* q, int B, const uint8_t* Wkvb,
                             const float* Skvb, const float2* rope_tab, int rope_pairing,
                             const int* seq_lens, int limit, __nv_bfloat16* qfull,
-                            cudaStream_t st) {
-  absorb_q_kernel<<<dim3(HEADS, KV_LORA / BLK), 128, 0, st>>>(q, B, Wkvb, Skvb, rope_tab,
-                                                             rope_pairing, seq_lens, limit, qfull);
-  return cudaGetLastError();
+                            cudaStream_t st, bool pdl) {
+  return launch_kernel(absorb_q_kernel, dim3(HEADS, KV_LORA / BLK), dim3(128), 0, st, pdl, q, B,
+                       Wkvb, Skvb, rope_tab, rope_pairing, seq_lens, limit, qfull);
 }
 
 cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* Wkvb,
-                              const float* Skvb, __nv_bfloat16* out, cudaStream_t st) {
-  absorb_out_kernel<<<HEADS * VDIM / 8, 256, 0, st>>>(o_lat, B, Wkvb, Skvb, out);
-  return cudaGetLastError();
+                              const float* Skvb, __nv_bfloat16* out, cudaStream_t st, bool pdl) {
+  return launch_kernel(absorb_out_kernel, dim3(HEADS * VDIM / 8), dim3(256), 0, st, pdl, o_lat, B,
+                       Wkvb, Skvb, out);
 }
 
 cudaError_t init_kernels() {

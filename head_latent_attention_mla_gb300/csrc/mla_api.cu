@@ -322,6 +322,9 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
   const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(x);
   __nv_bfloat16* C = static_cast<__nv_bfloat16*>(cache);
 
+  // Every kernel after the first is launched with programmatic dependent launch: it may start
+  // (and fetch its weights) while its predecessor finishes, and waits for the predecessor's
+  // results before reading them.
   // Split-KV schedule: about two work items per SM, each a run of `chunk` positions.
   long total = 0;
   for (int b = 0; b < B; ++b) total += (long)lens_host[b] + 1;
@@ -348,22 +351,26 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
   MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
   MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, 1, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
                                     c->cfg.rope_pairing, lens_dev, C, cap, limit, cq, nullptr,
-                                    c->d_err, s));
+                                    c->d_err, s, true));
   Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
-  MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, B, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+  MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, B, Q_LORA, &p2, 1, at<float>(ws, L.gpart),
+                                     c->num_sms, c->d_err, s, nullptr, 0, 0, true));
   MLA_LAUNCH("absorb_q", launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
-                             c->cfg.rope_pairing, lens_dev, limit, qfull, s));
+                             c->cfg.rope_pairing, lens_dev, limit, qfull, s, true));
   MLA_LAUNCH("decode_attention", launch_decode_attention_tc(qfull, C, cap, lens_dev, plan,
                                                             c->cfg.softmax_scale, opart, ml,
-                                                            c->d_err, s));
-  MLA_LAUNCH("decode_combine", launch_decode_combine(lens_dev, plan, opart, ml, olat, c->d_err, s));
-  MLA_LAUNCH("absorb_out", launch_absorb_out(olat, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], attn, s));
+                                                            c->d_err, s, true));
+  MLA_LAUNCH("decode_combine", launch_decode_combine(lens_dev, plan, opart, ml, olat, c->d_err, s,
+                                                         true));
+  MLA_LAUNCH("absorb_out", launch_absorb_out(olat, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], attn, s,
+                                                 true));
   Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
   if (gemm_can_advance(B) && B <= 128) {  // the length update rides on the last kernel
     MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
-                                     c->num_sms, c->d_err, s, lens_dev, B, 1));
+                                     c->num_sms, c->d_err, s, lens_dev, B, 1, true));
   } else {
-    MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+    MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
+                                     c->num_sms, c->d_err, s, nullptr, 0, 0, true));
     MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, 1, s));
   }
   return MLA_OK;

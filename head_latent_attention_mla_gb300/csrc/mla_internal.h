@@ -29,6 +29,32 @@ constexpr int O_IN = HEADS * VDIM;         // 8192
 constexpr int G1_N = Q_LORA + KVA_N;       // 2112: q_a and kv_a outputs side by side
 constexpr int BLK = 128;                   // FP8 weight block (weight_block_size)
 
+// Programmatic dependent launch.  A kernel launched with pdl=true may start while the previous
+// kernel in the stream is still running; it must call pdl_wait() before touching anything that
+// kernel (or an earlier one) writes.  pdl_wait() is a no-op for a normal launch, and every
+// kernel calls pdl_launch_dependents() early so that its successor can be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // Device error word values (read back by mla_get_device_status).
 constexpr int DEV_ERR_NONE = 0;
 constexpr int DEV_ERR_RANGE = 1;    // a cache position outside [0, cap) was skipped
@@ -54,7 +80,7 @@ struct Proj {
 // adv[0..adv_n) (the call's length bookkeeping, riding on its last kernel; adv_n <= 128).
 cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
                         float* partial, int num_sms, int* err, cudaStream_t st,
-                        int* adv = nullptr, int adv_n = 0, int adv_by = 0);
+                        int* adv = nullptr, int adv_n = 0, int adv_by = 0, bool pdl = false);
 bool gemm_can_advance(int M);  // whether launch_gemm honours adv for this M
 cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
                            float* partial, int num_sms, int* err, cudaStream_t st);
@@ -71,7 +97,8 @@ cudaError_t launch_norm_rope_cache(const float* g1, int B, int T, const __nv_bfl
                                    const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
                                    int rope_pairing, const int* seq_lens, __nv_bfloat16* cache,
                                    int cap, int limit, __nv_bfloat16* cq_out,
-                                   __nv_bfloat16* ckv_out, int* err, cudaStream_t st);
+                                   __nv_bfloat16* ckv_out, int* err, cudaStream_t st,
+                                   bool pdl = false);
 
 // In-place RoPE of the rotary slice of q [M, HEADS, QHEAD] (prefill).
 cudaError_t launch_rope_q(__nv_bfloat16* q, int B, int T, const float2* rope_tab,
@@ -81,7 +108,7 @@ cudaError_t launch_rope_q(__nv_bfloat16* q, int B, int T, const float2* rope_tab
 cudaError_t launch_absorb_q(const __nv_bfloat16* q, int B, const uint8_t* Wkvb,
                             const float* Skvb, const float2* rope_tab, int rope_pairing,
                             const int* seq_lens, int limit, __nv_bfloat16* qfull,
-                            cudaStream_t st);
+                            cudaStream_t st, bool pdl = false);
 
 // Split-KV decode attention over the latent cache, then the log-sum-exp combine.
 struct DecodePlan {
@@ -91,14 +118,14 @@ struct DecodePlan {
 };
 cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const float* o_part,
                                   const float* ml_part, __nv_bfloat16* o_lat, int* err,
-                                  cudaStream_t st);
+                                  cudaStream_t st, bool pdl = false);
 
 // Split-KV decode attention over the latent cache on the tcgen05 tensor cores (TMA-fed,
 // accumulators in tensor memory): per work item, unnormalised partial outputs and (m, l).
 cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bfloat16* cache,
                                        int cap, const int* seq_lens, DecodePlan plan,
                                        float scale, float* o_part, float* ml_part, int* err,
-                                       cudaStream_t st);
+                                       cudaStream_t st, bool pdl = false);
 cudaError_t init_decode_tc_kernel();
 
 // One-time kernel attributes (dynamic shared memory opt-in); called by mla_create so that
@@ -107,7 +134,8 @@ cudaError_t init_kernels();
 
 // Decode output absorption: out[b, h*VDIM + v] = sum_c W_UV,h[v, c] o_lat[b, h, c].
 cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* Wkvb,
-                              const float* Skvb, __nv_bfloat16* out, cudaStream_t st);
+                              const float* Skvb, __nv_bfloat16* out, cudaStream_t st,
+                              bool pdl = false);
 
 // Causal prefill attention on the tcgen05 tensor cores: q [M, HEADS, QHEAD] (rotated),
 // kv [M, HEADS, 256] (k_nope | v), rotated k_pe from the cache rows; writes attn_out
