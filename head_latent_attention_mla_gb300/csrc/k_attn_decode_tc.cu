@@ -8,9 +8,7 @@
 //
 // One CTA per work item (a run of positions of one sequence), 7 warps:
 //   warp 0      TMA producer: the query block once, then 64-position cache tiles into a
-//               two-stage ring (9 boxes of 64 rows x 64 columns, 128-byte swizzle).  Tiles
-//               further ahead are bulk-prefetched into L2, so that the two shared-memory
-//               stages are refilled from L2 while HBM streams the next tiles;
+//               two-stage ring (9 boxes of 64 rows x 64 columns, 128-byte swizzle);
 //   warp 1      allocates tensor memory and issues, from one thread,
 //                 MMA1  S[64 heads, 64 pos]   = Q[64, 576] . C[64, 576]^T    (M=64,  N=64);
 //   warp 6      issues, from one thread,
@@ -44,7 +42,6 @@ constexpr int OFF_ALPHA = OFF_MISC + 16;
 constexpr int DA_SMEM = OFF_ALPHA + HEADS * 4 + 1024;  // + slack for 1024-byte alignment
 constexpr uint32_t TM_O = 0, TM_S = 256;
 constexpr float RESCALE_LOG2 = 8.f;             // tolerated growth of p before rescaling O
-constexpr int PF_TILES = 4;                     // tiles prefetched into L2 ahead of the ring
 
 __device__ __forceinline__ int find_item_tc(const int* seq_lens, int B, int chunk, int item,
                                             int* local) {
@@ -62,9 +59,8 @@ __device__ __forceinline__ int find_item_tc(const int* seq_lens, int B, int chun
 
 __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
     const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_c,
-    const __nv_bfloat16* __restrict__ cache, const int* __restrict__ seq_lens, int B, int cap,
-    int chunk, float scale_log2, float* __restrict__ o_part, float* __restrict__ ml_part,
-    int* err) {
+    const int* __restrict__ seq_lens, int B, int cap, int chunk, float scale_log2,
+    float* __restrict__ o_part, float* __restrict__ ml_part, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
@@ -132,16 +128,9 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
         mbar_expect_tx(q_full, DA_TILE_BYTES);
         for (int c = 0; c < DA_NBOX; ++c)
           tma_load_2d(smem + OFF_Q + c * DA_BOX, &map_q, q_full, 64 * c, HEADS * b);
-        auto prefetch = [&](int t) {
-          const int first = p0 + DA_TILE * t;
-          const int rows = min(DA_TILE, p1 - first);
-          prefetch_l2(cache + ((size_t)b * cap + first) * LAT, (uint32_t)rows * LAT * 2);
-        };
-        for (int t = 2; t < min(nt, 2 + PF_TILES); ++t) prefetch(t);
         int issued = 0;
         for (int t = 0; t < nt; ++t) {
           const int st = t & 1;
-          if (t >= 1 && t + 2 + PF_TILES - 1 < nt) prefetch(t + 2 + PF_TILES - 1);
           if (t >= 2 && !mbar_wait(&c_empty[st], ((t - 2) >> 1) & 1, err, abort_flag)) break;
           mbar_expect_tx(&c_full[st], DA_TILE_BYTES);
           const int row = b * cap + p0 + DA_TILE * t;
@@ -378,7 +367,7 @@ cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bf
       !make_tmap_2d(&mc, true, cache, LAT, (uint64_t)plan.B * cap, LAT * 2, 64, 64))
     return cudaErrorInvalidValue;
   return launch_kernel(decode_attn_tc_kernel, dim3(plan.items), dim3(DA_THREADS), DA_SMEM, st,
-                       pdl, mq, mc, cache, seq_lens, plan.B, cap, plan.chunk,
+                       pdl, mq, mc, seq_lens, plan.B, cap, plan.chunk,
                        scale * 1.4426950408889634f, o_part, ml_part, err);
 }
 
