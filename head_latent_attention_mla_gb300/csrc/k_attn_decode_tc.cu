@@ -6,7 +6,13 @@
 // softmax scale, and the latent output is o_lat,h = sum_j p_h(j) c_hat_j.  Each 64-position
 // latent tile is read from HBM once and serves as both key and value.
 //
-// One CTA per work item (a run of positions of one sequence), 7 warps:
+// Work split: the positions of all sequences, concatenated, are cut into G equal shares, one
+// per CTA (G = the SM count, fewer for short caches), so ragged batches stay balanced.  A share
+// can span several sequences; each piece ("segment") is attended with its own query block and
+// softmax state, and leaves one partial output in slot b + c (b the sequence, c the CTA: along
+// the staircase of (b, c) pairs this sum never repeats).  A combine kernel merges the slots.
+//
+// 7 warps per CTA:
 //   warp 0      TMA producer: the query block once, then 64-position cache tiles into a
 //               two-stage ring (9 boxes of 64 rows x 64 columns, 128-byte swizzle);
 //   warp 1      allocates tensor memory and issues, from one thread,
@@ -39,27 +45,15 @@ constexpr int OFF_C = OFF_Q + DA_TILE_BYTES;    // two stages
 constexpr int OFF_BAR = OFF_C + 2 * DA_TILE_BYTES;
 constexpr int OFF_MISC = OFF_BAR + 16 * 8;  // 13 barriers used
 constexpr int OFF_ALPHA = OFF_MISC + 16;
-constexpr int DA_SMEM = OFF_ALPHA + HEADS * 4 + 1024;  // + slack for 1024-byte alignment
+constexpr int MAX_SEG = 96;                     // segments one CTA can hold
+constexpr int OFF_SEG = OFF_ALPHA + HEADS * 4;
+constexpr int DA_SMEM = OFF_SEG + MAX_SEG * 12 + 16 + 1024;  // + slack for 1024-byte alignment
 constexpr uint32_t TM_O = 0, TM_S = 256;
 constexpr float RESCALE_LOG2 = 8.f;             // tolerated growth of p before rescaling O
 
-__device__ __forceinline__ int find_item_tc(const int* seq_lens, int B, int chunk, int item,
-                                            int* local) {
-  int acc = 0;
-  for (int b = 0; b < B; ++b) {
-    const int n = (seq_lens[b] + 1 + chunk - 1) / chunk;
-    if (item < acc + n) {
-      *local = item - acc;
-      return b;
-    }
-    acc += n;
-  }
-  return -1;
-}
-
 __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
     const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_c,
-    const int* __restrict__ seq_lens, int B, int cap, int chunk, float scale_log2,
+    const int* __restrict__ seq_lens, int B, int cap, int G, long long P, float scale_log2,
     float* __restrict__ o_part, float* __restrict__ ml_part, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -73,25 +67,40 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
   uint64_t* p_full = bars + 9;
   uint64_t* o_done = bars + 10;
   uint64_t* mma_idle = bars + 11;  // [2]: one per MMA-issuing thread
+  uint64_t* q_free = bars + 13;    // MMA1 finished with the segment's query block
+  uint64_t* o_free = bars + 14;    // the epilogue has read the segment's O^T
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-  int* s_item = reinterpret_cast<int*>(smem + OFF_MISC + 8);
+  int* s_nseg = reinterpret_cast<int*>(smem + OFF_MISC + 8);
   float* s_alpha = reinterpret_cast<float*>(smem + OFF_ALPHA);
+  int* seg = reinterpret_cast<int*>(smem + OFF_SEG);  // [MAX_SEG][3]: b, first, end
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = blockIdx.x;
+  const int cta = blockIdx.x;
   pdl_launch_dependents();
   pdl_wait();  // the query and the new cache row come from earlier kernels
   if (threadIdx.x == 0) {
-    int local = 0;
-    const int b = find_item_tc(seq_lens, B, chunk, item, &local);
-    s_item[0] = b;
-    s_item[1] = local;
-    if (b < 0) atomicExch(err, DEV_ERR_PLAN);
-    if (b >= 0 && seq_lens[b] + 1 > cap) {
-      atomicExch(err, DEV_ERR_RANGE);
-      s_item[0] = -1;
+    const long long r0 = decode_share_start(cta, G, P), r1 = decode_share_start(cta + 1, G, P);
+    long long acc = 0;
+    int nseg = 0;
+    bool bad = false;
+    for (int b = 0; b < B; ++b) {
+      const long long S = (long long)seq_lens[b] + 1;
+      if (S > cap) bad = true;
+      const long long lo = max(acc, r0), hi = min(acc + S, r1);
+      if (lo < hi) {
+        if (nseg < MAX_SEG) {
+          seg[3 * nseg] = b;
+          seg[3 * nseg + 1] = (int)(lo - acc);
+          seg[3 * nseg + 2] = (int)(hi - acc);
+        }
+        ++nseg;
+      }
+      acc += S;
     }
+    if (bad) atomicExch(err, DEV_ERR_RANGE);
+    if (acc != P || nseg > MAX_SEG) atomicExch(err, DEV_ERR_PLAN);
+    *s_nseg = (bad || acc != P || nseg > MAX_SEG) ? 0 : nseg;
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c_full[i], 1);
@@ -103,6 +112,8 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
     mbar_init(o_done, 1);
     mbar_init(&mma_idle[0], 1);
     mbar_init(&mma_idle[1], 1);
+    mbar_init(q_free, 1);
+    mbar_init(o_free, 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -114,59 +125,70 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int b = s_item[0];
-  const int p0 = s_item[1] * chunk;
-  const int p1 = b >= 0 ? min(seq_lens[b] + 1, p0 + chunk) : p0;
-  const int nt = (p1 - p0 + DA_TILE - 1) / DA_TILE;
+  const int nseg = *s_nseg;
+  auto seg_tiles = [&](int sg) { return (seg[3 * sg + 2] - seg[3 * sg + 1] + DA_TILE - 1) / DA_TILE; };
 
-  if (b >= 0 && nt > 0) {
+  if (nseg > 0) {
     if (warp == 0) {
       // ---------------------------------------------------------------- TMA producer
       if (lane == 0) {
         tma_prefetch_desc(&map_q);
         tma_prefetch_desc(&map_c);
-        mbar_expect_tx(q_full, DA_TILE_BYTES);
-        for (int c = 0; c < DA_NBOX; ++c)
-          tma_load_2d(smem + OFF_Q + c * DA_BOX, &map_q, q_full, 64 * c, HEADS * b);
-        int issued = 0;
-        for (int t = 0; t < nt; ++t) {
-          const int st = t & 1;
-          if (t >= 2 && !mbar_wait(&c_empty[st], ((t - 2) >> 1) & 1, err, abort_flag)) break;
-          mbar_expect_tx(&c_full[st], DA_TILE_BYTES);
-          const int row = b * cap + p0 + DA_TILE * t;
+        int t = 0, issued = 0, qloads = 0;
+        bool ok = true;
+        for (int sg = 0; ok && sg < nseg; ++sg) {
+          const int b = seg[3 * sg], p0 = seg[3 * sg + 1], nt = seg_tiles(sg);
+          if (sg > 0 && !(ok = mbar_wait(q_free, (sg - 1) & 1, err, abort_flag))) break;
+          mbar_expect_tx(q_full, DA_TILE_BYTES);
           for (int c = 0; c < DA_NBOX; ++c)
-            tma_load_2d(smem + OFF_C + st * DA_TILE_BYTES + c * DA_BOX, &map_c, &c_full[st],
-                        64 * c, row);
-          issued = t + 1;
+            tma_load_2d(smem + OFF_Q + c * DA_BOX, &map_q, q_full, 64 * c, HEADS * b);
+          qloads = sg + 1;
+          for (int i = 0; i < nt; ++i, ++t) {
+            const int st = t & 1;
+            if (t >= 2 && !(ok = mbar_wait(&c_empty[st], ((t - 2) >> 1) & 1, err, abort_flag)))
+              break;
+            mbar_expect_tx(&c_full[st], DA_TILE_BYTES);
+            const int row = b * cap + p0 + DA_TILE * i;
+            for (int c = 0; c < DA_NBOX; ++c)
+              tma_load_2d(smem + OFF_C + st * DA_TILE_BYTES + c * DA_BOX, &map_c, &c_full[st],
+                          64 * c, row);
+            issued = t + 1;
+          }
         }
         // Never leave the CTA with copies in flight: wait (bounded) for the last ones.
         volatile int no_abort = 0;
-        mbar_wait(q_full, 0, err, &no_abort);
-        for (int t = max(0, issued - 2); t < issued; ++t)
-          mbar_wait(&c_full[t & 1], (t >> 1) & 1, err, &no_abort);
+        if (qloads > 0) mbar_wait(q_full, (qloads - 1) & 1, err, &no_abort);
+        for (int u = max(0, issued - 2); u < issued; ++u)
+          mbar_wait(&c_full[u & 1], (u >> 1) & 1, err, &no_abort);
       }
     } else if (warp == 1) {
       // ---------------------------------------------------------------- MMA1 issuer
       if (lane == 0) {
         constexpr uint32_t idesc_s = idesc_bf16(64, 64, false, false);
         const uint32_t qb = sbase + OFF_Q;
-        bool ok = mbar_wait(q_full, 0, err, abort_flag);
-        for (int t = 0; ok && t < nt; ++t) {
-          const int st = t & 1;
-          ok = mbar_wait(&c_full[st], (t >> 1) & 1, err, abort_flag);
-          if (ok && t >= 2) ok = mbar_wait(&s_free[st], ((t - 2) >> 1) & 1, err, abort_flag);
-          if (!ok) break;
-          fence_after();
-          const uint32_t cb = sbase + OFF_C + st * DA_TILE_BYTES;
+        bool ok = true;
+        int t = 0;
+        for (int sg = 0; ok && sg < nseg; ++sg) {
+          const int nt = seg_tiles(sg);
+          if (!(ok = mbar_wait(q_full, sg & 1, err, abort_flag))) break;
+          for (int i = 0; i < nt; ++i, ++t) {
+            const int st = t & 1;
+            ok = mbar_wait(&c_full[st], (t >> 1) & 1, err, abort_flag);
+            if (ok && t >= 2) ok = mbar_wait(&s_free[st], ((t - 2) >> 1) & 1, err, abort_flag);
+            if (!ok) break;
+            fence_after();
+            const uint32_t cb = sbase + OFF_C + st * DA_TILE_BYTES;
 #pragma unroll
-          for (int c = 0; c < DA_NBOX; ++c)
+            for (int c = 0; c < DA_NBOX; ++c)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t a = sdesc_sw128(qb + c * DA_BOX + k * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(cb + c * DA_BOX + k * 32, 16, 1024);
-              mma_bf16(tmem + TM_S + 64 * st, a, bd, idesc_s, (c | k) != 0);
-            }
-          mma_commit(&s_full[st]);
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t a = sdesc_sw128(qb + c * DA_BOX + k * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128(cb + c * DA_BOX + k * 32, 16, 1024);
+                mma_bf16(tmem + TM_S + 64 * st, a, bd, idesc_s, (c | k) != 0);
+              }
+            mma_commit(&s_full[st]);
+          }
+          mma_commit(q_free);  // the query block may be replaced once these MMAs are done
         }
         // All issued MMAs must finish before tensor memory is released.
         mma_commit(&mma_idle[0]);
@@ -177,21 +199,28 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
       // ---------------------------------------------------------------- MMA2 issuer
       if (lane == 0) {
         constexpr uint32_t idesc_o = idesc_bf16(128, 64, true, false);
-        for (int u = 0; u < nt; ++u) {
-          if (!mbar_wait(p_full, u & 1, err, abort_flag)) break;
-          fence_after();
-          const uint32_t cb = sbase + OFF_C + (u & 1) * DA_TILE_BYTES;
+        bool ok = true;
+        int t = 0;
+        for (int sg = 0; ok && sg < nseg; ++sg) {
+          const int nt = seg_tiles(sg);
+          if (sg > 0 && !(ok = mbar_wait(o_free, (sg - 1) & 1, err, abort_flag))) break;
+          for (int i = 0; i < nt; ++i, ++t) {
+            const int st = t & 1;
+            if (!(ok = mbar_wait(p_full, t & 1, err, abort_flag))) break;
+            fence_after();
+            const uint32_t cb = sbase + OFF_C + st * DA_TILE_BYTES;
 #pragma unroll
-          for (int d = 0; d < 4; ++d)
+            for (int d = 0; d < 4; ++d)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              // A = C^T: MN-major, 128 latent dims (2 boxes, DA_BOX apart) x 16 positions.
-              const uint64_t a = sdesc_sw128(cb + 2 * d * DA_BOX + k * 2048, DA_BOX, 1024);
-              const uint64_t bd = sdesc_sw128(cb + 8 * DA_BOX + k * 32, 16, 1024);
-              mma_bf16(tmem + TM_O + 64 * d, a, bd, idesc_o, (u > 0) || (k > 0));
-            }
-          mma_commit(o_done);
-          mma_commit(&c_empty[u & 1]);
+              for (int k = 0; k < 4; ++k) {
+                // A = C^T: MN-major, 128 latent dims (2 boxes, DA_BOX apart) x 16 positions.
+                const uint64_t a = sdesc_sw128(cb + 2 * d * DA_BOX + k * 2048, DA_BOX, 1024);
+                const uint64_t bd = sdesc_sw128(cb + 8 * DA_BOX + k * 32, 16, 1024);
+                mma_bf16(tmem + TM_O + 64 * d, a, bd, idesc_o, (i > 0) || (k > 0));
+              }
+            mma_commit(o_done);
+            mma_commit(&c_empty[st]);
+          }
         }
         mma_commit(&mma_idle[1]);
         volatile int no_abort = 0;
@@ -204,95 +233,101 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
       const bool own = lane < 16;
       const int tid = threadIdx.x - 64;       // 0..127
       const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-      float m = -INFINITY, l = 0.f;
       bool ok = true;
-      for (int u = 0; u < nt; ++u) {
-        const int st = u & 1;
-        if (!(ok = mbar_wait(&s_full[st], (u >> 1) & 1, err, abort_flag))) break;
-        fence_after();
-        uint32_t r[2][32];
-        tmem_ld32(tmem + lane_off + TM_S + 64 * st, r[0]);
-        tmem_ld32(tmem + lane_off + TM_S + 64 * st + 32, r[1]);
-        tmem_wait_ld();
-        fence_before();
-        mbar_arrive(&s_free[st]);
-        const int n = min(DA_TILE, p1 - (p0 + DA_TILE * u));
-        float tmax = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float s = (j < n) ? __uint_as_float(r[j >> 5][j & 31]) * scale_log2 : -INFINITY;
-          r[j >> 5][j & 31] = __float_as_uint(s);
-          tmax = fmaxf(tmax, s);
-        }
-        bool need = false;
-        if (own) {
-          float alpha = 1.f;
-          if (tmax > m + RESCALE_LOG2) {
-            if (m != -INFINITY) {
-              alpha = exp2f(m - tmax);
-              need = true;
-            }
-            l *= alpha;
-            m = tmax;
-          }
-          s_alpha[h] = alpha;
-        }
-        uint32_t pk[32];
-        float lsum = 0.f;
-#pragma unroll
-        for (int j = 0; j < 64; j += 2) {
-          const float a = exp2f(__uint_as_float(r[j >> 5][j & 31]) - m);
-          const float c = exp2f(__uint_as_float(r[(j + 1) >> 5][(j + 1) & 31]) - m);
-          __nv_bfloat162 pr = __floats2bfloat162_rn(a, c);
-          lsum += __low2float(pr) + __high2float(pr);
-          pk[j >> 1] = *reinterpret_cast<uint32_t*>(&pr);
-        }
-        l += lsum;
-        // Box 8 (rotary dims) of this stage was last read by this tile's MMA1 and by MMA2 of
-        // tile u-2, both complete (the stage was refilled for tile u after the latter).
-        uint8_t* cst = smem + OFF_C + st * DA_TILE_BYTES;
-        if (own) {  // P row h: 64 bf16 = 8 chunks of 16 B, 128-byte swizzle, in box 8
-          uint8_t* prow = cst + 8 * DA_BOX + h * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) * 16)) =
-                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        }
-        if (n < DA_TILE) {  // rows past the sequence end must not reach MMA2 as NaN/Inf
-          const int chunks = (DA_TILE - n) * 8 * 8;
-          for (int e = tid; e < chunks; e += 128) {
-            const int row = n + e / 64, box = (e / 8) % 8, c16 = e % 8;
-            *reinterpret_cast<uint4*>(cst + box * DA_BOX + row * 128 + c16 * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-        }
-        // MMA2 of the previous tile must be complete before O^T may be rescaled, and every
-        // o_done phase is consumed here, in order, before this tile's MMA2 can be issued.
-        if (u >= 1 && !(ok = mbar_wait(o_done, (u - 1) & 1, err, abort_flag))) break;
-        if (named_bar_or(1, 128, need)) {
+      int t = 0;
+      for (int sg = 0; ok && sg < nseg; ++sg) {
+        const int b = seg[3 * sg], p0 = seg[3 * sg + 1], p1 = seg[3 * sg + 2];
+        const int nt = seg_tiles(sg);
+        float m = -INFINITY, l = 0.f;
+        for (int i = 0; i < nt; ++i, ++t) {
+          const int st = t & 1;
+          if (!(ok = mbar_wait(&s_full[st], (t >> 1) & 1, err, abort_flag))) break;
           fence_after();
+          uint32_t r[2][32];
+          tmem_ld32(tmem + lane_off + TM_S + 64 * st, r[0]);
+          tmem_ld32(tmem + lane_off + TM_S + 64 * st + 32, r[1]);
+          tmem_wait_ld();
+          fence_before();
+          mbar_arrive(&s_free[st]);
+          const int n = min(DA_TILE, p1 - (p0 + DA_TILE * i));
+          float tmax = -INFINITY;
 #pragma unroll
-          for (int d = 0; d < 4; ++d)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              uint32_t o[32];
-              const uint32_t ta = tmem + lane_off + TM_O + 64 * d + 32 * hh;
-              tmem_ld32(ta, o);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                o[i] = __float_as_uint(__uint_as_float(o[i]) * s_alpha[32 * hh + i]);
-              tmem_st32(ta, o);
+          for (int j = 0; j < 64; ++j) {
+            const float sc = (j < n) ? __uint_as_float(r[j >> 5][j & 31]) * scale_log2 : -INFINITY;
+            r[j >> 5][j & 31] = __float_as_uint(sc);
+            tmax = fmaxf(tmax, sc);
+          }
+          bool need = false;
+          if (own) {
+            float alpha = 1.f;
+            if (tmax > m + RESCALE_LOG2) {
+              if (m != -INFINITY) {
+                alpha = exp2f(m - tmax);
+                need = true;
+              }
+              l *= alpha;
+              m = tmax;
             }
-          tmem_wait_st();
+            s_alpha[h] = alpha;
+          }
+          uint32_t pk[32];
+          float lsum = 0.f;
+#pragma unroll
+          for (int j = 0; j < 64; j += 2) {
+            const float a = exp2f(__uint_as_float(r[j >> 5][j & 31]) - m);
+            const float c = exp2f(__uint_as_float(r[(j + 1) >> 5][(j + 1) & 31]) - m);
+            __nv_bfloat162 pr = __floats2bfloat162_rn(a, c);
+            lsum += __low2float(pr) + __high2float(pr);
+            pk[j >> 1] = *reinterpret_cast<uint32_t*>(&pr);
+          }
+          l += lsum;
+          // Box 8 (rotary dims) of this stage was last read by this tile's MMA1 and by MMA2 of
+          // tile t-2, both complete (the stage was refilled for tile t after the latter).
+          uint8_t* cst = smem + OFF_C + st * DA_TILE_BYTES;
+          if (own) {  // P row h: 64 bf16 = 8 chunks of 16 B, 128-byte swizzle, in box 8
+            uint8_t* prow = cst + 8 * DA_BOX + h * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) * 16)) =
+                  make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          }
+          if (n < DA_TILE) {  // rows past the segment end must not reach MMA2 as NaN/Inf
+            const int chunks = (DA_TILE - n) * 8 * 8;
+            for (int e = tid; e < chunks; e += 128) {
+              const int row = n + e / 64, box = (e / 8) % 8, c16 = e % 8;
+              *reinterpret_cast<uint4*>(cst + box * DA_BOX + row * 128 + c16 * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+          }
+          // MMA2 of the previous tile must be complete before O^T may be rescaled, and every
+          // o_done phase is consumed here, in order, before this tile's MMA2 can be issued.
+          if (t >= 1 && !(ok = mbar_wait(o_done, (t - 1) & 1, err, abort_flag))) break;
+          if (named_bar_or(1, 128, need)) {
+            fence_after();
+#pragma unroll
+            for (int d = 0; d < 4; ++d)
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                uint32_t o[32];
+                const uint32_t ta = tmem + lane_off + TM_O + 64 * d + 32 * hh;
+                tmem_ld32(ta, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  o[e] = __float_as_uint(__uint_as_float(o[e]) * s_alpha[32 * hh + e]);
+                tmem_st32(ta, o);
+              }
+            tmem_wait_st();
+          }
+          fence_proxy_async();
+          fence_before();
+          mbar_arrive(p_full);
         }
-        fence_proxy_async();
-        fence_before();
-        mbar_arrive(p_full);
-      }
-      if (ok && mbar_wait(o_done, (nt - 1) & 1, err, abort_flag)) {
+        if (!ok || !(ok = mbar_wait(o_done, (t - 1) & 1, err, abort_flag))) break;
+        // Segment epilogue: unnormalised O^T, m and l of every head into slot b + cta.
         fence_after();
-        float* op = o_part + (size_t)item * HEADS * KV_LORA;
+        const size_t slot = (size_t)b + cta;
+        float* op = o_part + slot * HEADS * KV_LORA;
 #pragma unroll
         for (int d = 0; d < 4; ++d) {
           const int dim = 128 * d + 32 * q + lane;
@@ -302,14 +337,16 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
             tmem_ld32(tmem + lane_off + TM_O + 64 * d + 32 * hh, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              op[(size_t)(32 * hh + i) * KV_LORA + dim] = __uint_as_float(o[i]);
+            for (int e = 0; e < 32; ++e)
+              op[(size_t)(32 * hh + e) * KV_LORA + dim] = __uint_as_float(o[e]);
           }
         }
         if (own) {
-          ml_part[((size_t)item * HEADS + h) * 2] = m;
-          ml_part[((size_t)item * HEADS + h) * 2 + 1] = l;
+          ml_part[(slot * HEADS + h) * 2] = m;
+          ml_part[(slot * HEADS + h) * 2 + 1] = l;
         }
+        fence_before();
+        mbar_arrive(o_free);
       }
     }
   }
@@ -366,8 +403,8 @@ cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bf
   if (!make_tmap_2d(&mq, true, qfull, LAT, (uint64_t)plan.B * HEADS, LAT * 2, 64, 64) ||
       !make_tmap_2d(&mc, true, cache, LAT, (uint64_t)plan.B * cap, LAT * 2, 64, 64))
     return cudaErrorInvalidValue;
-  return launch_kernel(decode_attn_tc_kernel, dim3(plan.items), dim3(DA_THREADS), DA_SMEM, st,
-                       pdl, mq, mc, seq_lens, plan.B, cap, plan.chunk,
+  return launch_kernel(decode_attn_tc_kernel, dim3(plan.G), dim3(DA_THREADS), DA_SMEM, st, pdl,
+                       mq, mc, seq_lens, plan.B, cap, plan.G, plan.P,
                        scale * 1.4426950408889634f, o_part, ml_part, err);
 }
 

@@ -7,30 +7,36 @@ namespace mla {
 
 namespace {
 
-constexpr int kMaxSplits = 512;   // per sequence; the host schedule keeps it far lower
+constexpr int kMaxSplits = 512;   // shares one sequence can span (at most the CTA count)
 
-// Combine of the split partials of sequence b, head h:
+// Combine of the partial outputs of sequence b, head h: the shares of CTAs c_first..c_last
+// cover its positions and left partials in slots b + c;
 // o = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i, M = max_i m_i.
-// The per-split weights are formed once in shared memory; each thread then sums 4 columns with
+// The per-share weights are formed once in shared memory; each thread then sums 4 columns with
 // independent loads.
 __global__ void __launch_bounds__(128) decode_combine_kernel(
-    const int* __restrict__ seq_lens, int B, int chunk, int items, const float* __restrict__ o_part,
+    const int* __restrict__ seq_lens, int B, int G, long long P, const float* __restrict__ o_part,
     const float* __restrict__ ml_part, __nv_bfloat16* __restrict__ o_lat, int* err) {
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   __shared__ int s_first, s_n;
   __shared__ float s_w[kMaxSplits];
+  __shared__ float s_red[8];
   pdl_launch_dependents();
   pdl_wait();
-  __shared__ float s_red[8];
   if (tid == 0) {
-    int acc = 0;
-    for (int bb = 0; bb < b; ++bb) acc += (seq_lens[bb] + 1 + chunk - 1) / chunk;
-    int n = (seq_lens[b] + 1 + chunk - 1) / chunk;
-    if (acc + n > items || n < 1 || n > kMaxSplits) {  // disagrees with the host schedule
+    long long start = 0;
+    for (int bb = 0; bb < b; ++bb) start += (long long)seq_lens[bb] + 1;
+    const long long end = start + seq_lens[b] + 1;
+    int c0 = 0, n = 0;
+    if (end <= P) {
+      c0 = decode_share_of(start, G, P);
+      n = decode_share_of(end - 1, G, P) - c0 + 1;
+    }
+    if (n < 1 || n > kMaxSplits) {  // device lengths disagree with the host schedule
       atomicExch(err, DEV_ERR_PLAN);
       n = 0;
     }
-    s_first = acc;
+    s_first = b + c0;  // slot of the first share
     s_n = n;
   }
   __syncthreads();
@@ -93,7 +99,7 @@ cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const fl
                                   cudaStream_t st, bool pdl) {
   if (plan.B == 0) return cudaSuccess;
   return launch_kernel(decode_combine_kernel, dim3(plan.B, HEADS), dim3(128), 0, st, pdl,
-                       seq_lens, plan.B, plan.chunk, plan.items, o_part, ml_part, o_lat, err);
+                       seq_lens, plan.B, plan.G, plan.P, o_part, ml_part, o_lat, err);
 }
 
 }  // namespace mla

@@ -325,17 +325,10 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
   // Every kernel after the first is launched with programmatic dependent launch: it may start
   // (and fetch its weights) while its predecessor finishes, and waits for the predecessor's
   // results before reading them.
-  // Split-KV schedule: about two work items per SM, each a run of `chunk` positions.
-  long total = 0;
-  for (int b = 0; b < B; ++b) total += (long)lens_host[b] + 1;
-  const long target = 2L * c->num_sms;
-  long chunk = (total + target - 1) / target;
-  chunk = ((chunk + 63) / 64) * 64;
-  if (chunk < 64) chunk = 64;
-  long items = 0;
-  for (int b = 0; b < B; ++b) items += ((long)lens_host[b] + 1 + chunk - 1) / chunk;
-  if (items > items_max(c, B)) return MLA_ERR_STATE;
-  DecodePlan plan{B, (int)chunk, (int)items};
+  // Split-KV schedule: the positions of all sequences cut into about one equal share per SM.
+  long long total = 0;
+  for (int b = 0; b < B; ++b) total += (long long)lens_host[b] + 1;
+  const DecodePlan plan = make_decode_plan(B, total, c->num_sms, items_max(c, B));
 
   float* g1 = at<float>(ws, L.g1);
   __nv_bfloat16* cq = at<__nv_bfloat16>(ws, L.cq);

@@ -113,9 +113,31 @@ cudaError_t launch_absorb_q(const __nv_bfloat16* q, int B, const uint8_t* Wkvb,
 // Split-KV decode attention over the latent cache, then the log-sum-exp combine.
 struct DecodePlan {
   int B;
-  int chunk;        // positions per work item
-  int items;        // total work items (sum over b of ceil((len_b + 1) / chunk))
+  int G;            // CTAs: the concatenated positions are cut into G equal shares
+  long long P;      // total positions, sum over b of (seq_lens[b] + 1)
 };
+// First position (in the concatenation of all sequences) of CTA c's share.
+__host__ __device__ inline long long decode_share_start(int c, int G, long long P) {
+  return (long long)c * P / G;
+}
+// The CTA whose share holds position pos.
+__host__ __device__ inline int decode_share_of(long long pos, int G, long long P) {
+  int c = (int)((pos * G) / P);
+  while (c + 1 < G && decode_share_start(c + 1, G, P) <= pos) ++c;
+  while (c > 0 && decode_share_start(c, G, P) > pos) --c;
+  return c;
+}
+// Partial slots used by a plan: sequence b's share in CTA c goes to slot b + c.
+inline int decode_slots(const DecodePlan& p) { return p.B + p.G; }
+// The plan for B sequences holding P positions in total, on num_sms SMs, with at most
+// max_slots partial slots: about one share per SM, at least 64 positions per share.
+inline DecodePlan make_decode_plan(int B, long long P, int num_sms, int max_slots) {
+  long long G = (P + 63) / 64;
+  if (G > num_sms) G = num_sms;
+  if (G > max_slots - B) G = max_slots - B;
+  if (G < 1) G = 1;
+  return DecodePlan{B, (int)G, P};
+}
 cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const float* o_part,
                                   const float* ml_part, __nv_bfloat16* o_lat, int* err,
                                   cudaStream_t st, bool pdl = false);

@@ -10,8 +10,9 @@
 // every GPU that loads the library holds until the process exits.
 //
 // Limits and rules (also stated in include/mla.h):
-//   * at most kMaxBatch sequences per call; the attention uses at most kMaxItems split work
-//     items, so long sequences get longer splits than mla_decode would give them;
+//   * at most kMaxBatch sequences per call; the attention uses at most kMaxItems partial slots
+//     (sequences + shares), so long contexts are cut into fewer, longer shares than mla_decode
+//     would use;
 //   * every call shares the one array: calls whose work overlaps on the GPU (two streams, two
 //     threads, two contexts on one device) race with each other;
 //   * the array keeps the last call's contents; this path writes every scratch byte it reads
@@ -98,14 +99,8 @@ extern "C" mla_status mla_decode_noalloc(mla_ctx* c, const void* x, int B, void*
       return MLA_ERR_CAPACITY;
     total += (long)lens_host[b] + 1;
   }
-  // Split-KV schedule bounded by kMaxItems: with chunk >= total / (kMaxItems - B), the sum of
-  // ceil(S_b / chunk) is at most kMaxItems.
-  long chunk = (total + (kMaxItems - B) - 1) / (kMaxItems - B);
-  chunk = ((chunk + 63) / 64) * 64;
-  if (chunk < 64) chunk = 64;
-  long items = 0;
-  for (int b = 0; b < B; ++b) items += ((long)lens_host[b] + 1 + chunk - 1) / chunk;
-  if (items > kMaxItems) return MLA_ERR_STATE;
+  // Split-KV schedule with at most kMaxItems partial slots (B + shares).
+  const DecodePlan plan = make_decode_plan(B, total, c->num_sms, kMaxItems);
 
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return MLA_ERR_CUDA;
@@ -126,7 +121,6 @@ extern "C" mla_status mla_decode_noalloc(mla_ctx* c, const void* x, int B, void*
   const int limit = cap < c->cfg.max_positions ? cap : c->cfg.max_positions;
   const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(x);
   __nv_bfloat16* C = static_cast<__nv_bfloat16*>(cache);
-  const DecodePlan plan{B, (int)chunk, (int)items};
 
 #define NA_RUN(expr)                              \
   do {                                            \
