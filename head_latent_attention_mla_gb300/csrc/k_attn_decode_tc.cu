@@ -13,18 +13,21 @@
 // the staircase of (b, c) pairs this sum never repeats).  A combine kernel merges the slots.
 //
 // 7 warps per CTA:
-//   warp 0      TMA producer: the query block once, then 64-position cache tiles into a
-//               two-stage ring (9 boxes of 64 rows x 64 columns, 128-byte swizzle);
+//   warp 0      computes the CTA's segments (a warp-wide prefix sum of the lengths), then, as
+//               TMA producer, loads the query block once per segment and 64-position cache
+//               tiles into a two-stage ring (9 boxes of 64 rows x 64 columns, 128-byte swizzle);
 //   warp 1      allocates tensor memory and issues, from one thread,
 //                 MMA1  S[64 heads, 64 pos]   = Q[64, 576] . C[64, 576]^T    (M=64,  N=64);
 //   warp 6      issues, from one thread,
 //                 MMA2  O^T[512, 64 heads]   += C[64 pos, 0:512]^T . P^T     (M=128, N=64, x4).
 //               Two issuers keep MMA2 of a tile from queueing behind the next tile's load;
-//   warps 2..5  softmax: one head per thread (rows of S), online softmax in base 2 with a
-//               lazy rescale of O^T (only when a head's running maximum grows by more than
-//               2^8), P written as bf16 into the tile's rotary box (box 8), which MMA1 no
-//               longer needs; then the epilogue writes the unnormalised partial O, the
+//   warps 2..5  softmax: two threads per head (a row of S, 32 scores each), online softmax in
+//               base 2 with a lazy rescale of O^T (only when a head's running maximum grows by
+//               more than 2^8), P written as bf16 into the tile's rotary box (box 8), which
+//               MMA1 no longer needs; then the epilogue writes the unnormalised partial O, the
 //               maximum m and the sum l of every head.
+// A tile's MMA2 does not wait for the previous tile's: only a rescale of O^T needs the previous
+// MMA2 to be complete, and it is rare once a head's maximum has settled.
 // Tensor memory: O^T in columns [0, 256) (lane = latent dim, column = head within each of the
 // four 128-dim blocks), S in [256, 320) and [320, 384) (double buffer).
 #include "tc_common.cuh"
@@ -36,19 +39,23 @@ namespace {
 using namespace tc;
 
 constexpr int DA_TILE = 64;                     // positions per tile
-constexpr int DA_BOX = 64 * 128;                // one [64 rows x 64 bf16] box, bytes
+constexpr int DA_STAGES = 2;                    // tiles in flight
+constexpr int DA_QBOX = 64 * 128;               // one [64 heads x 64 bf16] query box, bytes
+constexpr int DA_BOX = DA_TILE * 128;           // one [32 rows x 64 bf16] cache box, bytes
 constexpr int DA_NBOX = LAT / 64;               // 9 boxes per 576-wide row block
-constexpr int DA_TILE_BYTES = DA_NBOX * DA_BOX;  // 73728
+constexpr int DA_Q_BYTES = DA_NBOX * DA_QBOX;    // 73728
+constexpr int DA_TILE_BYTES = DA_NBOX * DA_BOX;  // 36864
 constexpr int DA_THREADS = 224;
 constexpr int OFF_Q = 0;
-constexpr int OFF_C = OFF_Q + DA_TILE_BYTES;    // two stages
-constexpr int OFF_BAR = OFF_C + 2 * DA_TILE_BYTES;
-constexpr int OFF_MISC = OFF_BAR + 16 * 8;  // 13 barriers used
-constexpr int OFF_ALPHA = OFF_MISC + 16;
+constexpr int OFF_C = OFF_Q + DA_Q_BYTES;
+constexpr int OFF_BAR = OFF_C + DA_STAGES * DA_TILE_BYTES;
+constexpr int OFF_MISC = OFF_BAR + 24 * 8;  // 19 barriers used
+constexpr int OFF_ALPHA = OFF_MISC + 16;   // [2][HEADS] rescale factors, by tile parity
 constexpr int MAX_SEG = 96;                     // segments one CTA can hold
-constexpr int OFF_SEG = OFF_ALPHA + HEADS * 4;
+constexpr int OFF_SEG = OFF_ALPHA + 2 * HEADS * 4;
 constexpr int DA_SMEM = OFF_SEG + MAX_SEG * 12 + 16 + 1024;  // + slack for 1024-byte alignment
 constexpr uint32_t TM_O = 0, TM_S = 256;
+static_assert(DA_BOX == HEADS * DA_TILE * 2, "P (64 heads x DA_TILE bf16) must fill box 8");
 constexpr float RESCALE_LOG2 = 8.f;             // tolerated growth of p before rescaling O
 
 __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
@@ -60,15 +67,14 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* c_full = bars + 1;   // [2]
-  uint64_t* c_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;   // [2]
-  uint64_t* s_free = bars + 7;   // [2]
-  uint64_t* p_full = bars + 9;
-  uint64_t* o_done = bars + 10;
-  uint64_t* mma_idle = bars + 11;  // [2]: one per MMA-issuing thread
-  uint64_t* q_free = bars + 13;    // MMA1 finished with the segment's query block
-  uint64_t* o_free = bars + 14;    // the epilogue has read the segment's O^T
+  uint64_t* c_full = bars + 1;   // [DA_STAGES]
+  uint64_t* c_empty = bars + 5;  // [DA_STAGES]
+  uint64_t* s_full = bars + 9;   // [2]
+  uint64_t* s_free = bars + 11;  // [2]
+  uint64_t* p_full = bars + 13;  // [DA_STAGES]: P of the stage's tile is in box 8
+  uint64_t* mma_idle = bars + 17;  // [2]: one per MMA-issuing thread
+  uint64_t* q_free = bars + 19;    // MMA1 finished with the segment's query block
+  uint64_t* o_free = bars + 20;    // the epilogue has read the segment's O^T
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   int* s_nseg = reinterpret_cast<int*>(smem + OFF_MISC + 8);
@@ -78,38 +84,56 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
   pdl_launch_dependents();
-  pdl_wait();  // the query and the new cache row come from earlier kernels
-  if (threadIdx.x == 0) {
+  // The set-up below reads only the lengths, which no kernel of this decode step changes before
+  // the attention has finished, so it overlaps the tail of the previous kernel; the loads of
+  // the query and of the cache (whose new row an earlier kernel wrote) wait for it.
+  if (warp == 0) {
+    // This CTA's segments: the pieces of [r0, r1) in the concatenation of all sequences, found
+    // with a warp-wide prefix sum of the lengths, 32 sequences at a time.
     const long long r0 = decode_share_start(cta, G, P), r1 = decode_share_start(cta + 1, G, P);
-    long long acc = 0;
+    long long base = 0;
     int nseg = 0;
     bool bad = false;
-    for (int b = 0; b < B; ++b) {
-      const long long S = (long long)seq_lens[b] + 1;
-      if (S > cap) bad = true;
-      const long long lo = max(acc, r0), hi = min(acc + S, r1);
-      if (lo < hi) {
-        if (nseg < MAX_SEG) {
-          seg[3 * nseg] = b;
-          seg[3 * nseg + 1] = (int)(lo - acc);
-          seg[3 * nseg + 2] = (int)(hi - acc);
-        }
-        ++nseg;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      const int b = b0 + lane;
+      const long long S = b < B ? (long long)seq_lens[b] + 1 : 0;
+      long long inc = S;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += v;
       }
-      acc += S;
+      const long long acc = base + inc - S;  // first position of sequence b
+      const long long lo = max(acc, r0), hi = min(acc + S, r1);
+      const bool has = b < B && lo < hi;
+      const unsigned mask = __ballot_sync(0xffffffffu, has);
+      const int idx = nseg + __popc(mask & ((1u << lane) - 1u));
+      if (has && idx < MAX_SEG) {
+        seg[3 * idx] = b;
+        seg[3 * idx + 1] = (int)(lo - acc);
+        seg[3 * idx + 2] = (int)(hi - acc);
+      }
+      nseg += __popc(mask);
+      bad |= __any_sync(0xffffffffu, b < B && S > cap) != 0;
+      base += __shfl_sync(0xffffffffu, inc, 31);
     }
-    if (bad) atomicExch(err, DEV_ERR_RANGE);
-    if (acc != P || nseg > MAX_SEG) atomicExch(err, DEV_ERR_PLAN);
-    *s_nseg = (bad || acc != P || nseg > MAX_SEG) ? 0 : nseg;
+    if (lane == 0) {
+      if (bad) atomicExch(err, DEV_ERR_RANGE);
+      if (base != P || nseg > MAX_SEG) atomicExch(err, DEV_ERR_PLAN);
+      *s_nseg = (bad || base != P || nseg > MAX_SEG) ? 0 : nseg;
+    }
+  }
+  if (threadIdx.x == 32) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < DA_STAGES; ++i) {
       mbar_init(&c_full[i], 1);
       mbar_init(&c_empty[i], 1);
+      mbar_init(&p_full[i], 128);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 128);
     }
-    mbar_init(p_full, 128);
-    mbar_init(o_done, 1);
     mbar_init(&mma_idle[0], 1);
     mbar_init(&mma_idle[1], 1);
     mbar_init(q_free, 1);
@@ -127,6 +151,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
   const uint32_t tmem = *tmem_slot;
   const int nseg = *s_nseg;
   auto seg_tiles = [&](int sg) { return (seg[3 * sg + 2] - seg[3 * sg + 1] + DA_TILE - 1) / DA_TILE; };
+  pdl_wait();  // the query and the new cache row come from earlier kernels
 
   if (nseg > 0) {
     if (warp == 0) {
@@ -139,13 +164,14 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
         for (int sg = 0; ok && sg < nseg; ++sg) {
           const int b = seg[3 * sg], p0 = seg[3 * sg + 1], nt = seg_tiles(sg);
           if (sg > 0 && !(ok = mbar_wait(q_free, (sg - 1) & 1, err, abort_flag))) break;
-          mbar_expect_tx(q_full, DA_TILE_BYTES);
+          mbar_expect_tx(q_full, DA_Q_BYTES);
           for (int c = 0; c < DA_NBOX; ++c)
-            tma_load_2d(smem + OFF_Q + c * DA_BOX, &map_q, q_full, 64 * c, HEADS * b);
+            tma_load_2d(smem + OFF_Q + c * DA_QBOX, &map_q, q_full, 64 * c, HEADS * b);
           qloads = sg + 1;
           for (int i = 0; i < nt; ++i, ++t) {
-            const int st = t & 1;
-            if (t >= 2 && !(ok = mbar_wait(&c_empty[st], ((t - 2) >> 1) & 1, err, abort_flag)))
+            const int st = t % DA_STAGES;
+            if (t >= DA_STAGES &&
+                !(ok = mbar_wait(&c_empty[st], ((t / DA_STAGES) - 1) & 1, err, abort_flag)))
               break;
             mbar_expect_tx(&c_full[st], DA_TILE_BYTES);
             const int row = b * cap + p0 + DA_TILE * i;
@@ -158,13 +184,13 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
         // Never leave the CTA with copies in flight: wait (bounded) for the last ones.
         volatile int no_abort = 0;
         if (qloads > 0) mbar_wait(q_full, (qloads - 1) & 1, err, &no_abort);
-        for (int u = max(0, issued - 2); u < issued; ++u)
-          mbar_wait(&c_full[u & 1], (u >> 1) & 1, err, &no_abort);
+        for (int u = max(0, issued - DA_STAGES); u < issued; ++u)
+          mbar_wait(&c_full[u % DA_STAGES], (u / DA_STAGES) & 1, err, &no_abort);
       }
     } else if (warp == 1) {
       // ---------------------------------------------------------------- MMA1 issuer
       if (lane == 0) {
-        constexpr uint32_t idesc_s = idesc_bf16(64, 64, false, false);
+        constexpr uint32_t idesc_s = idesc_bf16(64, DA_TILE, false, false);
         const uint32_t qb = sbase + OFF_Q;
         bool ok = true;
         int t = 0;
@@ -172,9 +198,9 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
           const int nt = seg_tiles(sg);
           if (!(ok = mbar_wait(q_full, sg & 1, err, abort_flag))) break;
           for (int i = 0; i < nt; ++i, ++t) {
-            const int st = t & 1;
-            ok = mbar_wait(&c_full[st], (t >> 1) & 1, err, abort_flag);
-            if (ok && t >= 2) ok = mbar_wait(&s_free[st], ((t - 2) >> 1) & 1, err, abort_flag);
+            const int st = t % DA_STAGES, sb = t & 1;
+            ok = mbar_wait(&c_full[st], (t / DA_STAGES) & 1, err, abort_flag);
+            if (ok && t >= 2) ok = mbar_wait(&s_free[sb], ((t - 2) >> 1) & 1, err, abort_flag);
             if (!ok) break;
             fence_after();
             const uint32_t cb = sbase + OFF_C + st * DA_TILE_BYTES;
@@ -182,11 +208,11 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
             for (int c = 0; c < DA_NBOX; ++c)
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                const uint64_t a = sdesc_sw128(qb + c * DA_BOX + k * 32, 16, 1024);
+                const uint64_t a = sdesc_sw128(qb + c * DA_QBOX + k * 32, 16, 1024);
                 const uint64_t bd = sdesc_sw128(cb + c * DA_BOX + k * 32, 16, 1024);
-                mma_bf16(tmem + TM_S + 64 * st, a, bd, idesc_s, (c | k) != 0);
+                mma_bf16(tmem + TM_S + DA_TILE * sb, a, bd, idesc_s, (c | k) != 0);
               }
-            mma_commit(&s_full[st]);
+            mma_commit(&s_full[sb]);
           }
           mma_commit(q_free);  // the query block may be replaced once these MMAs are done
         }
@@ -205,21 +231,21 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
           const int nt = seg_tiles(sg);
           if (sg > 0 && !(ok = mbar_wait(o_free, (sg - 1) & 1, err, abort_flag))) break;
           for (int i = 0; i < nt; ++i, ++t) {
-            const int st = t & 1;
-            if (!(ok = mbar_wait(p_full, t & 1, err, abort_flag))) break;
+            const int st = t % DA_STAGES;
+            if (!(ok = mbar_wait(&p_full[st], (t / DA_STAGES) & 1, err, abort_flag))) break;
             fence_after();
             const uint32_t cb = sbase + OFF_C + st * DA_TILE_BYTES;
 #pragma unroll
             for (int d = 0; d < 4; ++d)
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
+              for (int k = 0; k < DA_TILE / 16; ++k) {
                 // A = C^T: MN-major, 128 latent dims (2 boxes, DA_BOX apart) x 16 positions.
                 const uint64_t a = sdesc_sw128(cb + 2 * d * DA_BOX + k * 2048, DA_BOX, 1024);
+                // B = P: K-major, 64 heads x 16 positions (rows of 128 B, 128-byte swizzle).
                 const uint64_t bd = sdesc_sw128(cb + 8 * DA_BOX + k * 32, 16, 1024);
                 mma_bf16(tmem + TM_O + 64 * d, a, bd, idesc_o, (i > 0) || (k > 0));
               }
-            mma_commit(o_done);
-            mma_commit(&c_empty[st]);
+            mma_commit(&c_empty[st]);  // also tells the softmax warps that MMA2(t) is done
           }
         }
         mma_commit(&mma_idle[1]);
@@ -228,9 +254,13 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
       }
     } else if (warp >= 2 && warp <= 5) {
       // ---------------------------------------------------------------- softmax warps
+      // S rows (heads) of an M=64 accumulator sit in lanes 0..15 of each 32-lane quarter.  The
+      // 16x64b load spreads such a quarter over the whole warp: thread `lane` reads row
+      // lane/4 + 8*(lane%2) of the quarter and the columns of parity (lane/2)%2, so every
+      // head is shared by two threads (lanes l and l^2), each holding 32 of its 64 scores.
       const int q = warp & 3;                 // tensor-memory lane quarter of this warp
-      const int h = 16 * q + lane;            // head of this thread's S row (lanes 0..15)
-      const bool own = lane < 16;
+      const int h = 16 * q + (lane >> 2) + 8 * (lane & 1);  // head of this thread's S row
+      const int par = (lane >> 1) & 1;        // this thread's column parity
       const int tid = threadIdx.x - 64;       // 0..127
       const uint32_t lane_off = (uint32_t)(32 * q) << 16;
       bool ok = true;
@@ -238,27 +268,27 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
       for (int sg = 0; ok && sg < nseg; ++sg) {
         const int b = seg[3 * sg], p0 = seg[3 * sg + 1], p1 = seg[3 * sg + 2];
         const int nt = seg_tiles(sg);
-        float m = -INFINITY, l = 0.f;
+        float m = -INFINITY, l = 0.f;         // running maximum; this thread's half of the sum
         for (int i = 0; i < nt; ++i, ++t) {
-          const int st = t & 1;
-          if (!(ok = mbar_wait(&s_full[st], (t >> 1) & 1, err, abort_flag))) break;
+          const int st = t % DA_STAGES, sb = t & 1;
+          if (!(ok = mbar_wait(&s_full[sb], (t >> 1) & 1, err, abort_flag))) break;
           fence_after();
-          uint32_t r[2][32];
-          tmem_ld32(tmem + lane_off + TM_S + 64 * st, r[0]);
-          tmem_ld32(tmem + lane_off + TM_S + 64 * st + 32, r[1]);
+          uint32_t r[32];                     // r[j] = S[h][2j + par]
+          tmem_ld16x64b_x32(tmem + lane_off + TM_S + DA_TILE * sb, r);
           tmem_wait_ld();
           fence_before();
-          mbar_arrive(&s_free[st]);
+          mbar_arrive(&s_free[sb]);
           const int n = min(DA_TILE, p1 - (p0 + DA_TILE * i));
           float tmax = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const float sc = (j < n) ? __uint_as_float(r[j >> 5][j & 31]) * scale_log2 : -INFINITY;
-            r[j >> 5][j & 31] = __float_as_uint(sc);
+          for (int j = 0; j < 32; ++j) {
+            const float sc = (2 * j + par < n) ? __uint_as_float(r[j]) * scale_log2 : -INFINITY;
+            r[j] = __float_as_uint(sc);
             tmax = fmaxf(tmax, sc);
           }
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
           bool need = false;
-          if (own) {
+          {
             float alpha = 1.f;
             if (tmax > m + RESCALE_LOG2) {
               if (m != -INFINITY) {
@@ -268,27 +298,41 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
               l *= alpha;
               m = tmax;
             }
-            s_alpha[h] = alpha;
+            if (par == 0) s_alpha[HEADS * sb + h] = alpha;
           }
-          uint32_t pk[32];
+          // p = 2^(s - m) rounded to bf16 (the MMA's operand type; l sums the rounded values).
+          uint32_t pb[16];                    // bf16 bits of this thread's 32 values, 2 per word
           float lsum = 0.f;
 #pragma unroll
-          for (int j = 0; j < 64; j += 2) {
-            const float a = exp2f(__uint_as_float(r[j >> 5][j & 31]) - m);
-            const float c = exp2f(__uint_as_float(r[(j + 1) >> 5][(j + 1) & 31]) - m);
-            __nv_bfloat162 pr = __floats2bfloat162_rn(a, c);
+          for (int j = 0; j < 32; j += 2) {
+            __nv_bfloat162 pr = __floats2bfloat162_rn(exp2f(__uint_as_float(r[j]) - m),
+                                                      exp2f(__uint_as_float(r[j + 1]) - m));
             lsum += __low2float(pr) + __high2float(pr);
-            pk[j >> 1] = *reinterpret_cast<uint32_t*>(&pr);
+            pb[j >> 1] = *reinterpret_cast<uint32_t*>(&pr);
           }
           l += lsum;
+          // Trade halves with the partner so that the even-column thread owns columns 0..31 and
+          // the odd-column thread columns 32..63: the even thread sends its values of columns
+          // 32..62, the odd thread its values of columns 1..31.
+          uint32_t pk[16];                    // bf16x2 of columns (2w, 2w+1) of this thread's half
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            const uint32_t send = par ? pb[w] : pb[8 + w];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
+            // send/recv carry two values: word w holds elements 2w and 2w+1 of a half.
+            const uint32_t mine = par ? pb[8 + w] : pb[w];
+            const uint32_t ev = par ? recv : mine, od = par ? mine : recv;  // even / odd cols
+            pk[2 * w] = (ev & 0xFFFFu) | (od << 16);
+            pk[2 * w + 1] = (ev >> 16) | (od & 0xFFFF0000u);
+          }
           // Box 8 (rotary dims) of this stage was last read by this tile's MMA1 and by MMA2 of
           // tile t-2, both complete (the stage was refilled for tile t after the latter).
           uint8_t* cst = smem + OFF_C + st * DA_TILE_BYTES;
-          if (own) {  // P row h: 64 bf16 = 8 chunks of 16 B, 128-byte swizzle, in box 8
+          {  // P row h: 64 bf16 = 8 chunks of 16 B, 128-byte swizzle; this thread's 4 chunks
             uint8_t* prow = cst + 8 * DA_BOX + h * 128;
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) * 16)) =
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<uint4*>(prow + (((4 * par + c) ^ (h & 7)) * 16)) =
                   make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
           }
           if (n < DA_TILE) {  // rows past the segment end must not reach MMA2 as NaN/Inf
@@ -299,10 +343,14 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
                   make_uint4(0, 0, 0, 0);
             }
           }
-          // MMA2 of the previous tile must be complete before O^T may be rescaled, and every
-          // o_done phase is consumed here, in order, before this tile's MMA2 can be issued.
-          if (t >= 1 && !(ok = mbar_wait(o_done, (t - 1) & 1, err, abort_flag))) break;
+          // O^T may only be rescaled once MMA2 of the previous tile is complete; its commit on
+          // that tile's stage barrier says so.  Without a rescale, this tile's MMA2 simply
+          // queues behind the previous one, so the tiles do not wait on each other.  (That
+          // barrier's next phase needs this warpgroup's P of tile t+3, so it cannot run ahead.)
           if (named_bar_or(1, 128, need)) {
+            if (!(ok = mbar_wait(&c_empty[(t - 1) % DA_STAGES], ((t - 1) / DA_STAGES) & 1, err,
+                                 abort_flag)))
+              break;
             fence_after();
 #pragma unroll
             for (int d = 0; d < 4; ++d)
@@ -314,16 +362,18 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
-                  o[e] = __float_as_uint(__uint_as_float(o[e]) * s_alpha[32 * hh + e]);
+                  o[e] = __float_as_uint(__uint_as_float(o[e]) * s_alpha[HEADS * sb + 32 * hh + e]);
                 tmem_st32(ta, o);
               }
             tmem_wait_st();
           }
           fence_proxy_async();
           fence_before();
-          mbar_arrive(p_full);
+          mbar_arrive(&p_full[st]);
         }
-        if (!ok || !(ok = mbar_wait(o_done, (t - 1) & 1, err, abort_flag))) break;
+        if (!ok || !(ok = mbar_wait(&c_empty[(t - 1) % DA_STAGES], ((t - 1) / DA_STAGES) & 1, err,
+                                    abort_flag)))
+          break;
         // Segment epilogue: unnormalised O^T, m and l of every head into slot b + cta.
         fence_after();
         const size_t slot = (size_t)b + cta;
@@ -331,19 +381,18 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
 #pragma unroll
         for (int d = 0; d < 4; ++d) {
           const int dim = 128 * d + 32 * q + lane;
+          uint32_t o[2][32];
+          tmem_ld32(tmem + lane_off + TM_O + 64 * d, o[0]);
+          tmem_ld32(tmem + lane_off + TM_O + 64 * d + 32, o[1]);
+          tmem_wait_ld();
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_off + TM_O + 64 * d + 32 * hh, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              op[(size_t)(32 * hh + e) * KV_LORA + dim] = __uint_as_float(o[e]);
-          }
+          for (int e = 0; e < 64; ++e)
+            op[(size_t)e * KV_LORA + dim] = __uint_as_float(o[e >> 5][e & 31]);
         }
-        if (own) {
+        const float lrow = l + __shfl_xor_sync(0xffffffffu, l, 2);
+        if (par == 0) {
           ml_part[(slot * HEADS + h) * 2] = m;
-          ml_part[(slot * HEADS + h) * 2 + 1] = l;
+          ml_part[(slot * HEADS + h) * 2 + 1] = lrow;
         }
         fence_before();
         mbar_arrive(o_free);
@@ -401,7 +450,7 @@ cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bf
   if (plan.B == 0) return cudaSuccess;
   CUtensorMap mq, mc;
   if (!make_tmap_2d(&mq, true, qfull, LAT, (uint64_t)plan.B * HEADS, LAT * 2, 64, 64) ||
-      !make_tmap_2d(&mc, true, cache, LAT, (uint64_t)plan.B * cap, LAT * 2, 64, 64))
+      !make_tmap_2d(&mc, true, cache, LAT, (uint64_t)plan.B * cap, LAT * 2, 64, DA_TILE))
     return cudaErrorInvalidValue;
   return launch_kernel(decode_attn_tc_kernel, dim3(plan.G), dim3(DA_THREADS), DA_SMEM, st, pdl,
                        mq, mc, seq_lens, plan.B, cap, plan.G, plan.P,

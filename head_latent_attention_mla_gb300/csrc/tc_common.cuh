@@ -148,6 +148,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       MLA_W8(0), MLA_W8(8), MLA_W8(16), MLA_W8(24)
       : "memory");
 }
+// 16 lanes x 64 columns of 32-bit values spread over a warp (the rows of an M=64 accumulator
+// in one lane quarter): thread t gets lane (base + t/4 + 8*(t%2)), columns 2j + (t/2)%2 for
+// j = 0..31, in r[j].
+__device__ __forceinline__ void tmem_ld16x64b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x64b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : MLA_R8(0), MLA_R8(8), MLA_R8(16), MLA_R8(24)
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
