@@ -28,6 +28,7 @@
 //               maximum m and the sum l of every head.
 // A tile's MMA2 does not wait for the previous tile's: only a rescale of O^T needs the previous
 // MMA2 to be complete, and it is rare once a head's maximum has settled.
+// Partial outputs: o_part[slot][dim][head] = O / l (fp16), ml_part[slot][head] = (m, l).
 // Tensor memory: O^T in columns [0, 256) (lane = latent dim, column = head within each of the
 // four 128-dim blocks), S in [256, 320) and [320, 384) (double buffer).
 #include "tc_common.cuh"
@@ -51,17 +52,25 @@ constexpr int OFF_C = OFF_Q + DA_Q_BYTES;
 constexpr int OFF_BAR = OFF_C + DA_STAGES * DA_TILE_BYTES;
 constexpr int OFF_MISC = OFF_BAR + 24 * 8;  // 19 barriers used
 constexpr int OFF_ALPHA = OFF_MISC + 16;   // [2][HEADS] rescale factors, by tile parity
+constexpr int OFF_INVL = OFF_ALPHA + 2 * HEADS * 4;  // [HEADS] 1 / l of the finished segment
 constexpr int MAX_SEG = 96;                     // segments one CTA can hold
-constexpr int OFF_SEG = OFF_ALPHA + 2 * HEADS * 4;
+constexpr int OFF_SEG = OFF_INVL + HEADS * 4;
 constexpr int DA_SMEM = OFF_SEG + MAX_SEG * 12 + 16 + 1024;  // + slack for 1024-byte alignment
 constexpr uint32_t TM_O = 0, TM_S = 256;
 static_assert(DA_BOX == HEADS * DA_TILE * 2, "P (64 heads x DA_TILE bf16) must fill box 8");
 constexpr float RESCALE_LOG2 = 8.f;             // tolerated growth of p before rescaling O
 
+// Eight consecutive 32-bit words to global memory in one 32-byte store (dst 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
     const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_c,
     const int* __restrict__ seq_lens, int B, int cap, int G, long long P, float scale_log2,
-    float* __restrict__ o_part, float* __restrict__ ml_part, int* err) {
+    __half* __restrict__ o_part, float* __restrict__ ml_part, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
@@ -79,6 +88,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   int* s_nseg = reinterpret_cast<int*>(smem + OFF_MISC + 8);
   float* s_alpha = reinterpret_cast<float*>(smem + OFF_ALPHA);
+  float* s_invl = reinterpret_cast<float*>(smem + OFF_INVL);
   int* seg = reinterpret_cast<int*>(smem + OFF_SEG);  // [MAX_SEG][3]: b, first, end
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -374,28 +384,44 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
         if (!ok || !(ok = mbar_wait(&c_empty[(t - 1) % DA_STAGES], ((t - 1) / DA_STAGES) & 1, err,
                                     abort_flag)))
           break;
-        // Segment epilogue: unnormalised O^T, m and l of every head into slot b + cta.
+        // Segment epilogue: O / l, m and l of every head into slot b + cta.  The partial is
+        // divided by its own sum, so its values are bounded by those of the cache rows, and
+        // stored as fp16 (11-bit mantissa), head-minor ([dim][head]): a thread writes the 64
+        // heads of its latent dimension (its TMEM lane) as four 32-byte vectors.
+        const float lrow = l + __shfl_xor_sync(0xffffffffu, l, 2);
+        if (par == 0) {
+          s_invl[h] = 1.f / lrow;
+          ml_part[((size_t)b + cta) * HEADS * 2 + 2 * h] = m;
+          ml_part[((size_t)b + cta) * HEADS * 2 + 2 * h + 1] = lrow;
+        }
+        named_bar(1, 128);
         fence_after();
         const size_t slot = (size_t)b + cta;
-        float* op = o_part + slot * HEADS * KV_LORA;
-#pragma unroll
+        __half* op = o_part + slot * HEADS * KV_LORA;
+#pragma unroll 1
         for (int d = 0; d < 4; ++d) {
           const int dim = 128 * d + 32 * q + lane;
           uint32_t o[2][32];
           tmem_ld32(tmem + lane_off + TM_O + 64 * d, o[0]);
           tmem_ld32(tmem + lane_off + TM_O + 64 * d + 32, o[1]);
           tmem_wait_ld();
+          uint32_t pk[32];
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
-            op[(size_t)e * KV_LORA + dim] = __uint_as_float(o[e >> 5][e & 31]);
-        }
-        const float lrow = l + __shfl_xor_sync(0xffffffffu, l, 2);
-        if (par == 0) {
-          ml_part[(slot * HEADS + h) * 2] = m;
-          ml_part[(slot * HEADS + h) * 2 + 1] = lrow;
+          for (int e = 0; e < 32; ++e) {
+            const int hh = 2 * e;
+            __half2 v = __floats2half2_rn(__uint_as_float(o[hh >> 5][hh & 31]) * s_invl[hh],
+                                          __uint_as_float(o[(hh + 1) >> 5][(hh + 1) & 31]) *
+                                              s_invl[hh + 1]);
+            pk[e] = *reinterpret_cast<uint32_t*>(&v);
+          }
+          __half* dst = op + (size_t)dim * HEADS;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) st_global_v8(dst + 16 * v, &pk[8 * v]);
         }
         fence_before();
         mbar_arrive(o_free);
+        // Every thread has read s_invl before the next segment's epilogue rewrites it: that
+        // epilogue is at least one tile (and its named barrier) away.
       }
     }
   }
@@ -445,7 +471,7 @@ cudaError_t init_decode_tc_kernel() {
 
 cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bfloat16* cache,
                                        int cap, const int* seq_lens, DecodePlan plan,
-                                       float scale, float* o_part, float* ml_part, int* err,
+                                       float scale, __half* o_part, float* ml_part, int* err,
                                        cudaStream_t st, bool pdl) {
   if (plan.B == 0) return cudaSuccess;
   CUtensorMap mq, mc;

@@ -69,7 +69,7 @@ Layout decode_layout(const mla_ctx* c, int B) {
   L.cq = take((size_t)B * Q_LORA * 2);
   L.q = take((size_t)B * QB_N * 2);
   L.qfull = take((size_t)B * HEADS * LAT * 2);
-  L.opart = take(items * HEADS * KV_LORA * 4);
+  L.opart = take(items * HEADS * KV_LORA * 2);
   L.ml = take(items * HEADS * 2 * 4);
   L.olat = take((size_t)B * HEADS * KV_LORA * 2);
   L.attn = take((size_t)B * O_IN * 2);
@@ -334,7 +334,7 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
   __nv_bfloat16* cq = at<__nv_bfloat16>(ws, L.cq);
   __nv_bfloat16* q = at<__nv_bfloat16>(ws, L.q);
   __nv_bfloat16* qfull = at<__nv_bfloat16>(ws, L.qfull);
-  float* opart = at<float>(ws, L.opart);
+  __half* opart = at<__half>(ws, L.opart);
   float* ml = at<float>(ws, L.ml);
   __nv_bfloat16* olat = at<__nv_bfloat16>(ws, L.olat);
   __nv_bfloat16* attn = at<__nv_bfloat16>(ws, L.attn);

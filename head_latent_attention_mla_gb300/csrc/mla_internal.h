@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -130,15 +131,18 @@ __host__ __device__ inline int decode_share_of(long long pos, int G, long long P
 // Partial slots used by a plan: sequence b's share in CTA c goes to slot b + c.
 inline int decode_slots(const DecodePlan& p) { return p.B + p.G; }
 // The plan for B sequences holding P positions in total, on num_sms SMs, with at most
-// max_slots partial slots: about one share per SM, at least 64 positions per share.
+// max_slots partial slots: about one share per SM (at most kMaxDecodeShares), at least 64
+// positions per share.
+constexpr int kMaxDecodeShares = 160;  // the combine kernel's bound on shares per sequence
 inline DecodePlan make_decode_plan(int B, long long P, int num_sms, int max_slots) {
   long long G = (P + 63) / 64;
   if (G > num_sms) G = num_sms;
+  if (G > kMaxDecodeShares) G = kMaxDecodeShares;
   if (G > max_slots - B) G = max_slots - B;
   if (G < 1) G = 1;
   return DecodePlan{B, (int)G, P};
 }
-cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const float* o_part,
+cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const __half* o_part,
                                   const float* ml_part, __nv_bfloat16* o_lat, int* err,
                                   cudaStream_t st, bool pdl = false);
 
@@ -146,7 +150,7 @@ cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const fl
 // accumulators in tensor memory): per work item, unnormalised partial outputs and (m, l).
 cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bfloat16* cache,
                                        int cap, const int* seq_lens, DecodePlan plan,
-                                       float scale, float* o_part, float* ml_part, int* err,
+                                       float scale, __half* o_part, float* ml_part, int* err,
                                        cudaStream_t st, bool pdl = false);
 cudaError_t init_decode_tc_kernel();
 

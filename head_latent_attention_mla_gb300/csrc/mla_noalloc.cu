@@ -47,7 +47,7 @@ constexpr Regions regions(int B) {
   r.cq = off;    off += up256((size_t)B * Q_LORA * 2);
   r.q = off;     off += up256((size_t)B * QB_N * 2);
   r.qfull = off; off += up256((size_t)B * HEADS * LAT * 2);
-  r.opart = off; off += up256((size_t)kMaxItems * HEADS * KV_LORA * 4);
+  r.opart = off; off += up256((size_t)kMaxItems * HEADS * KV_LORA * 2);
   r.ml = off;    off += up256((size_t)kMaxItems * HEADS * 2 * 4);
   r.olat = off;  off += up256((size_t)B * HEADS * KV_LORA * 2);
   r.attn = off;  off += up256((size_t)B * O_IN * 2);
@@ -110,7 +110,7 @@ extern "C" mla_status mla_decode_noalloc(mla_ctx* c, const void* x, int B, void*
   __nv_bfloat16* cq = reinterpret_cast<__nv_bfloat16*>(w + R.cq);
   __nv_bfloat16* q = reinterpret_cast<__nv_bfloat16*>(w + R.q);
   __nv_bfloat16* qfull = reinterpret_cast<__nv_bfloat16*>(w + R.qfull);
-  float* opart = reinterpret_cast<float*>(w + R.opart);
+  __half* opart = reinterpret_cast<__half*>(w + R.opart);
   float* ml = reinterpret_cast<float*>(w + R.ml);
   __nv_bfloat16* olat = reinterpret_cast<__nv_bfloat16*>(w + R.olat);
   __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(w + R.attn);
