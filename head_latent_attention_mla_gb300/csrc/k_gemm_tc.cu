@@ -10,15 +10,21 @@
 // so that both MMA operands are e4m3 and the weights feed the tensor cores exactly as stored:
 // two kind::f8f6f4 MMAs (hi, then lo) cost what one bf16 MMA would, and no weight conversion
 // is needed.  The weight is the 128-row MMA operand (D^T[n, m] = W . X^T), so any token count
-// works with N = BN tokens per MMA.  One CTA owns 128 output features (one scale row block) and
-// BN tokens over a run of 128-wide k blocks (split-K when the grid would otherwise be small):
+// works with N = BN tokens per MMA.
+//
+// Persistent kernel, one CTA per SM.  The work is cut into units (128 output features = one
+// scale row block) x (BN tokens) x (a run of 128-wide k blocks; split-K when there are few
+// tiles), and each CTA walks units c, c + G, ... with its pipelines running across unit
+// boundaries:
 //   warp 0      TMA producer: weight tile [128 x 128] and hi/lo token tiles [BN x 128] into a
 //               four-stage ring (128-byte swizzle);
 //   warp 1      allocates tensor memory; one thread issues 4 x 2 MMAs (K=32) per k block into
-//               one of two accumulators;
-//   warps 2..5  epilogue: per k block, read the accumulator (lane = feature n) and add it,
-//               times that block's scale, to fp32 registers; finally multiply by the token's
-//               sx and store Y[m, n] (or an fp32 split-K partial).
+//               one of four accumulators;
+//   warps 2..9  epilogue, two warpgroups each owning half of the BN token columns: per k
+//               block, read the accumulator (lane = feature n), release it, and add it, times
+//               that block's scale, to fp32 registers; at the end of a unit multiply by the
+//               token's sx and store Y[m, n] (or an fp32 split-K partial) while the MMAs of the
+//               next unit already run.
 // Each k block starts a fresh accumulator, so the weight's block scales are applied exactly.
 #include "tc_common.cuh"
 
@@ -28,8 +34,9 @@ namespace {
 
 using namespace tc;
 
-constexpr int GT_THREADS = 192;
+constexpr int GT_THREADS = 320;
 constexpr int GT_STAGES = 4;
+constexpr int GT_NACC = 4;                     // tensor-memory accumulators
 constexpr int W_TILE = 128 * 128;              // e4m3 bytes of one weight tile
 constexpr float E4M3_MAX = 448.f;
 
@@ -40,14 +47,18 @@ struct GemmSmem {
   static constexpr int OFF_IN = 0;
   static constexpr int OFF_BAR = OFF_IN + GT_STAGES * STAGE;
   static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
-  static constexpr int OFF_SCALE = OFF_MISC + 16;
-  static constexpr int OFF_SX = OFF_SCALE + 64 * 4;
-  static constexpr int BYTES = OFF_SX + BN * 4 + 1024;
+  static constexpr int BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int NGRP = BN >= 64 ? 2 : 1;  // epilogue warpgroups
+  static constexpr int CW = BN / NGRP;           // token columns per epilogue thread
+  static constexpr uint32_t TMEM_COLS = GT_NACC * BN < 32 ? 32 : GT_NACC * BN;
 };
 
 struct GemmTcArgs {
   int M, K;
   int n_tiles0;          // n tiles of problem 0
+  int n_tiles;           // n tiles of both problems
+  int m_tiles;
+  int units;             // n_tiles * m_tiles * splits
   int N[2];
   const float* S[2];     // weight block scales
   void* Y[2];
@@ -59,6 +70,27 @@ struct GemmTcArgs {
   int ldp;               // total N of both problems (partial row stride)
   int* err;
 };
+
+// Unit u: split fastest, then m tile, then n tile (CTAs running at the same time share weight
+// tiles through L2).
+struct Unit {
+  int prob, n0, m0, split, kb_begin, kb_end;
+};
+__device__ __forceinline__ Unit unit_of(const GemmTcArgs& a, int u, int BN) {
+  Unit r;
+  r.split = u % a.splits;
+  const int t = u / a.splits;
+  const int mt = t % a.m_tiles;
+  int nt = t / a.m_tiles;
+  r.prob = nt < a.n_tiles0 ? 0 : 1;
+  if (r.prob) nt -= a.n_tiles0;
+  r.n0 = nt * 128;
+  r.m0 = mt * BN;
+  const int nkb = a.K / BLK;
+  r.kb_begin = (int)((long)nkb * r.split / a.splits);
+  r.kb_end = (int)((long)nkb * (r.split + 1) / a.splits);
+  return r;
+}
 
 // One CTA per token row: sx = amax/448 (1 for an all-zero row), hi = e4m3(x/sx),
 // lo = e4m3(x/sx - hi), both rounded to nearest even with saturation.
@@ -123,152 +155,153 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
-  uint64_t* in_full = bars;                    // [4]  TMA transaction bytes
-  uint64_t* in_empty = bars + GT_STAGES;       // [4]  MMA commit
-  uint64_t* acc_full = bars + 2 * GT_STAGES;   // [2]  MMA commit
-  uint64_t* acc_empty = acc_full + 2;          // [2]  128 epilogue threads
-  uint64_t* mma_idle = acc_empty + 2;
+  uint64_t* in_full = bars;                        // [GT_STAGES]  TMA transaction bytes
+  uint64_t* in_empty = bars + GT_STAGES;           // [GT_STAGES]  MMA commit
+  uint64_t* acc_full = bars + 2 * GT_STAGES;       // [GT_NACC]    MMA commit
+  uint64_t* acc_empty = acc_full + GT_NACC;        // [GT_NACC]    epilogue threads
+  uint64_t* mma_idle = acc_empty + GT_NACC;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
-  float* s_scale = reinterpret_cast<float*>(smem + L::OFF_SCALE);
-  float* s_sx = reinterpret_cast<float*>(smem + L::OFF_SX);
-  constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int nt = blockIdx.x;
-  const int prob = nt < args.n_tiles0 ? 0 : 1;
-  if (prob) nt -= args.n_tiles0;
-  const int n0 = nt * 128, m0 = blockIdx.y * BN;
   const int nkb_all = args.K / BLK;
-  const int split = blockIdx.z;
-  const int kb_begin = (int)((long)nkb_all * split / args.splits);
-  const int kb_end = (int)((long)nkb_all * (split + 1) / args.splits);
-  const int nkb = kb_end - kb_begin;
-  const CUtensorMap* map_w = prob ? &map_w1 : &map_w0;
-  const float* scales = prob ? args.S[1] : args.S[0];
+  int* err = args.err;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < GT_STAGES; ++i) {
       mbar_init(&in_full[i], 1);
       mbar_init(&in_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < GT_NACC; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 128);
+      mbar_init(&acc_empty[i], 128 * L::NGRP);
     }
     mbar_init(mma_idle, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (threadIdx.x < 64 && threadIdx.x < nkb)
-    s_scale[threadIdx.x] = scales[(size_t)(n0 / BLK) * nkb_all + kb_begin + threadIdx.x];
-  for (int j = threadIdx.x; j < BN; j += GT_THREADS)
-    s_sx[j] = (m0 + j < args.M) ? args.sx[m0 + j] : 0.f;
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
     tmem_relinquish();
   }
   fence_before();
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  int* err = args.err;
 
-  if (nkb > 0) {
-    if (warp == 0) {
-      // ------------------------------------------------------------------ TMA producer
-      if (lane == 0) {
-        tma_prefetch_desc(map_w);
-        tma_prefetch_desc(&map_hi);
-        tma_prefetch_desc(&map_lo);
-        int issued = 0;
-        for (int i = 0; i < nkb; ++i) {
+  if (warp == 0) {
+    // -------------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&map_w0);
+      tma_prefetch_desc(&map_w1);
+      tma_prefetch_desc(&map_hi);
+      tma_prefetch_desc(&map_lo);
+      int i = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+        const Unit U = unit_of(args, u, BN);
+        const CUtensorMap* map_w = U.prob ? &map_w1 : &map_w0;
+        for (int kb = U.kb_begin; kb < U.kb_end; ++kb, ++i) {
           const int st = i % GT_STAGES;
           if (i >= GT_STAGES &&
-              !mbar_wait(&in_empty[st], ((i - GT_STAGES) / GT_STAGES) & 1, err, abort_flag))
+              !(ok = mbar_wait(&in_empty[st], ((i / GT_STAGES) - 1) & 1, err, abort_flag)))
             break;
           uint8_t* stg = smem + L::OFF_IN + st * L::STAGE;
-          const int k0 = (kb_begin + i) * BLK;
+          const int k0 = kb * BLK;
           mbar_expect_tx(&in_full[st], L::STAGE);
-          tma_load_2d(stg, map_w, &in_full[st], k0, n0);
-          tma_load_2d(stg + W_TILE, &map_hi, &in_full[st], k0, m0);
-          tma_load_2d(stg + W_TILE + L::X_TILE, &map_lo, &in_full[st], k0, m0);
-          issued = i + 1;
+          tma_load_2d(stg, map_w, &in_full[st], k0, U.n0);
+          tma_load_2d(stg + W_TILE, &map_hi, &in_full[st], k0, U.m0);
+          tma_load_2d(stg + W_TILE + L::X_TILE, &map_lo, &in_full[st], k0, U.m0);
         }
-        volatile int no_abort = 0;
-        for (int i = max(0, issued - GT_STAGES); i < issued; ++i)
-          mbar_wait(&in_full[i % GT_STAGES], (i / GT_STAGES) & 1, err, &no_abort);
       }
-    } else if (warp == 1) {
-      // ------------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        constexpr uint32_t idesc = idesc_e4m3(128, BN);
-        for (int i = 0; i < nkb; ++i) {
-          const int st = i % GT_STAGES, ab = i & 1;
-          if (!mbar_wait(&in_full[st], (i / GT_STAGES) & 1, err, abort_flag)) break;
-          if (i >= 2 && !mbar_wait(&acc_empty[ab], ((i - 2) >> 1) & 1, err, abort_flag)) break;
+      // Never leave the CTA with copies in flight: wait (bounded) for the last ones.
+      volatile int no_abort = 0;
+      for (int j = max(0, i - GT_STAGES); j < i; ++j)
+        mbar_wait(&in_full[j % GT_STAGES], (j / GT_STAGES) & 1, err, &no_abort);
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3(128, BN);
+      int i = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+        const Unit U = unit_of(args, u, BN);
+        for (int kb = U.kb_begin; kb < U.kb_end; ++kb, ++i) {
+          const int st = i % GT_STAGES, ab = i % GT_NACC;
+          if (!(ok = mbar_wait(&in_full[st], (i / GT_STAGES) & 1, err, abort_flag))) break;
+          if (i >= GT_NACC &&
+              !(ok = mbar_wait(&acc_empty[ab], ((i / GT_NACC) - 1) & 1, err, abort_flag)))
+            break;
           fence_after();
           const uint32_t w_base = sbase + L::OFF_IN + st * L::STAGE;
+          const uint64_t a0 = sdesc_sw128(w_base, 16, 1024);
+          const uint64_t h0 = sdesc_sw128(w_base + W_TILE, 16, 1024);
+          const uint64_t l0 = sdesc_sw128(w_base + W_TILE + L::X_TILE, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t a = sdesc_sw128(w_base + k * 32, 16, 1024);
-            const uint64_t bh = sdesc_sw128(w_base + W_TILE + k * 32, 16, 1024);
-            const uint64_t bl = sdesc_sw128(w_base + W_TILE + L::X_TILE + k * 32, 16, 1024);
-            mma_e4m3(tmem + ab * BN, a, bh, idesc, k > 0);
-            mma_e4m3(tmem + ab * BN, a, bl, idesc, true);
+          for (int k = 0; k < 4; ++k) {  // descriptor address field counts 16-byte units
+            mma_e4m3(tmem + ab * BN, a0 + 2 * k, h0 + 2 * k, idesc, k > 0);
+            mma_e4m3(tmem + ab * BN, a0 + 2 * k, l0 + 2 * k, idesc, true);
           }
           mma_commit(&acc_full[ab]);
           mma_commit(&in_empty[st]);
         }
-        mma_commit(mma_idle);
-        volatile int no_abort = 0;
-        mbar_wait(mma_idle, 0, err, &no_abort);
       }
-    } else {
-      // ------------------------------------------------------------------ epilogue
-      const int q = warp & 3;
-      const int n = n0 + 32 * q + lane;
-      const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-      float acc[BN];
+      mma_commit(mma_idle);
+      volatile int no_abort = 0;
+      mbar_wait(mma_idle, 0, err, &no_abort);
+    }
+  } else if ((warp - 2) / 4 < L::NGRP) {
+    // -------------------------------------------------------------------- epilogue
+    constexpr int CW = L::CW;
+    const int grp = (warp - 2) / 4, q = warp & 3;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    const int col0 = grp * CW;  // first token column of this warpgroup
+    int i = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+      const Unit U = unit_of(args, u, BN);
+      const float* scales = args.S[U.prob] + (size_t)(U.n0 / BLK) * nkb_all;
+      float acc[CW];
 #pragma unroll
-      for (int j = 0; j < BN; ++j) acc[j] = 0.f;
-      bool ok = true;
-      for (int i = 0; i < nkb; ++i) {
-        const int ab = i & 1;
-        if (!(ok = mbar_wait(&acc_full[ab], (i >> 1) & 1, err, abort_flag))) break;
+      for (int j = 0; j < CW; ++j) acc[j] = 0.f;
+      for (int kb = U.kb_begin; kb < U.kb_end; ++kb, ++i) {
+        const int ab = i % GT_NACC;
+        if (!(ok = mbar_wait(&acc_full[ab], (i / GT_NACC) & 1, err, abort_flag))) break;
         fence_after();
-        const float sc = s_scale[i];
+        uint32_t v[CW];
 #pragma unroll
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + ab * BN + c, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) acc[c + j] = fmaf(sc, __uint_as_float(v[j]), acc[c + j]);
-        }
+        for (int c = 0; c < CW; c += 32)
+          tmem_ld32(tmem + lane_off + ab * BN + col0 + c, *reinterpret_cast<uint32_t(*)[32]>(v + c));
+        tmem_wait_ld();
         fence_before();
-        mbar_arrive(&acc_empty[ab]);
+        mbar_arrive(&acc_empty[ab]);  // the values are in registers: the MMA may reuse it
+        const float sc = __ldg(scales + kb);
+#pragma unroll
+        for (int j = 0; j < CW; ++j) acc[j] = fmaf(sc, __uint_as_float(v[j]), acc[j]);
       }
-      if (ok && n < (prob ? args.N[1] : args.N[0])) {
-        const int mend = min(BN, args.M - m0);
-        const int ldy = prob ? args.ldy[1] : args.ldy[0];
+      if (!ok) break;
+      const int n = U.n0 + 32 * q + lane;
+      if (n < args.N[U.prob]) {
+        const int m0 = U.m0 + col0;
+        const int mend = min(CW, args.M - m0);
+        const int ldy = args.ldy[U.prob];
         if (args.splits > 1) {
-          float* p = args.partial + ((size_t)split * args.M + m0) * args.ldp +
-                     (prob ? args.N[0] : 0) + n;
+          float* p = args.partial + ((size_t)U.split * args.M + m0) * args.ldp +
+                     (U.prob ? args.N[0] : 0) + n;
 #pragma unroll
-          for (int j = 0; j < BN; ++j)
-            if (j < mend) p[(size_t)j * args.ldp] = acc[j] * s_sx[j];
-        } else if (prob ? args.y_fp32[1] : args.y_fp32[0]) {
-          float* y = reinterpret_cast<float*>(prob ? args.Y[1] : args.Y[0]) + (size_t)m0 * ldy + n;
+          for (int j = 0; j < CW; ++j)
+            if (j < mend) p[(size_t)j * args.ldp] = acc[j] * __ldg(args.sx + m0 + j);
+        } else if (args.y_fp32[U.prob]) {
+          float* y = reinterpret_cast<float*>(args.Y[U.prob]) + (size_t)m0 * ldy + n;
 #pragma unroll
-          for (int j = 0; j < BN; ++j)
-            if (j < mend) y[(size_t)j * ldy] = acc[j] * s_sx[j];
+          for (int j = 0; j < CW; ++j)
+            if (j < mend) y[(size_t)j * ldy] = acc[j] * __ldg(args.sx + m0 + j);
         } else {
-          __nv_bfloat16* y =
-              reinterpret_cast<__nv_bfloat16*>(prob ? args.Y[1] : args.Y[0]) + (size_t)m0 * ldy + n;
+          __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(args.Y[U.prob]) + (size_t)m0 * ldy + n;
 #pragma unroll
-          for (int j = 0; j < BN; ++j)
-            if (j < mend) y[(size_t)j * ldy] = __float2bfloat16_rn(acc[j] * s_sx[j]);
+          for (int j = 0; j < CW; ++j)
+            if (j < mend) y[(size_t)j * ldy] = __float2bfloat16_rn(acc[j] * __ldg(args.sx + m0 + j));
         }
       }
     }
@@ -278,7 +311,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
   if (warp == 1) {
     __syncwarp();
     fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc(tmem, L::TMEM_COLS);
   }
 }
 
@@ -298,8 +331,8 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
 
 template <int BN>
 cudaError_t launch_bn(const CUtensorMap* w, const CUtensorMap& hi, const CUtensorMap& lo,
-                      const GemmTcArgs& a, int n_tiles, cudaStream_t st) {
-  const dim3 grid(n_tiles, (a.M + BN - 1) / BN, a.splits);
+                      const GemmTcArgs& a, int num_sms, cudaStream_t st) {
+  const int grid = a.units < num_sms ? a.units : num_sms;
   gemm_f8w_tc_kernel<BN><<<grid, GT_THREADS, GemmSmem<BN>::BYTES, st>>>(w[0], w[1], hi, lo, a);
   return cudaGetLastError();
 }
@@ -313,14 +346,24 @@ bool make_tmap_2d(CUtensorMap* m, bool bf16, const void* base, uint64_t cols, ui
 
 int gemm_bn(int M) { return M <= 32 ? 32 : (M <= 64 ? 64 : 128); }
 
+// Split-K factor: 1 for large token counts (the tiles alone fill the SMs and fp32 partials
+// would cost more than they save); for few tokens the one that minimises the k blocks of the
+// busiest CTA, ceil(units / SMs) * ceil(k blocks / splits), the smaller on ties.
 int gemm_splits(int M, int N_total, int K, int num_sms) {
-  if (M <= 8) return 1;
+  if (M <= 8 || M > 128) return 1;
   const int bn = gemm_bn(M);
-  const int tiles = ((N_total + 127) / 128) * ((M + bn - 1) / bn);
+  const long tiles = (long)((N_total + 127) / 128) * ((M + bn - 1) / bn);
   const int nkb = K / BLK;
-  int s = (num_sms + tiles - 1) / tiles;
-  if (s > nkb / 4) s = nkb / 4;
-  return s < 1 ? 1 : s;
+  int best = 1;
+  long best_cost = -1;
+  for (int s = 1; s <= nkb / 2 || s == 1; ++s) {
+    const long cost = ((tiles * s + num_sms - 1) / num_sms) * ((nkb + s - 1) / s);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
 }
 
 // Scratch of one tensor-core GEMM: hi and lo e4m3 copies of X [M, K], sx [M], and the split-K
@@ -383,14 +426,16 @@ cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const 
       !make_tmap_2d(&ml, false, lo, (uint64_t)K, (uint64_t)M, (uint64_t)K, 128, bn))
     return cudaErrorInvalidValue;
   a.n_tiles0 = (p[0].N + 127) / 128;
-  const int n_tiles = a.n_tiles0 + (np > 1 ? (p[1].N + 127) / 128 : 0);
+  a.n_tiles = a.n_tiles0 + (np > 1 ? (p[1].N + 127) / 128 : 0);
+  a.m_tiles = (M + bn - 1) / bn;
   a.splits = gemm_splits(M, n_total, K, num_sms);
+  a.units = a.n_tiles * a.m_tiles * a.splits;
   a.partial = partial;
   a.ldp = n_total;
   switch (bn) {
-    case 32: e = launch_bn<32>(mw, mh, ml, a, n_tiles, st); break;
-    case 64: e = launch_bn<64>(mw, mh, ml, a, n_tiles, st); break;
-    default: e = launch_bn<128>(mw, mh, ml, a, n_tiles, st); break;
+    case 32: e = launch_bn<32>(mw, mh, ml, a, num_sms, st); break;
+    case 64: e = launch_bn<64>(mw, mh, ml, a, num_sms, st); break;
+    default: e = launch_bn<128>(mw, mh, ml, a, num_sms, st); break;
   }
   if (e != cudaSuccess || a.splits == 1) return e;
   for (int i = 0; i < np; ++i) {
