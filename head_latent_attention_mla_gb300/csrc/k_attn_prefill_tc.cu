@@ -5,11 +5,13 @@
 // softmax scale, key s visible from query t iff s <= t, fp32 softmax over keys, o = P v (128).
 // The head dimensions stay 192 / 128 (no padding of v to 192).
 //
-// One CTA per (128-query tile, head, sequence), 7 warps:
-//   warp 0      TMA producer: the query tile once (3 boxes of 64 columns), then for every
-//               128-key tile k_nope (2 boxes), the rotary key from the cache rows (1 box) and
-//               v (2 boxes) into a two-stage ring (128-byte swizzle, 3-D maps over
+// One CTA per (128-query tile, head, sequence), 8 warps:
+//   warp 0      TMA producer of the query tile (3 boxes of 64 columns) and, for every 128-key
+//               tile, of k = [k_nope (2 boxes) | rotary key from the cache rows (1 box)] into
+//               a two-stage ring that MMA1 releases (128-byte swizzle, 3-D maps over
 //               [tokens, heads, dims]);
+//   warp 7      TMA producer of v (2 boxes) into its own two-stage ring, which MMA2 releases,
+//               so that k runs ahead of the softmax;
 //   warp 1      allocates tensor memory and issues MMA1  S = Q K^T  (M=128, N=128, K=192);
 //   warp 6      issues MMA2  O += P V  (M=128, N=128, K=128) with P read from tensor memory
 //               and v read MN-major;
@@ -17,6 +19,8 @@
 //               softmax in base 2 with a lazy rescale of O (only when the running maximum
 //               grows by more than 2^8), P written to tensor memory as packed bf16; then the
 //               epilogue normalises O and stores it as bf16.
+// MMA2 of a tile does not wait for the previous tile's: only a rescale of O needs the previous
+// MMA2 to be complete, and the softmax waits for it then.
 // Tensor memory: O in columns [0,128), S in [128,256) and [256,384), P in [384,448) and
 // [448,512).
 #include "tc_common.cuh"
@@ -32,11 +36,11 @@ constexpr int PA_BOX = 128 * 128;                 // [128 rows x 64 bf16] box, b
 constexpr int PA_Q_BYTES = 3 * PA_BOX;            // q tile: 192 columns
 constexpr int PA_K_BYTES = 3 * PA_BOX;            // k tile: 128 nope + 64 rotary
 constexpr int PA_V_BYTES = 2 * PA_BOX;            // v tile: 128 columns
-constexpr int PA_STAGE = PA_K_BYTES + PA_V_BYTES;
-constexpr int PA_THREADS = 224;
+constexpr int PA_THREADS = 256;
 constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + PA_Q_BYTES;
-constexpr int OFF_BAR = OFF_KV + 2 * PA_STAGE;
+constexpr int OFF_K = OFF_Q + PA_Q_BYTES;          // two k stages
+constexpr int OFF_V = OFF_K + 2 * PA_K_BYTES;      // two v stages
+constexpr int OFF_BAR = OFF_V + 2 * PA_V_BYTES;
 constexpr int OFF_MISC = OFF_BAR + 16 * 8;
 constexpr int OFF_ALPHA_FLAG = OFF_MISC + 16;
 constexpr int PA_SMEM = OFF_ALPHA_FLAG + 16 + 1024;
@@ -71,13 +75,14 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* s_free = bars + 7;    // [2]
-  uint64_t* p_full = bars + 9;
-  uint64_t* o_done = bars + 10;
-  uint64_t* mma_idle = bars + 11; // [2]
+  uint64_t* k_full = bars + 1;    // [2]
+  uint64_t* k_empty = bars + 3;   // [2]  MMA1 of the stage's tile is done
+  uint64_t* v_full = bars + 5;    // [2]
+  uint64_t* v_empty = bars + 7;   // [2]  MMA2 of the stage's tile is done (also frees P)
+  uint64_t* s_full = bars + 9;    // [2]
+  uint64_t* s_free = bars + 11;   // [2]
+  uint64_t* p_full = bars + 13;   // [2]  P of the buffer's tile is in tensor memory
+  uint64_t* mma_idle = bars + 15; // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -91,14 +96,15 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 128);
+      mbar_init(&p_full[i], 128);
       mbar_init(&mma_idle[i], 1);
     }
-    mbar_init(p_full, 128);
-    mbar_init(o_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -124,21 +130,37 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
         const int st = j & 1;
-        if (j >= 2 && !mbar_wait(&kv_empty[st], ((j - 2) >> 1) & 1, err, abort_flag)) break;
-        uint8_t* stg = smem + OFF_KV + st * PA_STAGE;
-        mbar_expect_tx(&kv_full[st], PA_STAGE);
+        if (j >= 2 && !mbar_wait(&k_empty[st], ((j - 2) >> 1) & 1, err, abort_flag)) break;
+        uint8_t* stg = smem + OFF_K + st * PA_K_BYTES;
+        mbar_expect_tx(&k_full[st], PA_K_BYTES);
         const int k0 = j * PA_TILE;
-        tma_load_3d(stg, &map_kv, &kv_full[st], 0, h, tok0 + k0);
-        tma_load_3d(stg + PA_BOX, &map_kv, &kv_full[st], 64, h, tok0 + k0);
-        tma_load_2d(stg + 2 * PA_BOX, &map_c, &kv_full[st], KV_LORA, b * cap + k0);
-        tma_load_3d(stg + PA_K_BYTES, &map_kv, &kv_full[st], 128, h, tok0 + k0);
-        tma_load_3d(stg + PA_K_BYTES + PA_BOX, &map_kv, &kv_full[st], 192, h, tok0 + k0);
+        tma_load_3d(stg, &map_kv, &k_full[st], 0, h, tok0 + k0);
+        tma_load_3d(stg + PA_BOX, &map_kv, &k_full[st], 64, h, tok0 + k0);
+        tma_load_2d(stg + 2 * PA_BOX, &map_c, &k_full[st], KV_LORA, b * cap + k0);
         issued = j + 1;
       }
       volatile int no_abort = 0;
       mbar_wait(q_full, 0, err, &no_abort);
       for (int j = max(0, issued - 2); j < issued; ++j)
-        mbar_wait(&kv_full[j & 1], (j >> 1) & 1, err, &no_abort);
+        mbar_wait(&k_full[j & 1], (j >> 1) & 1, err, &no_abort);
+    }
+  } else if (warp == 7) {
+    // -------------------------------------------------------------------- v producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int j = 0; j < nt; ++j) {
+        const int st = j & 1;
+        if (j >= 2 && !mbar_wait(&v_empty[st], ((j - 2) >> 1) & 1, err, abort_flag)) break;
+        uint8_t* stg = smem + OFF_V + st * PA_V_BYTES;
+        mbar_expect_tx(&v_full[st], PA_V_BYTES);
+        const int k0 = j * PA_TILE;
+        tma_load_3d(stg, &map_kv, &v_full[st], 128, h, tok0 + k0);
+        tma_load_3d(stg + PA_BOX, &map_kv, &v_full[st], 192, h, tok0 + k0);
+        issued = j + 1;
+      }
+      volatile int no_abort = 0;
+      for (int j = max(0, issued - 2); j < issued; ++j)
+        mbar_wait(&v_full[j & 1], (j >> 1) & 1, err, &no_abort);
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------------- MMA1 issuer
@@ -147,11 +169,11 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
       bool ok = mbar_wait(q_full, 0, err, abort_flag);
       for (int j = 0; ok && j < nt; ++j) {
         const int st = j & 1;
-        ok = mbar_wait(&kv_full[st], (j >> 1) & 1, err, abort_flag);
+        ok = mbar_wait(&k_full[st], (j >> 1) & 1, err, abort_flag);
         if (ok && j >= 2) ok = mbar_wait(&s_free[st], ((j - 2) >> 1) & 1, err, abort_flag);
         if (!ok) break;
         fence_after();
-        const uint32_t kb = sbase + OFF_KV + st * PA_STAGE;
+        const uint32_t kb = sbase + OFF_K + st * PA_K_BYTES;
 #pragma unroll
         for (int ks = 0; ks < 12; ++ks) {
           const uint64_t a = sdesc_sw128(sbase + OFF_Q + (ks >> 2) * PA_BOX + (ks & 3) * 32, 16, 1024);
@@ -159,6 +181,7 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
           mma_bf16(tmem + TM_S + 128 * st, a, bd, idesc, ks > 0);
         }
         mma_commit(&s_full[st]);
+        mma_commit(&k_empty[st]);
       }
       mma_commit(&mma_idle[0]);
       volatile int no_abort = 0;
@@ -170,18 +193,17 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
       constexpr uint32_t idesc = idesc_bf16(128, 128, false, true);
       for (int j = 0; j < nt; ++j) {
         const int st = j & 1;
-        if (!mbar_wait(p_full, j & 1, err, abort_flag)) break;
-        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, err, abort_flag)) break;
+        if (!mbar_wait(&p_full[st], (j >> 1) & 1, err, abort_flag)) break;
+        if (!mbar_wait(&v_full[st], (j >> 1) & 1, err, abort_flag)) break;
         fence_after();
-        const uint32_t vb = sbase + OFF_KV + st * PA_STAGE + PA_K_BYTES;
+        const uint32_t vb = sbase + OFF_V + st * PA_V_BYTES;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           // B = v: MN-major, 128 value dims (2 boxes, PA_BOX apart) x 16 keys.
           const uint64_t bd = sdesc_sw128(vb + ks * 2048, PA_BOX, 1024);
           mma_bf16_ts(tmem + TM_O, tmem + TM_P + 64 * st + 8 * ks, bd, idesc, (j > 0) || (ks > 0));
         }
-        mma_commit(o_done);
-        mma_commit(&kv_empty[st]);
+        mma_commit(&v_empty[st]);
       }
       mma_commit(&mma_idle[1]);
       volatile int no_abort = 0;
@@ -198,21 +220,23 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
       const int st = j & 1;
       if (!(ok = mbar_wait(&s_full[st], (j >> 1) & 1, err, abort_flag))) break;
       fence_after();
-      uint32_t r[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + TM_S + 128 * st + 32 * c, r[c]);
-      tmem_wait_ld();
-      fence_before();
-      mbar_arrive(&s_free[st]);
+      // The row is read from tensor memory twice, 32 columns at a time, in rolled loops: the
+      // code stays small enough for the instruction cache, which the fully unrolled 128-column
+      // version overflowed.
+      const uint32_t s_addr = tmem + lane_off + TM_S + 128 * st;
       const int kbase = j * PA_TILE;
       const int vis = min(qi - kbase + 1, T - kbase);   // keys [kbase, kbase+vis) visible
-      float tmax = -INFINITY;
+      float tmax = -INFINITY;  // pass 1: maximum of the visible scores
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(s_addr + 32 * c, r);
+        tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float s = (c < vis) ? __uint_as_float(r[c >> 5][c & 31]) * scale_log2 : -INFINITY;
-        r[c >> 5][c & 31] = __float_as_uint(s);
-        tmax = fmaxf(tmax, s);
+        for (int i = 0; i < 32; ++i)
+          tmax = fmaxf(tmax, (32 * c + i < vis) ? __uint_as_float(r[i]) : -INFINITY);
       }
+      tmax *= scale_log2;  // the scale is positive
       float alpha = 1.f;
       bool need = false;
       if (tmax > m + RESCALE_LOG2) {
@@ -224,21 +248,35 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
         m = tmax;
       }
       const float mu = (m == -INFINITY) ? 0.f : m;   // rows past T see no key at all
-      uint32_t pk[64];
+      // P's buffer was last read by MMA2 of tile j-2, and O may only be rescaled once MMA2 of
+      // tile j-1 is done; their commits on the v stages say so.  (Neither stage barrier can run
+      // a phase ahead: its next phase needs this warpgroup's P of tile j or j+1.)
+      if (j >= 2 && !(ok = mbar_wait(&v_empty[st], ((j - 2) >> 1) & 1, err, abort_flag))) break;
+      // Pass 2: p = 2^(s * scale - m), rounded to bf16, into P (16 packed columns per chunk).
+      const uint32_t p_addr = tmem + lane_off + TM_P + 64 * st;
       float lsum = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(s_addr + 32 * c, r);
+        tmem_wait_ld();
+        uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        const float a = exp2f(__uint_as_float(r[c >> 5][c & 31]) - mu);
-        const float d = exp2f(__uint_as_float(r[(c + 1) >> 5][(c + 1) & 31]) - mu);
-        __nv_bfloat162 pr = __floats2bfloat162_rn(a, d);
-        lsum += __low2float(pr) + __high2float(pr);
-        pk[c >> 1] = *reinterpret_cast<uint32_t*>(&pr);
+        for (int i = 0; i < 32; i += 2) {
+          const int col = 32 * c + i;
+          const float e0 = exp2f(fmaf(__uint_as_float(r[i]), scale_log2, -mu));
+          const float e1 = exp2f(fmaf(__uint_as_float(r[i + 1]), scale_log2, -mu));
+          __nv_bfloat162 pr = __floats2bfloat162_rn(col < vis ? e0 : 0.f, col + 1 < vis ? e1 : 0.f);
+          lsum += __low2float(pr) + __high2float(pr);
+          pk[i >> 1] = *reinterpret_cast<uint32_t*>(&pr);
+        }
+        tmem_st16(p_addr + 16 * c, pk);
       }
+      fence_before();
+      mbar_arrive(&s_free[st]);  // S of this buffer has been read
       l += lsum;
-      // MMA2 of the previous tile must be done before P is overwritten or O rescaled; every
-      // o_done phase is consumed here, in order, before this tile's MMA2 is issued.
-      if (j >= 1 && !(ok = mbar_wait(o_done, (j - 1) & 1, err, abort_flag))) break;
       if (named_bar_or(1, 128, need)) {
+        if (!(ok = mbar_wait(&v_empty[st ^ 1], ((j - 1) >> 1) & 1, err, abort_flag))) break;
         fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -250,17 +288,11 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
           tmem_st32(tmem + lane_off + TM_O + 32 * c, o);
         }
       }
-      {
-        uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
-        uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
-        tmem_st32(tmem + lane_off + TM_P + 64 * st, p0);
-        tmem_st32(tmem + lane_off + TM_P + 64 * st + 32, p1);
-      }
       tmem_wait_st();
       fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[st]);
     }
-    if (ok && mbar_wait(o_done, (nt - 1) & 1, err, abort_flag)) {
+    if (ok && mbar_wait(&v_empty[(nt - 1) & 1], ((nt - 1) >> 1) & 1, err, abort_flag)) {
       fence_after();
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
       __nv_bfloat16* dst = attn_out + (size_t)(tok0 + qi) * O_IN + h * VDIM;
