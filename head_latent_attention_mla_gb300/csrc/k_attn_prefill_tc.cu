@@ -5,7 +5,7 @@
 // softmax scale, key s visible from query t iff s <= t, fp32 softmax over keys, o = P v (128).
 // The head dimensions stay 192 / 128 (no padding of v to 192).
 //
-// One CTA per (128-query tile, head, sequence), 8 warps:
+// One CTA per (128-query tile, head, sequence), 12 warps:
 //   warp 0      TMA producer of the query tile (3 boxes of 64 columns) and, for every 128-key
 //               tile, of k = [k_nope (2 boxes) | rotary key from the cache rows (1 box)] into
 //               a two-stage ring that MMA1 releases (128-byte swizzle, 3-D maps over
@@ -15,10 +15,11 @@
 //   warp 1      allocates tensor memory and issues MMA1  S = Q K^T  (M=128, N=128, K=192);
 //   warp 6      issues MMA2  O += P V  (M=128, N=128, K=128) with P read from tensor memory
 //               and v read MN-major;
-//   warps 2..5  softmax, one query row per thread: causal mask on the diagonal tile, online
-//               softmax in base 2 with a lazy rescale of O (only when the running maximum
-//               grows by more than 2^8), P written to tensor memory as packed bf16; then the
-//               epilogue normalises O and stores it as bf16.
+//   warps 2..5, 8..11  softmax, two threads per query row (columns 0..63 and 64..127 of S, P
+//               and O; the halves trade row maxima through shared memory): causal mask on the
+//               diagonal tile, online softmax in base 2 with a lazy rescale of O (only when the
+//               running maximum grows by more than 2^8), P written to tensor memory as packed
+//               bf16; then the epilogue normalises O and stores it as bf16.
 // MMA2 of a tile does not wait for the previous tile's: only a rescale of O needs the previous
 // MMA2 to be complete, and the softmax waits for it then.
 // Tensor memory: O in columns [0,128), S in [128,256) and [256,384), P in [384,448) and
@@ -36,14 +37,15 @@ constexpr int PA_BOX = 128 * 128;                 // [128 rows x 64 bf16] box, b
 constexpr int PA_Q_BYTES = 3 * PA_BOX;            // q tile: 192 columns
 constexpr int PA_K_BYTES = 3 * PA_BOX;            // k tile: 128 nope + 64 rotary
 constexpr int PA_V_BYTES = 2 * PA_BOX;            // v tile: 128 columns
-constexpr int PA_THREADS = 256;
+constexpr int PA_THREADS = 384;
+constexpr int PA_SM_THREADS = 256;                 // softmax threads (two per query row)
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + PA_Q_BYTES;          // two k stages
 constexpr int OFF_V = OFF_K + 2 * PA_K_BYTES;      // two v stages
 constexpr int OFF_BAR = OFF_V + 2 * PA_V_BYTES;
 constexpr int OFF_MISC = OFF_BAR + 16 * 8;
-constexpr int OFF_ALPHA_FLAG = OFF_MISC + 16;
-constexpr int PA_SMEM = OFF_ALPHA_FLAG + 16 + 1024;
+constexpr int OFF_XCH = OFF_MISC + 16;            // [2 tile parities][2 halves][128 rows]
+constexpr int PA_SMEM = OFF_XCH + 2 * 2 * 128 * 4 + 1024;
 constexpr uint32_t TM_O = 0, TM_S = 128, TM_P = 384;
 constexpr float RESCALE_LOG2 = 8.f;
 
@@ -101,11 +103,12 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&s_free[i], PA_SM_THREADS);
+      mbar_init(&p_full[i], PA_SM_THREADS);
       mbar_init(&mma_idle[i], 1);
     }
     *abort_flag = 0;
+    reinterpret_cast<volatile int*>(smem + OFF_MISC)[2] = 0;  // softmax failure flag
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -209,34 +212,44 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
       volatile int no_abort = 0;
       mbar_wait(&mma_idle[1], 0, err, &no_abort);
     }
-  } else if (warp >= 2 && warp <= 5) {
+  } else if ((warp >= 2 && warp <= 5) || warp >= 8) {
     // -------------------------------------------------------------------- softmax warps
+    // Every softmax thread reaches the same named barriers in every tile it starts; a failed
+    // wait is published in s_fail before the tile's second barrier, and all threads leave
+    // together after it, so no barrier is left waiting for a thread that has gone.
     const int qw = warp & 3;
+    const int half = warp >= 8 ? 1 : 0;           // columns [64 half, 64 half + 64)
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
-    const int qi = q0 + 32 * qw + lane;           // query position of this thread's row
-    float m = -INFINITY, l = 0.f;
+    const int row = 32 * qw + lane;
+    const int qi = q0 + row;                      // query position of this thread's row
+    float* xch = reinterpret_cast<float*>(smem + OFF_XCH);
+    volatile int* s_fail = reinterpret_cast<volatile int*>(smem + OFF_MISC) + 2;
+    float m = -INFINITY, l = 0.f;                 // running maximum; this half's sum
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       const int st = j & 1;
-      if (!(ok = mbar_wait(&s_full[st], (j >> 1) & 1, err, abort_flag))) break;
+      ok = mbar_wait(&s_full[st], (j >> 1) & 1, err, abort_flag);
       fence_after();
-      // The row is read from tensor memory twice, 32 columns at a time, in rolled loops: the
-      // code stays small enough for the instruction cache, which the fully unrolled 128-column
-      // version overflowed.
-      const uint32_t s_addr = tmem + lane_off + TM_S + 128 * st;
-      const int kbase = j * PA_TILE;
-      const int vis = min(qi - kbase + 1, T - kbase);   // keys [kbase, kbase+vis) visible
+      // The half row is read from tensor memory twice, 32 columns at a time, in rolled loops
+      // (small code: a fully unrolled row overflows the instruction cache).
+      const uint32_t s_addr = tmem + lane_off + TM_S + 128 * st + 64 * half;
+      const int kbase = j * PA_TILE + 64 * half;
+      const int vis = min(qi - kbase + 1, T - kbase);   // columns [0, vis) of this half visible
       float tmax = -INFINITY;  // pass 1: maximum of the visible scores
+      if (ok) {
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(s_addr + 32 * c, r);
-        tmem_wait_ld();
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[32];
+          tmem_ld32(s_addr + 32 * c, r);
+          tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          tmax = fmaxf(tmax, (32 * c + i < vis) ? __uint_as_float(r[i]) : -INFINITY);
+          for (int i = 0; i < 32; ++i)
+            tmax = fmaxf(tmax, (32 * c + i < vis) ? __uint_as_float(r[i]) : -INFINITY);
+        }
       }
-      tmax *= scale_log2;  // the scale is positive
+      xch[(2 * st + half) * 128 + row] = tmax;
+      named_bar(1, PA_SM_THREADS);
+      tmax = fmaxf(tmax, xch[(2 * st + (half ^ 1)) * 128 + row]) * scale_log2;  // scale > 0
       float alpha = 1.f;
       bool need = false;
       if (tmax > m + RESCALE_LOG2) {
@@ -251,55 +264,73 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
       // P's buffer was last read by MMA2 of tile j-2, and O may only be rescaled once MMA2 of
       // tile j-1 is done; their commits on the v stages say so.  (Neither stage barrier can run
       // a phase ahead: its next phase needs this warpgroup's P of tile j or j+1.)
-      if (j >= 2 && !(ok = mbar_wait(&v_empty[st], ((j - 2) >> 1) & 1, err, abort_flag))) break;
+      if (ok && j >= 2) ok = mbar_wait(&v_empty[st], ((j - 2) >> 1) & 1, err, abort_flag);
       // Pass 2: p = 2^(s * scale - m), rounded to bf16, into P (16 packed columns per chunk).
-      const uint32_t p_addr = tmem + lane_off + TM_P + 64 * st;
+      const uint32_t p_addr = tmem + lane_off + TM_P + 64 * st + 32 * half;
       float lsum = 0.f;
+      if (ok) {
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(s_addr + 32 * c, r);
-        tmem_wait_ld();
-        uint32_t pk[16];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[32];
+          tmem_ld32(s_addr + 32 * c, r);
+          tmem_wait_ld();
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int col = 32 * c + i;
-          const float e0 = exp2f(fmaf(__uint_as_float(r[i]), scale_log2, -mu));
-          const float e1 = exp2f(fmaf(__uint_as_float(r[i + 1]), scale_log2, -mu));
-          __nv_bfloat162 pr = __floats2bfloat162_rn(col < vis ? e0 : 0.f, col + 1 < vis ? e1 : 0.f);
-          lsum += __low2float(pr) + __high2float(pr);
-          pk[i >> 1] = *reinterpret_cast<uint32_t*>(&pr);
+          for (int i = 0; i < 32; i += 2) {
+            const int col = 32 * c + i;
+            const float e0 = exp2f(fmaf(__uint_as_float(r[i]), scale_log2, -mu));
+            const float e1 = exp2f(fmaf(__uint_as_float(r[i + 1]), scale_log2, -mu));
+            __nv_bfloat162 pr =
+                __floats2bfloat162_rn(col < vis ? e0 : 0.f, col + 1 < vis ? e1 : 0.f);
+            lsum += __low2float(pr) + __high2float(pr);
+            pk[i >> 1] = *reinterpret_cast<uint32_t*>(&pr);
+          }
+          tmem_st16(p_addr + 16 * c, pk);
         }
-        tmem_st16(p_addr + 16 * c, pk);
+        fence_before();
+        mbar_arrive(&s_free[st]);  // S of this buffer has been read
       }
-      fence_before();
-      mbar_arrive(&s_free[st]);  // S of this buffer has been read
       l += lsum;
-      if (named_bar_or(1, 128, need)) {
-        if (!(ok = mbar_wait(&v_empty[st ^ 1], ((j - 1) >> 1) & 1, err, abort_flag))) break;
+      if (ok && need) ok = mbar_wait(&v_empty[st ^ 1], ((j - 1) >> 1) & 1, err, abort_flag);
+      if (!ok) *s_fail = 1;
+      const bool any_need = named_bar_or(1, PA_SM_THREADS, need);
+      if (*s_fail) {
+        ok = false;
+        break;
+      }
+      if (any_need) {  // MMA2 of tile j-1 is done for every thread that needed it: for all
+        if (!need) ok = mbar_wait(&v_empty[st ^ 1], ((j - 1) >> 1) & 1, err, abort_flag);
+        if (!ok) break;  // cannot happen once another thread's identical wait succeeded
         fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + TM_O + 32 * c, o);
+          const uint32_t ta = tmem + lane_off + TM_O + 64 * half + 32 * c;
+          tmem_ld32(ta, o);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tmem + lane_off + TM_O + 32 * c, o);
+          tmem_st32(ta, o);
         }
       }
       tmem_wait_st();
       fence_before();
       mbar_arrive(&p_full[st]);
     }
-    if (ok && mbar_wait(&v_empty[(nt - 1) & 1], ((nt - 1) >> 1) & 1, err, abort_flag)) {
+    // Epilogue: the row's sum from both halves, O / l as bf16, this half's 64 value dims.
+    if (ok) ok = mbar_wait(&v_empty[(nt - 1) & 1], ((nt - 1) >> 1) & 1, err, abort_flag);
+    if (!ok) *s_fail = 1;
+    xch[half * 128 + row] = l;
+    named_bar(1, PA_SM_THREADS);
+    if (!*s_fail) {
       fence_after();
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      __nv_bfloat16* dst = attn_out + (size_t)(tok0 + qi) * O_IN + h * VDIM;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      const float lrow = l + xch[(half ^ 1) * 128 + row];
+      const float inv = (lrow > 0.f) ? 1.f / lrow : 0.f;
+      __nv_bfloat16* dst = attn_out + (size_t)(tok0 + qi) * O_IN + h * VDIM + 64 * half;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + TM_O + 32 * c, o);
+        tmem_ld32(tmem + lane_off + TM_O + 64 * half + 32 * c, o);
         tmem_wait_ld();
         if (qi < T) {
 #pragma unroll
