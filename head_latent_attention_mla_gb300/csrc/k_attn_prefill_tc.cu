@@ -5,7 +5,7 @@
 // softmax scale, key s visible from query t iff s <= t, fp32 softmax over keys, o = P v (128).
 // The head dimensions stay 192 / 128 (no padding of v to 192).
 //
-// One CTA per (128-query tile, head, sequence), 12 warps:
+// One CTA per (head, 128-query tile, sequence), heaviest query tiles first, 12 warps:
 //   warp 0      TMA producer of the query tile (3 boxes of 64 columns) and, for every 128-key
 //               tile, of k = [k_nope (2 boxes) | rotary key from the cache rows (1 box)] into
 //               a two-stage ring that MMA1 releases (128-byte swizzle, 3-D maps over
@@ -90,8 +90,10 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = (T + PA_TILE - 1) / PA_TILE;
-  const int qt = nq - 1 - (int)blockIdx.x;        // heaviest (latest) query tiles first
-  const int h = blockIdx.y, b = blockIdx.z;
+  // Heads vary fastest in launch order, so all heads of the heaviest (latest) query tiles start
+  // first and the light tiles fill the tail.
+  const int qt = nq - 1 - (int)blockIdx.y;
+  const int h = blockIdx.x, b = blockIdx.z;
   const int q0 = qt * PA_TILE;
   const int nt = qt + 1;                           // key tiles 0..qt (causal)
 
@@ -401,7 +403,7 @@ cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloa
                     (uint64_t)HEADS * KVB_PER_HEAD * 2, 64, 1, 128) ||
       !make_tmap_2d(&mc, true, cache, LAT, (uint64_t)B * cap, LAT * 2, 64, 128))
     return cudaErrorInvalidValue;
-  const dim3 grid((T + PA_TILE - 1) / PA_TILE, HEADS, B);
+  const dim3 grid(HEADS, (T + PA_TILE - 1) / PA_TILE, B);
   prefill_attn_tc_kernel<<<grid, PA_THREADS, PA_SMEM, st>>>(mq, mkv, mc, T, cap,
                                                             scale * 1.4426950408889634f, attn_out,
                                                             err);
