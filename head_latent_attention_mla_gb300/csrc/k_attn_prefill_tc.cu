@@ -237,6 +237,8 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
       const uint32_t s_addr = tmem + lane_off + TM_S + 128 * st + 64 * half;
       const int kbase = j * PA_TILE + 64 * half;
       const int vis = min(qi - kbase + 1, T - kbase);   // columns [0, vis) of this half visible
+      // Tiles left of the diagonal are visible to every row: no mask there.
+      const bool full = j < qt;
       float tmax = -INFINITY;  // pass 1: maximum of the visible scores
       if (ok) {
 #pragma unroll 1
@@ -244,9 +246,14 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
           uint32_t r[32];
           tmem_ld32(s_addr + 32 * c, r);
           tmem_wait_ld();
+          if (full) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            tmax = fmaxf(tmax, (32 * c + i < vis) ? __uint_as_float(r[i]) : -INFINITY);
+            for (int i = 0; i < 32; ++i) tmax = fmaxf(tmax, __uint_as_float(r[i]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              tmax = fmaxf(tmax, (32 * c + i < vis) ? __uint_as_float(r[i]) : -INFINITY);
+          }
         }
       }
       xch[(2 * st + half) * 128 + row] = tmax;
@@ -267,7 +274,8 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
       // tile j-1 is done; their commits on the v stages say so.  (Neither stage barrier can run
       // a phase ahead: its next phase needs this warpgroup's P of tile j or j+1.)
       if (ok && j >= 2) ok = mbar_wait(&v_empty[st], ((j - 2) >> 1) & 1, err, abort_flag);
-      // Pass 2: p = 2^(s * scale - m), rounded to bf16, into P (16 packed columns per chunk).
+      // Pass 2: p = 2^(s * scale - m), rounded to bf16, into P (16 packed columns per chunk);
+      // l sums the unrounded p.
       const uint32_t p_addr = tmem + lane_off + TM_P + 64 * st + 32 * half;
       float lsum = 0.f;
       if (ok) {
@@ -277,16 +285,32 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
           tmem_ld32(s_addr + 32 * c, r);
           tmem_wait_ld();
           uint32_t pk[16];
+          float ls0 = 0.f, ls1 = 0.f;
+          if (full) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const int col = 32 * c + i;
-            const float e0 = exp2f(fmaf(__uint_as_float(r[i]), scale_log2, -mu));
-            const float e1 = exp2f(fmaf(__uint_as_float(r[i + 1]), scale_log2, -mu));
-            __nv_bfloat162 pr =
-                __floats2bfloat162_rn(col < vis ? e0 : 0.f, col + 1 < vis ? e1 : 0.f);
-            lsum += __low2float(pr) + __high2float(pr);
-            pk[i >> 1] = *reinterpret_cast<uint32_t*>(&pr);
+            for (int i = 0; i < 32; i += 2) {
+              const float e0 = exp2f(fmaf(__uint_as_float(r[i]), scale_log2, -mu));
+              const float e1 = exp2f(fmaf(__uint_as_float(r[i + 1]), scale_log2, -mu));
+              ls0 += e0;
+              ls1 += e1;
+              __nv_bfloat162 pr = __floats2bfloat162_rn(e0, e1);
+              pk[i >> 1] = *reinterpret_cast<uint32_t*>(&pr);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const int col = 32 * c + i;
+              const float e0 =
+                  col < vis ? exp2f(fmaf(__uint_as_float(r[i]), scale_log2, -mu)) : 0.f;
+              const float e1 =
+                  col + 1 < vis ? exp2f(fmaf(__uint_as_float(r[i + 1]), scale_log2, -mu)) : 0.f;
+              ls0 += e0;
+              ls1 += e1;
+              __nv_bfloat162 pr = __floats2bfloat162_rn(e0, e1);
+              pk[i >> 1] = *reinterpret_cast<uint32_t*>(&pr);
+            }
           }
+          lsum += ls0 + ls1;
           tmem_st16(p_addr + 16 * c, pk);
         }
         fence_before();
