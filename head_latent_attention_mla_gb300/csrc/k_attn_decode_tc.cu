@@ -315,8 +315,8 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
           float lsum = 0.f;
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            __nv_bfloat162 pr = __floats2bfloat162_rn(exp2f(__uint_as_float(r[j]) - m),
-                                                      exp2f(__uint_as_float(r[j + 1]) - m));
+            __nv_bfloat162 pr = __floats2bfloat162_rn(fast_exp2(__uint_as_float(r[j]) - m),
+                                                      fast_exp2(__uint_as_float(r[j + 1]) - m));
             lsum += __low2float(pr) + __high2float(pr);
             pb[j >> 1] = *reinterpret_cast<uint32_t*>(&pr);
           }

@@ -289,8 +289,8 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
           if (full) {
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-              const float e0 = exp2f(fmaf(__uint_as_float(r[i]), scale_log2, -mu));
-              const float e1 = exp2f(fmaf(__uint_as_float(r[i + 1]), scale_log2, -mu));
+              const float e0 = fast_exp2(fmaf(__uint_as_float(r[i]), scale_log2, -mu));
+              const float e1 = fast_exp2(fmaf(__uint_as_float(r[i + 1]), scale_log2, -mu));
               ls0 += e0;
               ls1 += e1;
               __nv_bfloat162 pr = __floats2bfloat162_rn(e0, e1);
@@ -301,9 +301,9 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
             for (int i = 0; i < 32; i += 2) {
               const int col = 32 * c + i;
               const float e0 =
-                  col < vis ? exp2f(fmaf(__uint_as_float(r[i]), scale_log2, -mu)) : 0.f;
+                  col < vis ? fast_exp2(fmaf(__uint_as_float(r[i]), scale_log2, -mu)) : 0.f;
               const float e1 =
-                  col + 1 < vis ? exp2f(fmaf(__uint_as_float(r[i + 1]), scale_log2, -mu)) : 0.f;
+                  col + 1 < vis ? fast_exp2(fmaf(__uint_as_float(r[i + 1]), scale_log2, -mu)) : 0.f;
               ls0 += e0;
               ls1 += e1;
               __nv_bfloat162 pr = __floats2bfloat162_rn(e0, e1);

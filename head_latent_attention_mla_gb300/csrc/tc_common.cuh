@@ -175,6 +175,14 @@ __device__ __forceinline__ void tmem_wait_st() {
 #undef MLA_R8
 #undef MLA_W8
 
+// 2^x by the PTX ex2.approx.ftz instruction (relative error about 2^-22; results below the
+// normal range flush to zero), for softmax weights.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------------ MMA
 // Shared-memory matrix descriptor, 128-byte swizzle (atoms of 8 rows x 128 B, 1024-byte
 // aligned).  lbo/sbo in bytes: sbo = stride between 8-row groups, lbo = stride between atoms
