@@ -145,6 +145,10 @@ def algorithmic_bytes(kernel, B, lengths):
         "decode_combine": B * 64 * 512 * 2,
         "absorb_out": 64 * 128 * 512 + 64 * 4 * 4 + B * 64 * 512 * 2 + B * 8192 * 2,
         "gemm_o": wbytes("o") + B * 8192 * 2 + B * 7168 * 2,
+        # few sequences: q_b_proj with the q-latent norm and the cache-row append fused in
+        "gemm_q_b_norm": wbytes("q_b") + B * 2112 * 4 + B * 12288 * 2 + B * LAT_BYTES,
+        # few sequences: the split combine fused with the W_UV absorption
+        "combine_absorb_out": 64 * 128 * 512 + 64 * 4 * 4 + B * 64 * 512 * 2 + B * 8192 * 2,
         "advance_lens": B * 8,
     }.get(kernel, 0)
 

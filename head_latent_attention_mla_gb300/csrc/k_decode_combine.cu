@@ -96,7 +96,125 @@ __global__ void __launch_bounds__(kThreads) decode_combine_kernel(
   }
 }
 
+// Combine and output absorption of one (head h, sequence b) for a few decode sequences:
+//   o_lat = sum_i v_i o_i as in decode_combine_kernel (rounded to bf16), then
+//   attn[b][128 h + v] = sum_c s[2h+1][c/128] * e4m3(W_kvb[256 h + 128 + v][c]) * o_lat[c]
+// ("Key content up-projection" page, W_UV,h = rows 128..255 of head h's 256).  Each warp owns 16
+// rows of W_UV,h, loaded into registers before the wait on the attention; one CTA per (h, b).
+__global__ void __launch_bounds__(256) combine_absorb_out_kernel(
+    const int* __restrict__ seq_lens, int B, int G, long long P, const __half* __restrict__ o_part,
+    const float* __restrict__ ml_part, const uint8_t* __restrict__ Wkvb,
+    const float* __restrict__ Skvb, __nv_bfloat16* __restrict__ attn, int* err) {
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  __shared__ int s_first, s_n;
+  __shared__ float s_w[kMaxSplits];
+  __shared__ float s_red[8];
+  __shared__ __align__(16) float ol[KV_LORA];
+  uint4 wv[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const uint8_t* src =
+        Wkvb + ((size_t)h * KVB_PER_HEAD + NOPE + 16 * warp + r) * KV_LORA + lane * 16;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(wv[r].x), "=r"(wv[r].y), "=r"(wv[r].z), "=r"(wv[r].w)
+                 : "l"(src));
+  }
+  const float sc = __ldg(Skvb + (size_t)(2 * h + 1) * (KV_LORA / BLK) + lane / 8);
+  pdl_launch_dependents();
+  pdl_wait();  // the attention's partials are complete
+  if (tid == 0) {
+    long long start = 0;
+    for (int bb = 0; bb < b; ++bb) start += (long long)seq_lens[bb] + 1;
+    const long long end = start + seq_lens[b] + 1;
+    int c0 = 0, n = 0;
+    if (end <= P) {
+      c0 = decode_share_of(start, G, P);
+      n = decode_share_of(end - 1, G, P) - c0 + 1;
+    }
+    if (n < 1 || n > kMaxSplits) {  // device lengths disagree with the host schedule
+      if (h == 0) atomicExch(err, DEV_ERR_PLAN);
+      n = 0;
+    }
+    s_first = b + c0;
+    s_n = n;
+  }
+  __syncthreads();
+  const int first = s_first, n = s_n;
+  if (n == 0) return;
+  // v_i = 2^(m_i - M) l_i / sum_j 2^(m_j - M) l_j  (n <= 256: one share per thread)
+  const float mi = tid < n ? ml_part[((size_t)(first + tid) * HEADS + h) * 2] : -INFINITY;
+  float M = mi;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) s_red[warp] = M;
+  __syncthreads();
+  M = s_red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, s_red[w]);
+  __syncthreads();
+  float wl = 0.f;
+  if (tid < n) wl = exp2f(mi - M) * ml_part[((size_t)(first + tid) * HEADS + h) * 2 + 1];
+  float L = wl;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  if (lane == 0) s_red[warp] = L;
+  __syncthreads();
+  L = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) L += s_red[w];
+  if (tid < n) s_w[tid] = wl / L;
+  __syncthreads();
+  for (int d = tid; d < KV_LORA; d += 256) {
+    const __half* op = o_part + ((size_t)first * KV_LORA + d) * HEADS + h;
+    float acc = 0.f;
+    for (int i0 = 0; i0 < n; i0 += 16) {  // 16 independent loads in flight
+      float v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        v[k] = i0 + k < n ? __half2float(op[(size_t)(i0 + k) * KV_LORA * HEADS]) : 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (i0 + k < n) acc = fmaf(s_w[i0 + k], v[k], acc);
+    }
+    ol[d] = __bfloat162float(__float2bfloat16_rn(acc));
+  }
+  __syncthreads();
+  float x[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) x[i] = ol[lane * 16 + i];
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const uint32_t u[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+    float p = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(u[q] & 0xFFFF), __NV_E4M3);
+      __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(u[q] >> 16), __NV_E4M3);
+      const float2 fa = __half22float2(*reinterpret_cast<__half2*>(&lo));
+      const float2 fb = __half22float2(*reinterpret_cast<__half2*>(&hi));
+      p = fmaf(fa.x, x[4 * q], p);
+      p = fmaf(fa.y, x[4 * q + 1], p);
+      p = fmaf(fb.x, x[4 * q + 2], p);
+      p = fmaf(fb.y, x[4 * q + 3], p);
+    }
+    float t = sc * p;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    if (lane == 0) attn[(size_t)b * O_IN + h * VDIM + 16 * warp + r] = __float2bfloat16_rn(t);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_combine_absorb_out(const int* seq_lens, DecodePlan plan, const __half* o_part,
+                                      const float* ml_part, const uint8_t* Wkvb,
+                                      const float* Skvb, __nv_bfloat16* attn, int* err,
+                                      cudaStream_t st, bool pdl) {
+  if (plan.B == 0) return cudaSuccess;
+  return launch_kernel(combine_absorb_out_kernel, dim3(HEADS, plan.B), dim3(256), 0, st, pdl,
+                       seq_lens, plan.B, plan.G, plan.P, o_part, ml_part, Wkvb, Skvb, attn, err);
+}
 
 cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const __half* o_part,
                                   const float* ml_part, __nv_bfloat16* o_lat, int* err,

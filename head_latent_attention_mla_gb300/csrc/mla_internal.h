@@ -146,6 +146,17 @@ cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const __
                                   const float* ml_part, __nv_bfloat16* o_lat, int* err,
                                   cudaStream_t st, bool pdl = false);
 
+// Decode for a few sequences: the combine fused with the output absorption (one CTA per
+// head and sequence), and q_b_proj fused with the q-latent norm plus the kv cache-row append.
+cudaError_t launch_combine_absorb_out(const int* seq_lens, DecodePlan plan, const __half* o_part,
+                                      const float* ml_part, const uint8_t* Wkvb,
+                                      const float* Skvb, __nv_bfloat16* attn, int* err,
+                                      cudaStream_t st, bool pdl = false);
+cudaError_t launch_qb_norm(const float* g1, int M, const Proj& p, const __nv_bfloat16* gq,
+                           const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
+                           int rope_pairing, const int* seq_lens, __nv_bfloat16* cache, int cap,
+                           int limit, int* err, cudaStream_t st, bool pdl = false);
+
 // Split-KV decode attention over the latent cache on the tcgen05 tensor cores (TMA-fed,
 // accumulators in tensor memory): per work item, unnormalised partial outputs and (m, l).
 cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bfloat16* cache,
