@@ -101,13 +101,21 @@ __global__ void __launch_bounds__(kThreads) decode_combine_kernel(
 //   attn[b][128 h + v] = sum_c s[2h+1][c/128] * e4m3(W_kvb[256 h + 128 + v][c]) * o_lat[c]
 // ("Key content up-projection" page, W_UV,h = rows 128..255 of head h's 256).  Each warp owns 16
 // rows of W_UV,h, loaded into registers before the wait on the attention; one CTA per (h, b).
+// The share ranges come from the host's plan (and the device length is checked against it),
+// and every load after the wait is issued at once: the work after the attention is one memory
+// round trip.
+struct ShareRanges {
+  int first[8], n[8], len[8];  // slot of the first share, number of shares, length (host)
+};
+constexpr int CAO_BATCH = 16;  // shares per round of loads
+
 __global__ void __launch_bounds__(256) combine_absorb_out_kernel(
-    const int* __restrict__ seq_lens, int B, int G, long long P, const __half* __restrict__ o_part,
-    const float* __restrict__ ml_part, const uint8_t* __restrict__ Wkvb,
-    const float* __restrict__ Skvb, __nv_bfloat16* __restrict__ attn, int* err) {
+    const int* __restrict__ seq_lens, const __grid_constant__ ShareRanges sr,
+    const __half* __restrict__ o_part, const float* __restrict__ ml_part,
+    const uint8_t* __restrict__ Wkvb, const float* __restrict__ Skvb,
+    __nv_bfloat16* __restrict__ attn, int* err) {
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  __shared__ int s_first, s_n;
   __shared__ float s_w[kMaxSplits];
   __shared__ float s_red[8];
   __shared__ __align__(16) float ol[KV_LORA];
@@ -121,29 +129,28 @@ __global__ void __launch_bounds__(256) combine_absorb_out_kernel(
                  : "l"(src));
   }
   const float sc = __ldg(Skvb + (size_t)(2 * h + 1) * (KV_LORA / BLK) + lane / 8);
+  const int first = sr.first[b], n = sr.n[b];
   pdl_launch_dependents();
   pdl_wait();  // the attention's partials are complete
-  if (tid == 0) {
-    long long start = 0;
-    for (int bb = 0; bb < b; ++bb) start += (long long)seq_lens[bb] + 1;
-    const long long end = start + seq_lens[b] + 1;
-    int c0 = 0, n = 0;
-    if (end <= P) {
-      c0 = decode_share_of(start, G, P);
-      n = decode_share_of(end - 1, G, P) - c0 + 1;
-    }
-    if (n < 1 || n > kMaxSplits) {  // device lengths disagree with the host schedule
-      if (h == 0) atomicExch(err, DEV_ERR_PLAN);
-      n = 0;
-    }
-    s_first = b + c0;
-    s_n = n;
+  // Loads first: (m, l) of share tid, and this thread's two dims of the first shares.
+  const bool own = tid < n;
+  float mi = -INFINITY, li = 0.f;
+  if (own) {
+    const float2 v = *reinterpret_cast<const float2*>(ml_part + ((size_t)(first + tid) * HEADS + h) * 2);
+    mi = v.x;
+    li = v.y;
   }
-  __syncthreads();
-  const int first = s_first, n = s_n;
-  if (n == 0) return;
+  const __half* op0 = o_part + ((size_t)first * KV_LORA + tid) * HEADS + h;
+  const __half* op1 = op0 + (size_t)256 * HEADS;
+  float v0[CAO_BATCH], v1[CAO_BATCH];
+#pragma unroll
+  for (int k = 0; k < CAO_BATCH; ++k) {
+    v0[k] = k < n ? __half2float(op0[(size_t)k * KV_LORA * HEADS]) : 0.f;
+    v1[k] = k < n ? __half2float(op1[(size_t)k * KV_LORA * HEADS]) : 0.f;
+  }
+  if (tid == 0 && h == 0 && seq_lens[b] != sr.len[b])  // lengths disagree with the host plan
+    atomicExch(err, DEV_ERR_PLAN);
   // v_i = 2^(m_i - M) l_i / sum_j 2^(m_j - M) l_j  (n <= 256: one share per thread)
-  const float mi = tid < n ? ml_part[((size_t)(first + tid) * HEADS + h) * 2] : -INFINITY;
   float M = mi;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -153,8 +160,7 @@ __global__ void __launch_bounds__(256) combine_absorb_out_kernel(
 #pragma unroll
   for (int w = 1; w < 8; ++w) M = fmaxf(M, s_red[w]);
   __syncthreads();
-  float wl = 0.f;
-  if (tid < n) wl = exp2f(mi - M) * ml_part[((size_t)(first + tid) * HEADS + h) * 2 + 1];
+  const float wl = own ? exp2f(mi - M) * li : 0.f;
   float L = wl;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
@@ -163,22 +169,30 @@ __global__ void __launch_bounds__(256) combine_absorb_out_kernel(
   L = 0.f;
 #pragma unroll
   for (int w = 0; w < 8; ++w) L += s_red[w];
-  if (tid < n) s_w[tid] = wl / L;
+  if (own) s_w[tid] = wl / L;
   __syncthreads();
-  for (int d = tid; d < KV_LORA; d += 256) {
-    const __half* op = o_part + ((size_t)first * KV_LORA + d) * HEADS + h;
-    float acc = 0.f;
-    for (int i0 = 0; i0 < n; i0 += 16) {  // 16 independent loads in flight
-      float v[16];
+  float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        v[k] = i0 + k < n ? __half2float(op[(size_t)(i0 + k) * KV_LORA * HEADS]) : 0.f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        if (i0 + k < n) acc = fmaf(s_w[i0 + k], v[k], acc);
+  for (int k = 0; k < CAO_BATCH; ++k)
+    if (k < n) {
+      a0 = fmaf(s_w[k], v0[k], a0);
+      a1 = fmaf(s_w[k], v1[k], a1);
     }
-    ol[d] = __bfloat162float(__float2bfloat16_rn(acc));
+  for (int i0 = CAO_BATCH; i0 < n; i0 += CAO_BATCH) {  // long contexts: more rounds
+#pragma unroll
+    for (int k = 0; k < CAO_BATCH; ++k) {
+      v0[k] = i0 + k < n ? __half2float(op0[(size_t)(i0 + k) * KV_LORA * HEADS]) : 0.f;
+      v1[k] = i0 + k < n ? __half2float(op1[(size_t)(i0 + k) * KV_LORA * HEADS]) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < CAO_BATCH; ++k)
+      if (i0 + k < n) {
+        a0 = fmaf(s_w[i0 + k], v0[k], a0);
+        a1 = fmaf(s_w[i0 + k], v1[k], a1);
+      }
   }
+  ol[tid] = __bfloat162float(__float2bfloat16_rn(a0));
+  ol[tid + 256] = __bfloat162float(__float2bfloat16_rn(a1));
   __syncthreads();
   float x[16];
 #pragma unroll
@@ -207,13 +221,26 @@ __global__ void __launch_bounds__(256) combine_absorb_out_kernel(
 
 }  // namespace
 
-cudaError_t launch_combine_absorb_out(const int* seq_lens, DecodePlan plan, const __half* o_part,
+cudaError_t launch_combine_absorb_out(const int* seq_lens, const int* lens_host,
+                                      DecodePlan plan, const __half* o_part,
                                       const float* ml_part, const uint8_t* Wkvb,
                                       const float* Skvb, __nv_bfloat16* attn, int* err,
                                       cudaStream_t st, bool pdl) {
   if (plan.B == 0) return cudaSuccess;
+  if (plan.B > 8) return cudaErrorInvalidValue;
+  ShareRanges sr{};
+  long long start = 0;
+  for (int b = 0; b < plan.B; ++b) {
+    const long long end = start + lens_host[b] + 1;
+    const int c0 = decode_share_of(start, plan.G, plan.P);
+    sr.first[b] = b + c0;
+    sr.n[b] = decode_share_of(end - 1, plan.G, plan.P) - c0 + 1;
+    sr.len[b] = lens_host[b];
+    if (sr.n[b] < 1 || sr.n[b] > kMaxSplits) return cudaErrorInvalidValue;
+    start = end;
+  }
   return launch_kernel(combine_absorb_out_kernel, dim3(HEADS, plan.B), dim3(256), 0, st, pdl,
-                       seq_lens, plan.B, plan.G, plan.P, o_part, ml_part, Wkvb, Skvb, attn, err);
+                       seq_lens, sr, o_part, ml_part, Wkvb, Skvb, attn, err);
 }
 
 cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const __half* o_part,

@@ -356,7 +356,7 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
                                                               c->cfg.softmax_scale, opart, ml,
                                                               c->d_err, s, true));
     MLA_LAUNCH("combine_absorb_out",
-               launch_combine_absorb_out(lens_dev, plan, opart, ml, c->W[MLA_W_KV_B],
+               launch_combine_absorb_out(lens_dev, lens_host, plan, opart, ml, c->W[MLA_W_KV_B],
                                          c->S[MLA_W_KV_B], attn, c->d_err, s, true));
     Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
     MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),

@@ -148,7 +148,8 @@ cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const __
 
 // Decode for a few sequences: the combine fused with the output absorption (one CTA per
 // head and sequence), and q_b_proj fused with the q-latent norm plus the kv cache-row append.
-cudaError_t launch_combine_absorb_out(const int* seq_lens, DecodePlan plan, const __half* o_part,
+cudaError_t launch_combine_absorb_out(const int* seq_lens, const int* lens_host,
+                                      DecodePlan plan, const __half* o_part,
                                       const float* ml_part, const uint8_t* Wkvb,
                                       const float* Skvb, __nv_bfloat16* attn, int* err,
                                       cudaStream_t st, bool pdl = false);
