@@ -69,7 +69,7 @@ __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* v) {
 
 __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
     const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_c,
-    const int* __restrict__ seq_lens, int B, int cap, int G, long long P, float scale_log2,
+    const int* __restrict__ seq_lens, int B, int cap, int G, long long P, int K, float scale_log2,
     __half* __restrict__ o_part, float* __restrict__ ml_part, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -106,15 +106,15 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
     bool bad = false;
     for (int b0 = 0; b0 < B; b0 += 32) {
       const int b = b0 + lane;
-      const long long S = b < B ? (long long)seq_lens[b] + 1 : 0;
+      const long long S = b < B ? (long long)seq_lens[b] + 1 + K : 0;
       long long inc = S;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const long long v = __shfl_up_sync(0xffffffffu, inc, off);
         if (lane >= off) inc += v;
       }
-      const long long acc = base + inc - S;  // first position of sequence b
-      const long long lo = max(acc, r0), hi = min(acc + S, r1);
+      const long long acc = base + inc - S + K;  // line position of sequence b's position 0
+      const long long lo = max(acc, r0), hi = min(acc + S - K, r1);
       const bool has = b < B && lo < hi;
       const unsigned mask = __ballot_sync(0xffffffffu, has);
       const int idx = nseg + __popc(mask & ((1u << lane) - 1u));
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
         seg[3 * idx + 2] = (int)(hi - acc);
       }
       nseg += __popc(mask);
-      bad |= __any_sync(0xffffffffu, b < B && S > cap) != 0;
+      bad |= __any_sync(0xffffffffu, b < B && S - K > cap) != 0;
       base += __shfl_sync(0xffffffffu, inc, 31);
     }
     if (lane == 0) {
@@ -479,7 +479,7 @@ cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bf
       !make_tmap_2d(&mc, true, cache, LAT, (uint64_t)plan.B * cap, LAT * 2, 64, DA_TILE))
     return cudaErrorInvalidValue;
   return launch_kernel(decode_attn_tc_kernel, dim3(plan.G), dim3(DA_THREADS), DA_SMEM, st, pdl,
-                       mq, mc, seq_lens, plan.B, cap, plan.G, plan.P,
+                       mq, mc, seq_lens, plan.B, cap, plan.G, plan.P, plan.K,
                        scale * 1.4426950408889634f, o_part, ml_part, err);
 }
 

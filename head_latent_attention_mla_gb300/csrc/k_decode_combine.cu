@@ -19,7 +19,7 @@ constexpr int kThreads = 256;
 // (one thread per head, each group every fourth share).  Partials are fp16 [slot][dim][head]:
 // a thread then owns two heads and four dims, so a warp reads 128 contiguous bytes per dim.
 __global__ void __launch_bounds__(kThreads) decode_combine_kernel(
-    const int* __restrict__ seq_lens, int B, int G, long long P,
+    const int* __restrict__ seq_lens, int B, int G, long long P, int K,
     const __half* __restrict__ o_part, const float* __restrict__ ml_part,
     __nv_bfloat16* __restrict__ o_lat, int* err) {
   const int b = blockIdx.x, tid = threadIdx.x;
@@ -29,8 +29,8 @@ __global__ void __launch_bounds__(kThreads) decode_combine_kernel(
   pdl_launch_dependents();
   pdl_wait();
   if (tid == 0) {
-    long long start = 0;
-    for (int bb = 0; bb < b; ++bb) start += (long long)seq_lens[bb] + 1;
+    long long start = K;  // line position of sequence b's position 0
+    for (int bb = 0; bb < b; ++bb) start += (long long)seq_lens[bb] + 1 + K;
     const long long end = start + seq_lens[b] + 1;
     int c0 = 0, n = 0;
     if (end <= P) {
@@ -229,7 +229,7 @@ cudaError_t launch_combine_absorb_out(const int* seq_lens, const int* lens_host,
   if (plan.B == 0) return cudaSuccess;
   if (plan.B > 8) return cudaErrorInvalidValue;
   ShareRanges sr{};
-  long long start = 0;
+  long long start = plan.K;  // line position of sequence b's position 0
   for (int b = 0; b < plan.B; ++b) {
     const long long end = start + lens_host[b] + 1;
     const int c0 = decode_share_of(start, plan.G, plan.P);
@@ -237,7 +237,7 @@ cudaError_t launch_combine_absorb_out(const int* seq_lens, const int* lens_host,
     sr.n[b] = decode_share_of(end - 1, plan.G, plan.P) - c0 + 1;
     sr.len[b] = lens_host[b];
     if (sr.n[b] < 1 || sr.n[b] > kMaxSplits) return cudaErrorInvalidValue;
-    start = end;
+    start = end + plan.K;
   }
   return launch_kernel(combine_absorb_out_kernel, dim3(HEADS, plan.B), dim3(256), 0, st, pdl,
                        seq_lens, sr, o_part, ml_part, Wkvb, Skvb, attn, err);
@@ -248,7 +248,8 @@ cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const __
                                   cudaStream_t st, bool pdl) {
   if (plan.B == 0) return cudaSuccess;
   return launch_kernel(decode_combine_kernel, dim3(plan.B, KV_LORA / kDims), dim3(kThreads), 0,
-                       st, pdl, seq_lens, plan.B, plan.G, plan.P, o_part, ml_part, o_lat, err);
+                       st, pdl, seq_lens, plan.B, plan.G, plan.P, plan.K, o_part, ml_part, o_lat,
+                       err);
 }
 
 }  // namespace mla

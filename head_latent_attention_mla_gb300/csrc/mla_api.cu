@@ -342,10 +342,11 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
   Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
                 {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
   MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-  if (gemm_can_advance(B)) {
-    // A few sequences: six kernels.  q_b_proj normalises the q latent itself (and one of its
-    // CTAs appends the cache rows); the combine is fused with the W_UV absorption; the length
-    // update rides on o_proj.
+  if (B <= 2) {
+    // One or two sequences: six kernels.  q_b_proj normalises the q latent itself (and one of
+    // its CTAs appends the cache rows); the combine is fused with the W_UV absorption; the
+    // length update rides on o_proj.  (Every q_b CTA normalises every token, and every
+    // (head, sequence) CTA reads its head's W_UV: both pay only for very few sequences.)
     Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
     MLA_LAUNCH("gemm_q_b_norm", launch_qb_norm(g1, B, p2, c->gain[0], c->gain[1], c->cfg.eps,
                                                c->rope_tab, c->cfg.rope_pairing, lens_dev, C, cap,
@@ -379,9 +380,14 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
   MLA_LAUNCH("absorb_out", launch_absorb_out(olat, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], attn, s,
                                                  true));
   Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
-  MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
-                                   c->num_sms, c->d_err, s, nullptr, 0, 0, true));
-  MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, 1, s));
+  if (gemm_can_advance(B)) {  // the length update rides on the last kernel
+    MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
+                                     c->num_sms, c->d_err, s, lens_dev, B, 1, true));
+  } else {
+    MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
+                                     c->num_sms, c->d_err, s, nullptr, 0, 0, true));
+    MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, 1, s));
+  }
   return MLA_OK;
 }
 

@@ -112,11 +112,16 @@ cudaError_t launch_absorb_q(const __nv_bfloat16* q, int B, const uint8_t* Wkvb,
                             cudaStream_t st, bool pdl = false);
 
 // Split-KV decode attention over the latent cache, then the log-sum-exp combine.
+// The shares are cut from a line on which sequence b occupies K positions that hold no work
+// (they stand for the cost of a segment: a query reload, a partial tile and an epilogue)
+// followed by its seq_lens[b] + 1 real positions; K = 0 for a single sequence.
 struct DecodePlan {
   int B;
-  int G;            // CTAs: the concatenated positions are cut into G equal shares
-  long long P;      // total positions, sum over b of (seq_lens[b] + 1)
+  int G;            // CTAs: the line is cut into G equal shares
+  long long P;      // length of the line, sum over b of (K + seq_lens[b] + 1)
+  int K;            // positions charged per sequence
 };
+constexpr int kDecodeSeqCost = 96;
 // First position (in the concatenation of all sequences) of CTA c's share.
 __host__ __device__ inline long long decode_share_start(int c, int G, long long P) {
   return (long long)c * P / G;
@@ -140,7 +145,8 @@ inline DecodePlan make_decode_plan(int B, long long P, int num_sms, int max_slot
   if (G > kMaxDecodeShares) G = kMaxDecodeShares;
   if (G > max_slots - B) G = max_slots - B;
   if (G < 1) G = 1;
-  return DecodePlan{B, (int)G, P};
+  const int K = B > 1 ? kDecodeSeqCost : 0;
+  return DecodePlan{B, (int)G, P + (long long)B * K, K};
 }
 cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const __half* o_part,
                                   const float* ml_part, __nv_bfloat16* o_lat, int* err,
