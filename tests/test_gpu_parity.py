@@ -142,9 +142,13 @@ def test_decode_config5_long_b8_sampled(layer):
     assert_close(got_rows, full[[0, 77777, L]], "long cache rows")
 
 
-@pytest.mark.parametrize("lengths", [[0], [1, 63, 64, 65, 127, 128, 129, 200]])
+# One sequence and two take the six-kernel decode (fused q-latent norm and cache append, fused
+# combine and W_UV); three to eight the separate kernels with GEMV projections.
+@pytest.mark.parametrize("lengths", [[0], [65, 300], [5, 64, 129],
+                                     [1, 63, 64, 65, 127, 128, 129, 200]])
 def test_decode_tile_edges_every_sequence(layer, lengths):
-    """Empty cache (p=0) and lengths around the 64-position tile edges, all sequences checked."""
+    """Empty cache (p=0) and lengths around the 64-position tile edges, all sequences checked,
+    with the cache row each decode appends."""
     W = oracle_weights(0)
     cap = max(lengths) + 3
     cache, lens = build_caches_gpu(layer, 0, lengths, cap)
@@ -152,11 +156,14 @@ def test_decode_tile_edges_every_sequence(layer, lengths):
     yd = layer.decode(to_dev(xb), cache, lens, lengths)
     torch.cuda.synchronize()
     assert layer.status() == mla.MLA_OK
+    assert lens.tolist() == [n + 1 for n in lengths]
     yd = yd.float().cpu().numpy()
     for b, n in enumerate(lengths):
         c_ref = oracle_cache(0, b, n, W) if n else None
         y_ref, _ = O.decode(O.bf16_to_f64(xb[b]), c_ref if n else np.zeros((0, 576)), W)
         assert_close(yd[b], y_ref, f"decode len {n}")
+        row_ref = O.cache_rows(O.bf16_to_f64(xb[b])[None], np.array([n]), W)
+        assert_close(cache[b, n:n + 1].float().cpu().numpy(), row_ref, f"appended row {n}")
 
 
 def test_decode_growing_scores_rescale(layer):
