@@ -5,7 +5,7 @@
 // softmax scale, key s visible from query t iff s <= t, fp32 softmax over keys, o = P v (128).
 // The head dimensions stay 192 / 128 (no padding of v to 192).
 //
-// One CTA per (head, 128-query tile, sequence), heaviest query tiles first, 12 warps:
+// One CTA per (head, 128-query tile, sequence), heaviest query tiles first, 20 warps:
 //   warp 0      TMA producer of the query tile (3 boxes of 64 columns) and, for every 128-key
 //               tile, of k = [k_nope (2 boxes) | rotary key from the cache rows (1 box)] into
 //               a two-stage ring that MMA1 releases (128-byte swizzle, 3-D maps over
@@ -15,8 +15,8 @@
 //   warp 1      allocates tensor memory and issues MMA1  S = Q K^T  (M=128, N=128, K=192);
 //   warp 6      issues MMA2  O += P V  (M=128, N=128, K=128) with P read from tensor memory
 //               and v read MN-major;
-//   warps 2..5, 8..11  softmax, two threads per query row (columns 0..63 and 64..127 of S, P
-//               and O; the halves trade row maxima through shared memory): causal mask on the
+//   warps 2..5, 8..19  softmax, four threads per query row (32 columns each of S, P and O;
+//               the four trade row maxima through shared memory): causal mask on the
 //               diagonal tile, online softmax in base 2 with a lazy rescale of O (only when the
 //               running maximum grows by more than 2^8), P written to tensor memory as packed
 //               bf16; then the epilogue normalises O and stores it as bf16.
@@ -37,15 +37,17 @@ constexpr int PA_BOX = 128 * 128;                 // [128 rows x 64 bf16] box, b
 constexpr int PA_Q_BYTES = 3 * PA_BOX;            // q tile: 192 columns
 constexpr int PA_K_BYTES = 3 * PA_BOX;            // k tile: 128 nope + 64 rotary
 constexpr int PA_V_BYTES = 2 * PA_BOX;            // v tile: 128 columns
-constexpr int PA_THREADS = 384;
-constexpr int PA_SM_THREADS = 256;                 // softmax threads (two per query row)
+constexpr int PA_NG = 4;                           // softmax threads per query row
+constexpr int PA_GC = PA_TILE / PA_NG;             // columns of S, P and O per thread (32)
+constexpr int PA_SM_THREADS = 128 * PA_NG;         // softmax threads
+constexpr int PA_THREADS = 128 + PA_SM_THREADS;    // + 4 warps: TMA k, MMA1, MMA2, TMA v
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + PA_Q_BYTES;          // two k stages
 constexpr int OFF_V = OFF_K + 2 * PA_K_BYTES;      // two v stages
 constexpr int OFF_BAR = OFF_V + 2 * PA_V_BYTES;
 constexpr int OFF_MISC = OFF_BAR + 16 * 8;
-constexpr int OFF_XCH = OFF_MISC + 16;            // [2 tile parities][2 halves][128 rows]
-constexpr int PA_SMEM = OFF_XCH + 2 * 2 * 128 * 4 + 1024;
+constexpr int OFF_XCH = OFF_MISC + 16;            // [2 tile parities][PA_NG groups][128 rows]
+constexpr int PA_SMEM = OFF_XCH + 2 * PA_NG * 128 * 4 + 1024;
 constexpr uint32_t TM_O = 0, TM_S = 128, TM_P = 384;
 constexpr float RESCALE_LOG2 = 8.f;
 
@@ -215,34 +217,35 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
       mbar_wait(&mma_idle[1], 0, err, &no_abort);
     }
   } else if ((warp >= 2 && warp <= 5) || warp >= 8) {
+    static_assert(PA_GC == 32, "one 32-column chunk per softmax thread");
     // -------------------------------------------------------------------- softmax warps
     // Every softmax thread reaches the same named barriers in every tile it starts; a failed
     // wait is published in s_fail before the tile's second barrier, and all threads leave
     // together after it, so no barrier is left waiting for a thread that has gone.
     const int qw = warp & 3;
-    const int half = warp >= 8 ? 1 : 0;           // columns [64 half, 64 half + 64)
+    const int grp = warp < 8 ? 0 : (warp - 4) / 4;  // columns [32 grp, 32 grp + 32)
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
     const int row = 32 * qw + lane;
     const int qi = q0 + row;                      // query position of this thread's row
     float* xch = reinterpret_cast<float*>(smem + OFF_XCH);
     volatile int* s_fail = reinterpret_cast<volatile int*>(smem + OFF_MISC) + 2;
-    float m = -INFINITY, l = 0.f;                 // running maximum; this half's sum
+    float m = -INFINITY, l = 0.f;                 // running maximum; this group's sum
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       const int st = j & 1;
       ok = mbar_wait(&s_full[st], (j >> 1) & 1, err, abort_flag);
       fence_after();
-      // The half row is read from tensor memory twice, 32 columns at a time, in rolled loops
-      // (small code: a fully unrolled row overflows the instruction cache).
-      const uint32_t s_addr = tmem + lane_off + TM_S + 128 * st + 64 * half;
-      const int kbase = j * PA_TILE + 64 * half;
-      const int vis = min(qi - kbase + 1, T - kbase);   // columns [0, vis) of this half visible
+      // The thread's 32 columns are read from tensor memory twice (the code stays small: a
+      // fully unrolled row overflows the instruction cache).
+      const uint32_t s_addr = tmem + lane_off + TM_S + 128 * st + PA_GC * grp;
+      const int kbase = j * PA_TILE + PA_GC * grp;
+      const int vis = min(qi - kbase + 1, T - kbase);   // columns [0, vis) of this group visible
       // Tiles left of the diagonal are visible to every row: no mask there.
       const bool full = j < qt;
       float tmax = -INFINITY;  // pass 1: maximum of the visible scores
       if (ok) {
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < PA_GC / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(s_addr + 32 * c, r);
           tmem_wait_ld();
@@ -256,9 +259,11 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
           }
         }
       }
-      xch[(2 * st + half) * 128 + row] = tmax;
+      xch[(PA_NG * st + grp) * 128 + row] = tmax;
       named_bar(1, PA_SM_THREADS);
-      tmax = fmaxf(tmax, xch[(2 * st + (half ^ 1)) * 128 + row]) * scale_log2;  // scale > 0
+#pragma unroll
+      for (int g = 0; g < PA_NG; ++g) tmax = fmaxf(tmax, xch[(PA_NG * st + g) * 128 + row]);
+      tmax *= scale_log2;  // scale > 0
       float alpha = 1.f;
       bool need = false;
       if (tmax > m + RESCALE_LOG2) {
@@ -276,11 +281,11 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
       if (ok && j >= 2) ok = mbar_wait(&v_empty[st], ((j - 2) >> 1) & 1, err, abort_flag);
       // Pass 2: p = 2^(s * scale - m), rounded to bf16, into P (16 packed columns per chunk);
       // l sums the unrounded p.
-      const uint32_t p_addr = tmem + lane_off + TM_P + 64 * st + 32 * half;
+      const uint32_t p_addr = tmem + lane_off + TM_P + 64 * st + (PA_GC / 2) * grp;
       float lsum = 0.f;
       if (ok) {
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < PA_GC / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(s_addr + 32 * c, r);
           tmem_wait_ld();
@@ -329,9 +334,9 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
         if (!ok) break;  // cannot happen once another thread's identical wait succeeded
         fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < PA_GC / 32; ++c) {
           uint32_t o[32];
-          const uint32_t ta = tmem + lane_off + TM_O + 64 * half + 32 * c;
+          const uint32_t ta = tmem + lane_off + TM_O + PA_GC * grp + 32 * c;
           tmem_ld32(ta, o);
           tmem_wait_ld();
 #pragma unroll
@@ -343,20 +348,22 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
       fence_before();
       mbar_arrive(&p_full[st]);
     }
-    // Epilogue: the row's sum from both halves, O / l as bf16, this half's 64 value dims.
+    // Epilogue: the row's sum from all groups, O / l as bf16, this group's 32 value dims.
     if (ok) ok = mbar_wait(&v_empty[(nt - 1) & 1], ((nt - 1) >> 1) & 1, err, abort_flag);
     if (!ok) *s_fail = 1;
-    xch[half * 128 + row] = l;
+    xch[grp * 128 + row] = l;
     named_bar(1, PA_SM_THREADS);
     if (!*s_fail) {
       fence_after();
-      const float lrow = l + xch[(half ^ 1) * 128 + row];
+      float lrow = 0.f;
+#pragma unroll
+      for (int g = 0; g < PA_NG; ++g) lrow += xch[g * 128 + row];
       const float inv = (lrow > 0.f) ? 1.f / lrow : 0.f;
-      __nv_bfloat16* dst = attn_out + (size_t)(tok0 + qi) * O_IN + h * VDIM + 64 * half;
+      __nv_bfloat16* dst = attn_out + (size_t)(tok0 + qi) * O_IN + h * VDIM + PA_GC * grp;
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < PA_GC / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + TM_O + 64 * half + 32 * c, o);
+        tmem_ld32(tmem + lane_off + TM_O + PA_GC * grp + 32 * c, o);
         tmem_wait_ld();
         if (qi < T) {
 #pragma unroll
