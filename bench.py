@@ -306,16 +306,38 @@ def prefill_flops(T):
     return gemm, attn
 
 
+def init_replicas(dist, backend):
+    """Rank, world size and local rank from the launcher's environment; joins the process group
+    when there is more than one rank.  Each rank is an independent replica of the whole step:
+    the only traffic between ranks is the barrier around the timed region and the reduction of
+    its result."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def aggregate_replicas(torch, dist, ms, units, device="cpu"):
+    """Whole-job figure over all replicas: the slowest rank's step time (ms), the units every
+    rank processed per step, and units per second over that time.  `dist` is None on one rank."""
+    if dist is None:
+        return ms, units, units * 1000.0 / ms
+    t_ms = torch.tensor([ms], dtype=torch.float64, device=device)
+    t_units = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t_ms, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t_units, op=dist.ReduceOp.SUM)
+    ms_max, total = float(t_ms.item()), int(round(t_units.item()))
+    return ms_max, total, total * 1000.0 / ms_max
+
+
 def gpu_arm(args):
     import torch
     import torch.distributed as dist
     from head_latent_attention_mla_gb300 import mla, synth
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    world, rank, local = init_replicas(dist, "nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     device = f"cuda:{local}"
     mla.load()
@@ -337,13 +359,8 @@ def gpu_arm(args):
         res = run_decode_workload(torch, mla, synth, layer, "decode_b1_p1000", [1000], "prefill",
                                   args.steps, args.warmup, device, flush, clk=clk)
     barrier()
-    ms = res["ms"]
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
     B = res["B"]
-    value = world * B * 1000.0 / ms
+    ms, _, value = aggregate_replicas(torch, dist if world > 1 else None, res["ms"], B, device)
     per = res["per_kernel_ms"]
     dom = max(per, key=per.get)
     abytes = algorithmic_bytes(dom, B, res["lengths"])
