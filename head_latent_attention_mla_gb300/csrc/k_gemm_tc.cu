@@ -35,22 +35,39 @@ namespace {
 using namespace tc;
 
 constexpr int GT_THREADS = 320;
-constexpr int GT_STAGES = 4;
-constexpr int GT_NACC = 4;                     // tensor-memory accumulators
-constexpr int W_TILE = 128 * 128;              // e4m3 bytes of one weight tile
 constexpr float E4M3_MAX = 448.f;
+constexpr int W_TILE = 128 * 128;              // e4m3 bytes of one weight tile
+// Bytes of the stage ring.  The loads, not the tensor cores, set the pace: a stage is busy for
+// its load latency (about 2 us under full load) plus its MMAs, so the ring is as large as
+// shared memory allows.  Stages of 128-byte rows: halving them to 64-byte rows (twice the
+// stages, twice the copy requests) measured slower.
+constexpr int GT_RING = 192 * 1024;
 
-template <int BN>
+// BN tokens per unit; WT weight tiles (of 128 features) per unit.  WT = 2 reads the token
+// tile once for 256 features: 1.5x the MMA work per staged byte.
+template <int BN, int WT>
 struct GemmSmem {
-  static constexpr int X_TILE = BN * 128;      // e4m3 token tile [BN x 128]
-  static constexpr int STAGE = W_TILE + 2 * X_TILE;
+  static constexpr int NACC = WT == 2 ? 2 : 4;   // tensor-memory accumulators
+  static constexpr int ACC_COLS = WT * BN;       // columns of one accumulator (WT halves)
+  static constexpr int X_TILE = BN * 128;        // e4m3 token tile [BN x 128]
+  static constexpr int W_BYTES = WT * W_TILE;
+  static constexpr int STAGE = W_BYTES + 2 * X_TILE;
+  static constexpr int STAGES = GT_RING / STAGE;
   static constexpr int OFF_IN = 0;
-  static constexpr int OFF_BAR = OFF_IN + GT_STAGES * STAGE;
+  static constexpr int OFF_BAR = OFF_IN + STAGES * STAGE;
   static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
   static constexpr int BYTES = OFF_MISC + 16 + 1024;
-  static constexpr int NGRP = BN >= 64 ? 2 : 1;  // epilogue warpgroups
-  static constexpr int CW = BN / NGRP;           // token columns per epilogue thread
-  static constexpr uint32_t TMEM_COLS = GT_NACC * BN < 32 ? 32 : GT_NACC * BN;
+  // Epilogue warpgroups: one per weight half when WT = 2 (each holds all BN token columns of
+  // its 128 features), else two (one) splitting the token columns.
+  static constexpr int NGRP = WT == 2 ? 2 : (BN >= 64 ? 2 : 1);
+  static constexpr int CW = WT == 2 ? BN : BN / NGRP;  // token columns per epilogue thread
+  static constexpr int CH = WT == 2 ? 16 : CW;    // columns read from TMEM at once
+  static constexpr uint32_t TMEM_COLS = NACC * ACC_COLS < 32 ? 32 : NACC * ACC_COLS;
+  static_assert(2 * STAGES + 2 * NACC + 1 <= 32, "barrier space");
+  static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte alignment of the ring");
+  static_assert(TMEM_COLS <= 512, "tensor memory");
+  static_assert(BYTES <= 227 * 1024, "shared memory");
+  static_assert(CW % 32 == 0 && CW % CH == 0 && (CH == 16 || CH % 32 == 0), "epilogue columns");
 };
 
 struct GemmTcArgs {
@@ -76,7 +93,7 @@ struct GemmTcArgs {
 struct Unit {
   int prob, n0, m0, split, kb_begin, kb_end;
 };
-__device__ __forceinline__ Unit unit_of(const GemmTcArgs& a, int u, int BN) {
+__device__ __forceinline__ Unit unit_of(const GemmTcArgs& a, int u, int BN, int WT) {
   Unit r;
   r.split = u % a.splits;
   const int t = u / a.splits;
@@ -84,7 +101,7 @@ __device__ __forceinline__ Unit unit_of(const GemmTcArgs& a, int u, int BN) {
   int nt = t / a.m_tiles;
   r.prob = nt < a.n_tiles0 ? 0 : 1;
   if (r.prob) nt -= a.n_tiles0;
-  r.n0 = nt * 128;
+  r.n0 = nt * 128 * WT;
   r.m0 = mt * BN;
   const int nkb = a.K / BLK;
   r.kb_begin = (int)((long)nkb * r.split / a.splits);
@@ -145,12 +162,14 @@ __global__ void __launch_bounds__(256) split_e4m3_kernel(const __nv_bfloat16* __
   }
 }
 
-template <int BN>
+template <int BN, int WT>
 __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
     const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
     const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo,
-    GemmTcArgs args) {
-  using L = GemmSmem<BN>;
+    const __grid_constant__ GemmTcArgs args) {
+  using L = GemmSmem<BN, WT>;
+  constexpr int GT_STAGES = L::STAGES;
+  constexpr int GT_NACC = L::NACC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
@@ -199,19 +218,22 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
       int i = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-        const Unit U = unit_of(args, u, BN);
+        const Unit U = unit_of(args, u, BN, WT);
         const CUtensorMap* map_w = U.prob ? &map_w1 : &map_w0;
-        for (int kb = U.kb_begin; kb < U.kb_end; ++kb, ++i) {
+        for (int kb = U.kb_begin; ok && kb < U.kb_end; ++kb, ++i) {
           const int st = i % GT_STAGES;
           if (i >= GT_STAGES &&
               !(ok = mbar_wait(&in_empty[st], ((i / GT_STAGES) - 1) & 1, err, abort_flag)))
             break;
           uint8_t* stg = smem + L::OFF_IN + st * L::STAGE;
           const int k0 = kb * BLK;
-          mbar_expect_tx(&in_full[st], L::STAGE);
-          tma_load_2d(stg, map_w, &in_full[st], k0, U.n0);
-          tma_load_2d(stg + W_TILE, &map_hi, &in_full[st], k0, U.m0);
-          tma_load_2d(stg + W_TILE + L::X_TILE, &map_lo, &in_full[st], k0, U.m0);
+          // A weight half that lies wholly past N is neither loaded nor multiplied.
+          const int wt = (WT == 2 && U.n0 + 128 >= args.N[U.prob]) ? 1 : WT;
+          mbar_expect_tx(&in_full[st], L::STAGE - (WT - wt) * W_TILE);
+          for (int h = 0; h < wt; ++h)
+            tma_load_2d(stg + h * W_TILE, map_w, &in_full[st], k0, U.n0 + 128 * h);
+          tma_load_2d(stg + L::W_BYTES, &map_hi, &in_full[st], k0, U.m0);
+          tma_load_2d(stg + L::W_BYTES + L::X_TILE, &map_lo, &in_full[st], k0, U.m0);
         }
       }
       // Never leave the CTA with copies in flight: wait (bounded) for the last ones.
@@ -226,8 +248,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
       int i = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-        const Unit U = unit_of(args, u, BN);
-        for (int kb = U.kb_begin; kb < U.kb_end; ++kb, ++i) {
+        const Unit U = unit_of(args, u, BN, WT);
+        const int wt = (WT == 2 && U.n0 + 128 >= args.N[U.prob]) ? 1 : WT;
+        for (int kb = U.kb_begin; ok && kb < U.kb_end; ++kb, ++i) {
           const int st = i % GT_STAGES, ab = i % GT_NACC;
           if (!(ok = mbar_wait(&in_full[st], (i / GT_STAGES) & 1, err, abort_flag))) break;
           if (i >= GT_NACC &&
@@ -235,13 +258,16 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
             break;
           fence_after();
           const uint32_t w_base = sbase + L::OFF_IN + st * L::STAGE;
-          const uint64_t a0 = sdesc_sw128(w_base, 16, 1024);
-          const uint64_t h0 = sdesc_sw128(w_base + W_TILE, 16, 1024);
-          const uint64_t l0 = sdesc_sw128(w_base + W_TILE + L::X_TILE, 16, 1024);
+          const uint64_t h0 = sdesc_sw128(w_base + L::W_BYTES, 16, 1024);
+          const uint64_t l0 = sdesc_sw128(w_base + L::W_BYTES + L::X_TILE, 16, 1024);
+          for (int h = 0; h < wt; ++h) {
+            const uint64_t a0 = sdesc_sw128(w_base + h * W_TILE, 16, 1024);
+            const uint32_t d = tmem + ab * L::ACC_COLS + h * BN;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {  // descriptor address field counts 16-byte units
-            mma_e4m3(tmem + ab * BN, a0 + 2 * k, h0 + 2 * k, idesc, k > 0);
-            mma_e4m3(tmem + ab * BN, a0 + 2 * k, l0 + 2 * k, idesc, true);
+            for (int k = 0; k < 4; ++k) {  // descriptor address field counts 16-byte units
+              mma_e4m3(d, a0 + 2 * k, h0 + 2 * k, idesc, k > 0);
+              mma_e4m3(d, a0 + 2 * k, l0 + 2 * k, idesc, true);
+            }
           }
           mma_commit(&acc_full[ab]);
           mma_commit(&in_empty[st]);
@@ -253,37 +279,63 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
     }
   } else if ((warp - 2) / 4 < L::NGRP) {
     // -------------------------------------------------------------------- epilogue
-    constexpr int CW = L::CW;
+    constexpr int CW = L::CW, CH = L::CH;
     const int grp = (warp - 2) / 4, q = warp & 3;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-    const int col0 = grp * CW;  // first token column of this warpgroup
+    const int half = WT == 2 ? grp : 0;       // weight half (128 features) of this warpgroup
+    const int col0 = WT == 2 ? 0 : grp * CW;  // first token column of this warpgroup
     int i = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-      const Unit U = unit_of(args, u, BN);
-      const float* scales = args.S[U.prob] + (size_t)(U.n0 / BLK) * nkb_all;
+      const Unit U = unit_of(args, u, BN, WT);
+      const int nh = U.n0 + 128 * half;       // first feature of this warpgroup's half
+      const bool live = nh < args.N[U.prob];  // a half wholly past N was not multiplied
+      const float* scales = args.S[U.prob] + (size_t)(nh / BLK) * nkb_all;
       float acc[CW];
 #pragma unroll
       for (int j = 0; j < CW; ++j) acc[j] = 0.f;
       for (int kb = U.kb_begin; kb < U.kb_end; ++kb, ++i) {
         const int ab = i % GT_NACC;
-        if (!(ok = mbar_wait(&acc_full[ab], (i / GT_NACC) & 1, err, abort_flag))) break;
+        ok = mbar_wait(&acc_full[ab], (i / GT_NACC) & 1, err, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {  // the warp leaves together (loads are warp-wide)
+          ok = false;
+          break;
+        }
         fence_after();
-        uint32_t v[CW];
+        const float sc = live ? __ldg(scales + kb) : 0.f;
+        const uint32_t t0 = tmem + lane_off + ab * L::ACC_COLS + half * BN + col0;
 #pragma unroll
-        for (int c = 0; c < CW; c += 32)
-          tmem_ld32(tmem + lane_off + ab * BN + col0 + c, *reinterpret_cast<uint32_t(*)[32]>(v + c));
-        tmem_wait_ld();
-        fence_before();
-        mbar_arrive(&acc_empty[ab]);  // the values are in registers: the MMA may reuse it
-        const float sc = __ldg(scales + kb);
+        for (int c = 0; c < CW; c += CH) {
+          uint32_t v[CH];
+          if constexpr (CH == 16) {
+            tmem_ld32x16(t0 + c, v);
+          } else {
 #pragma unroll
-        for (int j = 0; j < CW; ++j) acc[j] = fmaf(sc, __uint_as_float(v[j]), acc[j]);
+            for (int cc = 0; cc < CH; cc += 32)
+              tmem_ld32(t0 + c + cc, *reinterpret_cast<uint32_t(*)[32]>(v + cc));
+          }
+          tmem_wait_ld();
+          if (c + CH >= CW) {
+            fence_before();
+            mbar_arrive(&acc_empty[ab]);  // the values are in registers: the MMA may reuse it
+          }
+#pragma unroll
+          for (int j = 0; j < CH; ++j) acc[c + j] = fmaf(sc, __uint_as_float(v[j]), acc[c + j]);
+        }
       }
       if (!ok) break;
-      const int n = U.n0 + 32 * q + lane;
+      // Token scales: lane l holds sx[m0 + l + 32c]; the warp passes them round by shuffles.
+      const int m0 = U.m0 + col0;
+      float sxr[CW / 32];
+#pragma unroll
+      for (int c = 0; c < CW / 32; ++c) {
+        const int m = m0 + 32 * c + lane;
+        sxr[c] = m < args.M ? __ldg(args.sx + m) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < CW; ++j) acc[j] *= __shfl_sync(0xffffffffu, sxr[j >> 5], j & 31);
+      const int n = nh + 32 * q + lane;
       if (n < args.N[U.prob]) {
-        const int m0 = U.m0 + col0;
         const int mend = min(CW, args.M - m0);
         const int ldy = args.ldy[U.prob];
         if (args.splits > 1) {
@@ -291,17 +343,17 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
                      (U.prob ? args.N[0] : 0) + n;
 #pragma unroll
           for (int j = 0; j < CW; ++j)
-            if (j < mend) p[(size_t)j * args.ldp] = acc[j] * __ldg(args.sx + m0 + j);
+            if (j < mend) p[(size_t)j * args.ldp] = acc[j];
         } else if (args.y_fp32[U.prob]) {
           float* y = reinterpret_cast<float*>(args.Y[U.prob]) + (size_t)m0 * ldy + n;
 #pragma unroll
           for (int j = 0; j < CW; ++j)
-            if (j < mend) y[(size_t)j * ldy] = acc[j] * __ldg(args.sx + m0 + j);
+            if (j < mend) y[(size_t)j * ldy] = acc[j];
         } else {
           __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(args.Y[U.prob]) + (size_t)m0 * ldy + n;
 #pragma unroll
           for (int j = 0; j < CW; ++j)
-            if (j < mend) y[(size_t)j * ldy] = __float2bfloat16_rn(acc[j] * __ldg(args.sx + m0 + j));
+            if (j < mend) y[(size_t)j * ldy] = __float2bfloat16_rn(acc[j]);
         }
       }
     }
@@ -329,12 +381,20 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
     reinterpret_cast<__nv_bfloat16*>(Y)[(size_t)m * ldy + n] = __float2bfloat16_rn(s);
 }
 
-template <int BN>
+template <int BN, int WT>
 cudaError_t launch_bn(const CUtensorMap* w, const CUtensorMap& hi, const CUtensorMap& lo,
                       const GemmTcArgs& a, int num_sms, cudaStream_t st) {
   const int grid = a.units < num_sms ? a.units : num_sms;
-  gemm_f8w_tc_kernel<BN><<<grid, GT_THREADS, GemmSmem<BN>::BYTES, st>>>(w[0], w[1], hi, lo, a);
+  gemm_f8w_tc_kernel<BN, WT><<<grid, GT_THREADS, GemmSmem<BN, WT>::BYTES, st>>>(w[0], w[1], hi,
+                                                                                lo, a);
   return cudaGetLastError();
+}
+
+template <int BN, int WT>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(gemm_f8w_tc_kernel<BN, WT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              GemmSmem<BN, WT>::BYTES);
 }
 
 constexpr size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -366,6 +426,25 @@ int gemm_splits(int M, int N_total, int K, int num_sms) {
   return best;
 }
 
+// Weight tiles per unit for a token count M: 2 (256 features against one token tile) when
+// there are more than 128 tokens, the reduction is long enough (K >= 4096) for the wider
+// unit's end-of-unit stores to stay hidden, and the rounds of units over the SMs, weighted by
+// the wide unit's measured cost (kWideCost x a narrow unit, for twice the work), come out
+// lower; else 1.
+constexpr double kWideCost = 1.7;
+int gemm_weight_tiles(int M, int K, const Proj* p, int np, int num_sms) {
+  if (M <= 128 || K < 4096) return 1;
+  const long m_tiles = (M + 127) / 128;
+  long t1 = 0, t2 = 0;
+  for (int i = 0; i < np; ++i) {
+    t1 += (p[i].N + 127) / 128;
+    t2 += (p[i].N + 255) / 256;
+  }
+  const long r1 = (t1 * m_tiles + num_sms - 1) / num_sms;
+  const long r2 = (t2 * m_tiles + num_sms - 1) / num_sms;
+  return kWideCost * (double)r2 < (double)r1 ? 2 : 1;
+}
+
 // Scratch of one tensor-core GEMM: hi and lo e4m3 copies of X [M, K], sx [M], and the split-K
 // partials.
 size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms) {
@@ -376,15 +455,10 @@ size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms) {
 }
 
 cudaError_t init_gemm_tc_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(gemm_f8w_tc_kernel<32>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       GemmSmem<32>::BYTES);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_f8w_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             GemmSmem<64>::BYTES);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_f8w_tc_kernel<128>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, GemmSmem<128>::BYTES);
+  cudaError_t e = set_smem_attr<32, 1>();
+  if (e == cudaSuccess) e = set_smem_attr<64, 1>();
+  if (e == cudaSuccess) e = set_smem_attr<128, 1>();
+  if (e == cudaSuccess) e = set_smem_attr<128, 2>();
   return e;
 }
 
@@ -425,17 +499,21 @@ cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const 
   if (!make_tmap_2d(&mh, false, hi, (uint64_t)K, (uint64_t)M, (uint64_t)K, 128, bn) ||
       !make_tmap_2d(&ml, false, lo, (uint64_t)K, (uint64_t)M, (uint64_t)K, 128, bn))
     return cudaErrorInvalidValue;
-  a.n_tiles0 = (p[0].N + 127) / 128;
-  a.n_tiles = a.n_tiles0 + (np > 1 ? (p[1].N + 127) / 128 : 0);
   a.m_tiles = (M + bn - 1) / bn;
   a.splits = gemm_splits(M, n_total, K, num_sms);
+  const int wt = gemm_weight_tiles(M, K, p, np, num_sms);
+  a.n_tiles0 = (p[0].N + 128 * wt - 1) / (128 * wt);
+  a.n_tiles = a.n_tiles0 + (np > 1 ? (p[1].N + 128 * wt - 1) / (128 * wt) : 0);
   a.units = a.n_tiles * a.m_tiles * a.splits;
   a.partial = partial;
   a.ldp = n_total;
   switch (bn) {
-    case 32: e = launch_bn<32>(mw, mh, ml, a, num_sms, st); break;
-    case 64: e = launch_bn<64>(mw, mh, ml, a, num_sms, st); break;
-    default: e = launch_bn<128>(mw, mh, ml, a, num_sms, st); break;
+    case 32: e = launch_bn<32, 1>(mw, mh, ml, a, num_sms, st); break;
+    case 64: e = launch_bn<64, 1>(mw, mh, ml, a, num_sms, st); break;
+    default:
+      e = wt == 2 ? launch_bn<128, 2>(mw, mh, ml, a, num_sms, st)
+                  : launch_bn<128, 1>(mw, mh, ml, a, num_sms, st);
+      break;
   }
   if (e != cudaSuccess || a.splits == 1) return e;
   for (int i = 0; i < np; ++i) {

@@ -47,9 +47,12 @@ def test_dequant_bit_exact(layer, name):
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
-@pytest.mark.parametrize("T", [1, 16, 130])
+@pytest.mark.parametrize("T", [1, 16, 130, 1200])
 def test_prefill_small_every_element(layer, T):
-    """Config-1 size (T=16) and tile edge cases (T=1, T=130 = two tiles and a ragged tail)."""
+    """Config-1 size (T=16) and tile edge cases (T=1, T=130 = two tiles and a ragged tail).
+    T=1200 runs the q_a/kv_a and o projections with 256-feature units over ten token tiles
+    (the last one ragged), including the kv_a unit whose second weight half lies wholly past
+    N=576."""
     W = oracle_weights(0)
     xb, y, cache = run_prefill(layer, [0], T)
     y_ref, cache_ref = O.prefill(O.bf16_to_f64(xb[0]), W)
