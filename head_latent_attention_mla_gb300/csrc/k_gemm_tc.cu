@@ -45,8 +45,15 @@ constexpr int GT_RING = 192 * 1024;
 
 // BN tokens per unit; WT weight tiles (of 128 features) per unit.  WT = 2 reads the token
 // tile once for 256 features: 1.5x the MMA work per staged byte.
+//
+// Orientation of the accumulator.  With BN = 128 the token tile is the MMA's A operand
+// (M = 128 tokens) and the weight tiles its B operand (N = 128 WT features): tensor-memory
+// lane = token, column = feature, so each epilogue thread ends a unit holding a run of one
+// output row and writes it as 16-byte vectors.  With fewer tokens (BN = 32, 64) the weight
+// tile is the A operand (M = 128 features, N = BN tokens): lane = feature, column = token.
 template <int BN, int WT>
 struct GemmSmem {
+  static constexpr bool TR = BN == 128;          // lane = token (else lane = feature)
   static constexpr int NACC = WT == 2 ? 2 : 4;   // tensor-memory accumulators
   static constexpr int ACC_COLS = WT * BN;       // columns of one accumulator (WT halves)
   static constexpr int X_TILE = BN * 128;        // e4m3 token tile [BN x 128]
@@ -57,13 +64,14 @@ struct GemmSmem {
   static constexpr int OFF_BAR = OFF_IN + STAGES * STAGE;
   static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
   static constexpr int BYTES = OFF_MISC + 16 + 1024;
-  // Epilogue warpgroups: one per weight half when WT = 2 (each holds all BN token columns of
-  // its 128 features), else two (one) splitting the token columns.
+  // Epilogue warpgroups: one per weight half when WT = 2 (each holds the 128 accumulator
+  // columns of its 128 features), else two (one) splitting the accumulator's columns.
   static constexpr int NGRP = WT == 2 ? 2 : (BN >= 64 ? 2 : 1);
-  static constexpr int CW = WT == 2 ? BN : BN / NGRP;  // token columns per epilogue thread
+  static constexpr int CW = WT == 2 ? 128 : BN / NGRP;  // accumulator columns per thread
   static constexpr int CH = WT == 2 ? 16 : CW;    // columns read from TMEM at once
   static constexpr uint32_t TMEM_COLS = NACC * ACC_COLS < 32 ? 32 : NACC * ACC_COLS;
   static_assert(2 * STAGES + 2 * NACC + 1 <= 32, "barrier space");
+  static_assert(WT == 1 || TR, "two weight tiles only with the token-lane orientation");
   static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte alignment of the ring");
   static_assert(TMEM_COLS <= 512, "tensor memory");
   static_assert(BYTES <= 227 * 1024, "shared memory");
@@ -162,6 +170,12 @@ __global__ void __launch_bounds__(256) split_e4m3_kernel(const __nv_bfloat16* __
   }
 }
 
+// Two floats as bf16 (round to nearest even), the first in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 template <int BN, int WT>
 __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
     const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
@@ -244,7 +258,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
   } else if (warp == 1) {
     // -------------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3(128, BN);
+      constexpr uint32_t idesc = idesc_e4m3(128, L::TR ? 128 : BN);
+      constexpr uint32_t idesc2 = idesc_e4m3(128, 256);  // token-lane, two weight tiles
       int i = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
@@ -260,11 +275,23 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
           const uint32_t w_base = sbase + L::OFF_IN + st * L::STAGE;
           const uint64_t h0 = sdesc_sw128(w_base + L::W_BYTES, 16, 1024);
           const uint64_t l0 = sdesc_sw128(w_base + L::W_BYTES + L::X_TILE, 16, 1024);
-          for (int h = 0; h < wt; ++h) {
-            const uint64_t a0 = sdesc_sw128(w_base + h * W_TILE, 16, 1024);
-            const uint32_t d = tmem + ab * L::ACC_COLS + h * BN;
+          if constexpr (L::TR) {
+            // D[token, feature]: A = token tile (hi, then lo), B = the wt weight tiles, which
+            // sit back to back as one operand of 128 wt rows.
+            const uint64_t b0 = sdesc_sw128(w_base, 16, 1024);
+            const uint32_t id = wt == 2 ? idesc2 : idesc;
+            const uint32_t d = tmem + ab * L::ACC_COLS;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {  // descriptor address field counts 16-byte units
+              mma_e4m3(d, h0 + 2 * k, b0 + 2 * k, id, k > 0);
+              mma_e4m3(d, l0 + 2 * k, b0 + 2 * k, id, true);
+            }
+          } else {
+            // D[feature, token]: A = the weight tile, B = token tile (hi, then lo).
+            const uint64_t a0 = sdesc_sw128(w_base, 16, 1024);
+            const uint32_t d = tmem + ab * L::ACC_COLS;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
               mma_e4m3(d, a0 + 2 * k, h0 + 2 * k, idesc, k > 0);
               mma_e4m3(d, a0 + 2 * k, l0 + 2 * k, idesc, true);
             }
@@ -283,7 +310,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
     const int grp = (warp - 2) / 4, q = warp & 3;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     const int half = WT == 2 ? grp : 0;       // weight half (128 features) of this warpgroup
-    const int col0 = WT == 2 ? 0 : grp * CW;  // first token column of this warpgroup
+    const int col0 = WT == 2 ? 0 : grp * CW;  // first accumulator column within the half
     int i = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
@@ -324,6 +351,42 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
         }
       }
       if (!ok) break;
+      if constexpr (L::TR) {
+        // Thread = token m; acc[j] = feature nh + col0 + j.  16-byte stores along the row.
+        const int m = U.m0 + 32 * q + lane;
+        const int nb = nh + col0;
+        const int nend = args.N[U.prob];
+        if (m < args.M) {
+          const float sxm = __ldg(args.sx + m);  // applied as each vector is formed
+          if (args.splits > 1 || args.y_fp32[U.prob]) {
+            float* y = args.splits > 1
+                           ? args.partial + ((size_t)U.split * args.M + m) * args.ldp +
+                                 (U.prob ? args.N[0] : 0) + nb
+                           : reinterpret_cast<float*>(args.Y[U.prob]) +
+                                 (size_t)m * args.ldy[U.prob] + nb;
+#pragma unroll
+            for (int j = 0; j < CW; j += 4)
+              if (nb + j < nend)
+                *reinterpret_cast<float4*>(y + j) = make_float4(
+                    acc[j] * sxm, acc[j + 1] * sxm, acc[j + 2] * sxm, acc[j + 3] * sxm);
+          } else {
+            __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(args.Y[U.prob]) +
+                               (size_t)m * args.ldy[U.prob] + nb;
+#pragma unroll
+            for (int j = 0; j < CW; j += 8)
+              if (nb + j < nend) {
+                uint4 v;
+                v.x = pack_bf16x2(acc[j] * sxm, acc[j + 1] * sxm);
+                v.y = pack_bf16x2(acc[j + 2] * sxm, acc[j + 3] * sxm);
+                v.z = pack_bf16x2(acc[j + 4] * sxm, acc[j + 5] * sxm);
+                v.w = pack_bf16x2(acc[j + 6] * sxm, acc[j + 7] * sxm);
+                *reinterpret_cast<uint4*>(y + j) = v;
+              }
+          }
+        }
+        continue;
+      }
+      // Feature-lane orientation.
       // Token scales: lane l holds sx[m0 + l + 32c]; the warp passes them round by shuffles.
       const int m0 = U.m0 + col0;
       float sxr[CW / 32];
@@ -427,13 +490,13 @@ int gemm_splits(int M, int N_total, int K, int num_sms) {
 }
 
 // Weight tiles per unit for a token count M: 2 (256 features against one token tile) when
-// there are more than 128 tokens, the reduction is long enough (K >= 4096) for the wider
-// unit's end-of-unit stores to stay hidden, and the rounds of units over the SMs, weighted by
-// the wide unit's measured cost (kWideCost x a narrow unit, for twice the work), come out
-// lower; else 1.
-constexpr double kWideCost = 1.7;
+// there are more than 128 tokens, the reduction spans at least 8 k blocks, and the rounds of
+// units over the SMs, weighted by the wide unit's cost (kWideCost x a narrow unit, for twice
+// the work), come out lower; else 1.  Measured wide/narrow unit costs on GB300: 1.3-1.5 for
+// K = 1536..8192, 2.0 for K = 512 (too few k blocks to gain).
+constexpr double kWideCost = 1.45;
 int gemm_weight_tiles(int M, int K, const Proj* p, int np, int num_sms) {
-  if (M <= 128 || K < 4096) return 1;
+  if (M <= 128 || K < 1024) return 1;
   const long m_tiles = (M + 127) / 128;
   long t1 = 0, t2 = 0;
   for (int i = 0; i < np; ++i) {

@@ -116,23 +116,57 @@ __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
   }
 }
 
-// In-place RoPE of q's rotary slices: one CTA per token, 64 heads x 32 pairs.
-__global__ void __launch_bounds__(256) rope_q_kernel(__nv_bfloat16* __restrict__ q, int T,
-                                                     const float2* __restrict__ rope_tab,
-                                                     int pairing, const int* __restrict__ seq_lens,
-                                                     int limit) {
+// In-place RoPE of q's rotary slices.  One CTA per token; eight threads per head, each with one
+// 16-byte chunk (8 values) of the head's 64 rotary values, so a warp reads and writes four
+// whole 128-byte slices.  Adjacent pairs lie inside a chunk; half pairs (j, j + 32) join chunk c
+// and chunk c + 4, which swap values with a shuffle.  The token's angles are staged once in
+// shared memory.
+__global__ void __launch_bounds__(HEADS * 8) rope_q_kernel(__nv_bfloat16* __restrict__ q, int T,
+                                                           const float2* __restrict__ rope_tab,
+                                                           int pairing,
+                                                           const int* __restrict__ seq_lens,
+                                                           int limit) {
+  __shared__ float2 cs[ROPE / 2];
   const int token = blockIdx.x, b = token / T, t = token % T;
   const int pos = seq_lens[b] + t;
-  if (pos < 0 || pos >= limit) return;
-  for (int i = threadIdx.x; i < HEADS * (ROPE / 2); i += blockDim.x) {
-    const int h = i / (ROPE / 2), j = i % (ROPE / 2);
-    const int2 ij = pair_idx(j, pairing);
-    __nv_bfloat16* qp = q + ((size_t)token * HEADS + h) * QHEAD + NOPE;
-    const float2 r = rotate(__bfloat162float(qp[ij.x]), __bfloat162float(qp[ij.y]),
-                            rope_tab[(size_t)pos * (ROPE / 2) + j]);
-    qp[ij.x] = __float2bfloat16_rn(r.x);
-    qp[ij.y] = __float2bfloat16_rn(r.y);
+  if (pos < 0 || pos >= limit) return;  // the same for the whole CTA
+  if (threadIdx.x < ROPE / 2) cs[threadIdx.x] = rope_tab[(size_t)pos * (ROPE / 2) + threadIdx.x];
+  __syncthreads();
+  const int h = threadIdx.x >> 3, c = threadIdx.x & 7;
+  uint4* p = reinterpret_cast<uint4*>(q + ((size_t)token * HEADS + h) * QHEAD + NOPE) + c;
+  const uint4 v = *p;
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float f[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    f[2 * e] = __uint_as_float(w[e] << 16);
+    f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
   }
+  if (pairing == 0) {  // pair j = 4c + e is (f[2e], f[2e + 1])
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 r = rotate(f[2 * e], f[2 * e + 1], cs[4 * c + e]);
+      f[2 * e] = r.x;
+      f[2 * e + 1] = r.y;
+    }
+  } else {  // pair j = 8 (c % 4) + k is (value k of chunk c % 4, value k of chunk c % 4 + 4)
+    float g[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) g[k] = __shfl_xor_sync(0xffffffffu, f[k], 4);
+    const bool first = c < 4;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float2 a = cs[8 * (c & 3) + k];
+      f[k] = first ? f[k] * a.x - g[k] * a.y : f[k] * a.x + g[k] * a.y;
+    }
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 v2 = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
+    o[e] = *reinterpret_cast<const uint32_t*>(&v2);
+  }
+  *p = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float* f) {
@@ -302,7 +336,7 @@ cudaError_t launch_norm_rope_cache(const float* g1, int B, int T, const __nv_bfl
 cudaError_t launch_rope_q(__nv_bfloat16* q, int B, int T, const float2* rope_tab,
                           int rope_pairing, const int* seq_lens, int limit, cudaStream_t st) {
   if (B * T == 0) return cudaSuccess;
-  rope_q_kernel<<<B * T, 256, 0, st>>>(q, T, rope_tab, rope_pairing, seq_lens, limit);
+  rope_q_kernel<<<B * T, HEADS * 8, 0, st>>>(q, T, rope_tab, rope_pairing, seq_lens, limit);
   return cudaGetLastError();
 }
 

@@ -47,9 +47,10 @@ def test_dequant_bit_exact(layer, name):
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
-@pytest.mark.parametrize("T", [1, 16, 130, 1200])
+@pytest.mark.parametrize("T", [1, 16, 100, 130, 1200])
 def test_prefill_small_every_element(layer, T):
     """Config-1 size (T=16) and tile edge cases (T=1, T=130 = two tiles and a ragged tail).
+    T=100 runs the projections as split-K over one partly filled 128-token tile.
     T=1200 runs the q_a/kv_a and o projections with 256-feature units over ten token tiles
     (the last one ragged), including the kv_a unit whose second weight half lies wholly past
     N=576."""
@@ -66,6 +67,31 @@ def test_prefill_batch_of_two(layer):
     for b, s in enumerate([3, 4]):
         y_ref, _ = O.prefill(O.bf16_to_f64(xb[b]), W)
         assert_close(y[b], y_ref, f"batch row {b}")
+
+
+@pytest.mark.parametrize("T", [16, 200])
+def test_half_pairing_prefill_and_decode(T):
+    """The half RoPE pairing (j, j+32): prefill (T=16: separate q RoPE kernel; T=200: RoPE in
+    the q_b GEMM epilogue) and one decode step after it, every element against the oracle."""
+    wq, g = weights_and_gains(0)
+    L = mla.MlaLayer(wq, g, rope_pairing=mla.MLA_ROPE_HALF)
+    try:
+        W = oracle_weights(0)
+        xb = synth.hidden_states(0, 5, 0, T + 1)
+        cache = torch.zeros(1, T + 1, 576, dtype=torch.bfloat16, device="cuda")
+        lens = torch.zeros(1, dtype=torch.int32, device="cuda")
+        y = L.prefill(to_dev(xb[None, :T]), cache, lens, [0])
+        yd = L.decode(to_dev(xb[T:T + 1]), cache, lens, [T])
+        torch.cuda.synchronize()
+        assert L.status() == mla.MLA_OK and lens.item() == T + 1
+        xf = O.bf16_to_f64(xb)
+        y_ref, cache_ref = O.prefill(xf[:T], W, pairing="half")
+        yd_ref, full_ref = O.decode(xf[T], cache_ref, W, pairing="half")
+        assert_close(y[0].float().cpu().numpy(), y_ref, f"half pairing prefill T={T}")
+        assert_close(yd[0].float().cpu().numpy(), yd_ref, f"half pairing decode p={T}")
+        assert_close(cache[0].float().cpu().numpy(), full_ref, f"half pairing cache T={T}")
+    finally:
+        L.close()
 
 
 def test_decode_config2_p1000(layer):
