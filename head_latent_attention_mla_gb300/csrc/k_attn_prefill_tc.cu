@@ -19,7 +19,8 @@
 //               the four trade row maxima through shared memory): causal mask on the
 //               diagonal tile, online softmax in base 2 with a lazy rescale of O (only when the
 //               running maximum grows by more than 2^8), P written to tensor memory as packed
-//               bf16; then the epilogue normalises O and stores it as bf16.
+//               bf16; then the epilogue normalises O and stores it as bf16, or as the two
+//               e4m3 terms and per-(token, head) scale that the o_proj GEMM reads.
 // MMA2 of a tile does not wait for the previous tile's: only a rescale of O needs the previous
 // MMA2 to be complete, and the softmax waits for it then.
 // Tensor memory: O in columns [0,128), S in [128,256) and [256,384), P in [384,448) and
@@ -73,7 +74,8 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
     const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
     const __grid_constant__ CUtensorMap map_c, int T, int cap, float scale_log2,
-    __nv_bfloat16* __restrict__ attn_out, int* err) {
+    __nv_bfloat16* __restrict__ attn_out, uint8_t* __restrict__ o_hi, uint8_t* __restrict__ o_lo,
+    float* __restrict__ o_sx, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
@@ -359,12 +361,12 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
 #pragma unroll
       for (int g = 0; g < PA_NG; ++g) lrow += xch[g * 128 + row];
       const float inv = (lrow > 0.f) ? 1.f / lrow : 0.f;
-      __nv_bfloat16* dst = attn_out + (size_t)(tok0 + qi) * O_IN + h * VDIM + PA_GC * grp;
-#pragma unroll 1
-      for (int c = 0; c < PA_GC / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_off + TM_O + PA_GC * grp + 32 * c, o);
-        tmem_wait_ld();
+      static_assert(PA_GC == 32, "one 32-column load per thread");
+      uint32_t o[32];
+      tmem_ld32(tmem + lane_off + TM_O + PA_GC * grp, o);
+      tmem_wait_ld();
+      const size_t at = (size_t)(tok0 + qi) * O_IN + h * VDIM + PA_GC * grp;
+      if (o_hi == nullptr) {
         if (qi < T) {
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
@@ -376,8 +378,42 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
                                                         __uint_as_float(o[i + 2 * e + 1]) * inv);
               u[e] = *reinterpret_cast<uint32_t*>(&pr);
             }
-            *reinterpret_cast<uint4*>(dst + 32 * c + i) = v;
+            *reinterpret_cast<uint4*>(attn_out + at + i) = v;
           }
+        }
+      } else {
+        // The bf16 output values, split into two e4m3 terms with one scale per (token, head):
+        // s = amax over the head's 128 values / 448 (the four threads of the row trade their
+        // maxima in the idle second half of xch), hi = e4m3(v / s), lo = e4m3(v / s - hi).
+        float v[32];
+        float am = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(o[i]) * inv));
+          am = fmaxf(am, fabsf(v[i]));
+        }
+        xch[PA_NG * 128 + grp * 128 + row] = am;
+        named_bar(1, PA_SM_THREADS);
+        float amax = 0.f;
+#pragma unroll
+        for (int g = 0; g < PA_NG; ++g) amax = fmaxf(amax, xch[PA_NG * 128 + g * 128 + row]);
+        const float sc = amax > 0.f ? amax / 448.f : 1.f;
+        const float is = 1.f / sc;
+        if (qi < T) {
+          uint32_t hw[8] = {}, lw[8] = {};
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t hl = e4m3_split2(make_float2(v[2 * i] * is, v[2 * i + 1] * is));
+            hw[i >> 1] |= (hl & 0xFFFFu) << (16 * (i & 1));
+            lw[i >> 1] |= (hl >> 16) << (16 * (i & 1));
+          }
+          uint4* dh = reinterpret_cast<uint4*>(o_hi + at);
+          uint4* dl = reinterpret_cast<uint4*>(o_lo + at);
+          dh[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          dh[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+          dl[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          dl[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+          if (grp == 0) o_sx[(size_t)(tok0 + qi) * HEADS + h] = sc;
         }
       }
     }
@@ -424,8 +460,11 @@ cudaError_t init_prefill_tc_kernel() {
 
 cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloat16* kv,
                                         const __nv_bfloat16* cache, int cap, int B, int T,
-                                        float scale, __nv_bfloat16* attn_out, int* err,
-                                        cudaStream_t st) {
+                                        float scale, __nv_bfloat16* attn_out, uint8_t* o_hi,
+                                        uint8_t* o_lo, float* o_sx, int* err, cudaStream_t st) {
+  if ((o_hi == nullptr) != (o_lo == nullptr) || (o_hi == nullptr) != (o_sx == nullptr) ||
+      (o_hi == nullptr && attn_out == nullptr))
+    return cudaErrorInvalidValue;
   if (B * T == 0) return cudaSuccess;
   const uint64_t M = (uint64_t)B * T;
   CUtensorMap mq, mkv, mc;
@@ -437,7 +476,7 @@ cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloa
   const dim3 grid(HEADS, (T + PA_TILE - 1) / PA_TILE, B);
   prefill_attn_tc_kernel<<<grid, PA_THREADS, PA_SMEM, st>>>(mq, mkv, mc, T, cap,
                                                             scale * 1.4426950408889634f, attn_out,
-                                                            err);
+                                                            o_hi, o_lo, o_sx, err);
   return cudaGetLastError();
 }
 

@@ -289,10 +289,10 @@ cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Pro
       default: return launch_gemv<8>(X, ldx, K, ps, rows, st, pdl);
     }
   }
-  return launch_gemm_tc(X, ldx, M, K, p, np, partial, num_sms, err, st);
+  return launch_gemm_tc(X, ldx, M, K, p, np, partial, num_sms, err, st, adv, adv_n, adv_by);
 }
 
-bool gemm_can_advance(int M) { return M > 0 && M <= 8; }
+bool gemm_can_advance(int M) { return M > 0; }
 
 cudaError_t launch_qb_norm(const float* g1, int M, const Proj& p, const __nv_bfloat16* gq,
                            const __nv_bfloat16* gkv, float eps, const float2* rope_tab,

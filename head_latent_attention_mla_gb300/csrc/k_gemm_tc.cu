@@ -89,11 +89,13 @@ struct GemmTcArgs {
   void* Y[2];
   int ldy[2];
   int y_fp32[2];
-  const float* sx;       // [M] per-token activation scales
+  const float* sx;       // per-token activation scales [M], or [M][K/128] (SXB kernels)
   int splits;            // k-block ranges per (n tile, m tile)
   float* partial;        // [splits][M][ldp] fp32 when splits > 1
   int ldp;               // total N of both problems (partial row stride)
   int* err;
+  int* adv;              // CTA 0 adds adv_by to adv[0..adv_n) (the call's length update)
+  int adv_n, adv_by;
 };
 
 // Unit u: split fastest, then m tile, then n tile (CTAs running at the same time share weight
@@ -155,15 +157,10 @@ __global__ void __launch_bounds__(256) split_e4m3_kernel(const __nv_bfloat16* __
     uint32_t h[2] = {0u, 0u}, l[2] = {0u, 0u};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float2 f = make_float2(__uint_as_float(u[i] << 16) * inv,
-                                   __uint_as_float(u[i] & 0xFFFF0000u) * inv);
-      const __nv_fp8x2_storage_t hp = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
-      const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hp, __NV_E4M3);
-      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hh));
-      const __nv_fp8x2_storage_t lp =
-          __nv_cvt_float2_to_fp8x2(make_float2(f.x - hf.x, f.y - hf.y), __NV_SATFINITE, __NV_E4M3);
-      h[i >> 1] |= (uint32_t)hp << (16 * (i & 1));
-      l[i >> 1] |= (uint32_t)lp << (16 * (i & 1));
+      const uint32_t hl = e4m3_split2(make_float2(__uint_as_float(u[i] << 16) * inv,
+                                                  __uint_as_float(u[i] & 0xFFFF0000u) * inv));
+      h[i >> 1] |= (hl & 0xFFFFu) << (16 * (i & 1));
+      l[i >> 1] |= (hl >> 16) << (16 * (i & 1));
     }
     *reinterpret_cast<uint2*>(hi + (size_t)m * K + k) = make_uint2(h[0], h[1]);
     *reinterpret_cast<uint2*>(lo + (size_t)m * K + k) = make_uint2(l[0], l[1]);
@@ -176,12 +173,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int BN, int WT>
+// SXB: the activations carry one scale per (token, 128-wide k block), sx[m][kb], applied with
+// the weight's block scale to each k block's partial product (token-lane orientation only).
+template <int BN, int WT, bool SXB>
 __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
     const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
     const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo,
     const __grid_constant__ GemmTcArgs args) {
   using L = GemmSmem<BN, WT>;
+  static_assert(!SXB || L::TR, "block-scaled activations need the token-lane orientation");
   constexpr int GT_STAGES = L::STAGES;
   constexpr int GT_NACC = L::NACC;
   extern __shared__ uint8_t smem_raw[];
@@ -221,6 +221,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (blockIdx.x == 0 && args.adv != nullptr)  // every earlier kernel of the stream is done
+    for (int j = threadIdx.x; j < args.adv_n; j += GT_THREADS) args.adv[j] += args.adv_by;
 
   if (warp == 0) {
     // -------------------------------------------------------------------- TMA producer
@@ -318,6 +320,11 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
       const int nh = U.n0 + 128 * half;       // first feature of this warpgroup's half
       const bool live = nh < args.N[U.prob];  // a half wholly past N was not multiplied
       const float* scales = args.S[U.prob] + (size_t)(nh / BLK) * nkb_all;
+      // SXB: this thread's token (lane = token) and its block scales, one k block ahead.
+      const int mt = U.m0 + 32 * q + lane;
+      const int sxoff = (mt < args.M ? mt : -1) * nkb_all;  // < 0: token past M
+      float sx_next = 0.f;
+      if constexpr (SXB) sx_next = sxoff >= 0 ? __ldg(args.sx + sxoff + U.kb_begin) : 0.f;
       float acc[CW];
 #pragma unroll
       for (int j = 0; j < CW; ++j) acc[j] = 0.f;
@@ -329,7 +336,11 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
           break;
         }
         fence_after();
-        const float sc = live ? __ldg(scales + kb) : 0.f;
+        float sc = live ? __ldg(scales + kb) : 0.f;
+        if constexpr (SXB) {
+          sc *= sx_next;
+          sx_next = (sxoff >= 0 && kb + 1 < U.kb_end) ? __ldg(args.sx + sxoff + kb + 1) : 0.f;
+        }
         const uint32_t t0 = tmem + lane_off + ab * L::ACC_COLS + half * BN + col0;
 #pragma unroll
         for (int c = 0; c < CW; c += CH) {
@@ -357,7 +368,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
         const int nb = nh + col0;
         const int nend = args.N[U.prob];
         if (m < args.M) {
-          const float sxm = __ldg(args.sx + m);  // applied as each vector is formed
+          // Token scale, applied as each vector is formed (SXB: already in the block scales).
+          const float sxm = SXB ? 1.f : __ldg(args.sx + m);
           if (args.splits > 1 || args.y_fp32[U.prob]) {
             float* y = args.splits > 1
                            ? args.partial + ((size_t)U.split * args.M + m) * args.ldp +
@@ -444,18 +456,18 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
     reinterpret_cast<__nv_bfloat16*>(Y)[(size_t)m * ldy + n] = __float2bfloat16_rn(s);
 }
 
-template <int BN, int WT>
+template <int BN, int WT, bool SXB>
 cudaError_t launch_bn(const CUtensorMap* w, const CUtensorMap& hi, const CUtensorMap& lo,
                       const GemmTcArgs& a, int num_sms, cudaStream_t st) {
   const int grid = a.units < num_sms ? a.units : num_sms;
-  gemm_f8w_tc_kernel<BN, WT><<<grid, GT_THREADS, GemmSmem<BN, WT>::BYTES, st>>>(w[0], w[1], hi,
-                                                                                lo, a);
+  gemm_f8w_tc_kernel<BN, WT, SXB><<<grid, GT_THREADS, GemmSmem<BN, WT>::BYTES, st>>>(
+      w[0], w[1], hi, lo, a);
   return cudaGetLastError();
 }
 
-template <int BN, int WT>
+template <int BN, int WT, bool SXB>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_f8w_tc_kernel<BN, WT>,
+  return cudaFuncSetAttribute(gemm_f8w_tc_kernel<BN, WT, SXB>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               GemmSmem<BN, WT>::BYTES);
 }
@@ -518,32 +530,33 @@ size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms) {
 }
 
 cudaError_t init_gemm_tc_kernels() {
-  cudaError_t e = set_smem_attr<32, 1>();
-  if (e == cudaSuccess) e = set_smem_attr<64, 1>();
-  if (e == cudaSuccess) e = set_smem_attr<128, 1>();
-  if (e == cudaSuccess) e = set_smem_attr<128, 2>();
+  cudaError_t e = set_smem_attr<32, 1, false>();
+  if (e == cudaSuccess) e = set_smem_attr<64, 1, false>();
+  if (e == cudaSuccess) e = set_smem_attr<128, 1, false>();
+  if (e == cudaSuccess) e = set_smem_attr<128, 2, false>();
+  if (e == cudaSuccess) e = set_smem_attr<128, 1, true>();
+  if (e == cudaSuccess) e = set_smem_attr<128, 2, true>();
   return e;
 }
 
-cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
-                           float* scratch, int num_sms, int* err, cudaStream_t st) {
-  if (!scratch) return cudaErrorInvalidValue;
+namespace {
+
+// The GEMM proper on e4m3 hi/lo activations [M, K] with per-token (sxb = false) or per-(token,
+// k block) (sxb = true) scales; split-K partials in `partial`.
+cudaError_t gemm_tc_core(const uint8_t* hi, const uint8_t* lo, const float* sx, bool sxb, int M,
+                         int K, const Proj* p, int np, float* partial, int num_sms, int* err,
+                         cudaStream_t st, int* adv, int adv_n, int adv_by) {
   const int bn = gemm_bn(M);
-  uint8_t* base = reinterpret_cast<uint8_t*>(scratch);
-  uint8_t* hi = base;
-  uint8_t* lo = hi + up256((size_t)M * K);
-  float* sx = reinterpret_cast<float*>(lo + up256((size_t)M * K));
-  float* partial = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sx) + up256((size_t)M * 4));
-
-  split_e4m3_kernel<<<M, 256, 0, st>>>(X, ldx, K, hi, lo, sx);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
+  if (sxb && bn != 128) return cudaErrorInvalidValue;
+  cudaError_t e = cudaSuccess;
   GemmTcArgs a{};
   a.M = M;
   a.K = K;
   a.err = err;
   a.sx = sx;
+  a.adv = adv;
+  a.adv_n = adv_n;
+  a.adv_by = adv_by;
   CUtensorMap mw[2], mh, ml;
   int n_total = 0;
   for (int i = 0; i < 2; ++i) {
@@ -571,11 +584,15 @@ cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const 
   a.partial = partial;
   a.ldp = n_total;
   switch (bn) {
-    case 32: e = launch_bn<32, 1>(mw, mh, ml, a, num_sms, st); break;
-    case 64: e = launch_bn<64, 1>(mw, mh, ml, a, num_sms, st); break;
+    case 32: e = launch_bn<32, 1, false>(mw, mh, ml, a, num_sms, st); break;
+    case 64: e = launch_bn<64, 1, false>(mw, mh, ml, a, num_sms, st); break;
     default:
-      e = wt == 2 ? launch_bn<128, 2>(mw, mh, ml, a, num_sms, st)
-                  : launch_bn<128, 1>(mw, mh, ml, a, num_sms, st);
+      if (sxb)
+        e = wt == 2 ? launch_bn<128, 2, true>(mw, mh, ml, a, num_sms, st)
+                    : launch_bn<128, 1, true>(mw, mh, ml, a, num_sms, st);
+      else
+        e = wt == 2 ? launch_bn<128, 2, false>(mw, mh, ml, a, num_sms, st)
+                    : launch_bn<128, 1, false>(mw, mh, ml, a, num_sms, st);
       break;
   }
   if (e != cudaSuccess || a.splits == 1) return e;
@@ -587,6 +604,36 @@ cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const 
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
+                           float* scratch, int num_sms, int* err, cudaStream_t st, int* adv,
+                           int adv_n, int adv_by) {
+  if (!scratch) return cudaErrorInvalidValue;
+  uint8_t* base = reinterpret_cast<uint8_t*>(scratch);
+  uint8_t* hi = base;
+  uint8_t* lo = hi + up256((size_t)M * K);
+  float* sx = reinterpret_cast<float*>(lo + up256((size_t)M * K));
+  float* partial = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sx) + up256((size_t)M * 4));
+  split_e4m3_kernel<<<M, 256, 0, st>>>(X, ldx, K, hi, lo, sx);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return gemm_tc_core(hi, lo, sx, false, M, K, p, np, partial, num_sms, err, st, adv, adv_n,
+                      adv_by);
+}
+
+bool gemm_takes_split_blocks(int M) { return gemm_bn(M) == 128; }
+
+cudaError_t launch_gemm_tc_split(const uint8_t* hi, const uint8_t* lo, const float* sx,
+                                 bool block_scales, int M, int K, const Proj* p, int np,
+                                 float* scratch, int num_sms, int* err, cudaStream_t st, int* adv,
+                                 int adv_n, int adv_by) {
+  if (!scratch || !hi || !lo || !sx || M <= 8 || (block_scales && !gemm_takes_split_blocks(M)))
+    return cudaErrorInvalidValue;
+  return gemm_tc_core(hi, lo, sx, block_scales, M, K, p, np, scratch, num_sms, err, st, adv,
+                      adv_n, adv_by);
 }
 
 }  // namespace mla

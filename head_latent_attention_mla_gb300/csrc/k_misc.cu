@@ -17,6 +17,49 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t v) {
 }
 
 // Block-wide sum of two values (256 threads).
+__device__ __forceinline__ float2 block_max2(float a, float b, float2* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, off));
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = make_float2(a, b);
+  __syncthreads();
+  float2 t = make_float2(0.f, 0.f);
+  if (threadIdx.x < 32) {
+    t = (l < (int)(blockDim.x >> 5)) ? red[l] : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      t.x = fmaxf(t.x, __shfl_xor_sync(0xffffffffu, t.x, off));
+      t.y = fmaxf(t.y, __shfl_xor_sync(0xffffffffu, t.y, off));
+    }
+    if (l == 0) red[8] = t;
+  }
+  __syncthreads();
+  return red[8];
+}
+
+// The n values v[0..n) of one token (element tid + 256 i holds v[i]) as two e4m3 terms with
+// the token's scale s = amax / 448 (1 for an all-zero row): hi = e4m3(v / s), lo = e4m3(v / s
+// - hi), the split the tensor-core GEMM's own activation pass would make.
+template <int N>
+__device__ __forceinline__ void store_e4m3_split(const float (&v)[N], float amax, size_t row,
+                                                 int width, const E4m3Split& o) {
+  const float s = amax > 0.f ? amax / 448.f : 1.f;
+  const float inv = 1.f / s;
+  if (threadIdx.x == 0) o.sx[row] = s;
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    const uint32_t hl = e4m3_split2(make_float2(v[i] * inv, v[i + 1] * inv));
+    const size_t a = row * width + threadIdx.x + 256 * i;
+    o.hi[a] = (uint8_t)(hl & 0xFFu);
+    o.hi[a + 256] = (uint8_t)((hl >> 8) & 0xFFu);
+    o.lo[a] = (uint8_t)((hl >> 16) & 0xFFu);
+    o.lo[a + 256] = (uint8_t)(hl >> 24);
+  }
+}
+
 __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -58,15 +101,16 @@ __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
     const float* __restrict__ g1, int T, const __nv_bfloat16* __restrict__ gq,
     const __nv_bfloat16* __restrict__ gkv, float eps, const float2* __restrict__ rope_tab,
     int pairing, const int* __restrict__ seq_lens, __nv_bfloat16* __restrict__ cache, int cap,
-    int limit, __nv_bfloat16* __restrict__ cq_out, __nv_bfloat16* __restrict__ ckv_out, int* err) {
-  __shared__ float2 red[9];
+    int limit, __nv_bfloat16* __restrict__ cq_out, __nv_bfloat16* __restrict__ ckv_out, int* err,
+    E4m3Split q_split, E4m3Split kv_split) {
+  __shared__ float2 red[9], red2[9];
   __shared__ __align__(16) __nv_bfloat16 row[LAT];
   pdl_launch_dependents();
   pdl_wait();
   const int token = blockIdx.x, b = token / T, t = token % T;
   const int tid = threadIdx.x;
   const float* in = g1 + (size_t)token * G1_N;
-  const bool do_q = cq_out != nullptr;
+  const bool do_q = cq_out != nullptr || q_split.hi != nullptr;
 
   float xq[Q_LORA / 256], xk[KV_LORA / 256];
   float sq = 0.f, sk = 0.f;
@@ -83,19 +127,30 @@ __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
   const float2 ss = block_sum2(sq, sk, red);
   const float rq = rsqrtf(ss.x / Q_LORA + eps);
   const float rk = rsqrtf(ss.y / KV_LORA + eps);
+  float yq[Q_LORA / 256], yk[KV_LORA / 256];  // the bf16 outputs, as floats
+  float aq = 0.f, ak = 0.f;
   if (do_q) {
 #pragma unroll
     for (int i = 0; i < Q_LORA / 256; ++i) {
       const int c = tid + 256 * i;
-      cq_out[(size_t)token * Q_LORA + c] =
-          __float2bfloat16_rn(__bfloat162float(gq[c]) * bf16_round(xq[i] * rq));
+      const __nv_bfloat16 y = __float2bfloat16_rn(__bfloat162float(gq[c]) * bf16_round(xq[i] * rq));
+      yq[i] = __bfloat162float(y);
+      aq = fmaxf(aq, fabsf(yq[i]));
+      if (cq_out) cq_out[(size_t)token * Q_LORA + c] = y;
     }
   }
 #pragma unroll
   for (int i = 0; i < KV_LORA / 256; ++i) {
     const int c = tid + 256 * i;
     row[c] = __float2bfloat16_rn(__bfloat162float(gkv[c]) * bf16_round(xk[i] * rk));
+    yk[i] = __bfloat162float(row[c]);
+    ak = fmaxf(ak, fabsf(yk[i]));
     if (ckv_out) ckv_out[(size_t)token * KV_LORA + c] = row[c];
+  }
+  if (q_split.hi != nullptr || kv_split.hi != nullptr) {  // the same for every CTA
+    const float2 am = block_max2(aq, ak, red2);
+    if (q_split.hi != nullptr && do_q) store_e4m3_split(yq, am.x, token, Q_LORA, q_split);
+    if (kv_split.hi != nullptr) store_e4m3_split(yk, am.y, token, KV_LORA, kv_split);
   }
   const int pos = seq_lens[b] + t;
   if (pos < 0 || pos >= limit) {  // device lengths past the cache or the RoPE table
@@ -326,11 +381,13 @@ cudaError_t launch_norm_rope_cache(const float* g1, int B, int T, const __nv_bfl
                                    const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
                                    int rope_pairing, const int* seq_lens, __nv_bfloat16* cache,
                                    int cap, int limit, __nv_bfloat16* cq_out,
-                                   __nv_bfloat16* ckv_out, int* err, cudaStream_t st, bool pdl) {
+                                   __nv_bfloat16* ckv_out, int* err, cudaStream_t st, bool pdl,
+                                   const E4m3Split* q_split, const E4m3Split* kv_split) {
   if (B * T == 0) return cudaSuccess;
+  const E4m3Split none{nullptr, nullptr, nullptr};
   return launch_kernel(norm_rope_cache_kernel, dim3(B * T), dim3(256), 0, st, pdl, g1, T, gq, gkv,
                        eps, rope_tab, rope_pairing, seq_lens, cache, cap, limit, cq_out, ckv_out,
-                       err);
+                       err, q_split ? *q_split : none, kv_split ? *kv_split : none);
 }
 
 cudaError_t launch_rope_q(__nv_bfloat16* q, int B, int T, const float2* rope_tab,

@@ -28,8 +28,8 @@ bool ready(const mla_ctx* c) {
 
 // Workspace regions (byte offsets into the caller's buffer).
 struct Layout {
-  size_t g1 = 0, cq = 0, ckv = 0, q = 0, kv = 0, attn = 0, qfull = 0, opart = 0, ml = 0,
-         olat = 0, gpart = 0, total = 0;
+  size_t g1 = 0, cq = 0, cq_sx = 0, ckv = 0, ckv_sx = 0, q = 0, kv = 0, attn = 0, attn_sx = 0,
+         qfull = 0, opart = 0, ml = 0, olat = 0, gpart = 0, total = 0;
 };
 
 // Largest split-K partial buffer of the projections of one call with M token rows.
@@ -50,11 +50,14 @@ Layout prefill_layout(long M, int num_sms) {
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off += up256(bytes); return o; };
   L.g1 = take((size_t)M * G1_N * 4);
-  L.cq = take((size_t)M * Q_LORA * 2);
-  L.ckv = take((size_t)M * KV_LORA * 2);
+  L.cq = take((size_t)M * Q_LORA * 2);    // bf16, or its two e4m3 terms
+  L.cq_sx = take((size_t)M * 4);
+  L.ckv = take((size_t)M * KV_LORA * 2);  // bf16, or its two e4m3 terms
+  L.ckv_sx = take((size_t)M * 4);
   L.q = take((size_t)M * QB_N * 2);
   L.kv = take((size_t)M * KVB_N * 2);
-  L.attn = take((size_t)M * O_IN * 2);
+  L.attn = take((size_t)M * O_IN * 2);  // bf16, or its two e4m3 terms (M * O_IN bytes each)
+  L.attn_sx = take((size_t)M * HEADS * 4);
   L.gpart = take(gemm_partials(M, num_sms));
   L.total = off;
   return L;
@@ -293,19 +296,50 @@ mla_status mla_prefill(mla_ctx* c, const void* x, int B, int T, void* cache, int
   Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
                 {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
   MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, M, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-  MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
-                                    c->cfg.rope_pairing, lens_dev, C, cap, limit, cq, ckv,
-                                    c->d_err, s));
   Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
-  MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-  MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
   Proj p3{c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], KVB_N, kv, KVB_N, 0};
-  MLA_LAUNCH("gemm_kv_b", launch_gemm(ckv, KV_LORA, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-  MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, C, cap, B, T, c->cfg.softmax_scale, attn,
-                                                            c->d_err, s));
+  if (M > 8) {
+    // Tensor-core projections: the norm kernel writes q_b's and kv_b's e4m3 inputs itself (the
+    // two terms share the bf16 latents' regions; one scale per token).
+    const E4m3Split qsp{at<uint8_t>(ws, L.cq), at<uint8_t>(ws, L.cq) + (size_t)M * Q_LORA,
+                        at<float>(ws, L.cq_sx)};
+    const E4m3Split kvsp{at<uint8_t>(ws, L.ckv), at<uint8_t>(ws, L.ckv) + (size_t)M * KV_LORA,
+                         at<float>(ws, L.ckv_sx)};
+    MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
+                                      c->cfg.rope_pairing, lens_dev, C, cap, limit, nullptr, nullptr,
+                                      c->d_err, s, false, &qsp, &kvsp));
+    MLA_LAUNCH("gemm_q_b", launch_gemm_tc_split(qsp.hi, qsp.lo, qsp.sx, false, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
+    MLA_LAUNCH("gemm_kv_b", launch_gemm_tc_split(kvsp.hi, kvsp.lo, kvsp.sx, false, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+  } else {
+    MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
+                                      c->cfg.rope_pairing, lens_dev, C, cap, limit, cq, ckv,
+                                      c->d_err, s));
+    MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
+    MLA_LAUNCH("gemm_kv_b", launch_gemm(ckv, KV_LORA, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+  }
   Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
-  MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-  MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, T, s));
+  if (gemm_takes_split_blocks(M)) {
+    // The attention writes o_proj's e4m3 input itself (one scale per token and head).
+    uint8_t* a_hi = at<uint8_t>(ws, L.attn);
+    uint8_t* a_lo = a_hi + (size_t)M * O_IN;
+    float* a_sx = at<float>(ws, L.attn_sx);
+    MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, C, cap, B, T, c->cfg.softmax_scale, nullptr,
+                                                              a_hi, a_lo, a_sx, c->d_err, s));
+    MLA_LAUNCH("gemm_o", launch_gemm_tc_split(a_hi, a_lo, a_sx, true, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
+                                              lens_dev, B, T));
+  } else {
+    MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, C, cap, B, T, c->cfg.softmax_scale, attn,
+                                                              nullptr, nullptr, nullptr, c->d_err, s));
+    if (gemm_can_advance(M) && B <= 128) {  // the length update rides on o_proj
+      MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
+                                       lens_dev, B, T));
+    } else {
+      MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+      MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, T, s));
+    }
+  }
   return MLA_OK;
 }
 

@@ -72,19 +72,42 @@ struct Proj {
   int y_fp32;        // 1: float32 output, 0: bf16 output
 };
 
+// Two-term e4m3 split of two values already divided by their scale: hi = e4m3(f),
+// lo = e4m3(f - hi), both rounded to nearest even with saturation; f ~ hi + lo to a relative
+// 2^-8.  Returns the hi pair in bits 0..15 and the lo pair in bits 16..31 (first value in the
+// low byte of each).
+__device__ __forceinline__ uint32_t e4m3_split2(float2 f) {
+  const __nv_fp8x2_storage_t hp = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+  const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hp, __NV_E4M3);
+  const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hh));
+  const __nv_fp8x2_storage_t lp =
+      __nv_cvt_float2_to_fp8x2(make_float2(f.x - hf.x, f.y - hf.y), __NV_SATFINITE, __NV_E4M3);
+  return (uint32_t)hp | ((uint32_t)lp << 16);
+}
+
 // ---- launchers (each returns the launch's cudaError_t) ----------------------------------
 
 // Y = X W^T for up to two projections sharing X [M, K] (row stride ldx elements).  M <= 8
 // streams the weights through the CUDA cores; larger M runs on the tensor cores, split over K
 // when the grid would be small, with fp32 partials in `partial` (gemm_partial_bytes bytes).
-// With M <= 8 (the CUDA-core path) block 0 of the launch also adds adv_by to
-// adv[0..adv_n) (the call's length bookkeeping, riding on its last kernel; adv_n <= 128).
+// Block 0 of the launch also adds adv_by to adv[0..adv_n) (the call's length bookkeeping,
+// riding on its last kernel; adv_n <= 128 with M <= 8).
 cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
                         float* partial, int num_sms, int* err, cudaStream_t st,
                         int* adv = nullptr, int adv_n = 0, int adv_by = 0, bool pdl = false);
 bool gemm_can_advance(int M);  // whether launch_gemm honours adv for this M
 cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
-                           float* partial, int num_sms, int* err, cudaStream_t st);
+                           float* partial, int num_sms, int* err, cudaStream_t st,
+                           int* adv = nullptr, int adv_n = 0, int adv_by = 0);
+// The same GEMM (M > 8) on activations already split into two e4m3 terms, hi and lo [M, K],
+// with one scale per token, sx [M] (X[m, k] ~ sx[m] (hi + lo)), or with block_scales one per
+// (token, 128-wide k block), sx [M, K/128] (X[m, k] ~ sx[m][k/128] (hi + lo)); block scales
+// are accepted when gemm_takes_split_blocks(M).  `partial` as for launch_gemm_tc.
+bool gemm_takes_split_blocks(int M);
+cudaError_t launch_gemm_tc_split(const uint8_t* hi, const uint8_t* lo, const float* sx,
+                                 bool block_scales, int M, int K, const Proj* p, int np,
+                                 float* partial, int num_sms, int* err, cudaStream_t st,
+                                 int* adv = nullptr, int adv_n = 0, int adv_by = 0);
 size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms);
 cudaError_t init_gemm_tc_kernels();
 
@@ -94,12 +117,20 @@ cudaError_t init_gemm_tc_kernels();
 //   cq_out: bf16 [M, Q_LORA] normalised q latent (skipped if null).
 //   ckv_out: bf16 [M, KV_LORA] normalised kv latent, the same values as the cache rows
 //   (skipped if null).
+//   q_split / kv_split (optional, instead of cq_out / ckv_out): those bf16 latents as the two
+//   e4m3 terms and per-token scale that launch_gemm_tc_split reads (block_scales = false).
+struct E4m3Split {
+  uint8_t* hi;  // [M, n]
+  uint8_t* lo;  // [M, n]
+  float* sx;    // [M]
+};
 cudaError_t launch_norm_rope_cache(const float* g1, int B, int T, const __nv_bfloat16* gq,
                                    const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
                                    int rope_pairing, const int* seq_lens, __nv_bfloat16* cache,
                                    int cap, int limit, __nv_bfloat16* cq_out,
                                    __nv_bfloat16* ckv_out, int* err, cudaStream_t st,
-                                   bool pdl = false);
+                                   bool pdl = false, const E4m3Split* q_split = nullptr,
+                                   const E4m3Split* kv_split = nullptr);
 
 // In-place RoPE of the rotary slice of q [M, HEADS, QHEAD] (prefill).
 cudaError_t launch_rope_q(__nv_bfloat16* q, int B, int T, const float2* rope_tab,
@@ -184,10 +215,14 @@ cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* 
 // Causal prefill attention on the tcgen05 tensor cores: q [M, HEADS, QHEAD] (rotated),
 // kv [M, HEADS, 256] (k_nope | v), rotated k_pe from the cache rows; writes attn_out
 // [M, HEADS*VDIM] bf16.
+// The output goes to attn_out as bf16 [B*T, HEADS*VDIM], or, when o_hi/o_lo/o_sx are given
+// (attn_out may then be null), as the two e4m3 terms of those bf16 values, [B*T, HEADS*VDIM]
+// each, with one scale per (token, head) in o_sx [B*T, HEADS] (the input of
+// launch_gemm_tc_split).
 cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloat16* kv,
                                         const __nv_bfloat16* cache, int cap, int B, int T,
-                                        float scale, __nv_bfloat16* attn_out, int* err,
-                                        cudaStream_t st);
+                                        float scale, __nv_bfloat16* attn_out, uint8_t* o_hi,
+                                        uint8_t* o_lo, float* o_sx, int* err, cudaStream_t st);
 cudaError_t init_prefill_tc_kernel();
 
 // seq_lens[b] += T.
