@@ -40,24 +40,22 @@ __device__ __forceinline__ float2 block_max2(float a, float b, float2* red) {
   return red[8];
 }
 
-// The n values v[0..n) of one token (element tid + 256 i holds v[i]) as two e4m3 terms with
-// the token's scale s = amax / 448 (1 for an all-zero row): hi = e4m3(v / s), lo = e4m3(v / s
-// - hi), the split the tensor-core GEMM's own activation pass would make.
-template <int N>
-__device__ __forceinline__ void store_e4m3_split(const float (&v)[N], float amax, size_t row,
-                                                 int width, const E4m3Split& o) {
+// Eight consecutive values v of one token, starting at element `at` of the split rows, as two
+// e4m3 terms with the token's scale s = amax / 448 (1 for an all-zero row): hi = e4m3(v / s),
+// lo = e4m3(v / s - hi), the split the tensor-core GEMM's own activation pass would make.
+__device__ __forceinline__ void store_e4m3_split8(const float (&v)[8], float amax, size_t at,
+                                                  const E4m3Split& o) {
   const float s = amax > 0.f ? amax / 448.f : 1.f;
   const float inv = 1.f / s;
-  if (threadIdx.x == 0) o.sx[row] = s;
+  uint32_t h[2] = {0u, 0u}, l[2] = {0u, 0u};
 #pragma unroll
-  for (int i = 0; i < N; i += 2) {
-    const uint32_t hl = e4m3_split2(make_float2(v[i] * inv, v[i + 1] * inv));
-    const size_t a = row * width + threadIdx.x + 256 * i;
-    o.hi[a] = (uint8_t)(hl & 0xFFu);
-    o.hi[a + 256] = (uint8_t)((hl >> 8) & 0xFFu);
-    o.lo[a] = (uint8_t)((hl >> 16) & 0xFFu);
-    o.lo[a + 256] = (uint8_t)(hl >> 24);
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t hl = e4m3_split2(make_float2(v[2 * i] * inv, v[2 * i + 1] * inv));
+    h[i >> 1] |= (hl & 0xFFFFu) << (16 * (i & 1));
+    l[i >> 1] |= (hl >> 16) << (16 * (i & 1));
   }
+  *reinterpret_cast<uint2*>(o.hi + at) = make_uint2(h[0], h[1]);
+  *reinterpret_cast<uint2*>(o.lo + at) = make_uint2(l[0], l[1]);
 }
 
 __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
@@ -93,10 +91,13 @@ __device__ __forceinline__ int2 pair_idx(int j, int pairing) {
   return pairing == 0 ? make_int2(2 * j, 2 * j + 1) : make_int2(j, j + ROPE / 2);
 }
 
-// One CTA (256 threads) per token.
+// One CTA (256 threads) per token; threads 0..191 own eight consecutive q-latent values each,
+// threads 192..255 eight kv-latent values (16-byte loads and stores).
 // RMSNorm ("rmsnorm" excerpt): y = g * bf16(x * rsqrt(mean(x^2) + eps)), rounded to bf16,
 // for the q latent (1536) and the kv latent (512); the kv latent and the rotated shared
 // rotary key form the token's cache row [c_hat (512) | RoPE(k_pe) (64)].
+constexpr int NRC_QT = Q_LORA / 8;  // q threads
+static_assert(NRC_QT + KV_LORA / 8 == 256, "one 8-value run per thread");
 __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
     const float* __restrict__ g1, int T, const __nv_bfloat16* __restrict__ gq,
     const __nv_bfloat16* __restrict__ gkv, float eps, const float2* __restrict__ rope_tab,
@@ -111,46 +112,58 @@ __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
   const int tid = threadIdx.x;
   const float* in = g1 + (size_t)token * G1_N;
   const bool do_q = cq_out != nullptr || q_split.hi != nullptr;
+  const bool is_q = tid < NRC_QT;
+  const int c0 = is_q ? 8 * tid : 8 * (tid - NRC_QT);  // first element within its latent
 
-  float xq[Q_LORA / 256], xk[KV_LORA / 256];
+  float x[8] = {};
   float sq = 0.f, sk = 0.f;
+  if (!is_q || do_q) {
+    const float4* src = reinterpret_cast<const float4*>(in + (is_q ? 0 : Q_LORA) + c0);
+    const float4 a = src[0], b4 = src[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b4.x; x[5] = b4.y; x[6] = b4.z; x[7] = b4.w;
+    float s2 = 0.f;
 #pragma unroll
-  for (int i = 0; i < Q_LORA / 256; ++i) {
-    xq[i] = do_q ? in[tid + 256 * i] : 0.f;
-    sq += xq[i] * xq[i];
-  }
-#pragma unroll
-  for (int i = 0; i < KV_LORA / 256; ++i) {
-    xk[i] = in[Q_LORA + tid + 256 * i];
-    sk += xk[i] * xk[i];
+    for (int i = 0; i < 8; ++i) s2 += x[i] * x[i];
+    (is_q ? sq : sk) = s2;
   }
   const float2 ss = block_sum2(sq, sk, red);
-  const float rq = rsqrtf(ss.x / Q_LORA + eps);
-  const float rk = rsqrtf(ss.y / KV_LORA + eps);
-  float yq[Q_LORA / 256], yk[KV_LORA / 256];  // the bf16 outputs, as floats
-  float aq = 0.f, ak = 0.f;
-  if (do_q) {
+  const float rs = is_q ? rsqrtf(ss.x / Q_LORA + eps) : rsqrtf(ss.y / KV_LORA + eps);
+  float y[8];  // the bf16 outputs, as floats
+  float am = 0.f;
+  if (!is_q || do_q) {
+    const uint4 gv = *reinterpret_cast<const uint4*>((is_q ? gq : gkv) + c0);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    uint32_t ow[4];
 #pragma unroll
-    for (int i = 0; i < Q_LORA / 256; ++i) {
-      const int c = tid + 256 * i;
-      const __nv_bfloat16 y = __float2bfloat16_rn(__bfloat162float(gq[c]) * bf16_round(xq[i] * rq));
-      yq[i] = __bfloat162float(y);
-      aq = fmaxf(aq, fabsf(yq[i]));
-      if (cq_out) cq_out[(size_t)token * Q_LORA + c] = y;
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat16 y0 =
+          __float2bfloat16_rn(__uint_as_float(gw[i] << 16) * bf16_round(x[2 * i] * rs));
+      const __nv_bfloat16 y1 =
+          __float2bfloat16_rn(__uint_as_float(gw[i] & 0xFFFF0000u) * bf16_round(x[2 * i + 1] * rs));
+      y[2 * i] = __bfloat162float(y0);
+      y[2 * i + 1] = __bfloat162float(y1);
+      am = fmaxf(am, fmaxf(fabsf(y[2 * i]), fabsf(y[2 * i + 1])));
+      ow[i] = (uint32_t)__bfloat16_as_ushort(y0) | ((uint32_t)__bfloat16_as_ushort(y1) << 16);
+    }
+    const uint4 o4 = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    if (is_q) {
+      if (cq_out) *reinterpret_cast<uint4*>(cq_out + (size_t)token * Q_LORA + c0) = o4;
+    } else {
+      *reinterpret_cast<uint4*>(row + c0) = o4;
+      if (ckv_out) *reinterpret_cast<uint4*>(ckv_out + (size_t)token * KV_LORA + c0) = o4;
     }
   }
-#pragma unroll
-  for (int i = 0; i < KV_LORA / 256; ++i) {
-    const int c = tid + 256 * i;
-    row[c] = __float2bfloat16_rn(__bfloat162float(gkv[c]) * bf16_round(xk[i] * rk));
-    yk[i] = __bfloat162float(row[c]);
-    ak = fmaxf(ak, fabsf(yk[i]));
-    if (ckv_out) ckv_out[(size_t)token * KV_LORA + c] = row[c];
-  }
   if (q_split.hi != nullptr || kv_split.hi != nullptr) {  // the same for every CTA
-    const float2 am = block_max2(aq, ak, red2);
-    if (q_split.hi != nullptr && do_q) store_e4m3_split(yq, am.x, token, Q_LORA, q_split);
-    if (kv_split.hi != nullptr) store_e4m3_split(yk, am.y, token, KV_LORA, kv_split);
+    const float2 m2 = block_max2(is_q ? am : 0.f, is_q ? 0.f : am, red2);
+    if (is_q && do_q && q_split.hi != nullptr) {
+      store_e4m3_split8(y, m2.x, (size_t)token * Q_LORA + c0, q_split);
+      if (tid == 0) q_split.sx[token] = m2.x > 0.f ? m2.x / 448.f : 1.f;
+    }
+    if (!is_q && kv_split.hi != nullptr) {
+      store_e4m3_split8(y, m2.y, (size_t)token * KV_LORA + c0, kv_split);
+      if (tid == NRC_QT) kv_split.sx[token] = m2.y > 0.f ? m2.y / 448.f : 1.f;
+    }
   }
   const int pos = seq_lens[b] + t;
   if (pos < 0 || pos >= limit) {  // device lengths past the cache or the RoPE table
@@ -171,57 +184,74 @@ __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
   }
 }
 
-// In-place RoPE of q's rotary slices.  One CTA per token; eight threads per head, each with one
-// 16-byte chunk (8 values) of the head's 64 rotary values, so a warp reads and writes four
-// whole 128-byte slices.  Adjacent pairs lie inside a chunk; half pairs (j, j + 32) join chunk c
-// and chunk c + 4, which swap values with a shuffle.  The token's angles are staged once in
-// shared memory.
-__global__ void __launch_bounds__(HEADS * 8) rope_q_kernel(__nv_bfloat16* __restrict__ q, int T,
+// In-place RoPE of q's rotary slices.  One CTA per RQ_TOK tokens; eight threads per head,
+// each with one 16-byte chunk (8 values) of the head's 64 rotary values in every token, so a
+// warp reads and writes four whole 128-byte slices per token and each thread keeps RQ_TOK
+// loads in flight.  Adjacent pairs lie inside a chunk; half pairs (j, j + 32) join chunk c and
+// chunk c + 4, which swap values with a shuffle.  The tokens' angles are staged once in
+// shared memory; tokens whose position lies outside [0, limit) are left as they are.
+constexpr int RQ_TOK = 4;
+__global__ void __launch_bounds__(HEADS * 8) rope_q_kernel(__nv_bfloat16* __restrict__ q, int M,
+                                                           int T,
                                                            const float2* __restrict__ rope_tab,
                                                            int pairing,
                                                            const int* __restrict__ seq_lens,
                                                            int limit) {
-  __shared__ float2 cs[ROPE / 2];
-  const int token = blockIdx.x, b = token / T, t = token % T;
-  const int pos = seq_lens[b] + t;
-  if (pos < 0 || pos >= limit) return;  // the same for the whole CTA
-  if (threadIdx.x < ROPE / 2) cs[threadIdx.x] = rope_tab[(size_t)pos * (ROPE / 2) + threadIdx.x];
+  __shared__ float2 cs[RQ_TOK][ROPE / 2];
+  __shared__ int live[RQ_TOK];
+  const int tok0 = blockIdx.x * RQ_TOK;
+  if (threadIdx.x < RQ_TOK * (ROPE / 2)) {
+    const int k = threadIdx.x / (ROPE / 2), j = threadIdx.x % (ROPE / 2), token = tok0 + k;
+    int pos = -1;
+    if (token < M) pos = seq_lens[token / T] + token % T;
+    const bool ok = pos >= 0 && pos < limit;
+    cs[k][j] = ok ? rope_tab[(size_t)pos * (ROPE / 2) + j] : make_float2(1.f, 0.f);
+    if (j == 0) live[k] = ok;
+  }
   __syncthreads();
   const int h = threadIdx.x >> 3, c = threadIdx.x & 7;
-  uint4* p = reinterpret_cast<uint4*>(q + ((size_t)token * HEADS + h) * QHEAD + NOPE) + c;
-  const uint4 v = *p;
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  float f[8];
+  uint4 v[RQ_TOK];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    f[2 * e] = __uint_as_float(w[e] << 16);
-    f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-  }
-  if (pairing == 0) {  // pair j = 4c + e is (f[2e], f[2e + 1])
+  for (int k = 0; k < RQ_TOK; ++k)
+    if (live[k])
+      v[k] = reinterpret_cast<const uint4*>(q + ((size_t)(tok0 + k) * HEADS + h) * QHEAD + NOPE)[c];
+#pragma unroll
+  for (int k = 0; k < RQ_TOK; ++k) {
+    if (!live[k]) continue;  // the same for the whole CTA
+    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+    float f[8];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float2 r = rotate(f[2 * e], f[2 * e + 1], cs[4 * c + e]);
-      f[2 * e] = r.x;
-      f[2 * e + 1] = r.y;
+      f[2 * e] = __uint_as_float(w[e] << 16);
+      f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
     }
-  } else {  // pair j = 8 (c % 4) + k is (value k of chunk c % 4, value k of chunk c % 4 + 4)
-    float g[8];
+    if (pairing == 0) {  // pair j = 4c + e is (f[2e], f[2e + 1])
 #pragma unroll
-    for (int k = 0; k < 8; ++k) g[k] = __shfl_xor_sync(0xffffffffu, f[k], 4);
-    const bool first = c < 4;
+      for (int e = 0; e < 4; ++e) {
+        const float2 r = rotate(f[2 * e], f[2 * e + 1], cs[k][4 * c + e]);
+        f[2 * e] = r.x;
+        f[2 * e + 1] = r.y;
+      }
+    } else {  // pair j = 8 (c % 4) + i is (value i of chunk c % 4, value i of chunk c % 4 + 4)
+      float g[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float2 a = cs[8 * (c & 3) + k];
-      f[k] = first ? f[k] * a.x - g[k] * a.y : f[k] * a.x + g[k] * a.y;
+      for (int i = 0; i < 8; ++i) g[i] = __shfl_xor_sync(0xffffffffu, f[i], 4);
+      const bool first = c < 4;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float2 a = cs[k][8 * (c & 3) + i];
+        f[i] = first ? f[i] * a.x - g[i] * a.y : f[i] * a.x + g[i] * a.y;
+      }
     }
-  }
-  uint32_t o[4];
+    uint32_t o[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const __nv_bfloat162 v2 = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
-    o[e] = *reinterpret_cast<const uint32_t*>(&v2);
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 v2 = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
+      o[e] = *reinterpret_cast<const uint32_t*>(&v2);
+    }
+    reinterpret_cast<uint4*>(q + ((size_t)(tok0 + k) * HEADS + h) * QHEAD + NOPE)[c] =
+        make_uint4(o[0], o[1], o[2], o[3]);
   }
-  *p = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float* f) {
@@ -393,7 +423,9 @@ cudaError_t launch_norm_rope_cache(const float* g1, int B, int T, const __nv_bfl
 cudaError_t launch_rope_q(__nv_bfloat16* q, int B, int T, const float2* rope_tab,
                           int rope_pairing, const int* seq_lens, int limit, cudaStream_t st) {
   if (B * T == 0) return cudaSuccess;
-  rope_q_kernel<<<B * T, HEADS * 8, 0, st>>>(q, T, rope_tab, rope_pairing, seq_lens, limit);
+  const int M = B * T;
+  rope_q_kernel<<<(M + RQ_TOK - 1) / RQ_TOK, HEADS * 8, 0, st>>>(q, M, T, rope_tab, rope_pairing,
+                                                                 seq_lens, limit);
   return cudaGetLastError();
 }
 
