@@ -73,9 +73,10 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 
 __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
     const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
-    const __grid_constant__ CUtensorMap map_c, int T, int cap, float scale_log2,
+    const __grid_constant__ CUtensorMap map_c, int T, int cap, const int* __restrict__ seq_lens,
+    float scale_log2,
     __nv_bfloat16* __restrict__ attn_out, uint8_t* __restrict__ o_hi, uint8_t* __restrict__ o_lo,
-    float* __restrict__ o_sx, int* err) {
+    float* __restrict__ o_sx, long kv_rows, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
@@ -99,7 +100,19 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
   const int qt = nq - 1 - (int)blockIdx.y;
   const int h = blockIdx.x, b = blockIdx.z;
   const int q0 = qt * PA_TILE;
-  const int nt = qt + 1;                           // key tiles 0..qt (causal)
+  // Cached positions before this call (0 for a prefill over an empty cache): query i sits at
+  // position L + i and sees keys 0..L+i.  The sequence's keys are rows kvr0 .. kvr0+L+T-1 of
+  // kv (each sequence's L + T rows back to back).
+  int L = 0, kvr0 = 0;
+  if (seq_lens != nullptr) {
+    L = seq_lens[b];
+    for (int bb = 0; bb < b; ++bb) kvr0 += seq_lens[bb] + T;
+  } else {
+    kvr0 = b * T;
+  }
+  const int nt = (L + min(q0 + PA_TILE, T) - 1) / PA_TILE + 1;  // key tiles (causal)
+  if (threadIdx.x == 0 && blockIdx.x == 0 && (long)kvr0 + L + T > kv_rows)
+    atomicExch(err, DEV_ERR_PLAN);  // device lengths disagree with the host's kv layout
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -143,8 +156,8 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
         uint8_t* stg = smem + OFF_K + st * PA_K_BYTES;
         mbar_expect_tx(&k_full[st], PA_K_BYTES);
         const int k0 = j * PA_TILE;
-        tma_load_3d(stg, &map_kv, &k_full[st], 0, h, tok0 + k0);
-        tma_load_3d(stg + PA_BOX, &map_kv, &k_full[st], 64, h, tok0 + k0);
+        tma_load_3d(stg, &map_kv, &k_full[st], 0, h, kvr0 + k0);
+        tma_load_3d(stg + PA_BOX, &map_kv, &k_full[st], 64, h, kvr0 + k0);
         tma_load_2d(stg + 2 * PA_BOX, &map_c, &k_full[st], KV_LORA, b * cap + k0);
         issued = j + 1;
       }
@@ -163,8 +176,8 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
         uint8_t* stg = smem + OFF_V + st * PA_V_BYTES;
         mbar_expect_tx(&v_full[st], PA_V_BYTES);
         const int k0 = j * PA_TILE;
-        tma_load_3d(stg, &map_kv, &v_full[st], 128, h, tok0 + k0);
-        tma_load_3d(stg + PA_BOX, &map_kv, &v_full[st], 192, h, tok0 + k0);
+        tma_load_3d(stg, &map_kv, &v_full[st], 128, h, kvr0 + k0);
+        tma_load_3d(stg + PA_BOX, &map_kv, &v_full[st], 192, h, kvr0 + k0);
         issued = j + 1;
       }
       volatile int no_abort = 0;
@@ -241,9 +254,10 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
       // fully unrolled row overflows the instruction cache).
       const uint32_t s_addr = tmem + lane_off + TM_S + 128 * st + PA_GC * grp;
       const int kbase = j * PA_TILE + PA_GC * grp;
-      const int vis = min(qi - kbase + 1, T - kbase);   // columns [0, vis) of this group visible
-      // Tiles left of the diagonal are visible to every row: no mask there.
-      const bool full = j < qt;
+      const int vis = min(L + qi - kbase + 1, L + T - kbase);  // columns [0, vis) visible
+      // Tiles wholly at or before the tile's first query position are visible to every row: no
+      // mask there.
+      const bool full = (j + 1) * PA_TILE <= L + q0 + 1;
       float tmax = -INFINITY;  // pass 1: maximum of the visible scores
       if (ok) {
 #pragma unroll 1
@@ -460,8 +474,9 @@ cudaError_t init_prefill_tc_kernel() {
 
 cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloat16* kv,
                                         const __nv_bfloat16* cache, int cap, int B, int T,
-                                        float scale, __nv_bfloat16* attn_out, uint8_t* o_hi,
-                                        uint8_t* o_lo, float* o_sx, int* err, cudaStream_t st) {
+                                        const int* seq_lens, long kv_rows, float scale,
+                                        __nv_bfloat16* attn_out, uint8_t* o_hi, uint8_t* o_lo,
+                                        float* o_sx, int* err, cudaStream_t st) {
   if ((o_hi == nullptr) != (o_lo == nullptr) || (o_hi == nullptr) != (o_sx == nullptr) ||
       (o_hi == nullptr && attn_out == nullptr))
     return cudaErrorInvalidValue;
@@ -469,14 +484,14 @@ cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloa
   const uint64_t M = (uint64_t)B * T;
   CUtensorMap mq, mkv, mc;
   if (!make_tmap_3d(&mq, q, QHEAD, HEADS, M, QHEAD * 2, (uint64_t)HEADS * QHEAD * 2, 64, 1, 128) ||
-      !make_tmap_3d(&mkv, kv, KVB_PER_HEAD, HEADS, M, KVB_PER_HEAD * 2,
+      !make_tmap_3d(&mkv, kv, KVB_PER_HEAD, HEADS, (uint64_t)kv_rows, KVB_PER_HEAD * 2,
                     (uint64_t)HEADS * KVB_PER_HEAD * 2, 64, 1, 128) ||
       !make_tmap_2d(&mc, true, cache, LAT, (uint64_t)B * cap, LAT * 2, 64, 128))
     return cudaErrorInvalidValue;
   const dim3 grid(HEADS, (T + PA_TILE - 1) / PA_TILE, B);
-  prefill_attn_tc_kernel<<<grid, PA_THREADS, PA_SMEM, st>>>(mq, mkv, mc, T, cap,
+  prefill_attn_tc_kernel<<<grid, PA_THREADS, PA_SMEM, st>>>(mq, mkv, mc, T, cap, seq_lens,
                                                             scale * 1.4426950408889634f, attn_out,
-                                                            o_hi, o_lo, o_sx, err);
+                                                            o_hi, o_lo, o_sx, kv_rows, err);
   return cudaGetLastError();
 }
 

@@ -265,9 +265,10 @@ __device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float* f) {
 // Decode query absorption, q~_h = W_UK,h^T q_nope,h with W_UK,h = rows 0..127 of head h's 256
 // in kv_b_proj ("Key content up-projection" page, Explanation):
 //   qfull[b, h, c] = bf16( s[2h][c/128] * sum_i q_nope[b, h, i] * e4m3(W_kvb[256 h + i, c]) ).
-// CTA (h, cb) owns latent columns [128 cb, 128 cb + 128) (one scale); warp w sums rows
-// i in [32 w, 32 w + 32) for 4 columns per lane, and the 4 warps' partials meet in shared
-// memory.  The cb == 0 CTA also writes RoPE(q_pe) to columns [512, 576).
+// CTA (h, cb, z) owns latent columns [128 cb, 128 cb + 128) (one scale) of sequences
+// [8 z, 8 z + 8); warp w sums rows i in [32 w, 32 w + 32) for 4 columns per lane, and the 4
+// warps' partials meet in shared memory.  The cb == 0 CTAs also write RoPE(q_pe) to columns
+// [512, 576).
 constexpr int ABQ_B = 8;
 __global__ void __launch_bounds__(128) absorb_q_kernel(
     const __nv_bfloat16* __restrict__ q, int B, const uint8_t* __restrict__ Wkvb,
@@ -288,9 +289,9 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(
   }
   pdl_launch_dependents();
   pdl_wait();  // the weights above do not depend on earlier kernels; q does
-  for (int b0 = 0; b0 < B; b0 += ABQ_B) {
+  {
+    const int b0 = blockIdx.z * ABQ_B;  // this CTA's batch of sequences
     const int nb = min(ABQ_B, B - b0);
-    __syncthreads();
     for (int e = threadIdx.x; e < nb * NOPE; e += blockDim.x) {
       const int bb = e / NOPE, i = e % NOPE;
       qn[bb][i] = __bfloat162float(q[((size_t)(b0 + bb) * HEADS + h) * QHEAD + i]);
@@ -326,8 +327,9 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(
     }
   }
   if (cb == 0) {
-    for (int e = threadIdx.x; e < B * (ROPE / 2); e += blockDim.x) {
-      const int bb = e / (ROPE / 2), j = e % (ROPE / 2);
+    for (int e = threadIdx.x; e < min(ABQ_B, B - (int)blockIdx.z * ABQ_B) * (ROPE / 2);
+         e += blockDim.x) {
+      const int bb = blockIdx.z * ABQ_B + e / (ROPE / 2), j = e % (ROPE / 2);
       const int pos = seq_lens[bb];
       if (pos < 0 || pos >= limit) continue;
       const int2 ij = pair_idx(j, pairing);
@@ -343,15 +345,18 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(
 
 // Decode output absorption, one warp per output row (h, v):
 //   out[b, 128 h + v] = bf16( sum_c s[2h+1][c/128] * e4m3(W_kvb[256 h + 128 + v, c]) * o_lat[b, h, c] )
-// (W_UV,h = rows 128..255 of head h's 256).  Lane l holds columns [16 l, 16 l + 16).
+// (W_UV,h = rows 128..255 of head h's 256).  Lane l holds columns [16 l, 16 l + 16).  The
+// CTA's 8 rows belong to one head, whose o_lat rows it stages in shared memory 32 sequences at
+// a time (each row of o_lat is then read from L2 once per CTA, not once per warp).
 constexpr int ABO_B = 8;
+constexpr int ABO_CH = 32;  // sequences staged in shared memory at a time (32 KB)
 __global__ void __launch_bounds__(256) absorb_out_kernel(
     const __nv_bfloat16* __restrict__ o_lat, int B, const uint8_t* __restrict__ Wkvb,
     const float* __restrict__ Skvb, __nv_bfloat16* __restrict__ out) {
+  __shared__ __align__(16) __nv_bfloat16 xs[ABO_CH][KV_LORA];  // o_lat of this head
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;   // h * 128 + v
   const int lane = threadIdx.x & 31;
-  if (row >= HEADS * VDIM) return;
-  const int h = row / VDIM, v = row % VDIM;
+  const int h = row / VDIM, v = row % VDIM;  // h: the same for the CTA's 8 rows
   const uint4 wv = __ldg(reinterpret_cast<const uint4*>(
       Wkvb + (size_t)(h * KVB_PER_HEAD + NOPE + v) * KV_LORA + lane * 16));
   float w[16];
@@ -362,31 +367,42 @@ __global__ void __launch_bounds__(256) absorb_out_kernel(
   const float sc = Skvb[(size_t)(2 * h + 1) * (KV_LORA / BLK) + lane / 8];
   pdl_launch_dependents();
   pdl_wait();  // the weights above do not depend on earlier kernels; o_lat does
-  for (int b0 = 0; b0 < B; b0 += ABO_B) {
-    float acc[ABO_B];
-#pragma unroll
-    for (int bb = 0; bb < ABO_B; ++bb) {
-      acc[bb] = 0.f;
-      if (b0 + bb < B) {
-        const uint4* xp = reinterpret_cast<const uint4*>(
-            o_lat + ((size_t)(b0 + bb) * HEADS + h) * KV_LORA + lane * 16);
-        const uint4 x0 = __ldg(xp), x1 = __ldg(xp + 1);
-        const uint32_t u[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        float p = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          p = fmaf(w[2 * i], __uint_as_float(u[i] << 16), p);
-          p = fmaf(w[2 * i + 1], __uint_as_float(u[i] & 0xFFFF0000u), p);
-        }
-        acc[bb] = sc * p;
-      }
+  for (int c0 = 0; c0 < B; c0 += ABO_CH) {
+    // The head's o_lat rows of sequences [c0, c0 + nc), read once for the CTA's 8 rows.
+    const int nc = min(ABO_CH, B - c0);
+    __syncthreads();
+    for (int e = threadIdx.x; e < nc * (KV_LORA / 8); e += blockDim.x) {
+      const int bb = e / (KV_LORA / 8), k = e % (KV_LORA / 8);
+      reinterpret_cast<uint4*>(xs[bb])[k] = __ldg(
+          reinterpret_cast<const uint4*>(o_lat + ((size_t)(c0 + bb) * HEADS + h) * KV_LORA) + k);
     }
+    __syncthreads();
+    for (int b0 = 0; b0 < nc; b0 += ABO_B) {
+      float acc[ABO_B];
 #pragma unroll
-    for (int bb = 0; bb < ABO_B; ++bb) {
-      float t = acc[bb];
+      for (int bb = 0; bb < ABO_B; ++bb) {
+        acc[bb] = 0.f;
+        if (b0 + bb < nc) {
+          const uint4* xp = reinterpret_cast<const uint4*>(xs[b0 + bb] + lane * 16);
+          const uint4 x0 = xp[0], x1 = xp[1];
+          const uint32_t u[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          float p = 0.f;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-      if (lane == 0 && b0 + bb < B) out[(size_t)(b0 + bb) * O_IN + row] = __float2bfloat16_rn(t);
+          for (int i = 0; i < 8; ++i) {
+            p = fmaf(w[2 * i], __uint_as_float(u[i] << 16), p);
+            p = fmaf(w[2 * i + 1], __uint_as_float(u[i] & 0xFFFF0000u), p);
+          }
+          acc[bb] = sc * p;
+        }
+      }
+#pragma unroll
+      for (int bb = 0; bb < ABO_B; ++bb) {
+        float t = acc[bb];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+        if (lane == 0 && b0 + bb < nc)
+          out[(size_t)(c0 + b0 + bb) * O_IN + row] = __float2bfloat16_rn(t);
+      }
     }
   }
 }
@@ -433,7 +449,9 @@ cudaError_t launch_absorb_q(const __nv_bfloat16* q, int B, const uint8_t* Wkvb,
                             const float* Skvb, const float2* rope_tab, int rope_pairing,
                             const int* seq_lens, int limit, __nv_bfloat16* qfull,
                             cudaStream_t st, bool pdl) {
-  return launch_kernel(absorb_q_kernel, dim3(HEADS, KV_LORA / BLK), dim3(128), 0, st, pdl, q, B,
+  if (B <= 0) return cudaSuccess;
+  return launch_kernel(absorb_q_kernel, dim3(HEADS, KV_LORA / BLK, (B + ABQ_B - 1) / ABQ_B),
+                       dim3(128), 0, st, pdl, q, B,
                        Wkvb, Skvb, rope_tab, rope_pairing, seq_lens, limit, qfull);
 }
 

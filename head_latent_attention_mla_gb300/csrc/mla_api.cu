@@ -45,8 +45,12 @@ size_t gemm_partials(long M, int num_sms) {
 
 int items_max(const mla_ctx* c, int B) { return 2 * c->num_sms + B; }
 
-Layout prefill_layout(long M, int num_sms) {
+// Prefill / cache-append workspace for M new tokens.  kv_rows: rows of the rebuilt keys and
+// values (M over an empty cache; the sum of L_b + T with cached positions); kvb_M: the largest
+// per-sequence kv_b_proj over cache rows (0 when the cache is empty).
+Layout prefill_layout(long M, int num_sms, long kv_rows = -1, long kvb_M = 0) {
   Layout L;
+  if (kv_rows < 0) kv_rows = M;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off += up256(bytes); return o; };
   L.g1 = take((size_t)M * G1_N * 4);
@@ -55,10 +59,15 @@ Layout prefill_layout(long M, int num_sms) {
   L.ckv = take((size_t)M * KV_LORA * 2);  // bf16, or its two e4m3 terms
   L.ckv_sx = take((size_t)M * 4);
   L.q = take((size_t)M * QB_N * 2);
-  L.kv = take((size_t)M * KVB_N * 2);
+  L.kv = take((size_t)kv_rows * KVB_N * 2);
   L.attn = take((size_t)M * O_IN * 2);  // bf16, or its two e4m3 terms (M * O_IN bytes each)
   L.attn_sx = take((size_t)M * HEADS * 4);
-  L.gpart = take(gemm_partials(M, num_sms));
+  size_t gp = gemm_partials(M, num_sms);
+  if (kvb_M > 0) {
+    const size_t k = gemm_partial_bytes((int)kvb_M, KVB_N, KV_LORA, num_sms);
+    gp = k > gp ? k : gp;
+  }
+  L.gpart = take(gp);
   L.total = off;
   return L;
 }
@@ -245,11 +254,16 @@ mla_status mla_upload_norm(mla_ctx* c, int which, const void* g, int n) {
   return MLA_OK;
 }
 
-size_t mla_workspace_bytes(const mla_ctx* c, int B, int T) {
-  if (!c || B < 0 || T < 0) return 0;
-  const size_t p = prefill_layout((long)B * T, c ? c->num_sms : 0).total;
+size_t mla_workspace_bytes_len(const mla_ctx* c, int B, int T, int max_len) {
+  if (!c || B < 0 || T < 0 || max_len < T) return 0;
+  const size_t p = prefill_layout((long)B * T, c->num_sms, (long)B * max_len,
+                                  max_len > T ? max_len : 0).total;
   const size_t d = decode_layout(c, B).total;
   return p > d ? p : d;
+}
+
+size_t mla_workspace_bytes(const mla_ctx* c, int B, int T) {
+  return mla_workspace_bytes_len(c, B, T, T);
 }
 
 mla_status mla_cache_append(mla_ctx* c, const void* x, int B, int T, void* cache, int cap,
@@ -275,12 +289,21 @@ mla_status mla_cache_append(mla_ctx* c, const void* x, int B, int T, void* cache
 mla_status mla_prefill(mla_ctx* c, const void* x, int B, int T, void* cache, int cap,
                        int* lens_dev, const int* lens_host, void* out, void* ws,
                        size_t ws_bytes, void* stream) {
-  const Layout L = prefill_layout((long)B * T, c ? c->num_sms : 0);
+  // Cached positions before the call (chunked prefill when any is non-zero): the rebuilt keys
+  // and values then cover L_b + T rows per sequence.
+  long kv_rows = 0, kvb_M = 0;
+  bool chunked = false;
+  for (int b = 0; lens_host && b < B && B > 0 && T > 0; ++b) {
+    if (lens_host[b] < 0) break;  // rejected by check_tokens below
+    kv_rows += (long)lens_host[b] + T;
+    kvb_M = (long)lens_host[b] + T > kvb_M ? (long)lens_host[b] + T : kvb_M;
+    chunked = chunked || lens_host[b] != 0;
+  }
+  const Layout L = prefill_layout((long)B * T, c ? c->num_sms : 0, chunked ? kv_rows : -1,
+                                  chunked ? kvb_M : 0);
   mla_status st = check_tokens(c, x, B, T, cache, cap, lens_dev, lens_host, ws, ws_bytes, L.total);
   if (st != MLA_OK || B == 0 || T == 0) return st;
   if (!out || !aligned16(out) || out == x) return MLA_ERR_INVALID_ARG;
-  for (int b = 0; b < B; ++b)
-    if (lens_host[b] != 0) return MLA_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   log_reset(c);
   const int M = B * T, limit = cap < c->cfg.max_positions ? cap : c->cfg.max_positions;
@@ -298,7 +321,29 @@ mla_status mla_prefill(mla_ctx* c, const void* x, int B, int T, void* cache, int
   MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, M, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
   Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
   Proj p3{c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], KVB_N, kv, KVB_N, 0};
-  if (M > 8) {
+  if (chunked) {
+    // Keys and values of the cached and the new positions: kv_b_proj over each sequence's
+    // cache rows 0 .. L_b + T - 1 (the first 512 values of a row are its normalised latent),
+    // after the norm kernel has appended the new rows.
+    const E4m3Split qsp{at<uint8_t>(ws, L.cq), at<uint8_t>(ws, L.cq) + (size_t)M * Q_LORA,
+                        at<float>(ws, L.cq_sx)};
+    MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
+                                      c->cfg.rope_pairing, lens_dev, C, cap, limit, M > 8 ? nullptr : cq,
+                                      nullptr, c->d_err, s, false, M > 8 ? &qsp : nullptr, nullptr));
+    if (M > 8) {
+      MLA_LAUNCH("gemm_q_b", launch_gemm_tc_split(qsp.hi, qsp.lo, qsp.sx, false, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+    } else {
+      MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+    }
+    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
+    long r0 = 0;
+    for (int b = 0; b < B; ++b) {
+      const int Mb = lens_host[b] + T;
+      const Proj pb{c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], KVB_N, kv + (size_t)r0 * KVB_N, KVB_N, 0};
+      MLA_LAUNCH("gemm_kv_b", launch_gemm(C + (size_t)b * cap * LAT, LAT, Mb, KV_LORA, &pb, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+      r0 += Mb;
+    }
+  } else if (M > 8) {
     // Tensor-core projections: the norm kernel writes q_b's and kv_b's e4m3 inputs itself (the
     // two terms share the bf16 latents' regions; one scale per token).
     const E4m3Split qsp{at<uint8_t>(ws, L.cq), at<uint8_t>(ws, L.cq) + (size_t)M * Q_LORA,
@@ -325,12 +370,14 @@ mla_status mla_prefill(mla_ctx* c, const void* x, int B, int T, void* cache, int
     uint8_t* a_hi = at<uint8_t>(ws, L.attn);
     uint8_t* a_lo = a_hi + (size_t)M * O_IN;
     float* a_sx = at<float>(ws, L.attn_sx);
-    MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, C, cap, B, T, c->cfg.softmax_scale, nullptr,
+    MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, C, cap, B, T, chunked ? lens_dev : nullptr,
+                                                              chunked ? kv_rows : M, c->cfg.softmax_scale, nullptr,
                                                               a_hi, a_lo, a_sx, c->d_err, s));
     MLA_LAUNCH("gemm_o", launch_gemm_tc_split(a_hi, a_lo, a_sx, true, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
                                               lens_dev, B, T));
   } else {
-    MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, C, cap, B, T, c->cfg.softmax_scale, attn,
+    MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, C, cap, B, T, chunked ? lens_dev : nullptr,
+                                                              chunked ? kv_rows : M, c->cfg.softmax_scale, attn,
                                                               nullptr, nullptr, nullptr, c->d_err, s));
     if (gemm_can_advance(M) && B <= 128) {  // the length update rides on o_proj
       MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,

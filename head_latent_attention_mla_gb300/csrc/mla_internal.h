@@ -219,10 +219,15 @@ cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* 
 // (attn_out may then be null), as the two e4m3 terms of those bf16 values, [B*T, HEADS*VDIM]
 // each, with one scale per (token, head) in o_sx [B*T, HEADS] (the input of
 // launch_gemm_tc_split).
+// Queries: q [B*T, HEADS, QHEAD]; sequence b has seq_lens[b] cached positions before this call
+// (seq_lens null: none), and its keys/values are rows kvr0(b) .. kvr0(b) + L_b + T - 1 of kv
+// [kv_rows, HEADS, KVB_PER_HEAD] with kvr0(b) = sum over b' < b of (L_b' + T); the rotary keys
+// come from the cache rows.  Query t of sequence b sees positions 0 .. L_b + t.
 cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloat16* kv,
                                         const __nv_bfloat16* cache, int cap, int B, int T,
-                                        float scale, __nv_bfloat16* attn_out, uint8_t* o_hi,
-                                        uint8_t* o_lo, float* o_sx, int* err, cudaStream_t st);
+                                        const int* seq_lens, long kv_rows, float scale,
+                                        __nv_bfloat16* attn_out, uint8_t* o_hi, uint8_t* o_lo,
+                                        float* o_sx, int* err, cudaStream_t st);
 cudaError_t init_prefill_tc_kernel();
 
 // seq_lens[b] += T.

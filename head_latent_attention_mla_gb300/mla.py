@@ -41,6 +41,7 @@ _SIGS = {
     "mla_upload_weights": (_I, [_P, _I, _P, _P, _I, _I]),
     "mla_upload_norm": (_I, [_P, _I, _P, _I]),
     "mla_workspace_bytes": (ctypes.c_size_t, [_P, _I, _I]),
+    "mla_workspace_bytes_len": (ctypes.c_size_t, [_P, _I, _I, _I]),
     "mla_cache_append": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_prefill": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_decode": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -135,6 +136,10 @@ def mla_workspace_bytes(ctx: int, B: int, T: int) -> int:
     return int(load().mla_workspace_bytes(ctx, B, T))
 
 
+def mla_workspace_bytes_len(ctx: int, B: int, T: int, max_len: int) -> int:
+    return int(load().mla_workspace_bytes_len(ctx, B, T, max_len))
+
+
 def mla_cache_append(ctx, x, cache, seq_lens_dev, seq_lens_host, ws, stream=None) -> None:
     B, T = x.shape[0], x.shape[1]
     _check(load().mla_cache_append(ctx, _ptr(x), B, T, _ptr(cache), cache.shape[1],
@@ -215,16 +220,17 @@ class MlaLayer:
             mla_upload_norm(self.ctx, NORM_IDS[name], g)
         self.ws = torch.empty(0, dtype=torch.uint8, device=device)
 
-    def workspace(self, B: int, T: int) -> torch.Tensor:
-        need = mla_workspace_bytes(self.ctx, B, T)
+    def workspace(self, B: int, T: int, max_len: int | None = None) -> torch.Tensor:
+        need = mla_workspace_bytes_len(self.ctx, B, T, max(T, max_len or T))
         if self.ws.numel() < need:
             self.ws = torch.empty(need, dtype=torch.uint8, device=self.ws.device)
         return self.ws
 
     def prefill(self, x, cache, seq_lens_dev, seq_lens_host, out=None):
         out = torch.empty_like(x) if out is None else out
+        T = x.shape[1]
         mla_prefill(self.ctx, x, cache, seq_lens_dev, seq_lens_host, out,
-                    self.workspace(x.shape[0], x.shape[1]))
+                    self.workspace(x.shape[0], T, max(seq_lens_host) + T))
         return out
 
     def decode(self, x, cache, seq_lens_dev, seq_lens_host, out=None):

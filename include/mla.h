@@ -91,9 +91,15 @@ mla_status mla_upload_weights(mla_ctx* ctx, int which, const void* e4m3_dev,
 mla_status mla_upload_norm(mla_ctx* ctx, int which, const void* bf16_gain_dev, int n);
 
 /* Bytes of caller-provided device workspace that mla_prefill / mla_decode /
- * mla_cache_append need for B sequences of T new tokens each.  The same workspace may be
- * reused by consecutive calls on one stream; calls that overlap on the GPU need their own. */
+ * mla_cache_append need for B sequences of T new tokens each over an empty cache.  The same
+ * workspace may be reused by consecutive calls on one stream; calls that overlap on the GPU
+ * need their own. */
 size_t mla_workspace_bytes(const mla_ctx* ctx, int B, int T);
+
+/* The same for a prefill over a non-empty cache: max_len >= seq_lens_host[b] + T for every b
+ * (the largest total length a sequence reaches in the call).  Returns 0 for max_len < T or a
+ * null ctx.  mla_workspace_bytes(ctx, B, T) == mla_workspace_bytes_len(ctx, B, T, T). */
+size_t mla_workspace_bytes_len(const mla_ctx* ctx, int B, int T, int max_len);
 
 /* Appends T tokens per sequence to the latent cache without computing attention: for each
  * token, the normalised latent (512) and the rotated shared rotary key (64) ("mla-kv"
@@ -109,12 +115,17 @@ mla_status mla_cache_append(mla_ctx* ctx, const void* x_bf16, int B, int T, void
                             int cap, int* seq_lens_dev, const int* seq_lens_host, void* ws,
                             size_t ws_bytes, void* stream);
 
-/* Prefill over an empty cache ("Latent attention (dense block, prefill)" page: in
- * [B, T, 7168], out [B, T, 7168], the cache holds positions 0..T-1 afterwards).  Token t
- * attends to positions 0..t (causal mask), all 64 heads, scores scaled by softmax_scale,
- * softmax in float32.  Writes out_bf16 [B, T, 7168], fills cache rows 0..T-1 and sets
- * seq_lens_dev[b] = T.  seq_lens_host (host, [B]) must be all zero: a non-empty cache gives
- * MLA_ERR_UNSUPPORTED (chunked prefill is not provided).  out must not alias x. */
+/* Prefill of T new tokens per sequence ("Latent attention (dense block, prefill)" page: in
+ * [B, T, 7168], out [B, T, 7168]).  Sequence b holds L_b = seq_lens[b] cached positions before
+ * the call (0: prefill over an empty cache; more: a chunk of a longer prompt, "KV cache" page:
+ * kv_seq_len = T + cached length).  Token t sits at position L_b + t and attends to positions
+ * 0..L_b+t (the causal mask with the cache offset), all 64 heads, scores scaled by
+ * softmax_scale, softmax in float32; the keys and values of the cached positions are rebuilt
+ * from their latent rows (kv_b_proj), as for the new ones.  Writes out_bf16 [B, T, 7168],
+ * appends cache rows L_b..L_b+T-1 and advances seq_lens_dev[b] by T.  seq_lens_host (host,
+ * [B]) must equal the device lengths (a mismatch is flagged in the device status, not a
+ * fault); with any L_b > 0 the workspace must hold mla_workspace_bytes_len(ctx, B, T,
+ * max_b(L_b + T)) bytes.  out must not alias x. */
 mla_status mla_prefill(mla_ctx* ctx, const void* x_bf16, int B, int T, void* cache_bf16,
                        int cap, int* seq_lens_dev, const int* seq_lens_host, void* out_bf16,
                        void* ws, size_t ws_bytes, void* stream);

@@ -59,6 +59,7 @@ def test_host_argument_checks(lib):
     c.rope_pairing = 7
     assert lib.mla_create(ctypes.byref(c), ctypes.byref(ctx)) == mla.MLA_ERR_INVALID_ARG
     assert lib.mla_workspace_bytes(None, 1, 1) == 0
+    assert lib.mla_workspace_bytes_len(None, 1, 4, 8) == 0
     assert lib.mla_prefill(None, None, 1, 1, None, 1, None, None, None, None, 0, None) == \
         mla.MLA_ERR_INVALID_ARG
     assert lib.mla_decode(None, None, 1, None, 1, None, None, None, None, 0, None) == \

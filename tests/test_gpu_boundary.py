@@ -30,9 +30,14 @@ def test_capacity_and_mode_errors(layer):
     with pytest.raises(mla.MlaError) as e:
         mla.mla_prefill(layer.ctx, x, cache, lens, [3], out, ws)
     assert e.value.status in (mla.MLA_ERR_CAPACITY, mla.MLA_ERR_UNSUPPORTED)
+    # A chunk after 2000 cached positions needs room for 2002 rebuilt key/value rows: the
+    # workspace for an empty cache is refused (before the capacity check).
+    small = ws[:mla.mla_workspace_bytes(layer.ctx, 1, 2)]
+    assert mla.mla_workspace_bytes_len(layer.ctx, 1, 2, 2002) > small.numel()
     with pytest.raises(mla.MlaError) as e:
-        mla.mla_prefill(layer.ctx, x[:, :2].contiguous(), cache, lens, [1], out[:, :2].contiguous(), ws)
-    assert e.value.status == mla.MLA_ERR_UNSUPPORTED
+        mla.mla_prefill(layer.ctx, x[:, :2].contiguous(), cache, lens, [2000],
+                        out[:, :2].contiguous(), small)
+    assert e.value.status == mla.MLA_ERR_INVALID_ARG
     with pytest.raises(mla.MlaError) as e:
         mla.mla_decode(layer.ctx, x[0, :1].contiguous(), cache, lens, [8], out[0, :1].contiguous(), ws)
     assert e.value.status == mla.MLA_ERR_CAPACITY

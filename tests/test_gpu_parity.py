@@ -94,6 +94,53 @@ def test_half_pairing_prefill_and_decode(T):
         L.close()
 
 
+@pytest.mark.parametrize("L,T", [(100, 50), (128, 128), (300, 130), (37, 5)])
+def test_chunked_prefill_every_element(layer, L, T):
+    """A prompt prefilled in two chunks: L tokens over an empty cache, then T tokens against
+    the L cached positions (query t at position L + t sees keys 0..L+t, the cached keys and
+    values rebuilt from their latent rows).  Every element of the second chunk's output and
+    of the whole cache against the oracle's forward over the cached rows."""
+    W = oracle_weights(0)
+    xb = synth.hidden_states(0, 9, 0, L + T)
+    cache = torch.zeros(1, L + T + 3, 576, dtype=torch.bfloat16, device="cuda")
+    lens = torch.zeros(1, dtype=torch.int32, device="cuda")
+    layer.prefill(to_dev(xb[None, :L]), cache, lens, [0])
+    y = layer.prefill(to_dev(xb[None, L:]), cache, lens, [L])
+    torch.cuda.synchronize()
+    assert layer.status() == mla.MLA_OK and lens.item() == L + T
+    xf = O.bf16_to_f64(xb)
+    y_ref, full_ref = O.forward(xf[L:], O.cache_rows(xf[:L], np.arange(L), W), W)
+    assert_close(y[0].float().cpu().numpy(), y_ref, f"chunk L={L} T={T}")
+    assert_close(cache[0, :L + T].float().cpu().numpy(), full_ref, f"cache L={L} T={T}")
+
+
+def test_chunked_prefill_batch_with_different_offsets(layer):
+    """Three sequences with 0, 150 and 260 cached positions take a 70-token chunk together."""
+    W = oracle_weights(0)
+    Ls, T, seqs = [0, 150, 260], 70, [11, 12, 13]
+    xbs = [synth.hidden_states(0, s, 0, Lb + T) for s, Lb in zip(seqs, Ls)]
+    cap = max(Ls) + T
+    cache = torch.zeros(3, cap, 576, dtype=torch.bfloat16, device="cuda")
+    lens = torch.zeros(3, dtype=torch.int32, device="cuda")
+    for b, (Lb, xb) in enumerate(zip(Ls, xbs)):
+        if Lb:
+            one = torch.zeros(1, dtype=torch.int32, device="cuda")
+            c1 = torch.zeros(1, cap, 576, dtype=torch.bfloat16, device="cuda")
+            layer.prefill(to_dev(xb[None, :Lb]), c1, one, [0])
+            cache[b] = c1[0]
+    lens.copy_(torch.tensor(Ls, dtype=torch.int32))
+    x = torch.cat([to_dev(xb[None, Lb:]) for Lb, xb in zip(Ls, xbs)])
+    y = layer.prefill(x, cache, lens, Ls)
+    torch.cuda.synchronize()
+    assert layer.status() == mla.MLA_OK and lens.tolist() == [Lb + T for Lb in Ls]
+    for b, (Lb, xb) in enumerate(zip(Ls, xbs)):
+        xf = O.bf16_to_f64(xb)
+        cache_ref = O.cache_rows(xf[:Lb], np.arange(Lb), W) if Lb else None
+        y_ref, full_ref = O.forward(xf[Lb:], cache_ref, W)
+        assert_close(y[b].float().cpu().numpy(), y_ref, f"sequence {b} (L={Lb})")
+        assert_close(cache[b, :Lb + T].float().cpu().numpy(), full_ref, f"cache {b}")
+
+
 def test_decode_config2_p1000(layer):
     """Decode at position 1000 over a cache built by a causal prefill of 1000 tokens."""
     W = oracle_weights(0)

@@ -182,6 +182,20 @@ def test_decode_equals_last_prefill_row():
     np.testing.assert_allclose(cache2, cache_full, rtol=1e-12, atol=1e-14)
 
 
+def test_prefill_in_chunks_equals_one_prefill():
+    """Prefill of a prompt in chunks against the growing cache (each chunk at positions
+    L..L+T-1 sees keys 0..L+t) equals one causal prefill of the whole prompt, row for row."""
+    d, W = TINY, tiny_weights(23)
+    x = np.random.default_rng(24).normal(size=(17, d.hidden))
+    y_full, cache_full = O.prefill(x, W, d=d)
+    cache, ys = None, []
+    for a, b in ((0, 5), (5, 6), (6, 13), (13, 17)):
+        y, cache = O.forward(x[a:b], cache, W, d=d)
+        ys.append(y)
+    np.testing.assert_allclose(np.concatenate(ys), y_full, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(cache, cache_full, rtol=1e-12, atol=1e-14)
+
+
 def test_prefix_consistency():
     d, W = TINY, tiny_weights(13)
     x = np.random.default_rng(14).normal(size=(10, d.hidden))
