@@ -298,6 +298,47 @@ def run_prefill_workload(torch, mla, synth, layer, T, steps, warmup, device, flu
     return {"T": T, "ms": sum(times) / len(times), "per_kernel_ms": per}
 
 
+def run_chunk_workload(torch, mla, synth, layer, L, T, steps, warmup, device, flush):
+    """Chunked prefill: T new tokens after L cached positions (B=1).  The cache is built by a
+    prefill of the first L tokens outside the timed region; every step restores the length
+    to L, so each step recomputes the same chunk."""
+    xb = synth.hidden_states(0, 0, 0, L + T)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(device)[None]
+    cache = torch.zeros(1, L + T, 576, dtype=torch.bfloat16, device=device)
+    lens = torch.zeros(1, dtype=torch.int32, device=device)
+    layer.prefill(x[:, :L].contiguous(), cache, lens, [0])
+    torch.cuda.synchronize()
+    lens0 = lens.clone()
+    xc = x[:, L:].contiguous()
+    out = torch.empty_like(xc)
+    ws = layer.workspace(1, T, L + T)
+    stream = torch.cuda.Stream(device=device)
+    with torch.cuda.stream(stream):
+        mla.mla_prefill(layer.ctx, xc, cache, lens, [L], out, ws, stream=stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    lens.copy_(lens0)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        mla.mla_prefill(layer.ctx, xc, cache, lens, [L], out, ws)
+    time_graph(torch, g, stream, lens, lens0, flush, warmup)
+    times = time_graph(torch, g, stream, lens, lens0, flush, steps)
+    per = profile_kernels(torch, mla, layer, stream,
+                          lambda: mla.mla_prefill(layer.ctx, xc, cache, lens, [L], out, ws,
+                                                  stream=stream),
+                          lens, lens0, flush, max(2, steps // 2))
+    return {"ms": sum(times) / len(times), "per_kernel_ms": per}
+
+
+def chunk_flops(L, T):
+    """Algorithmic FLOPs of a T-token chunk after L cached positions: the projections of the T
+    new tokens, kv_b_proj over all L + T latent rows (the explicit form rebuilds the cached
+    keys and values), and the attention of query t over keys 0..L+t."""
+    gemm = 2 * T * (7168 * 2112 + 1536 * 12288 + 8192 * 7168) + 2 * (L + T) * 512 * 16384
+    pairs = T * L + T * (T + 1) // 2
+    return gemm, 2 * 64 * pairs * (192 + 128)
+
+
 def prefill_flops(T):
     """Algorithmic FLOPs of one causal prefill of T tokens (GEMMs + causal QK^T and PV)."""
     gemm = 2 * T * (7168 * 2112 + 1536 * 12288 + 512 * 16384 + 8192 * 7168)
@@ -432,6 +473,14 @@ def secondary(torch, mla, synth, layer, device, flush, pk, args):
                                 "tflops": (gemm + attn) / (r["ms"] * 1e-3) / 1e12,
                                 "tensor_frac": (gemm + attn) / (r["ms"] * 1e-3) / 1e12 / pk["bf16_tflops"],
                                 "per_kernel_ms": r["per_kernel_ms"]}
+    L, T = 4096, 1024
+    r = run_chunk_workload(torch, mla, synth, layer, L, T, max(3, steps // 3), 3, device, flush)
+    gemm, attn = chunk_flops(L, T)
+    out[f"prefill_chunk_l{L}_t{T}"] = {
+        "tokens_per_s": T * 1000.0 / r["ms"], "ms_per_step": r["ms"],
+        "tflops": (gemm + attn) / (r["ms"] * 1e-3) / 1e12,
+        "tensor_frac": (gemm + attn) / (r["ms"] * 1e-3) / 1e12 / pk["bf16_tflops"],
+        "per_kernel_ms": r["per_kernel_ms"]}
     return out
 
 
@@ -480,8 +529,9 @@ def reference_arm(args):
 
 def case_arm(args):
     """One workload, small enough to profile: `decode:B:L` (B sequences with L cached positions
-    each, cache built by append) or `prefill:T` (one sequence of T tokens).  Prints a short
-    JSON line with the step time and per-kernel device times."""
+    each, cache built by append), `prefill:T` (one sequence of T tokens) or `chunk:L:T` (T new
+    tokens after L cached positions).  Prints a short JSON line with the step time and
+    per-kernel device times."""
     import torch
     from head_latent_attention_mla_gb300 import mla, synth
     torch.cuda.set_device(0)
@@ -493,6 +543,9 @@ def case_arm(args):
         B, L = int(dims[0]), int(dims[1])
         r = run_decode_workload(torch, mla, synth, layer, args.case, [L] * B, "append",
                                 args.steps, args.warmup, device, flush, prof_steps=3, e2e=False)
+    elif kind == "chunk":
+        r = run_chunk_workload(torch, mla, synth, layer, int(dims[0]), int(dims[1]), args.steps,
+                               args.warmup, device, flush)
     else:
         r = run_prefill_workload(torch, mla, synth, layer, int(dims[0]), args.steps,
                                  args.warmup, device, flush)
@@ -508,7 +561,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="profiling case instead of the benchmark line: decode:B:L or prefill:T")
+                    help="profiling case instead of the benchmark line: decode:B:L, prefill:T "
+                         "or chunk:L:T")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
