@@ -32,10 +32,21 @@ Readings where the pages are silent (each is listed in the design notes):
     as the `mla-kv` excerpt builds them when the token is first seen, so the keys and values
     the scores see are the ones the pages' cache would return.
 
+  * YaRN (optional, off by default): config.json on the "KV cache" page declares rope_scaling
+    {type yarn, factor 32, original_max_position_embeddings 4096, beta_fast 1, beta_slow 1,
+    mscale 1, mscale_all_dim 1} without the formulas.  They follow the published YaRN method
+    (Peng et al., 2023, "NTK-by-parts" interpolation with an attention temperature), in the
+    parametrisation those config keys name: pair j keeps its frequency while its wavelength
+    turns more than beta_fast times over the original context, is divided by the factor
+    while it turns fewer than beta_slow times, with a linear ramp between; the score scale
+    is multiplied by m(factor, mscale_all_dim)^2 and cos/sin by m(factor, mscale) /
+    m(factor, mscale_all_dim), m(s, mu) = 0.1 mu ln s + 1 for s > 1, else 1.
+
 Parity is pinned by tests under tests/ (parameter counts, cache bytes, e4m3 table, RMSNorm and
 RoPE closed forms, softmax sums, decode-equals-prefill, prefix consistency, brute-force loops on
-tiny sizes and the absorbed form).  Parity unpinned: the RoPE pairing choice itself (no page
-value decides between adjacent and half pairing).
+tiny sizes, the absorbed form, YaRN's reductions to plain RoPE and its closed-form
+boundaries).  Parity unpinned: the RoPE pairing choice itself (no page value decides between
+adjacent and half pairing).
 """
 from __future__ import annotations
 
@@ -206,22 +217,63 @@ def rms_norm(x: np.ndarray, g: np.ndarray, eps: float = RMS_EPS) -> np.ndarray:
     return g * (x / np.sqrt(var + eps))
 
 
-def rope_angles(positions: np.ndarray, rope_dim: int, theta: float = ROPE_THETA) -> np.ndarray:
-    """angle[p, j] = pos_p * theta^(-2j/rope_dim) for the rope_dim/2 pairs."""
+@dataclass(frozen=True)
+class Yarn:
+    """rope_scaling of config.json ("KV cache" page); the values are Kimi-K2's."""
+    factor: float = 32.0
+    original_max_positions: int = 4096
+    beta_fast: float = 1.0
+    beta_slow: float = 1.0
+    mscale: float = 1.0
+    mscale_all_dim: float = 1.0
+
+
+def yarn_m(s: float, mu: float) -> float:
+    """YaRN's attention-temperature factor: 0.1 mu ln s + 1 for s > 1, else 1."""
+    return 0.1 * mu * np.log(s) + 1.0 if s > 1.0 else 1.0
+
+
+def yarn_pair_of_rotations(r: float, rope_dim: int, theta: float, original: int) -> float:
+    """The (fractional) pair index j whose wavelength 2 pi theta^(2j/rope_dim) fits r times
+    into the original context: original * theta^(-2j/rope_dim) / (2 pi) = r."""
+    return rope_dim * np.log(original / (2.0 * np.pi * r)) / (2.0 * np.log(theta))
+
+
+def rope_inv_freq(rope_dim: int, theta: float = ROPE_THETA, yarn: Yarn | None = None):
+    """Per-pair angular frequency: theta^(-2j/rope_dim); with YaRN, pairs below the
+    fast-rotation boundary keep it, pairs above the slow-rotation boundary take it divided by
+    the factor, and a linear ramp in j joins the two."""
     j = np.arange(rope_dim // 2, dtype=np.float64)
-    inv_freq = theta ** (-2.0 * j / rope_dim)
+    base = theta ** (-2.0 * j / rope_dim)
+    if yarn is None:
+        return base
+    lo = max(np.floor(yarn_pair_of_rotations(yarn.beta_fast, rope_dim, theta,
+                                             yarn.original_max_positions)), 0.0)
+    hi = min(np.ceil(yarn_pair_of_rotations(yarn.beta_slow, rope_dim, theta,
+                                            yarn.original_max_positions)), rope_dim - 1.0)
+    width = hi - lo if hi > lo else 1e-3          # one-pair ramp when the bounds meet
+    ramp = np.clip((j - lo) / width, 0.0, 1.0)    # 0: keep the frequency, 1: interpolate
+    return base * (1.0 - ramp) + (base / yarn.factor) * ramp
+
+
+def rope_angles(positions: np.ndarray, rope_dim: int, theta: float = ROPE_THETA,
+                yarn: Yarn | None = None) -> np.ndarray:
+    """angle[p, j] = pos_p * inv_freq_j for the rope_dim/2 pairs (plain: theta^(-2j/rope_dim))."""
+    inv_freq = rope_inv_freq(rope_dim, theta, yarn)
     return np.asarray(positions, np.float64)[:, None] * inv_freq[None, :]
 
 
 def apply_rope(x: np.ndarray, positions: np.ndarray, theta: float = ROPE_THETA,
-               pairing: str = "adjacent") -> np.ndarray:
+               pairing: str = "adjacent", yarn: Yarn | None = None) -> np.ndarray:
     """Rotate the rotary slice x[..., P, rope_dim] (P positions on axis -2) by its position.
 
     "adjacent": pair j = (x[2j], x[2j+1]); "half": pair j = (x[j], x[j + rope_dim/2]).
     Each pair (a, b) becomes (a cos - b sin, b cos + a sin), written back in place."""
     rope_dim = x.shape[-1]
-    ang = rope_angles(positions, rope_dim, theta)
-    c, s = np.cos(ang), np.sin(ang)
+    ang = rope_angles(positions, rope_dim, theta, yarn)
+    mag = 1.0 if yarn is None else yarn_m(yarn.factor, yarn.mscale) / yarn_m(yarn.factor,
+                                                                                 yarn.mscale_all_dim)
+    c, s = mag * np.cos(ang), mag * np.sin(ang)
     out = np.array(x, dtype=np.float64, copy=True)
     if pairing == "adjacent":
         a, b = x[..., 0::2], x[..., 1::2]
@@ -281,11 +333,12 @@ def latent(x: np.ndarray, W: Weights, d: Dims = KIMI_K2, eps: float = RMS_EPS):
 
 
 def cache_rows(x: np.ndarray, positions: np.ndarray, W: Weights, d: Dims = KIMI_K2,
-               eps: float = RMS_EPS, theta: float = ROPE_THETA, pairing: str = "adjacent"):
+               eps: float = RMS_EPS, theta: float = ROPE_THETA, pairing: str = "adjacent",
+               yarn: Yarn | None = None):
     """What one layer keeps for tokens x [P, hidden] at `positions`: the normalised latent and
     the rotated shared rotary key, concatenated to [P, kv_lora + rope]."""
     c_hat, k_pe = latent(x, W, d, eps)
-    k_rot = apply_rope(k_pe, positions, theta, pairing)
+    k_rot = apply_rope(k_pe, positions, theta, pairing, yarn)
     return np.concatenate([c_hat, k_rot], axis=-1)
 
 
@@ -340,7 +393,7 @@ def output(o: np.ndarray, W: Weights, d: Dims = KIMI_K2) -> np.ndarray:
 
 def forward(x: np.ndarray, cache: np.ndarray | None, W: Weights, d: Dims = KIMI_K2,
             eps: float = RMS_EPS, theta: float = ROPE_THETA, pairing: str = "adjacent",
-            scale: float | None = None, return_probs: bool = False):
+            scale: float | None = None, return_probs: bool = False, yarn: Yarn | None = None):
     """One layer over T new tokens x [T, hidden] of one sequence whose cache holds
     L = len(cache) positions (None or empty for prefill over an empty cache).
 
@@ -350,9 +403,11 @@ def forward(x: np.ndarray, cache: np.ndarray | None, W: Weights, d: Dims = KIMI_
     L = 0 if cache is None else cache.shape[0]
     pos = np.arange(L, L + x.shape[0])
     q_nope, q_pe = query(x, W, d, eps)
-    q_pe_rot = apply_rope(np.transpose(q_pe, (1, 0, 2)), pos, theta, pairing)
+    q_pe_rot = apply_rope(np.transpose(q_pe, (1, 0, 2)), pos, theta, pairing, yarn)
     q_pe_rot = np.transpose(q_pe_rot, (1, 0, 2))
-    new_rows = cache_rows(x, pos, W, d, eps, theta, pairing)
+    new_rows = cache_rows(x, pos, W, d, eps, theta, pairing, yarn)
+    if scale is None and yarn is not None:  # YaRN's temperature on the scores
+        scale = softmax_scale(d) * yarn_m(yarn.factor, yarn.mscale_all_dim) ** 2
     full = new_rows if L == 0 else np.concatenate([cache, new_rows], axis=0)
     res = attend(q_nope, q_pe_rot, pos, full, W, d, scale, return_probs=return_probs)
     o, probs = res if return_probs else (res, None)

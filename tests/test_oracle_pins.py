@@ -150,6 +150,54 @@ def test_rope_dot_depends_on_offset_only(pairing):
 
 
 # ----------------------------------------------------------------------------- attention
+def test_yarn_reduces_to_plain_rope():
+    """YaRN with factor 1, or with an original context so long that every pair turns more than
+    beta_fast times over it, leaves every frequency (and cos/sin magnitude) unchanged."""
+    base = O.rope_inv_freq(64, 50000.0)
+    np.testing.assert_array_equal(O.rope_inv_freq(64, 50000.0, O.Yarn(factor=1.0)), base)
+    np.testing.assert_allclose(O.rope_inv_freq(64, 50000.0, O.Yarn(original_max_positions=10**15)),
+                               base, rtol=0, atol=0)
+    x = np.random.default_rng(3).normal(size=(5, 64))
+    np.testing.assert_array_equal(O.apply_rope(x, np.arange(5), yarn=O.Yarn(factor=1.0)),
+                                  O.apply_rope(x, np.arange(5)))
+
+
+def test_yarn_boundary_for_kimi_config():
+    """Kimi-K2's rope_scaling (factor 32, original 4096, beta_fast = beta_slow = 1): a pair keeps
+    its frequency iff its wavelength turns at least once more over the original 4096 positions,
+    counted directly as 4096 theta^(-2j/64) / (2 pi); the others run 32 times slower.  The
+    temperature is m = 1 + 0.1 ln 32 and the score scale (1/sqrt 192) m^2."""
+    j = np.arange(32)
+    turns = 4096 * 50000.0 ** (-2.0 * j / 64) / (2 * np.pi)
+    keep = turns > 1.0
+    assert keep[:20].all() and not keep[20:].any()          # the boundary falls between 19 and 20
+    base = 50000.0 ** (-2.0 * j / 64)
+    f = O.rope_inv_freq(64, 50000.0, O.Yarn())
+    np.testing.assert_array_equal(f[keep], base[keep])
+    np.testing.assert_allclose(f[~keep], base[~keep] / 32.0, rtol=1e-15)
+    assert abs(O.yarn_m(32.0, 1.0) - (1.0 + 0.1 * np.log(32.0))) < 1e-15
+    d, W = TINY, tiny_weights(25)
+    x = np.random.default_rng(26).normal(size=(6, d.hidden))
+    yy = O.Yarn(factor=4.0, original_max_positions=8)
+    y_default, _ = O.prefill(x, W, d=d, yarn=yy)
+    y_explicit, _ = O.prefill(x, W, d=d, yarn=yy,
+                              scale=O.softmax_scale(d) * (1 + 0.1 * np.log(4.0)) ** 2)
+    np.testing.assert_allclose(y_default, y_explicit, rtol=1e-13, atol=1e-15)
+    y_plain_scale, _ = O.prefill(x, W, d=d, yarn=yy, scale=O.softmax_scale(d))
+    assert np.max(np.abs(y_default - y_plain_scale)) > 1e-6   # the temperature matters
+
+
+def test_yarn_dot_depends_on_offset_only():
+    rng = np.random.default_rng(27)
+    q, k = rng.normal(size=64), rng.normal(size=64)
+    yy = O.Yarn()
+    def dot(m, n):
+        return float(O.apply_rope(q[None], np.array([m]), yarn=yy)[0]
+                     @ O.apply_rope(k[None], np.array([n]), yarn=yy)[0])
+    assert abs(dot(10, 3) - dot(1007, 1000)) < 1e-9
+    assert abs(dot(5000, 5000) - dot(0, 0)) < 1e-9
+
+
 def test_softmax_rows_sum_to_one_and_mask_is_exact():
     d, W = TINY, tiny_weights(7)
     x = np.random.default_rng(8).normal(size=(9, d.hidden))
@@ -332,8 +380,9 @@ def test_planted_mistakes_are_caught(monkeypatch, mistake):
         monkeypatch.setattr(O, "split_kv_b", lambda Wk, dd=O.KIMI_K2: _swapped(Wk, dd))
     elif mistake == "rope_sign":
         orig_rope = O.apply_rope
-        monkeypatch.setattr(O, "apply_rope", lambda v, p, th=O.ROPE_THETA, pairing="adjacent":
-                            orig_rope(v, -np.asarray(p), th, pairing))
+        monkeypatch.setattr(O, "apply_rope",
+                            lambda v, p, th=O.ROPE_THETA, pairing="adjacent", yarn=None:
+                            orig_rope(v, -np.asarray(p), th, pairing, yarn))
     elif mistake == "no_scale":
         monkeypatch.setattr(O, "softmax_scale", lambda dd=O.KIMI_K2: 1.0)
     elif mistake == "mask_off_by_one":
