@@ -134,6 +134,39 @@ mla_status check_tokens(const mla_ctx* c, const void* x, int B, int T, const voi
   return MLA_OK;
 }
 
+// YaRN's attention temperature m(s, mu) = 0.1 mu ln s + 1 (s > 1), else 1.
+double yarn_temperature(double s, double mu) { return s > 1.0 ? 0.1 * mu * std::log(s) + 1.0 : 1.0; }
+
+// Angular frequency of each rotary pair and the cos/sin gain.  Plain RoPE: theta^(-2j/64).
+// YaRN (Peng et al., 2023, in the parametrisation of config.json's rope_scaling keys): the
+// pair whose wavelength turns r times over the original context is
+// j(r) = 64 ln(original / (2 pi r)) / (2 ln theta); pairs up to floor(j(beta_fast)) keep their
+// frequency, pairs from ceil(j(beta_slow)) on run `factor` times slower, and the frequency
+// ramps linearly in j between the two (bounds clamped to [0, 63]; a zero-width ramp is one
+// thousandth of a pair wide).  The gain is m(factor, mscale) / m(factor, mscale_all_dim).
+void rope_frequencies(const mla_config& cfg, double* w, double* gain) {
+  const double theta = cfg.rope_theta;
+  for (int j = 0; j < ROPE / 2; ++j) w[j] = std::pow(theta, -2.0 * j / ROPE);
+  *gain = 1.0;
+  if (cfg.rope_scaling != MLA_ROPE_YARN) return;
+  const double pi = 3.14159265358979323846;
+  auto pair_of = [&](double r) {
+    return ROPE * std::log((double)cfg.yarn_original_max_positions / (2.0 * pi * r)) /
+           (2.0 * std::log(theta));
+  };
+  double lo = std::floor(pair_of(cfg.yarn_beta_fast)), hi = std::ceil(pair_of(cfg.yarn_beta_slow));
+  lo = lo < 0.0 ? 0.0 : lo;
+  hi = hi > ROPE - 1.0 ? ROPE - 1.0 : hi;
+  const double width = hi > lo ? hi - lo : 1e-3;
+  for (int j = 0; j < ROPE / 2; ++j) {
+    double t = (j - lo) / width;
+    t = t < 0.0 ? 0.0 : (t > 1.0 ? 1.0 : t);
+    w[j] = w[j] * (1.0 - t) + (w[j] / cfg.yarn_factor) * t;
+  }
+  *gain = yarn_temperature(cfg.yarn_factor, cfg.yarn_mscale) /
+          yarn_temperature(cfg.yarn_factor, cfg.yarn_mscale_all_dim);
+}
+
 }  // namespace
 
 extern "C" {
@@ -152,6 +185,13 @@ void mla_default_config(mla_config* cfg) {
   cfg->softmax_scale = (float)(1.0 / std::sqrt((double)(NOPE + ROPE)));
   cfg->max_positions = 131073;
   cfg->rope_pairing = MLA_ROPE_ADJACENT;
+  cfg->rope_scaling = MLA_ROPE_PLAIN;
+  cfg->yarn_factor = 32.0f;
+  cfg->yarn_original_max_positions = 4096;
+  cfg->yarn_beta_fast = 1.0f;
+  cfg->yarn_beta_slow = 1.0f;
+  cfg->yarn_mscale = 1.0f;
+  cfg->yarn_mscale_all_dim = 1.0f;
 }
 
 mla_status mla_create(const mla_config* cfg, mla_ctx** out) {
@@ -164,6 +204,13 @@ mla_status mla_create(const mla_config* cfg, mla_ctx** out) {
   if (cfg->max_positions <= 0 || !(cfg->eps >= 0.f) || !(cfg->rope_theta > 0.f) ||
       !(cfg->softmax_scale > 0.f))
     return MLA_ERR_INVALID_ARG;
+  if (cfg->rope_scaling != MLA_ROPE_PLAIN && cfg->rope_scaling != MLA_ROPE_YARN)
+    return MLA_ERR_INVALID_ARG;
+  if (cfg->rope_scaling == MLA_ROPE_YARN &&
+      (!(cfg->yarn_factor >= 1.f) || cfg->yarn_original_max_positions <= 0 ||
+       !(cfg->yarn_beta_fast > 0.f) || !(cfg->yarn_beta_slow > 0.f) ||
+       !(cfg->yarn_mscale >= 0.f) || !(cfg->yarn_mscale_all_dim >= 0.f)))
+    return MLA_ERR_INVALID_ARG;
   mla_ctx* c = new (std::nothrow) mla_ctx();
   if (!c) return MLA_ERR_INVALID_ARG;
   c->cfg = *cfg;
@@ -172,14 +219,20 @@ mla_status mla_create(const mla_config* cfg, mla_ctx** out) {
     delete c;
     return MLA_ERR_CUDA;
   }
-  // RoPE table in double precision: angle = pos * theta^(-2j/64), stored as float (cos, sin).
+  // RoPE table in double precision: angle = pos * w_j, stored as float (g cos, g sin).
+  // Plain: w_j = theta^(-2j/64), g = 1.  YaRN: see rope_frequencies.
+  double w[ROPE / 2], g = 1.0;
+  rope_frequencies(*cfg, w, &g);
+  if (cfg->rope_scaling == MLA_ROPE_YARN) {
+    const double m = yarn_temperature(cfg->yarn_factor, cfg->yarn_mscale_all_dim);
+    c->cfg.softmax_scale = (float)((double)cfg->softmax_scale * m * m);
+  }
   const size_t n = (size_t)cfg->max_positions * (ROPE / 2);
   std::vector<float2> tab(n);
   for (int j = 0; j < ROPE / 2; ++j) {
-    const double inv = std::pow((double)cfg->rope_theta, -2.0 * j / ROPE);
     for (int p = 0; p < cfg->max_positions; ++p) {
-      const double a = (double)p * inv;
-      tab[(size_t)p * (ROPE / 2) + j] = make_float2((float)std::cos(a), (float)std::sin(a));
+      const double a = (double)p * w[j];
+      tab[(size_t)p * (ROPE / 2) + j] = make_float2((float)(g * std::cos(a)), (float)(g * std::sin(a)));
     }
   }
   if (cudaMalloc(&c->rope_tab, n * sizeof(float2)) != cudaSuccess) {

@@ -54,6 +54,8 @@ enum { MLA_W_Q_A = 0, MLA_W_Q_B = 1, MLA_W_KV_A = 2, MLA_W_KV_B = 3, MLA_W_O = 4
 enum { MLA_NORM_Q = 0, MLA_NORM_KV = 1 };
 /* RoPE pairing of the 64-wide rotary slice: pair j = (2j, 2j+1) or (j, j+32). */
 enum { MLA_ROPE_ADJACENT = 0, MLA_ROPE_HALF = 1 };
+/* RoPE frequencies: plain theta^(-2j/64), or YaRN (config.json rope_scaling, "KV cache" page). */
+enum { MLA_ROPE_PLAIN = 0, MLA_ROPE_YARN = 1 };
 
 typedef struct {
   int hidden, q_lora, kv_lora, heads, nope, rope, vdim; /* must be 7168,1536,512,64,128,64,128 */
@@ -62,11 +64,24 @@ typedef struct {
   float softmax_scale; /* score scale; 1/sqrt(nope+rope) by default                     */
   int max_positions;   /* RoPE table rows: positions 0 .. max_positions-1 are allowed   */
   int rope_pairing;    /* MLA_ROPE_ADJACENT (default) or MLA_ROPE_HALF                  */
+  int rope_scaling;    /* MLA_ROPE_PLAIN (default) or MLA_ROPE_YARN                     */
+  float yarn_factor;              /* rope_scaling.factor (32)                           */
+  int yarn_original_max_positions; /* rope_scaling.original_max_position_embeddings (4096) */
+  float yarn_beta_fast, yarn_beta_slow;     /* rope_scaling.beta_fast / beta_slow (1, 1) */
+  float yarn_mscale, yarn_mscale_all_dim;   /* rope_scaling.mscale / mscale_all_dim (1, 1) */
 } mla_config;
 
 /* Fills *cfg with Kimi-K2's dimensions (config.json on the "KV cache" page), eps 1e-6,
  * theta 50000, scale 1/sqrt(192), max_positions 131073 (max_position_embeddings 131072 is
- * not enforced by the pages' code, so position 131072 itself is allowed), adjacent pairs. */
+ * not enforced by the pages' code, so position 131072 itself is allowed), adjacent pairs,
+ * plain RoPE, and Kimi-K2's YaRN parameters ready for rope_scaling = MLA_ROPE_YARN.
+ *
+ * YaRN (published method, Peng et al. 2023; the pages give only the parameters): pair j
+ * keeps its frequency while its wavelength turns more than beta_fast times over
+ * original_max_positions, runs factor times slower below beta_slow turns, with a linear ramp
+ * in j between the two boundary pairs; cos/sin are scaled by m(factor, mscale) /
+ * m(factor, mscale_all_dim) and the score scale by m(factor, mscale_all_dim)^2, where
+ * m(s, mu) = 0.1 mu ln s + 1 for s > 1, else 1. */
 void mla_default_config(mla_config* cfg);
 
 /* Creates a context on the current CUDA device.  Checks the dimensions (anything but

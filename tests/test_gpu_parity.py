@@ -141,6 +141,34 @@ def test_chunked_prefill_batch_with_different_offsets(layer):
         assert_close(cache[b, :Lb + T].float().cpu().numpy(), full_ref, f"cache {b}")
 
 
+def test_yarn_chunk_and_decode_at_6000():
+    """YaRN RoPE with Kimi-K2's rope_scaling: a cache of 6000 positions built by append, a
+    16-token chunk at positions 6000..6015, then one decode step at 6016 -- far enough that the
+    interpolated pairs turn -- every element against the oracle with the same option (which
+    also takes the score temperature)."""
+    wq, g = weights_and_gains(0)
+    Lr = mla.MlaLayer(wq, g, rope_scaling=mla.MLA_ROPE_YARN)
+    try:
+        W, Y, P = oracle_weights(0), O.Yarn(), 6000
+        xb = synth.hidden_states(0, 21, 0, P + 17)
+        cache = torch.zeros(1, P + 17, 576, dtype=torch.bfloat16, device="cuda")
+        lens = torch.zeros(1, dtype=torch.int32, device="cuda")
+        Lr.cache_append(to_dev(xb[None, :P]), cache, lens, [0])
+        y = Lr.prefill(to_dev(xb[None, P:P + 16]), cache, lens, [P])
+        yd = Lr.decode(to_dev(xb[P + 16:P + 17]), cache, lens, [P + 16])
+        torch.cuda.synchronize()
+        assert Lr.status() == mla.MLA_OK and lens.item() == P + 17
+        xf = O.bf16_to_f64(xb)
+        cache_ref = O.cache_rows(xf[:P], np.arange(P), W, yarn=Y)
+        y_ref, full = O.forward(xf[P:P + 16], cache_ref, W, yarn=Y)
+        yd_ref, full2 = O.decode(xf[P + 16], full, W, yarn=Y)
+        assert_close(y[0].float().cpu().numpy(), y_ref, "yarn chunk")
+        assert_close(yd[0].float().cpu().numpy(), yd_ref, "yarn decode")
+        assert_close(cache[0].float().cpu().numpy(), full2, "yarn cache")
+    finally:
+        Lr.close()
+
+
 def test_decode_config2_p1000(layer):
     """Decode at position 1000 over a cache built by a causal prefill of 1000 tokens."""
     W = oracle_weights(0)
