@@ -54,6 +54,7 @@ constexpr int OFF_MISC = OFF_BAR + 24 * 8;  // 19 barriers used
 constexpr int OFF_ALPHA = OFF_MISC + 16;   // [2][HEADS] rescale factors, by tile parity
 constexpr int OFF_INVL = OFF_ALPHA + 2 * HEADS * 4;  // [HEADS] 1 / l of the finished segment
 constexpr int MAX_SEG = 96;                     // segments one CTA can hold
+constexpr int DA_L2_AHEAD = 1;                  // tiles prefetched into L2 ahead of the ring
 constexpr int OFF_SEG = OFF_INVL + HEADS * 4;
 constexpr int DA_SMEM = OFF_SEG + MAX_SEG * 12 + 16 + 1024;  // + slack for 1024-byte alignment
 constexpr uint32_t TM_O = 0, TM_S = 256;
@@ -188,6 +189,19 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
             for (int c = 0; c < DA_NBOX; ++c)
               tma_load_2d(smem + OFF_C + st * DA_TILE_BYTES + c * DA_BOX, &map_c, &c_full[st],
                           64 * c, row);
+            // The two-stage ring holds few bytes in flight: start the DRAM reads of the tile
+            // DA_L2_AHEAD later into L2, so its own load later finds it there.  At the last
+            // tile of a segment, the next segment's query block and first tile instead.
+            if (i + DA_L2_AHEAD < nt) {
+              for (int c = 0; c < DA_NBOX; ++c)
+                tma_prefetch_l2_2d(&map_c, 64 * c, row + DA_TILE * DA_L2_AHEAD);
+            } else if (i == nt - 1 && sg + 1 < nseg) {
+              const int bn = seg[3 * (sg + 1)], rn = bn * cap + seg[3 * (sg + 1) + 1];
+              for (int c = 0; c < DA_NBOX; ++c) {
+                tma_prefetch_l2_2d(&map_q, 64 * c, HEADS * bn);
+                tma_prefetch_l2_2d(&map_c, 64 * c, rn);
+              }
+            }
             issued = t + 1;
           }
         }
