@@ -445,6 +445,85 @@ cudaError_t launch_rope_q(__nv_bfloat16* q, int B, int T, const float2* rope_tab
   return cudaGetLastError();
 }
 
+// The same output absorption for many sequences (B > 8) as a small tiled product per head:
+// CTA (h, vb) computes out[b, 128 h + v] for the 32 rows v in [32 vb, 32 vb + 32) and every
+// sequence.  It stages W_UV,h's 32 rows as fp32 with their block scale folded in, transposed
+// to [512 c][32 v], and the head's o_lat rows of up to 64 sequences transposed to
+// [512 c][64 b] (bf16); thread (r, s) then accumulates a 4-row x 2-sequence tile over the 512
+// latent columns (one 16-byte and one 4-byte shared load per 8 FMAs).
+constexpr int ABT_V = 32;    // output rows per CTA
+constexpr int ABT_S = 64;    // sequences per staged chunk
+constexpr int ABT_THREADS = (ABT_V / 4) * (ABT_S / 2);  // 256
+constexpr size_t ABT_SMEM = (size_t)KV_LORA * ABT_V * 4 + (size_t)KV_LORA * ABT_S * 2;
+__global__ void __launch_bounds__(ABT_THREADS) absorb_out_tiled_kernel(
+    const __nv_bfloat16* __restrict__ o_lat, int B, const uint8_t* __restrict__ Wkvb,
+    const float* __restrict__ Skvb, __nv_bfloat16* __restrict__ out) {
+  extern __shared__ __align__(16) uint8_t abt_smem[];
+  float* ws = reinterpret_cast<float*>(abt_smem);                              // [512][32]
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(abt_smem + KV_LORA * ABT_V * 4);  // [512][64]
+  const int h = blockIdx.x, v0 = blockIdx.y * ABT_V;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  {  // W_UV rows (lane = row), 16 columns per chunk, 4 chunks per thread
+    const uint8_t* wrow = Wkvb + (size_t)(h * KVB_PER_HEAD + NOPE + v0 + lane) * KV_LORA;
+    for (int k = 0; k < KV_LORA / 16 / (ABT_THREADS / 32); ++k) {
+      const int c0 = (warp * (KV_LORA / 16 / (ABT_THREADS / 32)) + k) * 16;
+      const float sc = Skvb[(size_t)(2 * h + 1) * (KV_LORA / BLK) + c0 / BLK];
+      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wrow + c0));
+      float f[16];
+      e4m3x4_to_f32(wv.x, f);
+      e4m3x4_to_f32(wv.y, f + 4);
+      e4m3x4_to_f32(wv.z, f + 8);
+      e4m3x4_to_f32(wv.w, f + 12);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ws[(c0 + i) * ABT_V + lane] = f[i] * sc;
+    }
+  }
+  pdl_launch_dependents();
+  pdl_wait();  // the weights above do not depend on earlier kernels; o_lat does
+  const int r0 = (threadIdx.x % (ABT_V / 4)) * 4, s0 = (threadIdx.x / (ABT_V / 4)) * 2;
+  for (int b0 = 0; b0 < B; b0 += ABT_S) {
+    const int nb = min(ABT_S, B - b0);
+    __syncthreads();  // the previous chunk's reads of xs are done (and ws is written)
+    // o_lat rows of this head: 8 columns per 16-byte load, written transposed.
+    for (int e = threadIdx.x; e < nb * (KV_LORA / 8); e += ABT_THREADS) {
+      const int sb = e % nb, c0 = (e / nb) * 8;
+      const uint4 x = __ldg(reinterpret_cast<const uint4*>(
+          o_lat + ((size_t)(b0 + sb) * HEADS + h) * KV_LORA + c0));
+      const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xs[(c0 + i) * ABT_S + sb] = xb[i];
+    }
+    __syncthreads();
+    if (s0 < nb) {
+      float acc[4][2] = {};
+#pragma unroll 4
+      for (int c = 0; c < KV_LORA; ++c) {
+        const float4 w = *reinterpret_cast<const float4*>(ws + c * ABT_V + r0);
+        const uint32_t xp = *reinterpret_cast<const uint32_t*>(xs + c * ABT_S + s0);
+        const float x0 = __uint_as_float(xp << 16), x1 = __uint_as_float(xp & 0xFFFF0000u);
+        acc[0][0] = fmaf(w.x, x0, acc[0][0]);
+        acc[1][0] = fmaf(w.y, x0, acc[1][0]);
+        acc[2][0] = fmaf(w.z, x0, acc[2][0]);
+        acc[3][0] = fmaf(w.w, x0, acc[3][0]);
+        acc[0][1] = fmaf(w.x, x1, acc[0][1]);
+        acc[1][1] = fmaf(w.y, x1, acc[1][1]);
+        acc[2][1] = fmaf(w.z, x1, acc[2][1]);
+        acc[3][1] = fmaf(w.w, x1, acc[3][1]);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (s0 + j >= nb) break;
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0][j], acc[1][j]);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2][j], acc[3][j]);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(out + (size_t)(b0 + s0 + j) * O_IN + h * VDIM + v0 + r0) = pk;
+      }
+    }
+  }
+}
+
 cudaError_t launch_absorb_q(const __nv_bfloat16* q, int B, const uint8_t* Wkvb,
                             const float* Skvb, const float2* rope_tab, int rope_pairing,
                             const int* seq_lens, int limit, __nv_bfloat16* qfull,
@@ -457,12 +536,17 @@ cudaError_t launch_absorb_q(const __nv_bfloat16* q, int B, const uint8_t* Wkvb,
 
 cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* Wkvb,
                               const float* Skvb, __nv_bfloat16* out, cudaStream_t st, bool pdl) {
+  if (B > 8)
+    return launch_kernel(absorb_out_tiled_kernel, dim3(HEADS, VDIM / ABT_V), dim3(ABT_THREADS),
+                         ABT_SMEM, st, pdl, o_lat, B, Wkvb, Skvb, out);
   return launch_kernel(absorb_out_kernel, dim3(HEADS * VDIM / 8), dim3(256), 0, st, pdl, o_lat, B,
                        Wkvb, Skvb, out);
 }
 
 cudaError_t init_kernels() {
-  cudaError_t e = init_decode_tc_kernel();
+  cudaError_t e = cudaFuncSetAttribute(absorb_out_tiled_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ABT_SMEM);
+  if (e == cudaSuccess) e = init_decode_tc_kernel();
   if (e == cudaSuccess) e = init_prefill_tc_kernel();
   return e != cudaSuccess ? e : init_gemm_tc_kernels();
 }
