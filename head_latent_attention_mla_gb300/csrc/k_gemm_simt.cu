@@ -277,7 +277,7 @@ cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Pro
   if (np > 1) ps.p[1] = p[1];
   ps.rows0 = p[0].N;
   const int rows = p[0].N + (np > 1 ? p[1].N : 0);
-  if (M <= 8) {
+  if (M <= kGemvMaxM) {
     switch (M) {
       case 1: return launch_gemv<1>(X, ldx, K, ps, rows, st, pdl);
       case 2: return launch_gemv<2>(X, ldx, K, ps, rows, st, pdl);

@@ -485,7 +485,7 @@ int gemm_bn(int M) { return M <= 32 ? 32 : (M <= 64 ? 64 : 128); }
 // would cost more than they save); for few tokens the one that minimises the k blocks of the
 // busiest CTA, ceil(units / SMs) * ceil(k blocks / splits), the smaller on ties.
 int gemm_splits(int M, int N_total, int K, int num_sms) {
-  if (M <= 8 || M > 128) return 1;
+  if (M <= kGemvMaxM || M > 128) return 1;
   const int bn = gemm_bn(M);
   const long tiles = (long)((N_total + 127) / 128) * ((M + bn - 1) / bn);
   const int nkb = K / BLK;
@@ -523,7 +523,7 @@ int gemm_weight_tiles(int M, int K, const Proj* p, int np, int num_sms) {
 // Scratch of one tensor-core GEMM: hi and lo e4m3 copies of X [M, K], sx [M], and the split-K
 // partials.
 size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms) {
-  if (M <= 8) return 0;
+  if (M <= kGemvMaxM) return 0;
   const int s = gemm_splits(M, N_total, K, num_sms);
   return 2 * up256((size_t)M * K) + up256((size_t)M * 4) +
          (s > 1 ? (size_t)s * M * N_total * sizeof(float) : 0);
@@ -630,7 +630,8 @@ cudaError_t launch_gemm_tc_split(const uint8_t* hi, const uint8_t* lo, const flo
                                  bool block_scales, int M, int K, const Proj* p, int np,
                                  float* scratch, int num_sms, int* err, cudaStream_t st, int* adv,
                                  int adv_n, int adv_by) {
-  if (!scratch || !hi || !lo || !sx || M <= 8 || (block_scales && !gemm_takes_split_blocks(M)))
+  if (!scratch || !hi || !lo || !sx || M <= kGemvMaxM ||
+      (block_scales && !gemm_takes_split_blocks(M)))
     return cudaErrorInvalidValue;
   return gemm_tc_core(hi, lo, sx, block_scales, M, K, p, np, scratch, num_sms, err, st, adv,
                       adv_n, adv_by);

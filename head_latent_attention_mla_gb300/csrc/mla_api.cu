@@ -381,9 +381,9 @@ mla_status mla_prefill(mla_ctx* c, const void* x, int B, int T, void* cache, int
     const E4m3Split qsp{at<uint8_t>(ws, L.cq), at<uint8_t>(ws, L.cq) + (size_t)M * Q_LORA,
                         at<float>(ws, L.cq_sx)};
     MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
-                                      c->cfg.rope_pairing, lens_dev, C, cap, limit, M > 8 ? nullptr : cq,
-                                      nullptr, c->d_err, s, false, M > 8 ? &qsp : nullptr, nullptr));
-    if (M > 8) {
+                                      c->cfg.rope_pairing, lens_dev, C, cap, limit, M > kGemvMaxM ? nullptr : cq,
+                                      nullptr, c->d_err, s, false, M > kGemvMaxM ? &qsp : nullptr, nullptr));
+    if (M > kGemvMaxM) {
       MLA_LAUNCH("gemm_q_b", launch_gemm_tc_split(qsp.hi, qsp.lo, qsp.sx, false, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
     } else {
       MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
@@ -396,7 +396,7 @@ mla_status mla_prefill(mla_ctx* c, const void* x, int B, int T, void* cache, int
       MLA_LAUNCH("gemm_kv_b", launch_gemm(C + (size_t)b * cap * LAT, LAT, Mb, KV_LORA, &pb, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
       r0 += Mb;
     }
-  } else if (M > 8) {
+  } else if (M > kGemvMaxM) {
     // Tensor-core projections: the norm kernel writes q_b's and kv_b's e4m3 inputs itself (the
     // two terms share the bf16 latents' regions; one scale per token).
     const E4m3Split qsp{at<uint8_t>(ws, L.cq), at<uint8_t>(ws, L.cq) + (size_t)M * Q_LORA,

@@ -30,6 +30,7 @@ namespace {
 constexpr int kMaxBatch = 8;
 constexpr int kMaxItems = 48;
 constexpr size_t kScratchBytes = size_t(8) << 20;
+constexpr size_t kGemmScratch = size_t(7) << 19;  // tensor-core GEMM scratch (B > kGemvMaxM)
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
@@ -37,7 +38,7 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 constexpr size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Regions {
-  size_t g1, cq, q, qfull, opart, ml, olat, attn, total;
+  size_t g1, cq, q, qfull, opart, ml, olat, attn, gpart, total;
 };
 
 constexpr Regions regions(int B) {
@@ -51,6 +52,7 @@ constexpr Regions regions(int B) {
   r.ml = off;    off += up256((size_t)kMaxItems * HEADS * 2 * 4);
   r.olat = off;  off += up256((size_t)B * HEADS * KV_LORA * 2);
   r.attn = off;  off += up256((size_t)B * O_IN * 2);
+  r.gpart = off; off += kGemmScratch;
   r.total = off;
   return r;
 }
@@ -101,6 +103,11 @@ extern "C" mla_status mla_decode_noalloc(mla_ctx* c, const void* x, int B, void*
   }
   // Split-KV schedule with at most kMaxItems partial slots (B + shares).
   const DecodePlan plan = make_decode_plan(B, total, c->num_sms, kMaxItems);
+  // The tensor-core projections' scratch (more than kGemvMaxM sequences) must fit its region.
+  if (gemm_partial_bytes(B, Q_LORA + KVA_N, HIDDEN, c->num_sms) > kGemmScratch ||
+      gemm_partial_bytes(B, QB_N, Q_LORA, c->num_sms) > kGemmScratch ||
+      gemm_partial_bytes(B, HIDDEN, O_IN, c->num_sms) > kGemmScratch)
+    return MLA_ERR_CAPACITY;
 
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return MLA_ERR_CUDA;
@@ -114,6 +121,7 @@ extern "C" mla_status mla_decode_noalloc(mla_ctx* c, const void* x, int B, void*
   float* ml = reinterpret_cast<float*>(w + R.ml);
   __nv_bfloat16* olat = reinterpret_cast<__nv_bfloat16*>(w + R.olat);
   __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(w + R.attn);
+  float* gpart = reinterpret_cast<float*>(w + R.gpart);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   c->n_launch = 0;  // this call keeps no launch log
@@ -128,12 +136,12 @@ extern "C" mla_status mla_decode_noalloc(mla_ctx* c, const void* x, int B, void*
   } while (0)
   Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
                 {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
-  NA_RUN(launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, nullptr, c->num_sms, c->d_err, s));
+  NA_RUN(launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, gpart, c->num_sms, c->d_err, s));
   NA_RUN(launch_norm_rope_cache(g1, B, 1, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
                                 c->cfg.rope_pairing, lens_dev, C, cap, limit, cq, nullptr,
                                 c->d_err, s));
   Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
-  NA_RUN(launch_gemm(cq, Q_LORA, B, Q_LORA, &p2, 1, nullptr, c->num_sms, c->d_err, s));
+  NA_RUN(launch_gemm(cq, Q_LORA, B, Q_LORA, &p2, 1, gpart, c->num_sms, c->d_err, s));
   NA_RUN(launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
                          c->cfg.rope_pairing, lens_dev, limit, qfull, s));
   NA_RUN(launch_decode_attention_tc(qfull, C, cap, lens_dev, plan, c->cfg.softmax_scale, opart,
@@ -141,7 +149,7 @@ extern "C" mla_status mla_decode_noalloc(mla_ctx* c, const void* x, int B, void*
   NA_RUN(launch_decode_combine(lens_dev, plan, opart, ml, olat, c->d_err, s));
   NA_RUN(launch_absorb_out(olat, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], attn, s));
   Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
-  NA_RUN(launch_gemm(attn, O_IN, B, O_IN, &p4, 1, nullptr, c->num_sms, c->d_err, s));
+  NA_RUN(launch_gemm(attn, O_IN, B, O_IN, &p4, 1, gpart, c->num_sms, c->d_err, s));
   NA_RUN(launch_advance_lens(lens_dev, B, 1, s));
 #undef NA_RUN
   return MLA_OK;
