@@ -138,6 +138,62 @@ def test_rope_preserves_pair_norms_and_angles():
     assert abs(r[0, 0] - math.cos(3)) < 1e-15 and abs(r[0, 1] - math.sin(3)) < 1e-15
 
 
+def half_pairs_turn_by_exact_angles(rope) -> bool:
+    """Whether `rope` (the oracle's apply_rope signature) turns pair j = (x[j], x[j+32]) of a
+    64-wide slice by +pos * theta^(-2j/64) for the "half" pairing, element by element, with
+    every pair's norm kept.  Written out from the rotation itself, one scalar at a time."""
+    rng = np.random.default_rng(28)
+    x = rng.normal(size=(6, 64))
+    pos = np.array([1, 3, 17, 1000, 4095, 131072])
+    y = rope(x, pos, pairing="half")
+    for t in range(6):
+        for j in range(32):
+            a, b = x[t, j], x[t, j + 32]
+            ang = pos[t] * 50000.0 ** (-2.0 * j / 64)
+            ca, sa = math.cos(ang), math.sin(ang)
+            if abs(y[t, j] - (a * ca - b * sa)) > 1e-12:
+                return False
+            if abs(y[t, j + 32] - (a * sa + b * ca)) > 1e-12:
+                return False
+    return True
+
+
+def test_rope_half_pairs_turn_by_exact_angles():
+    """The half pairing (j, j+32), element by element: a unit vector in element j turns into
+    (cos, sin) at elements (j, j+32) by pos * theta^(-2j/64), in the positive direction."""
+    assert half_pairs_turn_by_exact_angles(O.apply_rope)
+    for j in (0, 1, 13, 31):
+        e = np.zeros((1, 64)); e[0, j] = 1.0
+        r = O.apply_rope(e, np.array([5]), pairing="half")
+        ang = 5 * 50000.0 ** (-2.0 * j / 64)
+        expect = np.zeros(64); expect[j] = math.cos(ang); expect[j + 32] = math.sin(ang)
+        np.testing.assert_allclose(r[0], expect, rtol=0, atol=1e-15)
+
+
+def _rope_half_planted(kind):
+    """The oracle's apply_rope with one plausible slip planted in its half branch only."""
+    orig = O.apply_rope
+    def rope(x, positions, theta=O.ROPE_THETA, pairing="adjacent", yarn=None):
+        if pairing != "half":
+            return orig(x, positions, theta, pairing, yarn)
+        if kind == "sign":                     # rotation in the negative direction
+            return orig(x, -np.asarray(positions), theta, pairing, yarn)
+        if kind == "freq_order":               # pair j given pair 31-j's frequency
+            h = x.shape[-1] // 2
+            perm = np.concatenate([np.arange(h)[::-1], h + np.arange(h)[::-1]])  # an involution
+            return orig(x[..., perm], positions, theta, pairing, yarn)[..., perm]
+        if kind == "adjacent_inside":          # the half switch silently ignored
+            return orig(x, positions, theta, "adjacent", yarn)
+        raise ValueError(kind)
+    return rope
+
+
+@pytest.mark.parametrize("kind", ["sign", "freq_order", "adjacent_inside"])
+def test_planted_half_rope_mistakes_are_caught(kind):
+    """Each slip planted in the half branch (on the CPU) fails the element-by-element pin."""
+    assert not half_pairs_turn_by_exact_angles(_rope_half_planted(kind))
+
+
 @pytest.mark.parametrize("pairing", ["adjacent", "half"])
 def test_rope_dot_depends_on_offset_only(pairing):
     rng = np.random.default_rng(6)
@@ -265,11 +321,12 @@ def test_chunked_evaluation_is_the_same_sum():
     np.testing.assert_allclose(O.output(o, W, d), y, rtol=1e-12, atol=1e-14)
 
 
-def brute_force_layer(x, W, d, L_cache_x=None, theta=50000.0, eps=1e-6):
+def brute_force_layer(x, W, d, L_cache_x=None, theta=50000.0, eps=1e-6, pairing="adjacent"):
     """The whole layer as plain Python loops over floats, written from the pages' equations:
     q_a -> RMSNorm -> q_b (per head nope|rope); kv_a -> split latent|k_pe -> RMSNorm latent;
-    RoPE on adjacent pairs; k_nope, v from kv_b rows (per head: nope rows then v rows);
-    causal scores scaled by 1/sqrt(nope+rope); softmax; value mix; o_proj."""
+    RoPE on adjacent pairs (2j, 2j+1), or with pairing="half" on (j, j + rope/2); k_nope, v
+    from kv_b rows (per head: nope rows then v rows); causal scores scaled by
+    1/sqrt(nope+rope); softmax; value mix; o_proj."""
     xs = [list(map(float, r)) for r in x]
     def mv(Wm, v):
         return [sum(float(Wm[i][k]) * v[k] for k in range(len(v))) for i in range(len(Wm))]
@@ -280,9 +337,10 @@ def brute_force_layer(x, W, d, L_cache_x=None, theta=50000.0, eps=1e-6):
         out = list(v)
         for j in range(len(v) // 2):
             ang = pos * theta ** (-2.0 * j / len(v))
-            a, b = v[2 * j], v[2 * j + 1]
-            out[2 * j] = a * math.cos(ang) - b * math.sin(ang)
-            out[2 * j + 1] = b * math.cos(ang) + a * math.sin(ang)
+            i0, i1 = (2 * j, 2 * j + 1) if pairing == "adjacent" else (j, j + len(v) // 2)
+            a, b = v[i0], v[i1]
+            out[i0] = a * math.cos(ang) - b * math.sin(ang)
+            out[i1] = b * math.cos(ang) + a * math.sin(ang)
         return out
     hd = d.nope + d.vdim
     c_hat, k_rot, qn, qr = [], [], [], []
@@ -325,6 +383,27 @@ def test_forward_equals_brute_force_loops():
     x = np.random.default_rng(18).normal(size=(6, d.hidden))
     y, _ = O.prefill(x, W, d=d)
     np.testing.assert_allclose(y, brute_force_layer(x, W, d), rtol=1e-10, atol=1e-13)
+
+
+def test_forward_half_pairing_equals_brute_force_loops():
+    d, W = TINY, tiny_weights(29)
+    x = np.random.default_rng(30).normal(size=(6, d.hidden))
+    y, _ = O.prefill(x, W, d=d, pairing="half")
+    np.testing.assert_allclose(y, brute_force_layer(x, W, d, pairing="half"), rtol=1e-10,
+                               atol=1e-13)
+    # the two pairings are different layers: the pin tells them apart
+    y_adj, _ = O.prefill(x, W, d=d)
+    assert not np.allclose(y, y_adj, rtol=1e-6, atol=1e-9)
+
+
+@pytest.mark.parametrize("kind", ["sign", "freq_order"])
+def test_planted_half_rope_mistakes_fail_the_layer_loop(monkeypatch, kind):
+    d, W = TINY, tiny_weights(31)
+    x = np.random.default_rng(32).normal(size=(5, d.hidden))
+    ref = brute_force_layer(x, W, d, pairing="half")
+    monkeypatch.setattr(O, "apply_rope", _rope_half_planted(kind))
+    y, _ = O.prefill(x, W, d=d, pairing="half")
+    assert not np.allclose(y, ref, rtol=1e-6, atol=1e-9)
 
 
 def absorbed_decode(x_new, cache, W, d):
