@@ -50,7 +50,7 @@ def peaks():
 
 # ------------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while running."""
+    """nvidia-smi samples (100 ms) of SM clock and throttle reasons while running."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
@@ -67,7 +67,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.idx)], stdout=subprocess.PIPE,
+                 "-lms", "100", "-i", str(self.idx)], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -183,6 +183,22 @@ def time_graph(torch, g, stream, lens, lens0, flush, steps):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def steps_for(torch, g, stream, lens, lens0, flush, steps, min_ms):
+    """At least `steps` steps, and enough for `min_ms` of timed device work (estimated from a
+    short trial), so that short workloads are timed over many steps."""
+    trial = time_graph(torch, g, stream, lens, lens0, flush, 5)
+    per = max(1e-3, sum(trial) / len(trial))
+    return max(steps, int(min_ms / per) + 1)
+
+
+def soak(torch, g, stream, lens, lens0, flush, seconds):
+    """Untimed replays for `seconds` of wall time: the clocks settle under load and the clock
+    sampler sees the workload before the timed steps."""
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        time_graph(torch, g, stream, lens, lens0, flush, 50)
+
+
 def profile_kernels(torch, mla, layer, stream, call, lens, lens0, flush, steps):
     """Average device ms of each kernel of one call, from CUDA events the library records on
     the launching stream around every launch.  A bounded spin kernel (torch.cuda._sleep)
@@ -203,7 +219,7 @@ def profile_kernels(torch, mla, layer, stream, call, lens, lens0, flush, steps):
 
 
 def run_decode_workload(torch, mla, synth, layer, name, lengths, build, steps, warmup, device,
-                        flush, prof_steps=50, e2e=True, clk=None):
+                        flush, prof_steps=50, e2e=True, soak_s=0.0, min_ms=0.0):
     B = len(lengths)
     cache, lens, xb, x = setup_decode(torch, mla, synth, layer, 0, lengths, build, device)
     lens0 = lens.clone()
@@ -229,14 +245,13 @@ def run_decode_workload(torch, mla, synth, layer, name, lengths, build, steps, w
     graphs[False] = g
     launches = mla.load().mla_last_launches(layer.ctx, 0, None, None)
 
-    if clk:
-        clk.start()
     time_graph(torch, graphs[False], stream, lens, lens0, flush, warmup)
+    soak(torch, graphs[False], stream, lens, lens0, flush, soak_s)
+    if min_ms > 0:
+        steps = steps_for(torch, graphs[False], stream, lens, lens0, flush, steps, min_ms)
     t0 = time.perf_counter()
     times = time_graph(torch, graphs[False], stream, lens, lens0, flush, steps)
     wall = time.perf_counter() - t0
-    if clk:
-        clk.stop()
     ms = sum(times) / len(times)
 
     per_ms = profile_kernels(torch, mla, layer, stream, lambda: call(stream), lens, lens0,
@@ -268,11 +283,12 @@ def run_decode_workload(torch, mla, synth, layer, name, lengths, build, steps, w
                    "ms_per_step": e2e_ms, "path": "mla_decode via ctypes, pinned host buffers"}
     del cache
     return {"name": name, "B": B, "lengths": lengths, "ms": ms, "times": times, "wall": wall,
+            "steps": steps,
             "per_kernel_ms": per_ms, "launches_per_step": launches, "e2e": e2e_res,
             "xb": xb}
 
 
-def run_prefill_workload(torch, mla, synth, layer, T, steps, warmup, device, flush):
+def run_prefill_workload(torch, mla, synth, layer, T, steps, warmup, device, flush, min_ms=0.0):
     xb = synth.hidden_states(0, 0, 0, T)
     x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(device)[None]
     cache = torch.zeros(1, T, 576, dtype=torch.bfloat16, device=device)
@@ -290,15 +306,17 @@ def run_prefill_workload(torch, mla, synth, layer, T, steps, warmup, device, flu
     with torch.cuda.graph(g, stream=stream):
         mla.mla_prefill(layer.ctx, x, cache, lens, [0], out, ws)
     time_graph(torch, g, stream, lens, lens0, flush, warmup)
+    if min_ms > 0:
+        steps = steps_for(torch, g, stream, lens, lens0, flush, steps, min_ms)
     times = time_graph(torch, g, stream, lens, lens0, flush, steps)
     per = profile_kernels(torch, mla, layer, stream,
                           lambda: mla.mla_prefill(layer.ctx, x, cache, lens, [0], out, ws,
                                                   stream=stream),
                           lens, lens0, flush, max(2, steps // 2))
-    return {"T": T, "ms": sum(times) / len(times), "per_kernel_ms": per}
+    return {"T": T, "ms": sum(times) / len(times), "per_kernel_ms": per, "steps": steps}
 
 
-def run_chunk_workload(torch, mla, synth, layer, L, T, steps, warmup, device, flush):
+def run_chunk_workload(torch, mla, synth, layer, L, T, steps, warmup, device, flush, min_ms=0.0):
     """Chunked prefill: T new tokens after L cached positions (B=1).  The cache is built by a
     prefill of the first L tokens outside the timed region; every step restores the length
     to L, so each step recomputes the same chunk."""
@@ -322,12 +340,14 @@ def run_chunk_workload(torch, mla, synth, layer, L, T, steps, warmup, device, fl
     with torch.cuda.graph(g, stream=stream):
         mla.mla_prefill(layer.ctx, xc, cache, lens, [L], out, ws)
     time_graph(torch, g, stream, lens, lens0, flush, warmup)
+    if min_ms > 0:
+        steps = steps_for(torch, g, stream, lens, lens0, flush, steps, min_ms)
     times = time_graph(torch, g, stream, lens, lens0, flush, steps)
     per = profile_kernels(torch, mla, layer, stream,
                           lambda: mla.mla_prefill(layer.ctx, xc, cache, lens, [L], out, ws,
                                                   stream=stream),
                           lens, lens0, flush, max(2, steps // 2))
-    return {"ms": sum(times) / len(times), "per_kernel_ms": per}
+    return {"ms": sum(times) / len(times), "per_kernel_ms": per, "steps": steps}
 
 
 def chunk_flops(L, T):
@@ -396,9 +416,12 @@ def gpu_arm(args):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     gpu_idx = int(vis.split(",")[local]) if vis and vis.split(",")[local].isdigit() else local
     barrier()
+    # The clock sampler runs from the start of the warm-up (which replays the step for a
+    # third of a second, so it holds samples under load) to the end of the timed steps.
     with ClockSampler(gpu_idx) as clk:
+        clk.start()
         res = run_decode_workload(torch, mla, synth, layer, "decode_b1_p1000", [1000], "prefill",
-                                  args.steps, args.warmup, device, flush, clk=clk)
+                                  args.steps, args.warmup, device, flush, soak_s=0.35)
     barrier()
     B = res["B"]
     ms, _, value = aggregate_replicas(torch, dist if world > 1 else None, res["ms"], B, device)
@@ -411,7 +434,10 @@ def gpu_arm(args):
 
     extra = {}
     if not args.headline_only and rank == 0:
-        extra = secondary(torch, mla, synth, layer, device, flush, pk, args)
+        with ClockSampler(gpu_idx) as clk2:
+            clk2.start()
+            extra = secondary(torch, mla, synth, layer, device, flush, pk, args)
+        extra["clocks"] = clk2.summary()
 
     if rank != 0:
         if world > 1:
@@ -453,31 +479,32 @@ def gpu_arm(args):
 def secondary(torch, mla, synth, layer, device, flush, pk, args):
     """The other workloads' headline figures (not the bench value)."""
     out = {}
-    steps = max(5, min(args.steps // 20, 30))
+    steps, min_ms = 5, 200.0    # each workload is timed over at least 200 ms of steps
     for name, lengths, build in (("decode_long_b8_131072", [131072] * 8, "append"),
                                  ("decode_ragged_b64", synth.ragged_lengths(0, 64, 512, 8192).tolist(), "append")):
         r = run_decode_workload(torch, mla, synth, layer, name, lengths, build, steps, 3, device,
-                                flush, prof_steps=10, e2e=False)
+                                flush, prof_steps=20, e2e=False, min_ms=min_ms)
         att = r["per_kernel_ms"].get("decode_attention")
         cb = sum(n + 1 for n in lengths) * LAT_BYTES
         gbs = cb / (att * 1e-3) / 1e9 if att else None
         out[name] = {"tokens_per_s": len(lengths) * 1000.0 / r["ms"], "ms_per_step": r["ms"],
                      "decode_attention_ms": att, "attention_cache_gbs": gbs,
                      "attention_hbm_frac": gbs / pk["hbm_gbs"] if gbs else None,
-                     "per_kernel_ms": r["per_kernel_ms"]}
+                     "timed_steps": r["steps"], "per_kernel_ms": r["per_kernel_ms"]}
         torch.cuda.empty_cache()
     for T in (4096, 16):
-        r = run_prefill_workload(torch, mla, synth, layer, T, max(3, steps // 3), 3, device, flush)
+        r = run_prefill_workload(torch, mla, synth, layer, T, steps, 3, device, flush, min_ms)
         gemm, attn = prefill_flops(T)
         out[f"prefill_t{T}"] = {"tokens_per_s": T * 1000.0 / r["ms"], "ms_per_step": r["ms"],
+                                "timed_steps": r["steps"],
                                 "tflops": (gemm + attn) / (r["ms"] * 1e-3) / 1e12,
                                 "tensor_frac": (gemm + attn) / (r["ms"] * 1e-3) / 1e12 / pk["bf16_tflops"],
                                 "per_kernel_ms": r["per_kernel_ms"]}
     L, T = 4096, 1024
-    r = run_chunk_workload(torch, mla, synth, layer, L, T, max(3, steps // 3), 3, device, flush)
+    r = run_chunk_workload(torch, mla, synth, layer, L, T, steps, 3, device, flush, min_ms)
     gemm, attn = chunk_flops(L, T)
     out[f"prefill_chunk_l{L}_t{T}"] = {
-        "tokens_per_s": T * 1000.0 / r["ms"], "ms_per_step": r["ms"],
+        "tokens_per_s": T * 1000.0 / r["ms"], "ms_per_step": r["ms"], "timed_steps": r["steps"],
         "tflops": (gemm + attn) / (r["ms"] * 1e-3) / 1e12,
         "tensor_frac": (gemm + attn) / (r["ms"] * 1e-3) / 1e12 / pk["bf16_tflops"],
         "per_kernel_ms": r["per_kernel_ms"]}

@@ -479,28 +479,6 @@ constexpr size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 bool make_tmap_2d(CUtensorMap* m, bool bf16, const void* base, uint64_t cols, uint64_t rows,
                   uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows);
 
-int gemm_bn(int M) { return M <= 32 ? 32 : (M <= 64 ? 64 : 128); }
-
-// Split-K factor: 1 for large token counts (the tiles alone fill the SMs and fp32 partials
-// would cost more than they save); for few tokens the one that minimises the k blocks of the
-// busiest CTA, ceil(units / SMs) * ceil(k blocks / splits), the smaller on ties.
-int gemm_splits(int M, int N_total, int K, int num_sms) {
-  if (M <= kGemvMaxM || M > 128) return 1;
-  const int bn = gemm_bn(M);
-  const long tiles = (long)((N_total + 127) / 128) * ((M + bn - 1) / bn);
-  const int nkb = K / BLK;
-  int best = 1;
-  long best_cost = -1;
-  for (int s = 1; s <= nkb / 2 || s == 1; ++s) {
-    const long cost = ((tiles * s + num_sms - 1) / num_sms) * ((nkb + s - 1) / s);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best = s;
-    }
-  }
-  return best;
-}
-
 // Weight tiles per unit for a token count M: 2 (256 features against one token tile) when
 // there are more than 128 tokens, the reduction spans at least 8 k blocks, and the rounds of
 // units over the SMs, weighted by the wide unit's cost (kWideCost x a narrow unit, for twice
@@ -518,15 +496,6 @@ int gemm_weight_tiles(int M, int K, const Proj* p, int np, int num_sms) {
   const long r1 = (t1 * m_tiles + num_sms - 1) / num_sms;
   const long r2 = (t2 * m_tiles + num_sms - 1) / num_sms;
   return kWideCost * (double)r2 < (double)r1 ? 2 : 1;
-}
-
-// Scratch of one tensor-core GEMM: hi and lo e4m3 copies of X [M, K], sx [M], and the split-K
-// partials.
-size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms) {
-  if (M <= kGemvMaxM) return 0;
-  const int s = gemm_splits(M, N_total, K, num_sms);
-  return 2 * up256((size_t)M * K) + up256((size_t)M * 4) +
-         (s > 1 ? (size_t)s * M * N_total * sizeof(float) : 0);
 }
 
 cudaError_t init_gemm_tc_kernels() {

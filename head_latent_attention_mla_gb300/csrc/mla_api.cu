@@ -104,8 +104,11 @@ void log_reset(mla_ctx* c) {
 
 // Records one kernel launch of the current call; with profiling on, brackets it with events
 // recorded on the launching stream.
+// A context created with MLA_TEST_FAIL_AFTER=n fails at launch n of every call, before it is
+// enqueued, exactly as a failed CUDA launch returns.
 #define MLA_LAUNCH(name, expr)                                                          \
   do {                                                                                  \
+    if (c->fail_at >= 0 && c->n_launch == c->fail_at) return MLA_ERR_CUDA;             \
     const int _k = c->n_launch < mla_ctx::kMaxLaunch ? c->n_launch : mla_ctx::kMaxLaunch - 1; \
     if (c->profiling && cudaEventRecord(c->ev[2 * _k], s) != cudaSuccess) return MLA_ERR_CUDA; \
     cudaError_t _e = (expr);                                                            \
@@ -214,8 +217,14 @@ mla_status mla_create(const mla_config* cfg, mla_ctx** out) {
   mla_ctx* c = new (std::nothrow) mla_ctx();
   if (!c) return MLA_ERR_INVALID_ARG;
   c->cfg = *cfg;
+  if (const char* f = std::getenv("MLA_TEST_FAIL_AFTER")) {
+    char* end = nullptr;
+    const long v = std::strtol(f, &end, 10);
+    if (end != f && *end == '\0' && v >= 0 && v < 1000) c->fail_at = (int)v;
+  }
   if (init_kernels() != cudaSuccess || cudaGetDevice(&c->device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess ||
+      noalloc_scratch_address(&c->noalloc_scratch) != cudaSuccess) {
     delete c;
     return MLA_ERR_CUDA;
   }
@@ -542,6 +551,11 @@ mla_status mla_get_device_status(mla_ctx* c, void* stream) {
   if (cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess) return MLA_ERR_CUDA;
   if (h == DEV_ERR_NONE) return MLA_OK;
   return h == DEV_ERR_TIMEOUT ? MLA_ERR_TIMEOUT : MLA_ERR_STATE;
+}
+
+mla_status mla_selftest_wait_timeout(mla_ctx* c, unsigned long long limit_ns, void* stream) {
+  if (!c || limit_ns > 2000000000ull) return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_wait_selftest(c->d_err, limit_ns, static_cast<cudaStream_t>(stream)));
 }
 
 const char* mla_status_string(mla_status s) {

@@ -91,13 +91,47 @@ __device__ __forceinline__ uint32_t e4m3_split2(float2 f) {
 // 111.9 us for 3 / 4 / 8 sequences (the GEMV re-reads every activation row per 4 weight rows).
 constexpr int kGemvMaxM = 3;
 
+// Token-tile width of the tensor-core GEMM for M token rows.
+constexpr int gemm_bn(int M) { return M <= 32 ? 32 : (M <= 64 ? 64 : 128); }
+
+// Split-K factor of the tensor-core GEMM: 1 for large token counts (the tiles alone fill the
+// SMs and fp32 partials would cost more than they save); for few tokens the one that minimises
+// the k blocks of the busiest CTA, ceil(units / SMs) * ceil(k blocks / splits), the smaller on
+// ties.
+constexpr int gemm_splits(int M, int N_total, int K, int num_sms) {
+  if (M <= kGemvMaxM || M > 128) return 1;
+  const int bn = gemm_bn(M);
+  const long tiles = (long)((N_total + 127) / 128) * ((M + bn - 1) / bn);
+  const int nkb = K / BLK;
+  int best = 1;
+  long best_cost = -1;
+  for (int s = 1; s <= nkb / 2 || s == 1; ++s) {
+    const long cost = ((tiles * s + num_sms - 1) / num_sms) * ((nkb + s - 1) / s);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+// Scratch of one tensor-core GEMM: hi and lo e4m3 copies of X [M, K], sx [M], and the split-K
+// partials (none for M <= kGemvMaxM, which runs on the CUDA cores).
+constexpr size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms) {
+  if (M <= kGemvMaxM) return 0;
+  const int s = gemm_splits(M, N_total, K, num_sms);
+  const size_t mk = ((size_t)M * K + 255) & ~size_t(255);
+  return 2 * mk + (((size_t)M * 4 + 255) & ~size_t(255)) +
+         (s > 1 ? (size_t)s * M * N_total * sizeof(float) : 0);
+}
+
 // ---- launchers (each returns the launch's cudaError_t) ----------------------------------
 
-// Y = X W^T for up to two projections sharing X [M, K] (row stride ldx elements).  M <= 8
-// streams the weights through the CUDA cores; larger M runs on the tensor cores, split over K
-// when the grid would be small, with fp32 partials in `partial` (gemm_partial_bytes bytes).
-// Block 0 of the launch also adds adv_by to adv[0..adv_n) (the call's length bookkeeping,
-// riding on its last kernel; adv_n <= 128 with M <= 8).
+// Y = X W^T for up to two projections sharing X [M, K] (row stride ldx elements).
+// M <= kGemvMaxM streams the weights through the CUDA cores; larger M runs on the tensor
+// cores, split over K when the grid would be small, with fp32 partials in `partial`
+// (gemm_partial_bytes bytes).  Block 0 of the launch also adds adv_by to adv[0..adv_n) (the
+// call's length bookkeeping, riding on its last kernel; adv_n <= 128 with M <= kGemvMaxM).
 cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
                         float* partial, int num_sms, int* err, cudaStream_t st,
                         int* adv = nullptr, int adv_n = 0, int adv_by = 0, bool pdl = false);
@@ -105,7 +139,7 @@ bool gemm_can_advance(int M);  // whether launch_gemm honours adv for this M
 cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
                            float* partial, int num_sms, int* err, cudaStream_t st,
                            int* adv = nullptr, int adv_n = 0, int adv_by = 0);
-// The same GEMM (M > 8) on activations already split into two e4m3 terms, hi and lo [M, K],
+// The same GEMM (M > kGemvMaxM) on activations already split into two e4m3 terms, hi and lo [M, K],
 // with one scale per token, sx [M] (X[m, k] ~ sx[m] (hi + lo)), or with block_scales one per
 // (token, 128-wide k block), sx [M, K/128] (X[m, k] ~ sx[m][k/128] (hi + lo)); block scales
 // are accepted when gemm_takes_split_blocks(M).  `partial` as for launch_gemm_tc.
@@ -114,7 +148,6 @@ cudaError_t launch_gemm_tc_split(const uint8_t* hi, const uint8_t* lo, const flo
                                  bool block_scales, int M, int K, const Proj* p, int np,
                                  float* partial, int num_sms, int* err, cudaStream_t st,
                                  int* adv = nullptr, int adv_n = 0, int adv_by = 0);
-size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms);
 cudaError_t init_gemm_tc_kernels();
 
 // RMSNorm of the q latent and kv latent, RoPE of k_pe, cache row store.  Positions at or
@@ -209,6 +242,13 @@ cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bf
                                        cudaStream_t st, bool pdl = false);
 cudaError_t init_decode_tc_kernel();
 
+// Device address of mla_decode_noalloc's static scratch array on the current device.
+cudaError_t noalloc_scratch_address(void** out);
+
+// One CTA waits on an mbarrier that nothing arrives at, with the library's bounded wait and
+// the given limit; it records DEV_ERR_TIMEOUT in *err when the limit runs out.
+cudaError_t launch_wait_selftest(int* err, unsigned long long limit_ns, cudaStream_t st);
+
 // One-time kernel attributes (dynamic shared memory opt-in); called by mla_create so that
 // later calls only enqueue work and can be captured into CUDA graphs.
 cudaError_t init_kernels();
@@ -255,6 +295,13 @@ struct mla_ctx {
   const __nv_bfloat16* gain[2] = {};
   float2* rope_tab = nullptr;  // [max_positions][32] (cos, sin)
   int* d_err = nullptr;
+  // Device address, on this context's device, of the static scratch array that
+  // mla_decode_noalloc uses (looked up by mla_create, with the device current).
+  void* noalloc_scratch = nullptr;
+  // Testing aid, from the environment variable MLA_TEST_FAIL_AFTER at creation: when >= 0,
+  // every token call fails at its launch with this index, as if that CUDA launch had failed
+  // (the launches before it are enqueued; it and the rest are not).  -1: off.
+  int fail_at = -1;
   // Launch log of the most recent token call (names, and device timings when profiling).
   static constexpr int kMaxLaunch = 32;
   bool profiling = false;

@@ -17,10 +17,9 @@
 //     threads, two contexts on one device) race with each other;
 //   * the array keeps the last call's contents; this path writes every scratch byte it reads
 //     before reading it, so nothing needs clearing between calls;
-//   * the first call on a device looks up the array's device address on that device (with
-//     that device current); make that first call before any stream capture.
-#include <mutex>
-
+//   * mla_create looks up the array's device address on the context's device (with that
+//     device current) and keeps it in the context, so the address lives and dies with the
+//     context; a call made with another device current is refused.
 #include "mla_internal.h"
 
 using namespace mla;
@@ -29,13 +28,29 @@ namespace {
 
 constexpr int kMaxBatch = 8;
 constexpr int kMaxItems = 48;
-constexpr size_t kScratchBytes = size_t(8) << 20;
-constexpr size_t kGemmScratch = size_t(7) << 19;  // tensor-core GEMM scratch (B > kGemvMaxM)
-constexpr int kMaxDevices = 64;
+constexpr size_t kScratchBytes = size_t(12) << 20;
+constexpr size_t kGemmScratch = size_t(29) << 18;  // 7.25 MiB: tensor-core GEMM scratch
+constexpr int kMaxSms = 1024;                       // SM counts the GEMM scratch is sized for
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 constexpr size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// The largest scratch the tensor-core projections of this path (kGemvMaxM < B <= kMaxBatch)
+// plan for, over every SM count up to kMaxSms: the split-K partials grow when few SMs make the
+// planner cut the reduction finer (on 5 SMs o_proj takes 32 splits, 7.1 MiB for 8 tokens).
+constexpr size_t max_gemm_scratch() {
+  size_t worst = 0;
+  for (int sms = 1; sms <= kMaxSms; ++sms)
+    for (int b = kGemvMaxM + 1; b <= kMaxBatch; ++b) {
+      const size_t v[3] = {gemm_partial_bytes(b, Q_LORA + KVA_N, HIDDEN, sms),
+                           gemm_partial_bytes(b, QB_N, Q_LORA, sms),
+                           gemm_partial_bytes(b, HIDDEN, O_IN, sms)};
+      for (size_t x : v) worst = x > worst ? x : worst;
+    }
+  return worst;
+}
+static_assert(max_gemm_scratch() <= kGemmScratch, "GEMM scratch too small for some SM count");
 
 struct Regions {
   size_t g1, cq, q, qfull, opart, ml, olat, attn, gpart, total;
@@ -58,30 +73,19 @@ constexpr Regions regions(int B) {
 }
 static_assert(regions(kMaxBatch).total <= kScratchBytes, "scratch too small for kMaxBatch");
 
-// Host code only knows a stand-in for g_decode_scratch; its device address is looked up once
-// per device, with that device current.
-std::mutex g_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
-  return cudaSuccess;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+namespace mla {
+
+// Host code holds only a stand-in for g_decode_scratch; this is its address on the current
+// device.
+cudaError_t noalloc_scratch_address(void** out) {
+  return cudaGetSymbolAddress(out, g_decode_scratch);
+}
+
+}  // namespace mla
 
 extern "C" mla_status mla_decode_noalloc(mla_ctx* c, const void* x, int B, void* cache, int cap,
                                          int* lens_dev, const int* lens_host, void* out,
@@ -103,14 +107,18 @@ extern "C" mla_status mla_decode_noalloc(mla_ctx* c, const void* x, int B, void*
   }
   // Split-KV schedule with at most kMaxItems partial slots (B + shares).
   const DecodePlan plan = make_decode_plan(B, total, c->num_sms, kMaxItems);
-  // The tensor-core projections' scratch (more than kGemvMaxM sequences) must fit its region.
-  if (gemm_partial_bytes(B, Q_LORA + KVA_N, HIDDEN, c->num_sms) > kGemmScratch ||
-      gemm_partial_bytes(B, QB_N, Q_LORA, c->num_sms) > kGemmScratch ||
-      gemm_partial_bytes(B, HIDDEN, O_IN, c->num_sms) > kGemmScratch)
+  // The tensor-core projections' scratch (more than kGemvMaxM sequences) fits its region on
+  // every SM count up to kMaxSms (checked at compile time); beyond that, check here.
+  if (c->num_sms > kMaxSms &&
+      (gemm_partial_bytes(B, Q_LORA + KVA_N, HIDDEN, c->num_sms) > kGemmScratch ||
+       gemm_partial_bytes(B, QB_N, Q_LORA, c->num_sms) > kGemmScratch ||
+       gemm_partial_bytes(B, HIDDEN, O_IN, c->num_sms) > kGemmScratch))
     return MLA_ERR_CAPACITY;
-
-  void* scratch = nullptr;
-  if (scratch_address(&scratch) != cudaSuccess) return MLA_ERR_CUDA;
+  // The scratch address belongs to the context's device.
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  if (dev != c->device || !c->noalloc_scratch) return MLA_ERR_INVALID_ARG;
+  void* scratch = c->noalloc_scratch;
   const Regions R = regions(B);
   char* w = static_cast<char*>(scratch);
   float* g1 = reinterpret_cast<float*>(w + R.g1);

@@ -54,6 +54,7 @@ _SIGS = {
     "mla_status_string": (ctypes.c_char_p, [_I]),
     "mla_decode_noalloc": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _P]),
     "mla_set_profiling": (_I, [_P, _I]),
+    "mla_selftest_wait_timeout": (_I, [_P, ctypes.c_ulonglong, _P]),
     "mla_last_launches": (_I, [_P, _I, ctypes.POINTER(ctypes.c_char_p),
                                ctypes.POINTER(ctypes.c_float)]),
 }
@@ -193,6 +194,12 @@ def mla_last_launches(ctx: int, max_launches: int = 32):
     ms = (ctypes.c_float * max_launches)()
     n = load().mla_last_launches(ctx, max_launches, names, ms)
     return [(names[i].decode(), float(ms[i])) for i in range(min(n, max_launches))]
+
+
+def mla_selftest_wait_timeout(ctx: int, limit_ns: int, stream=None) -> None:
+    """Enqueues the bounded-wait self-test; mla_get_device_status then reports the timeout."""
+    _check(load().mla_selftest_wait_timeout(ctx, limit_ns, _stream(stream)),
+           "mla_selftest_wait_timeout")
 
 
 def mla_status_string(status: int) -> str:

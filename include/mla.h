@@ -160,15 +160,17 @@ mla_status mla_decode(mla_ctx* ctx, const void* x_bf16, int B, void* cache_bf16,
 /* mla_decode for callers that cannot allocate device memory when they decode (an arena that
  * owns all GPU memory, a runtime that forbids allocation after start-up): the same step and
  * the same arguments as mla_decode without the workspace.  The paper has no counterpart; this
- * is a deployment convenience.  Its scratch is one static 8 MiB device array inside the
+ * is a deployment convenience.  Its scratch is one static 12 MiB device array inside the
  * library, held by every GPU that loads it until the process exits.
- *   - B must be at most 8 (else MLA_ERR_CAPACITY); the split-KV attention uses at most 48
- *     work items, so long contexts run with fewer, longer splits than mla_decode's.
+ *   - B must be at most 8 (else MLA_ERR_CAPACITY), on any GPU of up to 1024 SMs; the split-KV
+ *     attention uses at most 48 work items, so long contexts run with fewer, longer splits
+ *     than mla_decode's.
  *   - Every call shares the array: calls that overlap on the GPU race and must be serialised
  *     by the caller (one stream, one host thread).  The array keeps the last call's
  *     contents; nothing in it needs clearing, since every byte read is written first.
- *   - The first call on a device looks up the array's address on that device (the device
- *     must be current); make that first call before capturing a stream.
+ *   - mla_create looks up the array's address on the context's device (then current) and
+ *     keeps it in the context; calling with another device current gives
+ *     MLA_ERR_INVALID_ARG.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
 mla_status mla_decode_noalloc(mla_ctx* ctx, const void* x_bf16, int B, void* cache_bf16, int cap,
                               int* seq_lens_dev, const int* seq_lens_host, void* out_bf16,
@@ -194,6 +196,24 @@ mla_status mla_set_profiling(mla_ctx* ctx, int on);
  * strings, may be NULL) and ms (device milliseconds of each launch when that call ran with
  * profiling on, else -1; waits for the launch to finish; may be NULL). */
 int mla_last_launches(mla_ctx* ctx, int max, const char** names, float* ms);
+
+/* Self-test of the device-side bounded waits.  Every wait inside this library's kernels (on
+ * an mbarrier completed by a TMA copy, an MMA or another warp) gives up after a limit (2 s),
+ * records a timeout in the context's device error word and lets the kernel unwind, so a lost
+ * completion never hangs the GPU.  This call enqueues one small kernel that waits, with the
+ * same code and the given limit (at most 2e9 ns), on an mbarrier that nothing arrives at: the
+ * wait runs out and a following mla_get_device_status returns MLA_ERR_TIMEOUT (and clears the
+ * word), after which the context works as before.  MLA_ERR_INVALID_ARG for a NULL ctx or a
+ * larger limit.
+ *
+ * Host-side failure injection (testing aid): a context created while the environment
+ * variable MLA_TEST_FAIL_AFTER holds a number n >= 0 fails every later mla_cache_append,
+ * mla_prefill and mla_decode call at the call's launch number n (0-based) with MLA_ERR_CUDA,
+ * exactly as a failed CUDA launch returns: launches 0..n-1 are enqueued and run, launch n and
+ * the rest are not.  Every token call advances seq_lens only in its last launch, so a call
+ * that failed this way never advances them; it may have written the cache row at position
+ * seq_lens[b], which lies past the sequence and is written again by the next call. */
+mla_status mla_selftest_wait_timeout(mla_ctx* ctx, unsigned long long limit_ns, void* stream);
 
 /* Static, human-readable name of a status code. */
 const char* mla_status_string(mla_status s);

@@ -1,6 +1,7 @@
 """Shared helpers of the GPU parity tests: seeded inputs, oracle references computed from the
 same bytes, and the error measures the parity bar is stated in."""
 import functools
+import os
 
 import numpy as np
 import torch
@@ -36,8 +37,15 @@ def errors(got, ref):
             float(np.max(np.abs(got - ref))))
 
 
+# (test id, what, rel_fro, max_abs) of every comparison in this process; the terminal summary
+# prints them so a run shows how far inside the bar each case sits.
+MARGINS: list = []
+
+
 def assert_close(got, ref, what=""):
     rel, mx = errors(got, ref)
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0].split("::")[-1]
+    MARGINS.append((test, what, rel, mx))
     assert rel <= REL_FRO_TOL and mx <= MAX_ABS_TOL, f"{what}: rel_fro={rel:.3e} max_abs={mx:.3e}"
     return rel, mx
 

@@ -78,3 +78,102 @@ def test_repeat_runs_are_bitwise_identical(layer):
         outs.append((y.clone(), yd.clone(), cache.clone()))
     for a, b in zip(outs[0], outs[1]):
         assert torch.equal(a, b)
+
+
+def _injected_layer(n):
+    """A layer whose context fails every token call at launch n (MLA_TEST_FAIL_AFTER)."""
+    import os
+    wq, g = weights_and_gains(0)
+    os.environ["MLA_TEST_FAIL_AFTER"] = str(n)
+    try:
+        return mla.MlaLayer(wq, g)
+    finally:
+        del os.environ["MLA_TEST_FAIL_AFTER"]
+
+
+@pytest.mark.parametrize("B,p", [(1, 100), (5, 70)])
+def test_injected_launch_failure_never_advances_lengths(layer, B, p):
+    """A decode that fails at launch n (host-side injection, for every n the call has):
+    MLA_ERR_CUDA reaches the caller, the device lengths stay, the cached rows 0..p-1 are
+    untouched, the device status stays clean, and the same state then decodes correctly."""
+    xb = np.stack([synth.hidden_states(0, b, 0, p + 1) for b in range(B)])
+    cache = torch.zeros(B, p + 1, 576, dtype=torch.bfloat16, device="cuda")
+    lens = torch.zeros(B, dtype=torch.int32, device="cuda")
+    layer.prefill(to_dev(xb[:, :p]), cache, lens, [0] * B)
+    x = to_dev(xb[:, p])
+    ref = layer.decode(x, cache.clone(), lens.clone(), [p] * B)
+    n_launch = len(mla.mla_last_launches(layer.ctx))
+    assert n_launch >= 5
+    before = cache[:, :p].clone()
+    for n in range(n_launch):
+        bad = _injected_layer(n)
+        try:
+            out = torch.zeros_like(x)
+            with pytest.raises(mla.MlaError) as e:
+                bad.decode(x, cache, lens, [p] * B, out=out)
+            assert e.value.status == mla.MLA_ERR_CUDA
+            torch.cuda.synchronize()
+            assert bad.status() == mla.MLA_OK
+            assert lens.tolist() == [p] * B, f"lengths advanced by a call failed at launch {n}"
+            assert torch.equal(cache[:, :p], before)
+        finally:
+            bad.close()
+    got = layer.decode(x, cache, lens, [p] * B)
+    torch.cuda.synchronize()
+    assert lens.tolist() == [p + 1] * B
+    assert torch.equal(got, ref)
+
+
+def test_injected_failure_in_prefill(layer):
+    xb = synth.hidden_states(0, 3, 0, 40)
+    x = to_dev(xb[None])
+    for n in (0, 2, 5):
+        bad = _injected_layer(n)
+        try:
+            cache = torch.zeros(1, 40, 576, dtype=torch.bfloat16, device="cuda")
+            lens = torch.zeros(1, dtype=torch.int32, device="cuda")
+            with pytest.raises(mla.MlaError) as e:
+                bad.prefill(x, cache, lens, [0])
+            assert e.value.status == mla.MLA_ERR_CUDA
+            torch.cuda.synchronize()
+            assert lens.item() == 0
+        finally:
+            bad.close()
+
+
+def test_bounded_wait_gives_up_and_context_stays_usable(layer):
+    """The library's bounded wait on an mbarrier nothing arrives at (1 ms limit) records a
+    timeout: MLA_ERR_TIMEOUT from the status call, which clears it; a decode then runs
+    normally."""
+    mla.mla_selftest_wait_timeout(layer.ctx, 1_000_000)
+    assert layer.status() == mla.MLA_ERR_TIMEOUT
+    assert layer.status() == mla.MLA_OK
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_selftest_wait_timeout(layer.ctx, 3_000_000_000)
+    assert e.value.status == mla.MLA_ERR_INVALID_ARG
+    xb = synth.hidden_states(0, 4, 0, 33)
+    cache = torch.zeros(1, 33, 576, dtype=torch.bfloat16, device="cuda")
+    lens = torch.zeros(1, dtype=torch.int32, device="cuda")
+    layer.prefill(to_dev(xb[None, :32]), cache, lens, [0])
+    layer.decode(to_dev(xb[32:33]), cache, lens, [32])
+    torch.cuda.synchronize()
+    assert layer.status() == mla.MLA_OK and lens.item() == 33
+
+
+def test_ragged_b64_decode_is_bitwise_repeatable(layer):
+    """The B > 8 path (log-sum-exp combine over shares that cut sequences anywhere, tiled
+    W_UV absorption, tensor-core projections) gives the same bits on repeated runs."""
+    from tests.mla_cases import build_caches_gpu
+    lengths = synth.ragged_lengths(1, 64, 100, 1500).tolist()
+    cache, lens = build_caches_gpu(layer, 1, lengths, max(lengths) + 1)
+    xb = np.stack([synth.hidden_states(1, b, lengths[b], 1)[0] for b in range(64)])
+    x = to_dev(xb)
+    outs = []
+    for _ in range(3):
+        c, l = cache.clone(), lens.clone()
+        y = layer.decode(x, c, l, lengths)
+        torch.cuda.synchronize()
+        outs.append((y, torch.stack([c[b, lengths[b]] for b in range(64)])))
+    assert layer.status() == mla.MLA_OK
+    for a, b in outs[1:]:
+        assert torch.equal(a[0], outs[0][0]) and torch.equal(a[1], outs[0][1])

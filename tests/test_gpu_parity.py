@@ -200,36 +200,68 @@ def test_decode_matches_last_prefill_row_on_gpu(layer):
 
 
 def test_prefill_config3_t4096_sampled(layer):
-    """Full-size prefill (T=4096): sampled rows against the oracle."""
+    """Full-size prefill (T=4096): every cache row, and 160 output rows against the oracle --
+    the tile edges of the first, middle and last 128-query tiles plus 128 rows drawn at
+    random (seeded) over the whole prompt."""
     W = oracle_weights(0)
     T = 4096
     xb, y, cache = run_prefill(layer, [0], T)
     xf = O.bf16_to_f64(xb[0])
     cache_ref = O.cache_rows(xf, np.arange(T), W)
     assert_close(cache[0], cache_ref, "cache T=4096")
-    rows = np.array([0, 1, 63, 64, 65, 127, 1000, 2047, 2048, 3333, 4094, 4095])
-    assert_close(y[0, rows], oracle_rows(xf, rows, cache_ref, W), "prefill T=4096 rows")
+    edges = [0, 1, 63, 64, 65, 127, 128, 129, 2047, 2048, 2049, 3967, 3968, 4094, 4095]
+    rnd = np.random.default_rng(40).choice(T, 145, replace=False)
+    rows = np.unique(np.concatenate([edges, rnd]))
+    assert_close(y[0, rows], oracle_rows(xf, rows, cache_ref, W), f"prefill T=4096 {len(rows)} rows")
+
+
+def _one_at_a_time(layer, x, cache0, lens0, lengths):
+    """mla_decode of each sequence alone (B=1: another split-KV plan and the GEMV
+    projections) on copies of the caches as they were before the batched step."""
+    outs = []
+    for b, n in enumerate(lengths):
+        outs.append(layer.decode(x[b:b + 1], cache0[b:b + 1], lens0[b:b + 1], [n])[0])
+    torch.cuda.synchronize()
+    return torch.stack(outs)
 
 
 def test_decode_config4_ragged_b64_sampled(layer):
+    """Ragged decode, B=64, lengths ~U[512, 8192].  Against the oracle: 16 sequences spread
+    over the length range (shortest to longest) and every sequence's appended cache row.
+    Against the same layer run one sequence at a time: all 64 outputs and appended rows
+    (the batched share plan cuts sequences at places the single-sequence plan does not)."""
     W = oracle_weights(0)
     lengths = synth.ragged_lengths(0, 64, 512, 8192).tolist()
     cap = max(lengths) + 1
     cache, lens = build_caches_gpu(layer, 0, lengths, cap)
+    cache0, lens0 = cache.clone(), lens.clone()
     xb = np.stack([synth.hidden_states(0, b, lengths[b], 1)[0] for b in range(64)])
-    yd = layer.decode(to_dev(xb), cache, lens, lengths)
+    x = to_dev(xb)
+    yd_dev = layer.decode(x, cache, lens, lengths)
     torch.cuda.synchronize()
     assert layer.status() == mla.MLA_OK
     assert lens.tolist() == [n + 1 for n in lengths]
-    yd = yd.float().cpu().numpy()
+    yd = yd_dev.float().cpu().numpy()
+    # every appended row against the oracle
+    rows_ref = np.stack([O.cache_rows(O.bf16_to_f64(xb[b])[None], np.array([lengths[b]]), W)[0]
+                         for b in range(64)])
+    rows_got = torch.stack([cache[b, lengths[b]] for b in range(64)]).float().cpu().numpy()
+    assert_close(rows_got, rows_ref, "ragged appended rows (64)")
     order = np.argsort(lengths)
-    for b in (int(order[0]), int(order[31]), int(order[-1])):
+    for b in [int(order[i]) for i in np.linspace(0, 63, 16).round().astype(int)]:
         c_ref = oracle_cache(0, b, lengths[b], W)
         y_ref, _ = O.decode(O.bf16_to_f64(xb[b]), c_ref, W)
         assert_close(yd[b], y_ref, f"ragged decode seq {b} (len {lengths[b]})")
+    single = _one_at_a_time(layer, x, cache0, lens0, lengths)
+    assert layer.status() == mla.MLA_OK
+    assert_close(yd, single.float().cpu().numpy(), "ragged B=64 vs one at a time")
+    got1 = torch.stack([cache0[b, lengths[b]] for b in range(64)]).float().cpu().numpy()
+    assert_close(got1, rows_got, "ragged appended rows vs one at a time")
 
 
-def test_decode_config5_long_b8_sampled(layer):
+def test_decode_config5_long_b8_every_sequence(layer):
+    """Long-context decode, B=8 x 131,072 cached positions: all eight outputs and appended
+    rows against the oracle, plus sampled cache rows."""
     W = oracle_weights(0)
     L = 131072
     cache, lens = build_caches_gpu(layer, 0, [L] * 8, L + 1)
@@ -237,17 +269,19 @@ def test_decode_config5_long_b8_sampled(layer):
     yd = layer.decode(to_dev(xb), cache, lens, [L] * 8)
     torch.cuda.synchronize()
     assert layer.status() == mla.MLA_OK
+    assert lens.tolist() == [L + 1] * 8
     yd = yd.float().cpu().numpy()
-    b = 5
-    c_ref = oracle_cache(0, b, L, W)
-    y_ref, full = O.decode(O.bf16_to_f64(xb[b]), c_ref, W)
-    assert_close(yd[b], y_ref, "long decode seq 5")
-    got_rows = cache[b, [0, 77777, L]].float().cpu().numpy()
-    assert_close(got_rows, full[[0, 77777, L]], "long cache rows")
+    for b in range(8):
+        c_ref = oracle_cache(0, b, L, W)
+        y_ref, full = O.decode(O.bf16_to_f64(xb[b]), c_ref, W)
+        assert_close(yd[b], y_ref, f"long decode seq {b}")
+        idx = [0, 4095, 4096, 77777, L - 1, L]
+        assert_close(cache[b, idx].float().cpu().numpy(), full[idx], f"long cache rows seq {b}")
 
 
 # One sequence and two take the six-kernel decode (fused q-latent norm and cache append, fused
-# combine and W_UV); three to eight the separate kernels with GEMV projections.
+# combine and W_UV); three the separate kernels with GEMV projections; four to eight the
+# separate kernels with tensor-core projections.
 @pytest.mark.parametrize("lengths", [[0], [65, 300], [5, 64, 129],
                                      [1, 63, 64, 65, 127, 128, 129, 200]])
 def test_decode_tile_edges_every_sequence(layer, lengths):
