@@ -175,5 +175,5 @@ def test_ragged_b64_decode_is_bitwise_repeatable(layer):
         torch.cuda.synchronize()
         outs.append((y, torch.stack([c[b, lengths[b]] for b in range(64)])))
     assert layer.status() == mla.MLA_OK
-    for a, b in outs[1:]:
-        assert torch.equal(a[0], outs[0][0]) and torch.equal(a[1], outs[0][1])
+    for y, rows in outs[1:]:
+        assert torch.equal(y, outs[0][0]) and torch.equal(rows, outs[0][1])
