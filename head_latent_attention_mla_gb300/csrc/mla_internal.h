@@ -125,6 +125,12 @@ constexpr size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms) {
          (s > 1 ? (size_t)s * M * N_total * sizeof(float) : 0);
 }
 
+// A byte range of device memory that a kernel prefetches into L2 for a later kernel.
+struct L2Region {
+  const void* p;
+  size_t bytes;
+};
+
 // ---- launchers (each returns the launch's cudaError_t) ----------------------------------
 
 // Y = X W^T for up to two projections sharing X [M, K] (row stride ldx elements).
@@ -132,9 +138,30 @@ constexpr size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms) {
 // cores, split over K when the grid would be small, with fp32 partials in `partial`
 // (gemm_partial_bytes bytes).  Block 0 of the launch also adds adv_by to adv[0..adv_n) (the
 // call's length bookkeeping, riding on its last kernel; adv_n <= 128 with M <= kGemvMaxM).
+// With 1..kGemvMaxM rows and K of 1536, 7168 or 8192 the weights are streamed by
+// launch_gemv_stream, which also starts the L2 prefetch of the regions pf[0..npf).
 cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
                         float* partial, int num_sms, int* err, cudaStream_t st,
-                        int* adv = nullptr, int adv_n = 0, int adv_by = 0, bool pdl = false);
+                        int* adv = nullptr, int adv_n = 0, int adv_by = 0, bool pdl = false,
+                        const L2Region* pf = nullptr, int npf = 0);
+
+// Persistent weight-streaming GEMV (1..kGemvMaxM token rows; K = 1536, 7168 or 8192): one CTA
+// per SM streams a contiguous run of weight rows through a shared-memory ring with bulk
+// copies, and prefetches the regions pf[0..npf) (at most 3) into L2 for later kernels.
+bool gemv_stream_supports(int M, int K);
+cudaError_t launch_gemv_stream(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p,
+                               int np, int num_sms, int* err, cudaStream_t st, bool pdl,
+                               int* adv, int adv_n, int adv_by, const L2Region* pf, int npf);
+// The same for q_b_proj of a decode step, with the q-latent RMSNorm of the fp32 q_a outputs
+// g1 [M, 2112] done on the fly, and one extra CTA that normalises the kv latent, rotates the
+// shared rotary key and appends each token's cache row (token m is sequence m, at position
+// seq_lens[m]; positions at or past `limit` are skipped and flagged).
+cudaError_t launch_qb_norm_stream(const float* g1, int M, const Proj& p, const __nv_bfloat16* gq,
+                                  const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
+                                  int rope_pairing, const int* seq_lens, __nv_bfloat16* cache,
+                                  int cap, int limit, int num_sms, int* err, cudaStream_t st,
+                                  bool pdl, const L2Region* pf, int npf);
+cudaError_t init_gemv_stream_kernels();
 bool gemm_can_advance(int M);  // whether launch_gemm honours adv for this M
 cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
                            float* partial, int num_sms, int* err, cudaStream_t st,
@@ -223,16 +250,12 @@ cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const __
                                   cudaStream_t st, bool pdl = false);
 
 // Decode for a few sequences: the combine fused with the output absorption (one CTA per
-// head and sequence), and q_b_proj fused with the q-latent norm plus the kv cache-row append.
+// head and sequence).
 cudaError_t launch_combine_absorb_out(const int* seq_lens, const int* lens_host,
                                       DecodePlan plan, const __half* o_part,
                                       const float* ml_part, const uint8_t* Wkvb,
                                       const float* Skvb, __nv_bfloat16* attn, int* err,
                                       cudaStream_t st, bool pdl = false);
-cudaError_t launch_qb_norm(const float* g1, int M, const Proj& p, const __nv_bfloat16* gq,
-                           const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
-                           int rope_pairing, const int* seq_lens, __nv_bfloat16* cache, int cap,
-                           int limit, int* err, cudaStream_t st, bool pdl = false);
 
 // Split-KV decode attention over the latent cache on the tcgen05 tensor cores (TMA-fed,
 // accumulators in tensor memory): per work item, unnormalised partial outputs and (m, l).
