@@ -37,7 +37,6 @@ namespace {
 using namespace tc;
 
 constexpr int GS_RING = 96 * 1024;  // bytes of the slot ring per CTA
-constexpr int GS_GR = 32;           // rows per reduction group
 constexpr int GS_PF_CHUNK = 32 * 1024;
 
 struct L2Prefetch {
@@ -79,18 +78,21 @@ struct GemvCfg {
   static constexpr int CH = K >= 4096 ? 16 : 8;        // bytes of a row per lane
   static constexpr int NW = K / (32 * CH);             // consumer warps
   static constexpr int RPS = K >= 4096 ? 1 : 8192 / K; // rows per slot
+  static constexpr int SPB = K >= 4096 ? 4 : 1;        // slots a consumer batch takes
+  static constexpr int RB = RPS * SPB;                 // rows per consumer batch
+  static constexpr int GR = RB * 8;                    // rows per reduction group
   static constexpr int SLOT = RPS * K;
-  static constexpr int NSLOT = GS_RING / SLOT;
+  static constexpr int NSLOT = (GS_RING / SLOT) / SPB * SPB;
   static constexpr int THREADS = (NW + 1) * 32;
   static constexpr int OFF_BAR = NSLOT * SLOT;
   static constexpr int OFF_RED = OFF_BAR + 2 * NSLOT * 8;
-  static constexpr int RED_FLOATS = 2 * NW * GS_GR * M;
+  static constexpr int RED_FLOATS = 2 * NW * GR * M;
   static constexpr int OFF_NSUM = OFF_RED + RED_FLOATS * 4;
   static constexpr int OFF_MISC = OFF_NSUM + NW * M * 4;
   static constexpr int BYTES = OFF_MISC + 16;
   static_assert(NW * 32 * CH == K, "k slices cover a row");
   static_assert(128 % CH == 0, "a lane's run lies in one 128-wide k block");
-  static_assert(SLOT % 16 == 0 && NSLOT >= 2, "slot ring");
+  static_assert(SLOT % 16 == 0 && NSLOT >= 2 * SPB, "slot ring");
   static_assert(THREADS <= 1024 && NW <= 32, "block shape");
 };
 
@@ -193,28 +195,35 @@ __global__ void __launch_bounds__(GemvCfg<M, K>::THREADS, 1) gemv_stream_kernel(
 
   if (warp == NW) {
     // ---------------------------------------------------------------- producer
+    // Lane 0 fills the ring first; only then do lanes 1..31 queue the L2 prefetches, so this
+    // kernel's own reads are never queued behind them.
+    auto issue = [&](int s) {
+      const int st = s % NSLOT;
+      const int j0 = s * RPS, cnt = min(RPS, nrows - j0);
+      mbar_expect_tx(&full[st], (uint32_t)(cnt * K));
+      uint8_t* dst = smem + st * C::SLOT;
+      // The slot's rows are contiguous in memory except where they cross from p[0] to p[1].
+      int g = r0 + j0, left = cnt;
+      while (left > 0) {
+        const bool second = g >= args.rows0;
+        const int n = second ? g - args.rows0 : g;
+        const int run = second ? left : min(left, args.rows0 - g);
+        const uint8_t* src = args.p[second ? 1 : 0].W + (size_t)n * K;
+        bulk_load(dst, src, (uint32_t)(run * K), &full[st]);
+        dst += run * K;
+        g += run;
+        left -= run;
+      }
+    };
+    const int first = min(NSLOT, nslots);
+    if (lane == 0)
+      for (int s = 0; s < first; ++s) issue(s);
+    __syncwarp();
     if (lane == 0) {
-      int s = 0;
-      bool ok = true;
+      int s = first;
       for (; s < nslots; ++s) {
-        const int st = s % NSLOT;
-        if (s >= NSLOT && !(ok = mbar_wait(&empty[st], ((s / NSLOT) - 1) & 1, err, abort_flag)))
-          break;
-        const int j0 = s * RPS, cnt = min(RPS, nrows - j0);
-        mbar_expect_tx(&full[st], (uint32_t)(cnt * K));
-        uint8_t* dst = smem + st * C::SLOT;
-        // The slot's rows are contiguous in memory except where they cross from p[0] to p[1].
-        int g = r0 + j0, left = cnt;
-        while (left > 0) {
-          const bool second = g >= args.rows0;
-          const int n = second ? g - args.rows0 : g;
-          const int run = second ? left : min(left, args.rows0 - g);
-          const uint8_t* src = args.p[second ? 1 : 0].W + (size_t)n * K;
-          bulk_load(dst, src, (uint32_t)(run * K), &full[st]);
-          dst += run * K;
-          g += run;
-          left -= run;
-        }
+        if (!mbar_wait(&empty[s % NSLOT], ((s / NSLOT) - 1) & 1, err, abort_flag)) break;
+        issue(s);
       }
       // Never leave the CTA with copies in flight: wait (bounded) for the last ones.
       volatile int no_abort = 0;
@@ -290,84 +299,107 @@ __global__ void __launch_bounds__(GemvCfg<M, K>::THREADS, 1) gemv_stream_kernel(
     }
   }
 
+  // Rows go in batches of RB (SPB slots): the RB x M warp reductions are independent
+  // shuffle chains, so their latencies overlap.
+  constexpr int RB = C::RB, SPB = C::SPB, GR = C::GR;
   int cur_rb = -1, cur_prob = -1;
   float sc = 0.f;
   bool ok = true;
-  for (int s = 0; s < nslots; ++s) {
-    const int st = s % NSLOT;
-    ok = mbar_wait(&full[st], (s / NSLOT) & 1, err, abort_flag);
+  for (int s0 = 0; s0 < nslots; s0 += SPB) {
+#pragma unroll
+    for (int q = 0; q < SPB; ++q)
+      if (ok && s0 + q < nslots)
+        ok = mbar_wait(&full[(s0 + q) % NSLOT], ((s0 + q) / NSLOT) & 1, err, abort_flag);
     if (!__all_sync(0xffffffffu, ok)) {
       ok = false;
       break;
     }
-    const uint8_t* slot = smem + st * C::SLOT;
-#pragma unroll 1
-    for (int rr = 0; rr < RPS; ++rr) {
-      const int j = s * RPS + rr;
-      if (j >= nrows) break;
-      const int g = r0 + j;
-      const int prob = g >= args.rows0 ? 1 : 0;
-      const int n = prob ? g - args.rows0 : g;
-      if (n / BLK != cur_rb || prob != cur_prob) {
-        cur_rb = n / BLK;
-        cur_prob = prob;
-        sc = __ldg(args.p[prob].S + (size_t)cur_rb * (K / BLK) + k0 / BLK);
+    const int jb = s0 * RPS;                 // first row of the batch
+    const int nb = min(RB, nrows - jb);      // rows in the batch
+    float part[RB][M];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      const int j = jb + r;
+#pragma unroll
+      for (int m = 0; m < M; ++m) part[r][m] = 0.f;
+      if (r < nb) {
+        const int g = r0 + j;
+        const int prob = g >= args.rows0 ? 1 : 0;
+        const int n = prob ? g - args.rows0 : g;
+        if (n / BLK != cur_rb || prob != cur_prob) {
+          cur_rb = n / BLK;
+          cur_prob = prob;
+          sc = __ldg(args.p[prob].S + (size_t)cur_rb * (K / BLK) + k0 / BLK);
+        }
+        // Row j sits in slot (j / RPS) % NSLOT at row j % RPS.
+        const uint8_t* wrow = smem + ((j / RPS) % NSLOT) * C::SLOT + (j % RPS) * K + k0;
+        float wf[CH];
+        if constexpr (CH == 16) {
+          const uint4 w = *reinterpret_cast<const uint4*>(wrow);
+          e4m3x4_to_f32(w.x, wf);
+          e4m3x4_to_f32(w.y, wf + 4);
+          e4m3x4_to_f32(w.z, wf + 8);
+          e4m3x4_to_f32(w.w, wf + 12);
+        } else {
+          const uint2 w = *reinterpret_cast<const uint2*>(wrow);
+          e4m3x4_to_f32(w.x, wf);
+          e4m3x4_to_f32(w.y, wf + 4);
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          float a = 0.f;
+#pragma unroll
+          for (int i = 0; i < CH; ++i) a = fmaf(wf[i], xr[m][i], a);
+          part[r][m] = a * sc;
+        }
       }
-      float wf[CH];
-      if constexpr (CH == 16) {
-        const uint4 w = *reinterpret_cast<const uint4*>(slot + rr * K + k0);
-        e4m3x4_to_f32(w.x, wf);
-        e4m3x4_to_f32(w.y, wf + 4);
-        e4m3x4_to_f32(w.z, wf + 8);
-        e4m3x4_to_f32(w.w, wf + 12);
-      } else {
-        const uint2 w = *reinterpret_cast<const uint2*>(slot + rr * K + k0);
-        e4m3x4_to_f32(w.x, wf);
-        e4m3x4_to_f32(w.y, wf + 4);
-      }
-      float part[M];
+    }
 #pragma unroll
-      for (int m = 0; m < M; ++m) {
-        float a = 0.f;
+    for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
-        for (int i = 0; i < CH; ++i) a = fmaf(wf[i], xr[m][i], a);
-        a *= sc;
+      for (int r = 0; r < RB; ++r)
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-        part[m] = a;
-      }
-      const int gb = (j / GS_GR) & 1, jr = j % GS_GR;
-      if (lane == 0)
+        for (int m = 0; m < M; ++m) part[r][m] += __shfl_xor_sync(0xffffffffu, part[r][m], off);
+    if (lane == 0)
 #pragma unroll
-        for (int m = 0; m < M; ++m) red[((gb * NW + warp) * GS_GR + jr) * M + m] = part[m];
-      // End of a group of rows (or of the CTA's rows): the warps meet, and each finishes a
-      // few rows: the sum over the warps' partials, then the store.
-      if (jr == GS_GR - 1 || j == nrows - 1) {
-        named_bar(1, NW * 32);
-        const int jg = j - jr;
-        for (int i = warp; i <= jr; i += NW) {
-          const int gg = r0 + jg + i;
-          const int pp = gg >= args.rows0 ? 1 : 0;
-          const int nn = pp ? gg - args.rows0 : gg;
-          const Proj& P = args.p[pp];
+      for (int r = 0; r < RB; ++r)
+        if (r < nb) {
+          const int j = jb + r;
 #pragma unroll
-          for (int m = 0; m < M; ++m) {
-            float v = lane < NW ? red[((gb * NW + lane) * GS_GR + i) * M + m] : 0.f;
+          for (int m = 0; m < M; ++m)
+            red[((((j / GR) & 1) * NW + warp) * GR + j % GR) * M + m] = part[r][m];
+        }
+    __syncwarp();
+    if (lane == 0)
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            if (lane == 0) {
-              if (P.y_fp32)
-                reinterpret_cast<float*>(P.Y)[(size_t)m * P.ldy + nn] = v;
-              else
-                reinterpret_cast<__nv_bfloat16*>(P.Y)[(size_t)m * P.ldy + nn] =
-                    __float2bfloat16_rn(v);
-            }
+      for (int q = 0; q < SPB; ++q)
+        if (s0 + q < nslots) mbar_arrive(&empty[(s0 + q) % NSLOT]);
+    // End of a group of rows (GR is a multiple of RB), or of the CTA's rows: the warps meet,
+    // and each finishes a few rows: the sum over the warps' partials, then the store.
+    const int jl = jb + nb - 1;
+    if (jl % GR == GR - 1 || jl == nrows - 1) {
+      named_bar(1, NW * 32);
+      const int gb = (jl / GR) & 1, jg = jl - jl % GR;
+      for (int i = warp; i <= jl % GR; i += NW) {
+        const int gg = r0 + jg + i;
+        const int pp = gg >= args.rows0 ? 1 : 0;
+        const int nn = pp ? gg - args.rows0 : gg;
+        const Proj& P = args.p[pp];
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          float v = lane < NW ? red[((gb * NW + lane) * GR + i) * M + m] : 0.f;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+          if (lane == 0) {
+            if (P.y_fp32)
+              reinterpret_cast<float*>(P.Y)[(size_t)m * P.ldy + nn] = v;
+            else
+              reinterpret_cast<__nv_bfloat16*>(P.Y)[(size_t)m * P.ldy + nn] =
+                  __float2bfloat16_rn(v);
           }
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
   }
 }
 
