@@ -195,8 +195,8 @@ __global__ void __launch_bounds__(GemvCfg<M, K>::THREADS, 1) gemv_stream_kernel(
 
   if (warp == NW) {
     // ---------------------------------------------------------------- producer
-    // Lane 0 fills the ring first; only then do lanes 1..31 queue the L2 prefetches, so this
-    // kernel's own reads are never queued behind them.
+    // Lane 0 fills the ring first; only then do lanes 1..31 queue the L2 prefetches (this
+    // CTA's remaining rows, then later kernels' weights), so the first copies go out first.
     auto issue = [&](int s) {
       const int st = s % NSLOT;
       const int j0 = s * RPS, cnt = min(RPS, nrows - j0);
@@ -230,7 +230,24 @@ __global__ void __launch_bounds__(GemvCfg<M, K>::THREADS, 1) gemv_stream_kernel(
       for (int u = max(0, s - NSLOT); u < s; ++u)
         mbar_wait(&full[u % NSLOT], (u / NSLOT) & 1, err, &no_abort);
     } else {
-      // L2 prefetch of later kernels' weights: this CTA's share of each region.
+      // First the rest of this CTA's own rows: the ring holds too few bytes to cover the DRAM
+      // latency under full load, so every row's read starts now and its bulk copy later
+      // finds it in L2.
+      {
+        const int g0 = r0 + first * RPS;
+        const int lanes = 31;
+        for (int part = 0; part < 2; ++part) {
+          const int a = part ? max(g0, args.rows0) : g0;
+          const int b = part ? r1 : min(r1, args.rows0);
+          if (a >= b) continue;
+          const uint8_t* base = args.p[part].W + (size_t)(a - (part ? args.rows0 : 0)) * K;
+          const unsigned long long len = (unsigned long long)(b - a) * K;
+          for (unsigned long long o = (unsigned long long)(lane - 1) * GS_PF_CHUNK; o < len;
+               o += (unsigned long long)lanes * GS_PF_CHUNK)
+            prefetch_l2_bulk(base + o, (uint32_t)min((unsigned long long)GS_PF_CHUNK, len - o));
+        }
+      }
+      // Then the L2 prefetch of later kernels' weights: this CTA's share of each region.
       for (int i = 0; i < args.pf.n; ++i) {
         const unsigned long long len = args.pf.bytes[i] & ~15ull;
         const unsigned long long lo = (len * c / args.ncta) & ~15ull;
