@@ -1,7 +1,5 @@
-// FP8 block-scaled projections for a few tokens with K = 512 (kv_b_proj over a chunk's first
-// cached rows): a GEMV on the CUDA cores, one warp per weight row.  The other shapes of one to
-// three rows stream their weights in k_gemv_stream.cu; larger token counts run on the
-// tensor-core kernel in k_gemm_tc.cu.
+// FP8 block-scaled projections for a few tokens: a weight-streaming GEMV on the CUDA cores
+// (larger token counts go to the tensor-core kernel in k_gemm_tc.cu).
 //
 // Y[m, n] = sum_k X[m, k] * e4m3(W[n, k]) * S[n/128][k/128]  ("linear" excerpt of the
 // "Key-value latent" page: fmt e4m3, weight_block_size [128, 128]; nn.Linear without bias).
@@ -45,7 +43,16 @@ struct ProjSet {
   int rows0;    // rows of p[0]
   int* adv;     // optional: adv[i] += adv_by for i < adv_n, by block 0 (lengths bookkeeping)
   int adv_n, adv_by;
+  L2Region pf[2];  // weights of later kernels: each CTA starts the L2 reads of its share
+  int npf;
 };
+
+// Thread 0 of CTA `cta` starts the L2 reads of its share of each region.  The loads of this
+// kernel go through the load/store units; these go through the otherwise idle bulk-copy unit.
+__device__ __forceinline__ void prefetch_later(const L2Region* pf, int npf, int cta, int ncta) {
+  if (threadIdx.x == 0)
+    for (int i = 0; i < npf; ++i) prefetch_l2_share(pf[i], cta, ncta);
+}
 
 template <int M, int NCH>
 __global__ void __launch_bounds__(128) gemv_f8w_kernel(const __nv_bfloat16* __restrict__ X,
@@ -70,6 +77,7 @@ __global__ void __launch_bounds__(128) gemv_f8w_kernel(const __nv_bfloat16* __re
   uint4 w[NCH];
 #pragma unroll
   for (int u = 0; u < NCH; ++u) w[u] = ld_stream(wrow + u * 512 + lane * 16);
+  prefetch_later(ps.pf, ps.npf, blockIdx.x, gridDim.x);
   // The weights do not depend on earlier kernels; the activations do.
   pdl_wait();
   if (ps.adv && blockIdx.x == 0 && (int)threadIdx.x < ps.adv_n) ps.adv[threadIdx.x] += ps.adv_by;
@@ -112,12 +120,159 @@ __global__ void __launch_bounds__(128) gemv_f8w_kernel(const __nv_bfloat16* __re
   }
 }
 
+// q_b_proj for a few decode tokens with the q-latent RMSNorm done on the fly ("rmsnorm"
+// excerpt: cq = g * bf16(x * rsqrt(mean(x^2) + eps))): every CTA normalises the tokens' fp32
+// q_a outputs (g1[m][0:1536], 6 KB each from L2) into shared memory and then streams its four
+// weight rows like gemv_f8w_kernel.  One extra CTA at the end normalises the kv latent,
+// rotates the shared rotary key and appends each token's cache row, the other half of the
+// norm kernel of the prefill path.
+struct NormArgs {
+  L2Region pf[2];                // weights of later kernels (see prefetch_later)
+  int npf;
+  const float* g1;               // [M][2112] fp32 q_a | kv_a outputs
+  const __nv_bfloat16* gq;       // q_a_layernorm gain [1536]
+  const __nv_bfloat16* gkv;      // kv_a_layernorm gain [512]
+  float eps;
+  const float2* rope_tab;
+  int pairing;
+  const int* seq_lens;
+  __nv_bfloat16* cache;
+  int cap, limit;
+  int* err;
+};
+
+__device__ __forceinline__ float bf16r(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// Sum over the 128 threads of a CTA (red: 4 floats of shared memory).
+__device__ __forceinline__ float cta_sum128(float v, float* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  return (red[0] + red[1]) + (red[2] + red[3]);
+}
+
+template <int M>
+__global__ void __launch_bounds__(128) gemv_norm_qb_kernel(Proj P, NormArgs na) {
+  constexpr int K = Q_LORA, NCH = K / 512;
+  __shared__ __align__(16) __nv_bfloat16 xs[M][K];
+  __shared__ float red[4];
+  __shared__ __align__(16) __nv_bfloat16 row[LAT];
+  pdl_launch_dependents();
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31, tid = threadIdx.x;
+  const bool kv_cta = blockIdx.x == gridDim.x - 1;
+  const int n = warp;
+  uint4 w[NCH];
+  if (!kv_cta) {
+    const uint8_t* wrow = P.W + (size_t)n * K;
+#pragma unroll
+    for (int u = 0; u < NCH; ++u) w[u] = ld_stream(wrow + u * 512 + lane * 16);
+  }
+  prefetch_later(na.pf, na.npf, blockIdx.x, gridDim.x);
+  pdl_wait();  // g1 comes from the previous kernel
+  if (kv_cta) {
+    // kv latent norm, rotary key and the cache row of every token.
+    for (int m = 0; m < M; ++m) {
+      const float* in = na.g1 + (size_t)m * G1_N + Q_LORA;
+      float xk[KV_LORA / 128];
+      float sk = 0.f;
+#pragma unroll
+      for (int i = 0; i < KV_LORA / 128; ++i) {
+        xk[i] = in[tid + 128 * i];
+        sk += xk[i] * xk[i];
+      }
+      const float rk = rsqrtf(cta_sum128(sk, red) / KV_LORA + na.eps);
+#pragma unroll
+      for (int i = 0; i < KV_LORA / 128; ++i) {
+        const int c = tid + 128 * i;
+        row[c] = __float2bfloat16_rn(__bfloat162float(na.gkv[c]) * bf16r(xk[i] * rk));
+      }
+      const int pos = na.seq_lens[m];
+      const bool bad = pos < 0 || pos >= na.limit;
+      if (bad && tid == 0) atomicExch(na.err, DEV_ERR_RANGE);
+      if (!bad && tid < ROPE / 2) {
+        const int2 ij = na.pairing == 0 ? make_int2(2 * tid, 2 * tid + 1)
+                                        : make_int2(tid, tid + ROPE / 2);
+        const float2 cs = na.rope_tab[(size_t)pos * (ROPE / 2) + tid];
+        const float a = in[KV_LORA + ij.x], b = in[KV_LORA + ij.y];
+        row[KV_LORA + ij.x] = __float2bfloat16_rn(a * cs.x - b * cs.y);
+        row[KV_LORA + ij.y] = __float2bfloat16_rn(b * cs.x + a * cs.y);
+      }
+      __syncthreads();
+      if (!bad && tid < LAT / 8)
+        reinterpret_cast<uint4*>(na.cache + ((size_t)m * na.cap + pos) * LAT)[tid] =
+            reinterpret_cast<const uint4*>(row)[tid];
+      __syncthreads();
+    }
+    return;
+  }
+  // q latent norm of every token into shared memory.
+  for (int m = 0; m < M; ++m) {
+    const float* in = na.g1 + (size_t)m * G1_N;
+    float xq[K / 128];
+    float sq = 0.f;
+#pragma unroll
+    for (int i = 0; i < K / 128; ++i) {
+      xq[i] = in[tid + 128 * i];
+      sq += xq[i] * xq[i];
+    }
+    const float rq = rsqrtf(cta_sum128(sq, red) / K + na.eps);
+#pragma unroll
+    for (int i = 0; i < K / 128; ++i) {
+      const int c = tid + 128 * i;
+      xs[m][c] = __float2bfloat16_rn(__bfloat162float(na.gq[c]) * bf16r(xq[i] * rq));
+    }
+  }
+  __syncthreads();
+  if (n >= P.N) return;
+  const float* srow = P.S + (size_t)(n / BLK) * (K / BLK);
+  float acc[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) acc[m] = 0.f;
+#pragma unroll
+  for (int u = 0; u < NCH; ++u) {
+    const int k = u * 512 + lane * 16;
+    float wf[16];
+    e4m3x4_to_f32(w[u].x, wf);
+    e4m3x4_to_f32(w[u].y, wf + 4);
+    e4m3x4_to_f32(w[u].z, wf + 8);
+    e4m3x4_to_f32(w[u].w, wf + 12);
+    const float sc = __ldg(srow + k / BLK);
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      const uint4* xp = reinterpret_cast<const uint4*>(&xs[m][k]);
+      float xf[16];
+      bf16x8_to_f32(xp[0], xf);
+      bf16x8_to_f32(xp[1], xf + 8);
+      float part = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) part = fmaf(wf[i], xf[i], part);
+      acc[m] = fmaf(sc, part, acc[m]);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    float v = acc[m];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0)
+      reinterpret_cast<__nv_bfloat16*>(P.Y)[(size_t)m * P.ldy + n] = __float2bfloat16_rn(v);
+  }
+}
+
 template <int M>
 cudaError_t launch_gemv(const __nv_bfloat16* X, int ldx, int K, const ProjSet& ps, int rows,
                         cudaStream_t st, bool pdl) {
   const dim3 grid((rows + 3) / 4), block(128);
-  if (K != KV_LORA) return cudaErrorInvalidValue;
-  return launch_kernel(gemv_f8w_kernel<M, 1>, grid, block, 0, st, pdl, X, ldx, ps);
+  switch (K) {
+    case 512: return launch_kernel(gemv_f8w_kernel<M, 1>, grid, block, 0, st, pdl, X, ldx, ps);
+    case 1536: return launch_kernel(gemv_f8w_kernel<M, 3>, grid, block, 0, st, pdl, X, ldx, ps);
+    case 7168: return launch_kernel(gemv_f8w_kernel<M, 14>, grid, block, 0, st, pdl, X, ldx, ps);
+    case 8192: return launch_kernel(gemv_f8w_kernel<M, 16>, grid, block, 0, st, pdl, X, ldx, ps);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -131,23 +286,47 @@ cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Pro
   ps.adv = adv;
   ps.adv_n = adv_n;
   ps.adv_by = adv_by;
+  for (int i = 0; i < npf && i < 2; ++i) ps.pf[ps.npf++] = pf[i];
   ps.p[0] = p[0];
   if (np > 1) ps.p[1] = p[1];
   ps.rows0 = p[0].N;
   const int rows = p[0].N + (np > 1 ? p[1].N : 0);
   if (M <= kGemvMaxM) {
-    if (gemv_stream_supports(M, K))
-      return launch_gemv_stream(X, ldx, M, K, p, np, num_sms, err, st, pdl, adv, adv_n, adv_by,
-                                pf, npf);
     switch (M) {
       case 1: return launch_gemv<1>(X, ldx, K, ps, rows, st, pdl);
       case 2: return launch_gemv<2>(X, ldx, K, ps, rows, st, pdl);
-      default: return launch_gemv<3>(X, ldx, K, ps, rows, st, pdl);
+      case 3: return launch_gemv<3>(X, ldx, K, ps, rows, st, pdl);
+      case 4: return launch_gemv<4>(X, ldx, K, ps, rows, st, pdl);
+      case 5: return launch_gemv<5>(X, ldx, K, ps, rows, st, pdl);
+      case 6: return launch_gemv<6>(X, ldx, K, ps, rows, st, pdl);
+      case 7: return launch_gemv<7>(X, ldx, K, ps, rows, st, pdl);
+      default: return launch_gemv<8>(X, ldx, K, ps, rows, st, pdl);
     }
   }
   return launch_gemm_tc(X, ldx, M, K, p, np, partial, num_sms, err, st, adv, adv_n, adv_by);
 }
 
 bool gemm_can_advance(int M) { return M > 0; }
+
+cudaError_t launch_qb_norm(const float* g1, int M, const Proj& p, const __nv_bfloat16* gq,
+                           const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
+                           int rope_pairing, const int* seq_lens, __nv_bfloat16* cache, int cap,
+                           int limit, int* err, cudaStream_t st, bool pdl, const L2Region* pf,
+                           int npf) {
+  if (M < 1 || M > 8 || p.N != QB_N || p.y_fp32) return cudaErrorInvalidValue;
+  NormArgs na{{}, 0, g1, gq, gkv, eps, rope_tab, rope_pairing, seq_lens, cache, cap, limit, err};
+  for (int i = 0; i < npf && i < 2; ++i) na.pf[na.npf++] = pf[i];
+  const dim3 grid(p.N / 4 + 1), block(128);  // + the kv-cache CTA
+  switch (M) {
+    case 1: return launch_kernel(gemv_norm_qb_kernel<1>, grid, block, 0, st, pdl, p, na);
+    case 2: return launch_kernel(gemv_norm_qb_kernel<2>, grid, block, 0, st, pdl, p, na);
+    case 3: return launch_kernel(gemv_norm_qb_kernel<3>, grid, block, 0, st, pdl, p, na);
+    case 4: return launch_kernel(gemv_norm_qb_kernel<4>, grid, block, 0, st, pdl, p, na);
+    case 5: return launch_kernel(gemv_norm_qb_kernel<5>, grid, block, 0, st, pdl, p, na);
+    case 6: return launch_kernel(gemv_norm_qb_kernel<6>, grid, block, 0, st, pdl, p, na);
+    case 7: return launch_kernel(gemv_norm_qb_kernel<7>, grid, block, 0, st, pdl, p, na);
+    default: return launch_kernel(gemv_norm_qb_kernel<8>, grid, block, 0, st, pdl, p, na);
+  }
+}
 
 }  // namespace mla

@@ -499,10 +499,9 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
     // length update rides on o_proj.  (Every q_b CTA normalises every token, and every
     // (head, sequence) CTA reads its head's W_UV: both pay only for very few sequences.)
     Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
-    MLA_LAUNCH("gemm_q_b_norm", launch_qb_norm_stream(g1, B, p2, c->gain[0], c->gain[1],
-                                                      c->cfg.eps, c->rope_tab,
-                                                      c->cfg.rope_pairing, lens_dev, C, cap, limit,
-                                                      c->num_sms, c->d_err, s, true, pf2, 1));
+    MLA_LAUNCH("gemm_q_b_norm", launch_qb_norm(g1, B, p2, c->gain[0], c->gain[1], c->cfg.eps,
+                                               c->rope_tab, c->cfg.rope_pairing, lens_dev, C, cap,
+                                               limit, c->d_err, s, true, pf2, 1));
     MLA_LAUNCH("absorb_q", launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
                                            c->cfg.rope_pairing, lens_dev, limit, qfull, s, true));
     MLA_LAUNCH("decode_attention", launch_decode_attention_tc(qfull, C, cap, lens_dev, plan,
