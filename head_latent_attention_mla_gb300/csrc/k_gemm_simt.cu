@@ -43,16 +43,7 @@ struct ProjSet {
   int rows0;    // rows of p[0]
   int* adv;     // optional: adv[i] += adv_by for i < adv_n, by block 0 (lengths bookkeeping)
   int adv_n, adv_by;
-  L2Region pf[2];  // weights of later kernels: each CTA starts the L2 reads of its share
-  int npf;
 };
-
-// Thread 0 of CTA `cta` starts the L2 reads of its share of each region.  The loads of this
-// kernel go through the load/store units; these go through the otherwise idle bulk-copy unit.
-__device__ __forceinline__ void prefetch_later(const L2Region* pf, int npf, int cta, int ncta) {
-  if (threadIdx.x == 0)
-    for (int i = 0; i < npf; ++i) prefetch_l2_share(pf[i], cta, ncta);
-}
 
 template <int M, int NCH>
 __global__ void __launch_bounds__(128) gemv_f8w_kernel(const __nv_bfloat16* __restrict__ X,
@@ -77,7 +68,6 @@ __global__ void __launch_bounds__(128) gemv_f8w_kernel(const __nv_bfloat16* __re
   uint4 w[NCH];
 #pragma unroll
   for (int u = 0; u < NCH; ++u) w[u] = ld_stream(wrow + u * 512 + lane * 16);
-  prefetch_later(ps.pf, ps.npf, blockIdx.x, gridDim.x);
   // The weights do not depend on earlier kernels; the activations do.
   pdl_wait();
   if (ps.adv && blockIdx.x == 0 && (int)threadIdx.x < ps.adv_n) ps.adv[threadIdx.x] += ps.adv_by;
@@ -127,8 +117,6 @@ __global__ void __launch_bounds__(128) gemv_f8w_kernel(const __nv_bfloat16* __re
 // rotates the shared rotary key and appends each token's cache row, the other half of the
 // norm kernel of the prefill path.
 struct NormArgs {
-  L2Region pf[2];                // weights of later kernels (see prefetch_later)
-  int npf;
   const float* g1;               // [M][2112] fp32 q_a | kv_a outputs
   const __nv_bfloat16* gq;       // q_a_layernorm gain [1536]
   const __nv_bfloat16* gkv;      // kv_a_layernorm gain [512]
@@ -170,7 +158,6 @@ __global__ void __launch_bounds__(128) gemv_norm_qb_kernel(Proj P, NormArgs na) 
 #pragma unroll
     for (int u = 0; u < NCH; ++u) w[u] = ld_stream(wrow + u * 512 + lane * 16);
   }
-  prefetch_later(na.pf, na.npf, blockIdx.x, gridDim.x);
   pdl_wait();  // g1 comes from the previous kernel
   if (kv_cta) {
     // kv latent norm, rotary key and the cache row of every token.
@@ -279,14 +266,13 @@ cudaError_t launch_gemv(const __nv_bfloat16* X, int ldx, int K, const ProjSet& p
 
 cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
                         float* partial, int num_sms, int* err, cudaStream_t st, int* adv,
-                        int adv_n, int adv_by, bool pdl, const L2Region* pf, int npf) {
+                        int adv_n, int adv_by, bool pdl) {
   if (M <= 0) return cudaSuccess;
   ProjSet ps{};
   ps.np = np;
   ps.adv = adv;
   ps.adv_n = adv_n;
   ps.adv_by = adv_by;
-  for (int i = 0; i < npf && i < 2; ++i) ps.pf[ps.npf++] = pf[i];
   ps.p[0] = p[0];
   if (np > 1) ps.p[1] = p[1];
   ps.rows0 = p[0].N;
@@ -311,11 +297,9 @@ bool gemm_can_advance(int M) { return M > 0; }
 cudaError_t launch_qb_norm(const float* g1, int M, const Proj& p, const __nv_bfloat16* gq,
                            const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
                            int rope_pairing, const int* seq_lens, __nv_bfloat16* cache, int cap,
-                           int limit, int* err, cudaStream_t st, bool pdl, const L2Region* pf,
-                           int npf) {
+                           int limit, int* err, cudaStream_t st, bool pdl) {
   if (M < 1 || M > 8 || p.N != QB_N || p.y_fp32) return cudaErrorInvalidValue;
-  NormArgs na{{}, 0, g1, gq, gkv, eps, rope_tab, rope_pairing, seq_lens, cache, cap, limit, err};
-  for (int i = 0; i < npf && i < 2; ++i) na.pf[na.npf++] = pf[i];
+  const NormArgs na{g1, gq, gkv, eps, rope_tab, rope_pairing, seq_lens, cache, cap, limit, err};
   const dim3 grid(p.N / 4 + 1), block(128);  // + the kv-cache CTA
   switch (M) {
     case 1: return launch_kernel(gemv_norm_qb_kernel<1>, grid, block, 0, st, pdl, p, na);

@@ -482,17 +482,9 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
   __nv_bfloat16* olat = at<__nv_bfloat16>(ws, L.olat);
   __nv_bfloat16* attn = at<__nv_bfloat16>(ws, L.attn);
 
-  // With few sequences the step streams 101 MB of weights through a chain of dependent
-  // kernels.  The weight-streaming projections start the DRAM reads of later kernels' weights
-  // into L2 (q_a + kv_a: those of q_b and kv_b; q_b: those of o_proj), so the reads overlap
-  // the chain instead of waiting for each kernel in turn.
-  const L2Region pf1[2] = {{c->W[MLA_W_Q_B], (size_t)QB_N * Q_LORA},
-                           {c->W[MLA_W_KV_B], (size_t)KVB_N * KV_LORA}};
-  const L2Region pf2[1] = {{c->W[MLA_W_O], (size_t)HIDDEN * O_IN}};
   Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
                 {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
-  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, at<float>(ws, L.gpart),
-                                          c->num_sms, c->d_err, s, nullptr, 0, 0, false, pf1, 2));
+  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
   if (B <= 2) {
     // One or two sequences: six kernels.  q_b_proj normalises the q latent itself (and one of
     // its CTAs appends the cache rows); the combine is fused with the W_UV absorption; the
@@ -501,7 +493,7 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
     Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
     MLA_LAUNCH("gemm_q_b_norm", launch_qb_norm(g1, B, p2, c->gain[0], c->gain[1], c->cfg.eps,
                                                c->rope_tab, c->cfg.rope_pairing, lens_dev, C, cap,
-                                               limit, c->d_err, s, true, pf2, 1));
+                                               limit, c->d_err, s, true));
     MLA_LAUNCH("absorb_q", launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
                                            c->cfg.rope_pairing, lens_dev, limit, qfull, s, true));
     MLA_LAUNCH("decode_attention", launch_decode_attention_tc(qfull, C, cap, lens_dev, plan,
@@ -520,7 +512,7 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
                                     c->d_err, s, true));
   Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
   MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, B, Q_LORA, &p2, 1, at<float>(ws, L.gpart),
-                                     c->num_sms, c->d_err, s, nullptr, 0, 0, true, pf2, 1));
+                                     c->num_sms, c->d_err, s, nullptr, 0, 0, true));
   MLA_LAUNCH("absorb_q", launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
                              c->cfg.rope_pairing, lens_dev, limit, qfull, s, true));
   MLA_LAUNCH("decode_attention", launch_decode_attention_tc(qfull, C, cap, lens_dev, plan,

@@ -125,28 +125,6 @@ constexpr size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms) {
          (s > 1 ? (size_t)s * M * N_total * sizeof(float) : 0);
 }
 
-// A byte range of device memory that a kernel prefetches into L2 for a later kernel.
-struct L2Region {
-  const void* p;
-  size_t bytes;
-};
-
-// Starts the DRAM reads of `bytes` (a multiple of 16, address 16-byte aligned) into L2 through
-// the SM's bulk-copy unit: no destination, no completion.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-// This CTA's share (CTA `cta` of `ncta`) of the region, in chunks of at most 64 KB, issued by
-// the calling thread.
-__device__ __forceinline__ void prefetch_l2_share(const L2Region& r, int cta, int ncta) {
-  const unsigned long long len = r.bytes & ~15ull;
-  const unsigned long long lo = (len * cta / ncta) & ~15ull;
-  const unsigned long long hi = cta + 1 == ncta ? len : (len * (cta + 1) / ncta) & ~15ull;
-  const uint8_t* base = static_cast<const uint8_t*>(r.p);
-  for (unsigned long long o = lo; o < hi; o += 65536ull)
-    prefetch_l2_bulk(base + o, (uint32_t)(hi - o < 65536ull ? hi - o : 65536ull));
-}
-
 // ---- launchers (each returns the launch's cudaError_t) ----------------------------------
 
 // Y = X W^T for up to two projections sharing X [M, K] (row stride ldx elements).
@@ -154,12 +132,9 @@ __device__ __forceinline__ void prefetch_l2_share(const L2Region& r, int cta, in
 // cores, split over K when the grid would be small, with fp32 partials in `partial`
 // (gemm_partial_bytes bytes).  Block 0 of the launch also adds adv_by to adv[0..adv_n) (the
 // call's length bookkeeping, riding on its last kernel; adv_n <= 128 with M <= kGemvMaxM).
-// On the CUDA-core path the CTAs also start the DRAM reads of the regions pf[0..npf) (at most
-// two) into L2, each its share, for later kernels of the call.
 cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
                         float* partial, int num_sms, int* err, cudaStream_t st,
-                        int* adv = nullptr, int adv_n = 0, int adv_by = 0, bool pdl = false,
-                        const L2Region* pf = nullptr, int npf = 0);
+                        int* adv = nullptr, int adv_n = 0, int adv_by = 0, bool pdl = false);
 bool gemm_can_advance(int M);  // whether launch_gemm honours adv for this M
 cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
                            float* partial, int num_sms, int* err, cudaStream_t st,
@@ -248,13 +223,11 @@ cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const __
                                   cudaStream_t st, bool pdl = false);
 
 // Decode for a few sequences: the combine fused with the output absorption (one CTA per
-// head and sequence), and q_b_proj fused with the q-latent norm plus the kv cache-row append
-// (whose CTAs also start the L2 reads of the regions pf[0..npf), at most two).
+// head and sequence), and q_b_proj fused with the q-latent norm plus the kv cache-row append.
 cudaError_t launch_qb_norm(const float* g1, int M, const Proj& p, const __nv_bfloat16* gq,
                            const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
                            int rope_pairing, const int* seq_lens, __nv_bfloat16* cache, int cap,
-                           int limit, int* err, cudaStream_t st, bool pdl = false,
-                           const L2Region* pf = nullptr, int npf = 0);
+                           int limit, int* err, cudaStream_t st, bool pdl = false);
 cudaError_t launch_combine_absorb_out(const int* seq_lens, const int* lens_host,
                                       DecodePlan plan, const __half* o_part,
                                       const float* ml_part, const uint8_t* Wkvb,
