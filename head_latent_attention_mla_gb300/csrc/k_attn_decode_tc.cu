@@ -70,7 +70,8 @@ __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* v) {
 
 __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
     const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_c,
-    const int* __restrict__ seq_lens, int B, int cap, int G, long long P, int K, float scale_log2,
+    const int* __restrict__ seq_lens, int B, const CacheRef cache, int G, long long P, int K,
+    float scale_log2,
     __half* __restrict__ o_part, float* __restrict__ ml_part, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
         seg[3 * idx + 2] = (int)(hi - acc);
       }
       nseg += __popc(mask);
-      bad |= __any_sync(0xffffffffu, b < B && S - K > cap) != 0;
+      bad |= __any_sync(0xffffffffu, b < B && S - K > cache.capacity()) != 0;
       base += __shfl_sync(0xffffffffu, inc, 31);
     }
     if (lane == 0) {
@@ -161,7 +162,22 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
   fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nseg = *s_nseg;
-  auto seg_tiles = [&](int sg) { return (seg[3 * sg + 2] - seg[3 * sg + 1] + DA_TILE - 1) / DA_TILE; };
+  // A segment [p0, p1) is read in tiles that start at multiples of DA_TILE within its sequence
+  // (so a tile never crosses a page of a paged cache): from a0 = p0 rounded down; positions
+  // before p0 in the first tile are masked.
+  auto seg_a0 = [&](int sg) { return seg[3 * sg + 1] & ~(DA_TILE - 1); };
+  auto seg_tiles = [&](int sg) { return (seg[3 * sg + 2] - seg_a0(sg) + DA_TILE - 1) / DA_TILE; };
+  // Cache row of a tile's first position; an invalid page reads past the array (zero fill)
+  // and is flagged.
+  const long long c_rows = cache.rows(B);
+  auto tile_row = [&](int b, int pos) -> int {
+    const long long r = cache.row(b, pos);
+    if (r < 0) {
+      atomicExch(err, DEV_ERR_RANGE);
+      return (int)c_rows;
+    }
+    return (int)r;
+  };
   pdl_wait();  // the query and the new cache row come from earlier kernels
 
   if (nseg > 0) {
@@ -173,7 +189,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
         int t = 0, issued = 0, qloads = 0;
         bool ok = true;
         for (int sg = 0; ok && sg < nseg; ++sg) {
-          const int b = seg[3 * sg], p0 = seg[3 * sg + 1], nt = seg_tiles(sg);
+          const int b = seg[3 * sg], a0 = seg_a0(sg), nt = seg_tiles(sg);
           if (sg > 0 && !(ok = mbar_wait(q_free, (sg - 1) & 1, err, abort_flag))) break;
           mbar_expect_tx(q_full, DA_Q_BYTES);
           for (int c = 0; c < DA_NBOX; ++c)
@@ -185,7 +201,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
                 !(ok = mbar_wait(&c_empty[st], ((t / DA_STAGES) - 1) & 1, err, abort_flag)))
               break;
             mbar_expect_tx(&c_full[st], DA_TILE_BYTES);
-            const int row = b * cap + p0 + DA_TILE * i;
+            const int row = tile_row(b, a0 + DA_TILE * i);
             for (int c = 0; c < DA_NBOX; ++c)
               tma_load_2d(smem + OFF_C + st * DA_TILE_BYTES + c * DA_BOX, &map_c, &c_full[st],
                           64 * c, row);
@@ -193,10 +209,11 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
             // DA_L2_AHEAD later into L2, so its own load later finds it there.  At the last
             // tile of a segment, the next segment's query block and first tile instead.
             if (i + DA_L2_AHEAD < nt) {
+              const int ra = tile_row(b, a0 + DA_TILE * (i + DA_L2_AHEAD));
               for (int c = 0; c < DA_NBOX; ++c)
-                tma_prefetch_l2_2d(&map_c, 64 * c, row + DA_TILE * DA_L2_AHEAD);
+                tma_prefetch_l2_2d(&map_c, 64 * c, ra);
             } else if (i == nt - 1 && sg + 1 < nseg) {
-              const int bn = seg[3 * (sg + 1)], rn = bn * cap + seg[3 * (sg + 1) + 1];
+              const int bn = seg[3 * (sg + 1)], rn = tile_row(bn, seg_a0(sg + 1));
               for (int c = 0; c < DA_NBOX; ++c) {
                 tma_prefetch_l2_2d(&map_q, 64 * c, HEADS * bn);
                 tma_prefetch_l2_2d(&map_c, 64 * c, rn);
@@ -302,11 +319,14 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
           tmem_wait_ld();
           fence_before();
           mbar_arrive(&s_free[sb]);
-          const int n = min(DA_TILE, p1 - (p0 + DA_TILE * i));
+          const int a0 = p0 & ~(DA_TILE - 1);
+          const int n = min(DA_TILE, p1 - (a0 + DA_TILE * i));  // columns [lo, n) are valid
+          const int lo = i == 0 ? p0 - a0 : 0;
           float tmax = -INFINITY;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float sc = (2 * j + par < n) ? __uint_as_float(r[j]) * scale_log2 : -INFINITY;
+            const int col = 2 * j + par;
+            const float sc = (col >= lo && col < n) ? __uint_as_float(r[j]) * scale_log2 : -INFINITY;
             r[j] = __float_as_uint(sc);
             tmax = fmaxf(tmax, sc);
           }
@@ -483,17 +503,19 @@ cudaError_t init_decode_tc_kernel() {
                               DA_SMEM);
 }
 
-cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bfloat16* cache,
-                                       int cap, const int* seq_lens, DecodePlan plan,
+cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const CacheRef& cache,
+                                       const int* seq_lens, DecodePlan plan,
                                        float scale, __half* o_part, float* ml_part, int* err,
                                        cudaStream_t st, bool pdl) {
   if (plan.B == 0) return cudaSuccess;
+  const long long rows = cache.rows(plan.B);
+  if (rows <= 0 || rows + DA_TILE > 0x7FFFFFFFll) return cudaErrorInvalidValue;
   CUtensorMap mq, mc;
   if (!make_tmap_2d(&mq, true, qfull, LAT, (uint64_t)plan.B * HEADS, LAT * 2, 64, 64) ||
-      !make_tmap_2d(&mc, true, cache, LAT, (uint64_t)plan.B * cap, LAT * 2, 64, DA_TILE))
+      !make_tmap_2d(&mc, true, cache.base, LAT, (uint64_t)rows, LAT * 2, 64, DA_TILE))
     return cudaErrorInvalidValue;
   return launch_kernel(decode_attn_tc_kernel, dim3(plan.G), dim3(DA_THREADS), DA_SMEM, st, pdl,
-                       mq, mc, seq_lens, plan.B, cap, plan.G, plan.P, plan.K,
+                       mq, mc, seq_lens, plan.B, cache, plan.G, plan.P, plan.K,
                        scale * 1.4426950408889634f, o_part, ml_part, err);
 }
 

@@ -73,7 +73,8 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 
 __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
     const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
-    const __grid_constant__ CUtensorMap map_c, int T, int cap, const int* __restrict__ seq_lens,
+    const __grid_constant__ CUtensorMap map_c, int T, const CacheRef cache,
+    const int* __restrict__ seq_lens,
     float scale_log2,
     __nv_bfloat16* __restrict__ attn_out, uint8_t* __restrict__ o_hi, uint8_t* __restrict__ o_lo,
     float* __restrict__ o_sx, long kv_rows, int* err) {
@@ -158,7 +159,23 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
         const int k0 = j * PA_TILE;
         tma_load_3d(stg, &map_kv, &k_full[st], 0, h, kvr0 + k0);
         tma_load_3d(stg + PA_BOX, &map_kv, &k_full[st], 64, h, kvr0 + k0);
-        tma_load_2d(stg + 2 * PA_BOX, &map_c, &k_full[st], KV_LORA, b * cap + k0);
+        if (!cache.paged()) {
+          tma_load_2d(stg + 2 * PA_BOX, &map_c, &k_full[st], KV_LORA, b * cache.page + k0);
+        } else {
+          // Two 64-position boxes, each inside one page.  A block of real keys (before
+          // L + T) on an invalid page is flagged; every out-of-range block reads zeros past the
+          // pool (its keys, if any, are masked).
+          for (int hb = 0; hb < 2; ++hb) {
+            const int pos = k0 + 64 * hb;
+            long long r = cache.row(b, pos);
+            if (r < 0) {
+              if (pos < L + T) atomicExch(err, DEV_ERR_RANGE);
+              r = cache.rows(0);
+            }
+            tma_load_2d(stg + 2 * PA_BOX + hb * (PA_BOX / 2), &map_c, &k_full[st], KV_LORA,
+                        (int)r);
+          }
+        }
         issued = j + 1;
       }
       volatile int no_abort = 0;
@@ -473,7 +490,7 @@ cudaError_t init_prefill_tc_kernel() {
 }
 
 cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloat16* kv,
-                                        const __nv_bfloat16* cache, int cap, int B, int T,
+                                        const CacheRef& cache, int B, int T,
                                         const int* seq_lens, long kv_rows, float scale,
                                         __nv_bfloat16* attn_out, uint8_t* o_hi, uint8_t* o_lo,
                                         float* o_sx, int* err, cudaStream_t st) {
@@ -486,10 +503,12 @@ cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloa
   if (!make_tmap_3d(&mq, q, QHEAD, HEADS, M, QHEAD * 2, (uint64_t)HEADS * QHEAD * 2, 64, 1, 128) ||
       !make_tmap_3d(&mkv, kv, KVB_PER_HEAD, HEADS, (uint64_t)kv_rows, KVB_PER_HEAD * 2,
                     (uint64_t)HEADS * KVB_PER_HEAD * 2, 64, 1, 128) ||
-      !make_tmap_2d(&mc, true, cache, LAT, (uint64_t)B * cap, LAT * 2, 64, 128))
+      !make_tmap_2d(&mc, true, cache.base, LAT, (uint64_t)cache.rows(B), LAT * 2, 64,
+                    cache.paged() ? 64 : 128))
     return cudaErrorInvalidValue;
+  if (cache.rows(B) + PA_TILE > 0x7FFFFFFFll) return cudaErrorInvalidValue;
   const dim3 grid(HEADS, (T + PA_TILE - 1) / PA_TILE, B);
-  prefill_attn_tc_kernel<<<grid, PA_THREADS, PA_SMEM, st>>>(mq, mkv, mc, T, cap, seq_lens,
+  prefill_attn_tc_kernel<<<grid, PA_THREADS, PA_SMEM, st>>>(mq, mkv, mc, T, cache, seq_lens,
                                                             scale * 1.4426950408889634f, attn_out,
                                                             o_hi, o_lo, o_sx, kv_rows, err);
   return cudaGetLastError();

@@ -124,8 +124,8 @@ struct NormArgs {
   const float2* rope_tab;
   int pairing;
   const int* seq_lens;
-  __nv_bfloat16* cache;
-  int cap, limit;
+  CacheRef cache;
+  int limit;
   int* err;
 };
 
@@ -177,7 +177,9 @@ __global__ void __launch_bounds__(128) gemv_norm_qb_kernel(Proj P, NormArgs na) 
         row[c] = __float2bfloat16_rn(__bfloat162float(na.gkv[c]) * bf16r(xk[i] * rk));
       }
       const int pos = na.seq_lens[m];
-      const bool bad = pos < 0 || pos >= na.limit;
+      // positions past the cache or the RoPE table, or an invalid page: skipped and flagged
+      const long long crow = (pos < 0 || pos >= na.limit) ? -1 : na.cache.row(m, pos);
+      const bool bad = crow < 0;
       if (bad && tid == 0) atomicExch(na.err, DEV_ERR_RANGE);
       if (!bad && tid < ROPE / 2) {
         const int2 ij = na.pairing == 0 ? make_int2(2 * tid, 2 * tid + 1)
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(128) gemv_norm_qb_kernel(Proj P, NormArgs na) 
       }
       __syncthreads();
       if (!bad && tid < LAT / 8)
-        reinterpret_cast<uint4*>(na.cache + ((size_t)m * na.cap + pos) * LAT)[tid] =
+        reinterpret_cast<uint4*>(na.cache.base + (size_t)crow * LAT)[tid] =
             reinterpret_cast<const uint4*>(row)[tid];
       __syncthreads();
     }
@@ -296,10 +298,10 @@ bool gemm_can_advance(int M) { return M > 0; }
 
 cudaError_t launch_qb_norm(const float* g1, int M, const Proj& p, const __nv_bfloat16* gq,
                            const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
-                           int rope_pairing, const int* seq_lens, __nv_bfloat16* cache, int cap,
+                           int rope_pairing, const int* seq_lens, const CacheRef& cache,
                            int limit, int* err, cudaStream_t st, bool pdl) {
   if (M < 1 || M > 8 || p.N != QB_N || p.y_fp32) return cudaErrorInvalidValue;
-  const NormArgs na{g1, gq, gkv, eps, rope_tab, rope_pairing, seq_lens, cache, cap, limit, err};
+  const NormArgs na{g1, gq, gkv, eps, rope_tab, rope_pairing, seq_lens, cache, limit, err};
   const dim3 grid(p.N / 4 + 1), block(128);  // + the kv-cache CTA
   switch (M) {
     case 1: return launch_kernel(gemv_norm_qb_kernel<1>, grid, block, 0, st, pdl, p, na);

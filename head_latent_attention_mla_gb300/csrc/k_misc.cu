@@ -101,8 +101,7 @@ static_assert(NRC_QT + KV_LORA / 8 == 256, "one 8-value run per thread");
 __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
     const float* __restrict__ g1, int T, const __nv_bfloat16* __restrict__ gq,
     const __nv_bfloat16* __restrict__ gkv, float eps, const float2* __restrict__ rope_tab,
-    int pairing, const int* __restrict__ seq_lens, __nv_bfloat16* __restrict__ cache, int cap,
-    int limit, __nv_bfloat16* __restrict__ cq_out, __nv_bfloat16* __restrict__ ckv_out, int* err,
+    int pairing, const int* __restrict__ seq_lens, const CacheRef cache, int limit, __nv_bfloat16* __restrict__ cq_out, __nv_bfloat16* __restrict__ ckv_out, int* err,
     E4m3Split q_split, E4m3Split kv_split) {
   __shared__ float2 red[9], red2[9];
   __shared__ __align__(16) __nv_bfloat16 row[LAT];
@@ -166,7 +165,9 @@ __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
     }
   }
   const int pos = seq_lens[b] + t;
-  if (pos < 0 || pos >= limit) {  // device lengths past the cache or the RoPE table
+  // Device lengths past the cache or the RoPE table, or an invalid page: skipped and flagged.
+  const long long crow = (pos < 0 || pos >= limit) ? -1 : cache.row(b, pos);
+  if (crow < 0) {
     if (tid == 0) atomicExch(err, DEV_ERR_RANGE);
     return;
   }
@@ -179,9 +180,28 @@ __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
   }
   __syncthreads();
   if (tid < LAT / 8) {
-    uint4* dst = reinterpret_cast<uint4*>(cache + ((size_t)b * cap + pos) * LAT);
+    uint4* dst = reinterpret_cast<uint4*>(cache.base + (size_t)crow * LAT);
     dst[tid] = reinterpret_cast<const uint4*>(row)[tid];
   }
+}
+
+// Row t of sequence b's latents (its first KV_LORA cache values) to row r0(b) + t of out, with
+// r0(b) = sum over b' < b of (seq_lens[b'] + T): one CTA (64 threads, 16 bytes each) per row.
+__global__ void __launch_bounds__(KV_LORA / 8) gather_latent_kernel(
+    const CacheRef cache, const int* __restrict__ seq_lens, int T, long kv_rows,
+    __nv_bfloat16* __restrict__ out, int* err) {
+  const int t = blockIdx.x, b = blockIdx.y;
+  const int n = seq_lens[b] + T;
+  if (t >= n) return;
+  long r0 = 0;
+  for (int bb = 0; bb < b; ++bb) r0 += seq_lens[bb] + T;
+  const long long crow = cache.row(b, t);
+  if (r0 + n > kv_rows || crow < 0) {  // the host's layout or the block table is wrong
+    if (threadIdx.x == 0) atomicExch(err, crow < 0 ? DEV_ERR_RANGE : DEV_ERR_PLAN);
+    return;
+  }
+  const uint4 v = reinterpret_cast<const uint4*>(cache.base + (size_t)crow * LAT)[threadIdx.x];
+  reinterpret_cast<uint4*>(out + (size_t)(r0 + t) * KV_LORA)[threadIdx.x] = v;
 }
 
 // In-place RoPE of q's rotary slices.  One CTA per RQ_TOK tokens; eight threads per head,
@@ -425,15 +445,24 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ W, const float* __res
 
 cudaError_t launch_norm_rope_cache(const float* g1, int B, int T, const __nv_bfloat16* gq,
                                    const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
-                                   int rope_pairing, const int* seq_lens, __nv_bfloat16* cache,
-                                   int cap, int limit, __nv_bfloat16* cq_out,
+                                   int rope_pairing, const int* seq_lens, const CacheRef& cache,
+                                   int limit, __nv_bfloat16* cq_out,
                                    __nv_bfloat16* ckv_out, int* err, cudaStream_t st, bool pdl,
                                    const E4m3Split* q_split, const E4m3Split* kv_split) {
   if (B * T == 0) return cudaSuccess;
   const E4m3Split none{nullptr, nullptr, nullptr};
   return launch_kernel(norm_rope_cache_kernel, dim3(B * T), dim3(256), 0, st, pdl, g1, T, gq, gkv,
-                       eps, rope_tab, rope_pairing, seq_lens, cache, cap, limit, cq_out, ckv_out,
+                       eps, rope_tab, rope_pairing, seq_lens, cache, limit, cq_out, ckv_out,
                        err, q_split ? *q_split : none, kv_split ? *kv_split : none);
+}
+
+cudaError_t launch_gather_latent(const CacheRef& cache, const int* seq_lens, int B, int T,
+                                 int max_len, long kv_rows, __nv_bfloat16* out, int* err,
+                                 cudaStream_t st) {
+  if (B * T == 0 || max_len <= 0) return cudaSuccess;
+  gather_latent_kernel<<<dim3(max_len, B), KV_LORA / 8, 0, st>>>(cache, seq_lens, T, kv_rows,
+                                                                 out, err);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_rope_q(__nv_bfloat16* q, int B, int T, const float2* rope_tab,

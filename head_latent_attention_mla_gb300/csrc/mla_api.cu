@@ -29,7 +29,7 @@ bool ready(const mla_ctx* c) {
 // Workspace regions (byte offsets into the caller's buffer).
 struct Layout {
   size_t g1 = 0, cq = 0, cq_sx = 0, ckv = 0, ckv_sx = 0, q = 0, kv = 0, attn = 0, attn_sx = 0,
-         qfull = 0, opart = 0, ml = 0, olat = 0, gpart = 0, total = 0;
+         qfull = 0, opart = 0, ml = 0, olat = 0, gpart = 0, gather = 0, total = 0;
 };
 
 // Largest split-K partial buffer of the projections of one call with M token rows.
@@ -47,7 +47,9 @@ int items_max(const mla_ctx* c, int B) { return 2 * c->num_sms + B; }
 
 // Prefill / cache-append workspace for M new tokens.  kv_rows: rows of the rebuilt keys and
 // values (M over an empty cache; the sum of L_b + T with cached positions); kvb_M: the largest
-// per-sequence kv_b_proj over cache rows (0 when the cache is empty).
+// per-sequence kv_b_proj over cache rows (0 when the cache is empty).  With cached positions
+// the layout also holds the latents of all kv_rows gathered from a paged cache (and the
+// GEMM scratch of one kv_b_proj over all of them).
 Layout prefill_layout(long M, int num_sms, long kv_rows = -1, long kvb_M = 0) {
   Layout L;
   if (kv_rows < 0) kv_rows = M;
@@ -64,8 +66,11 @@ Layout prefill_layout(long M, int num_sms, long kv_rows = -1, long kvb_M = 0) {
   L.attn_sx = take((size_t)M * HEADS * 4);
   size_t gp = gemm_partials(M, num_sms);
   if (kvb_M > 0) {
-    const size_t k = gemm_partial_bytes((int)kvb_M, KVB_N, KV_LORA, num_sms);
+    size_t k = gemm_partial_bytes((int)kvb_M, KVB_N, KV_LORA, num_sms);
     gp = k > gp ? k : gp;
+    k = gemm_partial_bytes((int)kv_rows, KVB_N, KV_LORA, num_sms);
+    gp = k > gp ? k : gp;
+    L.gather = take((size_t)kv_rows * KV_LORA * 2);
   }
   L.gpart = take(gp);
   L.total = off;
@@ -119,9 +124,9 @@ void log_reset(mla_ctx* c) {
   } while (0)
 
 // Common checks of the token calls.  Lengths come from the host copy.
-mla_status check_tokens(const mla_ctx* c, const void* x, int B, int T, const void* cache, int cap,
-                        const int* lens_dev, const int* lens_host, void* ws, size_t ws_bytes,
-                        size_t need) {
+mla_status check_tokens(const mla_ctx* c, const void* x, int B, int T, const void* cache,
+                        long long cap, const int* lens_dev, const int* lens_host, void* ws,
+                        size_t ws_bytes, size_t need) {
   if (!c) return MLA_ERR_INVALID_ARG;
   if (B < 0 || T < 0 || cap < 0) return MLA_ERR_INVALID_ARG;
   if (B == 0 || T == 0) return MLA_OK;
@@ -131,7 +136,7 @@ mla_status check_tokens(const mla_ctx* c, const void* x, int B, int T, const voi
   if (ws_bytes < need) return MLA_ERR_INVALID_ARG;
   for (int b = 0; b < B; ++b) {
     if (lens_host[b] < 0) return MLA_ERR_INVALID_ARG;
-    if ((long)lens_host[b] + T > cap || (long)lens_host[b] + T > c->cfg.max_positions)
+    if ((long long)lens_host[b] + T > cap || (long)lens_host[b] + T > c->cfg.max_positions)
       return MLA_ERR_CAPACITY;
   }
   return MLA_OK;
@@ -168,6 +173,243 @@ void rope_frequencies(const mla_config& cfg, double* w, double* gain) {
   }
   *gain = yarn_temperature(cfg.yarn_factor, cfg.yarn_mscale) /
           yarn_temperature(cfg.yarn_factor, cfg.yarn_mscale_all_dim);
+}
+
+// Positions allowed in a call: inside the cache and the RoPE table.
+int limit_of(const mla_ctx* c, const CacheRef& CR) {
+  const long long cap = CR.capacity();
+  return cap < c->cfg.max_positions ? (int)cap : c->cfg.max_positions;
+}
+
+// The paged cache descriptor as a CacheRef, or MLA_ERR_INVALID_ARG.
+mla_status paged_ref(const mla_paged_cache* pc, CacheRef* out) {
+  if (!pc || !pc->pool || !pc->block_table || !aligned16(pc->pool) ||
+      (reinterpret_cast<uintptr_t>(pc->block_table) & 3u))
+    return MLA_ERR_INVALID_ARG;
+  if (pc->page_size <= 0 || pc->page_size % 64 != 0 || pc->num_pages <= 0 || pc->max_pages <= 0)
+    return MLA_ERR_INVALID_ARG;
+  // Pool rows and positions must stay within the 32-bit coordinates of the tile copies.
+  if ((long long)pc->num_pages * pc->page_size > 0x7FFFFFFFll - 256 ||
+      (long long)pc->max_pages * pc->page_size > 0x7FFFFFFFll)
+    return MLA_ERR_INVALID_ARG;
+  *out = CacheRef{static_cast<__nv_bfloat16*>(pc->pool), pc->page_size, pc->block_table,
+                  pc->max_pages, pc->num_pages};
+  return MLA_OK;
+}
+
+mla_status cache_append_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef& CR,
+                             int* lens_dev, const int* lens_host, void* ws, size_t ws_bytes,
+                             void* stream) {
+  const Layout L = prefill_layout((long)B * T, c ? c->num_sms : 0);
+  mla_status st = check_tokens(c, x, B, T, CR.base, CR.capacity(), lens_dev, lens_host, ws,
+                               ws_bytes, L.total);
+  if (st != MLA_OK || B == 0 || T == 0) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  log_reset(c);
+  const int M = B * T, limit = limit_of(c, CR);
+  float* g1 = at<float>(ws, L.g1);
+  Proj p{c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1};
+  MLA_LAUNCH("gemm_kv_a", launch_gemm(static_cast<const __nv_bfloat16*>(x), HIDDEN, M, HIDDEN, &p, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+  MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
+                                    c->cfg.rope_pairing, lens_dev, CR, limit, nullptr,
+                                    nullptr, c->d_err, s));
+  MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, T, s));
+  return MLA_OK;
+}
+
+mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef& CR,
+                        int* lens_dev, const int* lens_host, void* out, void* ws,
+                        size_t ws_bytes, void* stream) {
+  // Cached positions before the call (chunked prefill when any is non-zero): the rebuilt keys
+  // and values then cover L_b + T rows per sequence.
+  long kv_rows = 0, kvb_M = 0;
+  bool chunked = false;
+  for (int b = 0; lens_host && b < B && B > 0 && T > 0; ++b) {
+    if (lens_host[b] < 0) break;  // rejected by check_tokens below
+    kv_rows += (long)lens_host[b] + T;
+    kvb_M = (long)lens_host[b] + T > kvb_M ? (long)lens_host[b] + T : kvb_M;
+    chunked = chunked || lens_host[b] != 0;
+  }
+  const Layout L = prefill_layout((long)B * T, c ? c->num_sms : 0, chunked ? kv_rows : -1,
+                                  chunked ? kvb_M : 0);
+  mla_status st = check_tokens(c, x, B, T, CR.base, CR.capacity(), lens_dev, lens_host, ws,
+                               ws_bytes, L.total);
+  if (st != MLA_OK || B == 0 || T == 0) return st;
+  if (!out || !aligned16(out) || out == x) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  log_reset(c);
+  const int M = B * T, limit = limit_of(c, CR);
+  const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(x);
+  float* g1 = at<float>(ws, L.g1);
+  __nv_bfloat16* cq = at<__nv_bfloat16>(ws, L.cq);
+  __nv_bfloat16* ckv = at<__nv_bfloat16>(ws, L.ckv);
+  __nv_bfloat16* q = at<__nv_bfloat16>(ws, L.q);
+  __nv_bfloat16* kv = at<__nv_bfloat16>(ws, L.kv);
+  __nv_bfloat16* attn = at<__nv_bfloat16>(ws, L.attn);
+
+  Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
+                {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
+  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, M, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+  Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
+  Proj p3{c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], KVB_N, kv, KVB_N, 0};
+  if (chunked) {
+    // Keys and values of the cached and the new positions: kv_b_proj over each sequence's
+    // cache rows 0 .. L_b + T - 1 (the first 512 values of a row are its normalised latent),
+    // after the norm kernel has appended the new rows.
+    const E4m3Split qsp{at<uint8_t>(ws, L.cq), at<uint8_t>(ws, L.cq) + (size_t)M * Q_LORA,
+                        at<float>(ws, L.cq_sx)};
+    MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
+                                      c->cfg.rope_pairing, lens_dev, CR, limit, M > kGemvMaxM ? nullptr : cq,
+                                      nullptr, c->d_err, s, false, M > kGemvMaxM ? &qsp : nullptr, nullptr));
+    if (M > kGemvMaxM) {
+      MLA_LAUNCH("gemm_q_b", launch_gemm_tc_split(qsp.hi, qsp.lo, qsp.sx, false, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+    } else {
+      MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+    }
+    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
+    if (CR.paged()) {
+      // The cached latents are scattered over pages: gather all sequences' rows 0..L_b+T-1
+      // back to back, then one kv_b_proj over them.
+      __nv_bfloat16* lat = at<__nv_bfloat16>(ws, L.gather);
+      MLA_LAUNCH("gather_latent", launch_gather_latent(CR, lens_dev, B, T, (int)kvb_M, kv_rows, lat,
+                                                       c->d_err, s));
+      MLA_LAUNCH("gemm_kv_b", launch_gemm(lat, KV_LORA, (int)kv_rows, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+    } else {
+      long r0 = 0;
+      for (int b = 0; b < B; ++b) {
+        const int Mb = lens_host[b] + T;
+        const Proj pb{c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], KVB_N, kv + (size_t)r0 * KVB_N, KVB_N, 0};
+        MLA_LAUNCH("gemm_kv_b", launch_gemm(CR.base + (size_t)b * CR.page * LAT, LAT, Mb, KV_LORA, &pb, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+        r0 += Mb;
+      }
+    }
+  } else if (M > kGemvMaxM) {
+    // Tensor-core projections: the norm kernel writes q_b's and kv_b's e4m3 inputs itself (the
+    // two terms share the bf16 latents' regions; one scale per token).
+    const E4m3Split qsp{at<uint8_t>(ws, L.cq), at<uint8_t>(ws, L.cq) + (size_t)M * Q_LORA,
+                        at<float>(ws, L.cq_sx)};
+    const E4m3Split kvsp{at<uint8_t>(ws, L.ckv), at<uint8_t>(ws, L.ckv) + (size_t)M * KV_LORA,
+                         at<float>(ws, L.ckv_sx)};
+    MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
+                                      c->cfg.rope_pairing, lens_dev, CR, limit, nullptr, nullptr,
+                                      c->d_err, s, false, &qsp, &kvsp));
+    MLA_LAUNCH("gemm_q_b", launch_gemm_tc_split(qsp.hi, qsp.lo, qsp.sx, false, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
+    MLA_LAUNCH("gemm_kv_b", launch_gemm_tc_split(kvsp.hi, kvsp.lo, kvsp.sx, false, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+  } else {
+    MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
+                                      c->cfg.rope_pairing, lens_dev, CR, limit, cq, ckv,
+                                      c->d_err, s));
+    MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
+    MLA_LAUNCH("gemm_kv_b", launch_gemm(ckv, KV_LORA, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+  }
+  Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
+  if (gemm_takes_split_blocks(M)) {
+    // The attention writes o_proj's e4m3 input itself (one scale per token and head).
+    uint8_t* a_hi = at<uint8_t>(ws, L.attn);
+    uint8_t* a_lo = a_hi + (size_t)M * O_IN;
+    float* a_sx = at<float>(ws, L.attn_sx);
+    MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, CR, B, T, chunked ? lens_dev : nullptr,
+                                                              chunked ? kv_rows : M, c->cfg.softmax_scale, nullptr,
+                                                              a_hi, a_lo, a_sx, c->d_err, s));
+    MLA_LAUNCH("gemm_o", launch_gemm_tc_split(a_hi, a_lo, a_sx, true, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
+                                              lens_dev, B, T));
+  } else {
+    MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, CR, B, T, chunked ? lens_dev : nullptr,
+                                                              chunked ? kv_rows : M, c->cfg.softmax_scale, attn,
+                                                              nullptr, nullptr, nullptr, c->d_err, s));
+    if (gemm_can_advance(M) && B <= 128) {  // the length update rides on o_proj
+      MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
+                                       lens_dev, B, T));
+    } else {
+      MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+      MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, T, s));
+    }
+  }
+  return MLA_OK;
+}
+
+mla_status decode_impl(mla_ctx* c, const void* x, int B, const CacheRef& CR, int* lens_dev,
+                       const int* lens_host, void* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!c) return MLA_ERR_INVALID_ARG;
+  const Layout L = decode_layout(c, B < 0 ? 0 : B);
+  mla_status st = check_tokens(c, x, B, 1, CR.base, CR.capacity(), lens_dev, lens_host, ws,
+                               ws_bytes, L.total);
+  if (st != MLA_OK || B == 0) return st;
+  if (!out || !aligned16(out) || out == x) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  log_reset(c);
+  const int limit = limit_of(c, CR);
+  const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(x);
+
+  // Every kernel after the first is launched with programmatic dependent launch: it may start
+  // (and fetch its weights) while its predecessor finishes, and waits for the predecessor's
+  // results before reading them.
+  // Split-KV schedule: the positions of all sequences cut into about one equal share per SM.
+  long long total = 0;
+  for (int b = 0; b < B; ++b) total += (long long)lens_host[b] + 1;
+  const DecodePlan plan = make_decode_plan(B, total, c->num_sms, items_max(c, B));
+
+  float* g1 = at<float>(ws, L.g1);
+  __nv_bfloat16* cq = at<__nv_bfloat16>(ws, L.cq);
+  __nv_bfloat16* q = at<__nv_bfloat16>(ws, L.q);
+  __nv_bfloat16* qfull = at<__nv_bfloat16>(ws, L.qfull);
+  __half* opart = at<__half>(ws, L.opart);
+  float* ml = at<float>(ws, L.ml);
+  __nv_bfloat16* olat = at<__nv_bfloat16>(ws, L.olat);
+  __nv_bfloat16* attn = at<__nv_bfloat16>(ws, L.attn);
+
+  Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
+                {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
+  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+  if (B <= 2) {
+    // One or two sequences: six kernels.  q_b_proj normalises the q latent itself (and one of
+    // its CTAs appends the cache rows); the combine is fused with the W_UV absorption; the
+    // length update rides on o_proj.  (Every q_b CTA normalises every token, and every
+    // (head, sequence) CTA reads its head's W_UV: both pay only for very few sequences.)
+    Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
+    MLA_LAUNCH("gemm_q_b_norm", launch_qb_norm(g1, B, p2, c->gain[0], c->gain[1], c->cfg.eps,
+                                               c->rope_tab, c->cfg.rope_pairing, lens_dev, CR,
+                                               limit, c->d_err, s, true));
+    MLA_LAUNCH("absorb_q", launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
+                                           c->cfg.rope_pairing, lens_dev, limit, qfull, s, true));
+    MLA_LAUNCH("decode_attention", launch_decode_attention_tc(qfull, CR, lens_dev, plan,
+                                                              c->cfg.softmax_scale, opart, ml,
+                                                              c->d_err, s, true));
+    MLA_LAUNCH("combine_absorb_out",
+               launch_combine_absorb_out(lens_dev, lens_host, plan, opart, ml, c->W[MLA_W_KV_B],
+                                         c->S[MLA_W_KV_B], attn, c->d_err, s, true));
+    Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
+    MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
+                                     c->num_sms, c->d_err, s, lens_dev, B, 1, true));
+    return MLA_OK;
+  }
+  MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, 1, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
+                                    c->cfg.rope_pairing, lens_dev, CR, limit, cq, nullptr,
+                                    c->d_err, s, true));
+  Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
+  MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, B, Q_LORA, &p2, 1, at<float>(ws, L.gpart),
+                                     c->num_sms, c->d_err, s, nullptr, 0, 0, true));
+  MLA_LAUNCH("absorb_q", launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
+                             c->cfg.rope_pairing, lens_dev, limit, qfull, s, true));
+  MLA_LAUNCH("decode_attention", launch_decode_attention_tc(qfull, CR, lens_dev, plan,
+                                                            c->cfg.softmax_scale, opart, ml,
+                                                            c->d_err, s, true));
+  MLA_LAUNCH("decode_combine", launch_decode_combine(lens_dev, plan, opart, ml, olat, c->d_err, s,
+                                                         true));
+  MLA_LAUNCH("absorb_out", launch_absorb_out(olat, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], attn, s,
+                                                 true));
+  Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
+  if (gemm_can_advance(B)) {  // the length update rides on the last kernel
+    MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
+                                     c->num_sms, c->d_err, s, lens_dev, B, 1, true));
+  } else {
+    MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
+                                     c->num_sms, c->d_err, s, nullptr, 0, 0, true));
+    MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, 1, s));
+  }
+  return MLA_OK;
 }
 
 }  // namespace
@@ -331,209 +573,49 @@ size_t mla_workspace_bytes(const mla_ctx* c, int B, int T) {
 mla_status mla_cache_append(mla_ctx* c, const void* x, int B, int T, void* cache, int cap,
                             int* lens_dev, const int* lens_host, void* ws, size_t ws_bytes,
                             void* stream) {
-  const Layout L = prefill_layout((long)B * T, c ? c->num_sms : 0);
-  mla_status st = check_tokens(c, x, B, T, cache, cap, lens_dev, lens_host, ws, ws_bytes, L.total);
-  if (st != MLA_OK || B == 0 || T == 0) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  log_reset(c);
-  const int M = B * T, limit = cap < c->cfg.max_positions ? cap : c->cfg.max_positions;
-  float* g1 = at<float>(ws, L.g1);
-  Proj p{c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1};
-  MLA_LAUNCH("gemm_kv_a", launch_gemm(static_cast<const __nv_bfloat16*>(x), HIDDEN, M, HIDDEN, &p, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-  MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
-                                    c->cfg.rope_pairing, lens_dev,
-                                    static_cast<__nv_bfloat16*>(cache), cap, limit, nullptr,
-                                    nullptr, c->d_err, s));
-  MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, T, s));
-  return MLA_OK;
+  return cache_append_impl(c, x, B, T, dense_cache(cache, cap), lens_dev, lens_host, ws, ws_bytes,
+                           stream);
 }
 
 mla_status mla_prefill(mla_ctx* c, const void* x, int B, int T, void* cache, int cap,
                        int* lens_dev, const int* lens_host, void* out, void* ws,
                        size_t ws_bytes, void* stream) {
-  // Cached positions before the call (chunked prefill when any is non-zero): the rebuilt keys
-  // and values then cover L_b + T rows per sequence.
-  long kv_rows = 0, kvb_M = 0;
-  bool chunked = false;
-  for (int b = 0; lens_host && b < B && B > 0 && T > 0; ++b) {
-    if (lens_host[b] < 0) break;  // rejected by check_tokens below
-    kv_rows += (long)lens_host[b] + T;
-    kvb_M = (long)lens_host[b] + T > kvb_M ? (long)lens_host[b] + T : kvb_M;
-    chunked = chunked || lens_host[b] != 0;
-  }
-  const Layout L = prefill_layout((long)B * T, c ? c->num_sms : 0, chunked ? kv_rows : -1,
-                                  chunked ? kvb_M : 0);
-  mla_status st = check_tokens(c, x, B, T, cache, cap, lens_dev, lens_host, ws, ws_bytes, L.total);
-  if (st != MLA_OK || B == 0 || T == 0) return st;
-  if (!out || !aligned16(out) || out == x) return MLA_ERR_INVALID_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  log_reset(c);
-  const int M = B * T, limit = cap < c->cfg.max_positions ? cap : c->cfg.max_positions;
-  const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(x);
-  __nv_bfloat16* C = static_cast<__nv_bfloat16*>(cache);
-  float* g1 = at<float>(ws, L.g1);
-  __nv_bfloat16* cq = at<__nv_bfloat16>(ws, L.cq);
-  __nv_bfloat16* ckv = at<__nv_bfloat16>(ws, L.ckv);
-  __nv_bfloat16* q = at<__nv_bfloat16>(ws, L.q);
-  __nv_bfloat16* kv = at<__nv_bfloat16>(ws, L.kv);
-  __nv_bfloat16* attn = at<__nv_bfloat16>(ws, L.attn);
-
-  Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
-                {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
-  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, M, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-  Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
-  Proj p3{c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], KVB_N, kv, KVB_N, 0};
-  if (chunked) {
-    // Keys and values of the cached and the new positions: kv_b_proj over each sequence's
-    // cache rows 0 .. L_b + T - 1 (the first 512 values of a row are its normalised latent),
-    // after the norm kernel has appended the new rows.
-    const E4m3Split qsp{at<uint8_t>(ws, L.cq), at<uint8_t>(ws, L.cq) + (size_t)M * Q_LORA,
-                        at<float>(ws, L.cq_sx)};
-    MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
-                                      c->cfg.rope_pairing, lens_dev, C, cap, limit, M > kGemvMaxM ? nullptr : cq,
-                                      nullptr, c->d_err, s, false, M > kGemvMaxM ? &qsp : nullptr, nullptr));
-    if (M > kGemvMaxM) {
-      MLA_LAUNCH("gemm_q_b", launch_gemm_tc_split(qsp.hi, qsp.lo, qsp.sx, false, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-    } else {
-      MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-    }
-    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
-    long r0 = 0;
-    for (int b = 0; b < B; ++b) {
-      const int Mb = lens_host[b] + T;
-      const Proj pb{c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], KVB_N, kv + (size_t)r0 * KVB_N, KVB_N, 0};
-      MLA_LAUNCH("gemm_kv_b", launch_gemm(C + (size_t)b * cap * LAT, LAT, Mb, KV_LORA, &pb, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-      r0 += Mb;
-    }
-  } else if (M > kGemvMaxM) {
-    // Tensor-core projections: the norm kernel writes q_b's and kv_b's e4m3 inputs itself (the
-    // two terms share the bf16 latents' regions; one scale per token).
-    const E4m3Split qsp{at<uint8_t>(ws, L.cq), at<uint8_t>(ws, L.cq) + (size_t)M * Q_LORA,
-                        at<float>(ws, L.cq_sx)};
-    const E4m3Split kvsp{at<uint8_t>(ws, L.ckv), at<uint8_t>(ws, L.ckv) + (size_t)M * KV_LORA,
-                         at<float>(ws, L.ckv_sx)};
-    MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
-                                      c->cfg.rope_pairing, lens_dev, C, cap, limit, nullptr, nullptr,
-                                      c->d_err, s, false, &qsp, &kvsp));
-    MLA_LAUNCH("gemm_q_b", launch_gemm_tc_split(qsp.hi, qsp.lo, qsp.sx, false, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
-    MLA_LAUNCH("gemm_kv_b", launch_gemm_tc_split(kvsp.hi, kvsp.lo, kvsp.sx, false, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-  } else {
-    MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
-                                      c->cfg.rope_pairing, lens_dev, C, cap, limit, cq, ckv,
-                                      c->d_err, s));
-    MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
-    MLA_LAUNCH("gemm_kv_b", launch_gemm(ckv, KV_LORA, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-  }
-  Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
-  if (gemm_takes_split_blocks(M)) {
-    // The attention writes o_proj's e4m3 input itself (one scale per token and head).
-    uint8_t* a_hi = at<uint8_t>(ws, L.attn);
-    uint8_t* a_lo = a_hi + (size_t)M * O_IN;
-    float* a_sx = at<float>(ws, L.attn_sx);
-    MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, C, cap, B, T, chunked ? lens_dev : nullptr,
-                                                              chunked ? kv_rows : M, c->cfg.softmax_scale, nullptr,
-                                                              a_hi, a_lo, a_sx, c->d_err, s));
-    MLA_LAUNCH("gemm_o", launch_gemm_tc_split(a_hi, a_lo, a_sx, true, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
-                                              lens_dev, B, T));
-  } else {
-    MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, C, cap, B, T, chunked ? lens_dev : nullptr,
-                                                              chunked ? kv_rows : M, c->cfg.softmax_scale, attn,
-                                                              nullptr, nullptr, nullptr, c->d_err, s));
-    if (gemm_can_advance(M) && B <= 128) {  // the length update rides on o_proj
-      MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
-                                       lens_dev, B, T));
-    } else {
-      MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-      MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, T, s));
-    }
-  }
-  return MLA_OK;
+  return prefill_impl(c, x, B, T, dense_cache(cache, cap), lens_dev, lens_host, out, ws,
+                      ws_bytes, stream);
 }
 
 mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, int* lens_dev,
                       const int* lens_host, void* out, void* ws, size_t ws_bytes, void* stream) {
-  if (!c) return MLA_ERR_INVALID_ARG;
-  const Layout L = decode_layout(c, B < 0 ? 0 : B);
-  mla_status st = check_tokens(c, x, B, 1, cache, cap, lens_dev, lens_host, ws, ws_bytes, L.total);
-  if (st != MLA_OK || B == 0) return st;
-  if (!out || !aligned16(out) || out == x) return MLA_ERR_INVALID_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  log_reset(c);
-  const int limit = cap < c->cfg.max_positions ? cap : c->cfg.max_positions;
-  const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(x);
-  __nv_bfloat16* C = static_cast<__nv_bfloat16*>(cache);
-
-  // Every kernel after the first is launched with programmatic dependent launch: it may start
-  // (and fetch its weights) while its predecessor finishes, and waits for the predecessor's
-  // results before reading them.
-  // Split-KV schedule: the positions of all sequences cut into about one equal share per SM.
-  long long total = 0;
-  for (int b = 0; b < B; ++b) total += (long long)lens_host[b] + 1;
-  const DecodePlan plan = make_decode_plan(B, total, c->num_sms, items_max(c, B));
-
-  float* g1 = at<float>(ws, L.g1);
-  __nv_bfloat16* cq = at<__nv_bfloat16>(ws, L.cq);
-  __nv_bfloat16* q = at<__nv_bfloat16>(ws, L.q);
-  __nv_bfloat16* qfull = at<__nv_bfloat16>(ws, L.qfull);
-  __half* opart = at<__half>(ws, L.opart);
-  float* ml = at<float>(ws, L.ml);
-  __nv_bfloat16* olat = at<__nv_bfloat16>(ws, L.olat);
-  __nv_bfloat16* attn = at<__nv_bfloat16>(ws, L.attn);
-
-  Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
-                {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
-  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-  if (B <= 2) {
-    // One or two sequences: six kernels.  q_b_proj normalises the q latent itself (and one of
-    // its CTAs appends the cache rows); the combine is fused with the W_UV absorption; the
-    // length update rides on o_proj.  (Every q_b CTA normalises every token, and every
-    // (head, sequence) CTA reads its head's W_UV: both pay only for very few sequences.)
-    Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
-    MLA_LAUNCH("gemm_q_b_norm", launch_qb_norm(g1, B, p2, c->gain[0], c->gain[1], c->cfg.eps,
-                                               c->rope_tab, c->cfg.rope_pairing, lens_dev, C, cap,
-                                               limit, c->d_err, s, true));
-    MLA_LAUNCH("absorb_q", launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
-                                           c->cfg.rope_pairing, lens_dev, limit, qfull, s, true));
-    MLA_LAUNCH("decode_attention", launch_decode_attention_tc(qfull, C, cap, lens_dev, plan,
-                                                              c->cfg.softmax_scale, opart, ml,
-                                                              c->d_err, s, true));
-    MLA_LAUNCH("combine_absorb_out",
-               launch_combine_absorb_out(lens_dev, lens_host, plan, opart, ml, c->W[MLA_W_KV_B],
-                                         c->S[MLA_W_KV_B], attn, c->d_err, s, true));
-    Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
-    MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
-                                     c->num_sms, c->d_err, s, lens_dev, B, 1, true));
-    return MLA_OK;
-  }
-  MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, 1, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
-                                    c->cfg.rope_pairing, lens_dev, C, cap, limit, cq, nullptr,
-                                    c->d_err, s, true));
-  Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
-  MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, B, Q_LORA, &p2, 1, at<float>(ws, L.gpart),
-                                     c->num_sms, c->d_err, s, nullptr, 0, 0, true));
-  MLA_LAUNCH("absorb_q", launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
-                             c->cfg.rope_pairing, lens_dev, limit, qfull, s, true));
-  MLA_LAUNCH("decode_attention", launch_decode_attention_tc(qfull, C, cap, lens_dev, plan,
-                                                            c->cfg.softmax_scale, opart, ml,
-                                                            c->d_err, s, true));
-  MLA_LAUNCH("decode_combine", launch_decode_combine(lens_dev, plan, opart, ml, olat, c->d_err, s,
-                                                         true));
-  MLA_LAUNCH("absorb_out", launch_absorb_out(olat, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], attn, s,
-                                                 true));
-  Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
-  if (gemm_can_advance(B)) {  // the length update rides on the last kernel
-    MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
-                                     c->num_sms, c->d_err, s, lens_dev, B, 1, true));
-  } else {
-    MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
-                                     c->num_sms, c->d_err, s, nullptr, 0, 0, true));
-    MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, 1, s));
-  }
-  return MLA_OK;
+  return decode_impl(c, x, B, dense_cache(cache, cap), lens_dev, lens_host, out, ws, ws_bytes,
+                     stream);
 }
 
+mla_status mla_cache_append_paged(mla_ctx* c, const void* x, int B, int T,
+                                  const mla_paged_cache* cache, int* lens_dev,
+                                  const int* lens_host, void* ws, size_t ws_bytes, void* stream) {
+  CacheRef cr;
+  const mla_status st = paged_ref(cache, &cr);
+  if (st != MLA_OK) return st;
+  return cache_append_impl(c, x, B, T, cr, lens_dev, lens_host, ws, ws_bytes, stream);
+}
+
+mla_status mla_prefill_paged(mla_ctx* c, const void* x, int B, int T, const mla_paged_cache* cache,
+                             int* lens_dev, const int* lens_host, void* out, void* ws,
+                             size_t ws_bytes, void* stream) {
+  CacheRef cr;
+  const mla_status st = paged_ref(cache, &cr);
+  if (st != MLA_OK) return st;
+  return prefill_impl(c, x, B, T, cr, lens_dev, lens_host, out, ws, ws_bytes, stream);
+}
+
+mla_status mla_decode_paged(mla_ctx* c, const void* x, int B, const mla_paged_cache* cache,
+                            int* lens_dev, const int* lens_host, void* out, void* ws,
+                            size_t ws_bytes, void* stream) {
+  CacheRef cr;
+  const mla_status st = paged_ref(cache, &cr);
+  if (st != MLA_OK) return st;
+  return decode_impl(c, x, B, cr, lens_dev, lens_host, out, ws, ws_bytes, stream);
+}
 mla_status mla_dequant_weight(mla_ctx* c, int which, float* out, void* stream) {
   if (!c || which < 0 || which > 4 || !out) return MLA_ERR_INVALID_ARG;
   if (!c->W[which]) return MLA_ERR_STATE;

@@ -58,9 +58,42 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
 
 // Device error word values (read back by mla_get_device_status).
 constexpr int DEV_ERR_NONE = 0;
-constexpr int DEV_ERR_RANGE = 1;    // a cache position outside [0, cap) was skipped
+constexpr int DEV_ERR_RANGE = 1;    // a cache position outside the cache (or an invalid page)
 constexpr int DEV_ERR_TIMEOUT = 2;  // a bounded wait gave up
 constexpr int DEV_ERR_PLAN = 3;     // device lengths disagree with the host schedule
+
+// Where position `pos` of sequence `b` lives in the latent cache (rows of LAT bf16 values).
+//   dense (table == nullptr): an array [B, page, LAT]; row b * page + pos.
+//   paged: a pool [num_pages, page, LAT] of pages of `page` positions (a multiple of 64, so a
+//          64-position tile never crosses a page) and a block table [B, max_pages] of pool
+//          pages; row table[b][pos / page] * page + pos % page.
+// row() returns -1 for a logical page outside the table or a pool page outside the pool.
+struct CacheRef {
+  __nv_bfloat16* base;
+  int page;              // dense: positions per sequence (the capacity); paged: per page
+  const int* table;      // paged: device int32 [B, max_pages]; dense: nullptr
+  int max_pages;
+  int num_pages;
+  __host__ __device__ bool paged() const { return table != nullptr; }
+  __host__ __device__ long long capacity() const {
+    return paged() ? (long long)page * max_pages : (long long)page;
+  }
+  // Rows of the array a tensor map covers (B sequences of a dense cache, or the pool).
+  __host__ __device__ long long rows(int B) const {
+    return paged() ? (long long)num_pages * page : (long long)B * page;
+  }
+  __device__ __forceinline__ long long row(int b, int pos) const {
+    if (!paged()) return (long long)b * page + pos;
+    const int lp = pos / page;
+    if (pos < 0 || lp >= max_pages) return -1;
+    const int pg = __ldg(table + (size_t)b * max_pages + lp);
+    if (pg < 0 || pg >= num_pages) return -1;
+    return (long long)pg * page + pos % page;
+  }
+};
+inline CacheRef dense_cache(void* base, int cap) {
+  return CacheRef{static_cast<__nv_bfloat16*>(base), cap, nullptr, 0, 0};
+}
 
 // One FP8 block-scaled projection: Y[m, n] = sum_k X[m, k] * W[n, k] * S[n/128][k/128].
 struct Proj {
@@ -165,8 +198,8 @@ struct E4m3Split {
 };
 cudaError_t launch_norm_rope_cache(const float* g1, int B, int T, const __nv_bfloat16* gq,
                                    const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
-                                   int rope_pairing, const int* seq_lens, __nv_bfloat16* cache,
-                                   int cap, int limit, __nv_bfloat16* cq_out,
+                                   int rope_pairing, const int* seq_lens, const CacheRef& cache,
+                                   int limit, __nv_bfloat16* cq_out,
                                    __nv_bfloat16* ckv_out, int* err, cudaStream_t st,
                                    bool pdl = false, const E4m3Split* q_split = nullptr,
                                    const E4m3Split* kv_split = nullptr);
@@ -226,7 +259,7 @@ cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const __
 // head and sequence), and q_b_proj fused with the q-latent norm plus the kv cache-row append.
 cudaError_t launch_qb_norm(const float* g1, int M, const Proj& p, const __nv_bfloat16* gq,
                            const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
-                           int rope_pairing, const int* seq_lens, __nv_bfloat16* cache, int cap,
+                           int rope_pairing, const int* seq_lens, const CacheRef& cache,
                            int limit, int* err, cudaStream_t st, bool pdl = false);
 cudaError_t launch_combine_absorb_out(const int* seq_lens, const int* lens_host,
                                       DecodePlan plan, const __half* o_part,
@@ -236,8 +269,11 @@ cudaError_t launch_combine_absorb_out(const int* seq_lens, const int* lens_host,
 
 // Split-KV decode attention over the latent cache on the tcgen05 tensor cores (TMA-fed,
 // accumulators in tensor memory): per work item, unnormalised partial outputs and (m, l).
-cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const __nv_bfloat16* cache,
-                                       int cap, const int* seq_lens, DecodePlan plan,
+// Each sequence's share is read in 64-position tiles that start at multiples of 64 within
+// the sequence (positions before the share's start are masked), so a tile never crosses a
+// page of a paged cache.
+cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const CacheRef& cache,
+                                       const int* seq_lens, DecodePlan plan,
                                        float scale, __half* o_part, float* ml_part, int* err,
                                        cudaStream_t st, bool pdl = false);
 cudaError_t init_decode_tc_kernel();
@@ -270,11 +306,20 @@ cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* 
 // [kv_rows, HEADS, KVB_PER_HEAD] with kvr0(b) = sum over b' < b of (L_b' + T); the rotary keys
 // come from the cache rows.  Query t of sequence b sees positions 0 .. L_b + t.
 cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloat16* kv,
-                                        const __nv_bfloat16* cache, int cap, int B, int T,
+                                        const CacheRef& cache, int B, int T,
                                         const int* seq_lens, long kv_rows, float scale,
                                         __nv_bfloat16* attn_out, uint8_t* o_hi, uint8_t* o_lo,
                                         float* o_sx, int* err, cudaStream_t st);
 cudaError_t init_prefill_tc_kernel();
+
+// Chunked prefill over a paged cache: the normalised latents (the first KV_LORA values) of
+// every sequence's cache rows 0 .. seq_lens[b] + T - 1, packed sequence after sequence into
+// out [kv_rows, KV_LORA] bf16 (the layout the kv_b_proj of launch_prefill_attention_tc's keys
+// and values expects).  max_len >= seq_lens[b] + T bounds the grid; a layout that does not
+// fit kv_rows, or an invalid page, is flagged in *err and its rows are skipped.
+cudaError_t launch_gather_latent(const CacheRef& cache, const int* seq_lens, int B, int T,
+                                 int max_len, long kv_rows, __nv_bfloat16* out, int* err,
+                                 cudaStream_t st);
 
 // seq_lens[b] += T.
 cudaError_t launch_advance_lens(int* seq_lens, int B, int T, cudaStream_t st);

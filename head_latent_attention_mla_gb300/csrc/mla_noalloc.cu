@@ -145,14 +145,15 @@ extern "C" mla_status mla_decode_noalloc(mla_ctx* c, const void* x, int B, void*
   Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
                 {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
   NA_RUN(launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, gpart, c->num_sms, c->d_err, s));
+  const CacheRef CR = dense_cache(C, cap);
   NA_RUN(launch_norm_rope_cache(g1, B, 1, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
-                                c->cfg.rope_pairing, lens_dev, C, cap, limit, cq, nullptr,
+                                c->cfg.rope_pairing, lens_dev, CR, limit, cq, nullptr,
                                 c->d_err, s));
   Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
   NA_RUN(launch_gemm(cq, Q_LORA, B, Q_LORA, &p2, 1, gpart, c->num_sms, c->d_err, s));
   NA_RUN(launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
                          c->cfg.rope_pairing, lens_dev, limit, qfull, s));
-  NA_RUN(launch_decode_attention_tc(qfull, C, cap, lens_dev, plan, c->cfg.softmax_scale, opart,
+  NA_RUN(launch_decode_attention_tc(qfull, CR, lens_dev, plan, c->cfg.softmax_scale, opart,
                                     ml, c->d_err, s));
   NA_RUN(launch_decode_combine(lens_dev, plan, opart, ml, olat, c->d_err, s));
   NA_RUN(launch_absorb_out(olat, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], attn, s));

@@ -36,8 +36,15 @@ class mla_config(ctypes.Structure):
                 ("yarn_mscale", ctypes.c_float), ("yarn_mscale_all_dim", ctypes.c_float)]
 
 
+class mla_paged_cache(ctypes.Structure):
+    _fields_ = [("pool", ctypes.c_void_p), ("num_pages", ctypes.c_int),
+                ("page_size", ctypes.c_int), ("block_table", ctypes.c_void_p),
+                ("max_pages", ctypes.c_int)]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
+_PC = ctypes.POINTER(mla_paged_cache)
 _SIGS = {
     "mla_default_config": (None, [ctypes.POINTER(mla_config)]),
     "mla_create": (_I, [ctypes.POINTER(mla_config), ctypes.POINTER(_P)]),
@@ -49,6 +56,9 @@ _SIGS = {
     "mla_cache_append": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_prefill": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_decode": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "mla_cache_append_paged": (_I, [_P, _P, _I, _I, _PC, _P, _P, _P, ctypes.c_size_t, _P]),
+    "mla_prefill_paged": (_I, [_P, _P, _I, _I, _PC, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "mla_decode_paged": (_I, [_P, _P, _I, _PC, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_dequant_weight": (_I, [_P, _I, _P, _P]),
     "mla_get_device_status": (_I, [_P, _P]),
     "mla_status_string": (ctypes.c_char_p, [_I]),
@@ -175,6 +185,42 @@ def mla_decode_noalloc(ctx, x, cache, seq_lens_dev, seq_lens_host, out, stream=N
                                      _stream(stream)), "mla_decode_noalloc")
 
 
+def paged_cache(pool: torch.Tensor, block_table: torch.Tensor) -> mla_paged_cache:
+    """Descriptor of a paged latent cache: pool bf16 [num_pages, page_size, 576] and
+    block_table int32 [B, max_pages] (both CUDA tensors, kept alive by the caller)."""
+    assert pool.dtype == torch.bfloat16 and pool.dim() == 3 and pool.shape[2] == 576
+    assert block_table.dtype == torch.int32 and block_table.dim() == 2
+    return mla_paged_cache(_ptr(pool), pool.shape[0], pool.shape[1], _ptr(block_table),
+                           block_table.shape[1])
+
+
+def mla_cache_append_paged(ctx, x, cache: mla_paged_cache, seq_lens_dev, seq_lens_host, ws,
+                           stream=None) -> None:
+    B, T = x.shape[0], x.shape[1]
+    _check(load().mla_cache_append_paged(ctx, _ptr(x), B, T, ctypes.byref(cache),
+                                         _ptr(seq_lens_dev), _host_i32(seq_lens_host), _ptr(ws),
+                                         ws.numel() * ws.element_size(), _stream(stream)),
+           "mla_cache_append_paged")
+
+
+def mla_prefill_paged(ctx, x, cache: mla_paged_cache, seq_lens_dev, seq_lens_host, out, ws,
+                      stream=None) -> None:
+    B, T = x.shape[0], x.shape[1]
+    _check(load().mla_prefill_paged(ctx, _ptr(x), B, T, ctypes.byref(cache), _ptr(seq_lens_dev),
+                                    _host_i32(seq_lens_host), _ptr(out), _ptr(ws),
+                                    ws.numel() * ws.element_size(), _stream(stream)),
+           "mla_prefill_paged")
+
+
+def mla_decode_paged(ctx, x, cache: mla_paged_cache, seq_lens_dev, seq_lens_host, out, ws,
+                     stream=None) -> None:
+    B = x.shape[0]
+    _check(load().mla_decode_paged(ctx, _ptr(x), B, ctypes.byref(cache), _ptr(seq_lens_dev),
+                                   _host_i32(seq_lens_host), _ptr(out), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _stream(stream)),
+           "mla_decode_paged")
+
+
 def mla_dequant_weight(ctx: int, which: int, out: torch.Tensor, stream=None) -> None:
     _check(load().mla_dequant_weight(ctx, which, _ptr(out), _stream(stream)),
            "mla_dequant_weight")
@@ -253,6 +299,24 @@ class MlaLayer:
     def cache_append(self, x, cache, seq_lens_dev, seq_lens_host):
         mla_cache_append(self.ctx, x, cache, seq_lens_dev, seq_lens_host,
                          self.workspace(x.shape[0], x.shape[1]))
+
+    def prefill_paged(self, x, pool, block_table, seq_lens_dev, seq_lens_host, out=None):
+        out = torch.empty_like(x) if out is None else out
+        T = x.shape[1]
+        mla_prefill_paged(self.ctx, x, paged_cache(pool, block_table), seq_lens_dev,
+                          seq_lens_host, out,
+                          self.workspace(x.shape[0], T, max(seq_lens_host) + T))
+        return out
+
+    def decode_paged(self, x, pool, block_table, seq_lens_dev, seq_lens_host, out=None):
+        out = torch.empty_like(x) if out is None else out
+        mla_decode_paged(self.ctx, x, paged_cache(pool, block_table), seq_lens_dev,
+                         seq_lens_host, out, self.workspace(x.shape[0], 1))
+        return out
+
+    def cache_append_paged(self, x, pool, block_table, seq_lens_dev, seq_lens_host):
+        mla_cache_append_paged(self.ctx, x, paged_cache(pool, block_table), seq_lens_dev,
+                               seq_lens_host, self.workspace(x.shape[0], x.shape[1]))
 
     def dequant(self, name: str) -> torch.Tensor:
         q, _ = self.w[name]

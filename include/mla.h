@@ -157,6 +157,43 @@ mla_status mla_decode(mla_ctx* ctx, const void* x_bf16, int B, void* cache_bf16,
                       int* seq_lens_dev, const int* seq_lens_host, void* out_bf16, void* ws,
                       size_t ws_bytes, void* stream);
 
+/* A paged latent cache.  The "KV cache" page describes a cache with no fixed size that grows
+ * call by call (the cache's get_usable_length / update in the excerpt); here it is a pool of
+ * fixed-size pages and a block table per sequence, so sequences can grow without reserving
+ * their maximum length up front.  Position pos of sequence b is row
+ * block_table[b * max_pages + pos / page_size] * page_size + pos % page_size of the pool, a
+ * row holding the same 576 bf16 values as a dense cache row [c_hat (512) | RoPE(k_pe) (64)].
+ * The caller allocates and owns the pool and the table and assigns the pages (any pool page,
+ * in any order); the library only reads the table.  A table entry outside [0, num_pages)
+ * for a position a call writes or reads is never followed: the row is skipped (writes) or
+ * read as zeros (reads), and the device status reports MLA_ERR_STATE. */
+typedef struct {
+  void* pool;              /* device bf16 [num_pages, page_size, 576], 16-byte aligned        */
+  int num_pages;           /* pages in the pool (num_pages * page_size < 2^31 - 256)          */
+  int page_size;           /* positions per page: a positive multiple of 64                   */
+  const int* block_table;  /* device int32 [B, max_pages]: pool page of logical page i of b   */
+  int max_pages;           /* logical pages per sequence; capacity = max_pages * page_size    */
+} mla_paged_cache;
+
+/* mla_cache_append, mla_prefill and mla_decode over a paged latent cache: the same steps,
+ * arguments and errors, with `cache` (host pointer to the descriptor, read during the call)
+ * in place of the dense cache and its capacity; capacity errors (MLA_ERR_CAPACITY) are
+ * judged against max_pages * page_size.  A malformed descriptor (null pointers, a page size
+ * that is not a positive multiple of 64, an oversized pool) gives MLA_ERR_INVALID_ARG.  The
+ * workspace sizes are those of the dense calls (mla_workspace_bytes_len covers the gathered
+ * latents a chunk over a paged cache needs). */
+mla_status mla_cache_append_paged(mla_ctx* ctx, const void* x_bf16, int B, int T,
+                                  const mla_paged_cache* cache, int* seq_lens_dev,
+                                  const int* seq_lens_host, void* ws, size_t ws_bytes,
+                                  void* stream);
+mla_status mla_prefill_paged(mla_ctx* ctx, const void* x_bf16, int B, int T,
+                             const mla_paged_cache* cache, int* seq_lens_dev,
+                             const int* seq_lens_host, void* out_bf16, void* ws, size_t ws_bytes,
+                             void* stream);
+mla_status mla_decode_paged(mla_ctx* ctx, const void* x_bf16, int B, const mla_paged_cache* cache,
+                            int* seq_lens_dev, const int* seq_lens_host, void* out_bf16, void* ws,
+                            size_t ws_bytes, void* stream);
+
 /* mla_decode for callers that cannot allocate device memory when they decode (an arena that
  * owns all GPU memory, a runtime that forbids allocation after start-up): the same step and
  * the same arguments as mla_decode without the workspace.  The paper has no counterpart; this
