@@ -162,10 +162,11 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
   fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nseg = *s_nseg;
-  // A segment [p0, p1) is read in tiles that start at multiples of DA_TILE within its sequence
-  // (so a tile never crosses a page of a paged cache): from a0 = p0 rounded down; positions
-  // before p0 in the first tile are masked.
-  auto seg_a0 = [&](int sg) { return seg[3 * sg + 1] & ~(DA_TILE - 1); };
+  // A segment [p0, p1) is read in tiles from a0 = p0.  With a paged cache the tiles start at
+  // multiples of DA_TILE within the sequence instead (so a tile never crosses a page): a0 = p0
+  // rounded down, and positions before p0 in the first tile are masked.
+  const int align_mask = cache.paged() ? ~(DA_TILE - 1) : ~0;
+  auto seg_a0 = [&](int sg) { return seg[3 * sg + 1] & align_mask; };
   auto seg_tiles = [&](int sg) { return (seg[3 * sg + 2] - seg_a0(sg) + DA_TILE - 1) / DA_TILE; };
   // Cache row of a tile's first position; an invalid page reads past the array (zero fill)
   // and is flagged.
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
           tmem_wait_ld();
           fence_before();
           mbar_arrive(&s_free[sb]);
-          const int a0 = p0 & ~(DA_TILE - 1);
+          const int a0 = p0 & align_mask;
           const int n = min(DA_TILE, p1 - (a0 + DA_TILE * i));  // columns [lo, n) are valid
           const int lo = i == 0 ? p0 - a0 : 0;
           float tmax = -INFINITY;

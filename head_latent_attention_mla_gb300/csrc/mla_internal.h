@@ -269,9 +269,9 @@ cudaError_t launch_combine_absorb_out(const int* seq_lens, const int* lens_host,
 
 // Split-KV decode attention over the latent cache on the tcgen05 tensor cores (TMA-fed,
 // accumulators in tensor memory): per work item, unnormalised partial outputs and (m, l).
-// Each sequence's share is read in 64-position tiles that start at multiples of 64 within
-// the sequence (positions before the share's start are masked), so a tile never crosses a
-// page of a paged cache.
+// Each sequence's share is read in 64-position tiles from the share's first position; with a
+// paged cache the tiles start at multiples of 64 within the sequence instead (positions
+// before the share's start are masked), so a tile never crosses a page.
 cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const CacheRef& cache,
                                        const int* seq_lens, DecodePlan plan,
                                        float scale, __half* o_part, float* ml_part, int* err,
