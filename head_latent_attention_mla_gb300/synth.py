@@ -87,6 +87,12 @@ def make_gains(seed: int = 0, sizes: dict | None = None) -> dict:
     return out
 
 
+def make_input_gain(seed: int = 0, hidden: int = HIDDEN) -> np.ndarray:
+    """bf16 bits of 1 + U(-0.1, 0.1) for a decoder block's input_layernorm (its own stream)."""
+    u = _rng(seed, _TAG_GAIN, 2).uniform(-0.1, 0.1, size=hidden)
+    return to_bf16_bits((1.0 + u).astype(np.float32))
+
+
 def _hidden_chunk(seed: int, seq: int, chunk: int, rows: int, hidden: int) -> np.ndarray:
     x = _rng(seed, _TAG_HIDDEN, seq, chunk).standard_normal((rows, hidden), dtype=np.float32)
     return to_bf16_bits(x)

@@ -415,6 +415,19 @@ def forward(x: np.ndarray, cache: np.ndarray | None, W: Weights, d: Dims = KIMI_
     return (y, full, probs) if return_probs else (y, full)
 
 
+def block_forward(x: np.ndarray, cache: np.ndarray | None, W: Weights, g_in: np.ndarray,
+                  eps: float = RMS_EPS, **kw):
+    """The attention half of a decoder block ("Attention input" page, `block` excerpt): the
+    input is kept as the residual, normalised by input_layernorm (the `rmsnorm` excerpt with
+    the block's own gain over the hidden size), passed through the layer, and the layer's
+    output is added back to the residual.  (The post-attention norm and the FFN that follow
+    in the block are not part of it.)  Returns (y [T, hidden], the grown cache)."""
+    x = np.asarray(x, np.float64)
+    h = rms_norm(x, g_in, eps)
+    y, full = forward(h, cache, W, eps=eps, **kw)[:2]
+    return x + y, full
+
+
 def prefill(x: np.ndarray, W: Weights, **kw):
     """Prefill over an empty cache: x [T, hidden] -> (y [T, hidden], cache [T, 576])."""
     return forward(x, None, W, **kw)

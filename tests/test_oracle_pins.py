@@ -477,3 +477,83 @@ def test_planted_mistakes_are_caught(monkeypatch, mistake):
 def _swapped(W_kvb, d):
     per_head = W_kvb.reshape(d.heads, d.nope + d.vdim, d.kv_lora)
     return per_head[:, d.vdim:, :][:, : d.nope], per_head[:, : d.vdim, :]
+
+
+# ----------------------------------------------------------------------------- decoder block
+def brute_force_block(x, W, d, g_in, eps=1e-6):
+    """The attention half of the block as loops: each token normalised by the input gain
+    (float arithmetic, one token at a time), the brute-force layer on the normalised tokens,
+    and the token itself added back."""
+    xs = np.asarray(x, np.float64)
+    hs = []
+    for row in xs:
+        ms = sum(float(v) * float(v) for v in row) / len(row)
+        hs.append([float(g_in[i]) * float(row[i]) / math.sqrt(ms + eps) for i in range(len(row))])
+    y = brute_force_layer(np.array(hs), W, d, eps=eps)
+    return np.array([[float(xs[t][i]) + float(y[t][i]) for i in range(len(xs[t]))]
+                     for t in range(len(xs))])
+
+
+def tiny_input_gain(seed, d=TINY):
+    return 1 + np.random.default_rng(seed).uniform(-0.1, 0.1, d.hidden)
+
+
+def test_block_equals_brute_force_loops():
+    d, W = TINY, tiny_weights(33)
+    g = tiny_input_gain(34)
+    x = np.random.default_rng(35).normal(size=(6, d.hidden)) * 3.0
+    y, _ = O.block_forward(x, None, W, g, d=d)
+    np.testing.assert_allclose(y, brute_force_block(x, W, d, g), rtol=1e-10, atol=1e-12)
+
+
+def test_block_with_zero_output_projection_is_the_identity():
+    d, W = TINY, tiny_weights(36)
+    W = O.Weights(**{**W.__dict__, "o": np.zeros_like(W.o)})
+    x = np.random.default_rng(37).normal(size=(5, d.hidden))
+    y, _ = O.block_forward(x, None, W, tiny_input_gain(38), d=d)
+    np.testing.assert_array_equal(y, x)
+
+
+def test_block_attention_part_is_scale_invariant_without_eps():
+    """With eps = 0 the input norm removes any positive scale of the input, so the block's
+    addition to the residual, y - x, is the same for x and 7.5 x."""
+    d, W = TINY, tiny_weights(39)
+    g = tiny_input_gain(40)
+    x = np.random.default_rng(41).normal(size=(5, d.hidden))
+    y1, _ = O.block_forward(x, None, W, g, d=d, eps=0.0)
+    y2, _ = O.block_forward(7.5 * x, None, W, g, d=d, eps=0.0)
+    np.testing.assert_allclose(y2 - 7.5 * x, y1 - x, rtol=1e-9, atol=1e-12)
+
+
+def test_block_decode_equals_last_block_prefill_row():
+    d, W = TINY, tiny_weights(42)
+    g = tiny_input_gain(43)
+    x = np.random.default_rng(44).normal(size=(9, d.hidden))
+    y_full, _ = O.block_forward(x, None, W, g, d=d)
+    _, cache = O.block_forward(x[:-1], None, W, g, d=d)
+    y_dec, _ = O.block_forward(x[-1:], cache, W, g, d=d)
+    np.testing.assert_allclose(y_dec[0], y_full[-1], rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("mistake", ["no_residual", "norm_after", "no_gain"])
+def test_planted_block_mistakes_are_caught(monkeypatch, mistake):
+    d, W = TINY, tiny_weights(45)
+    g = tiny_input_gain(46)
+    x = np.random.default_rng(47).normal(size=(4, d.hidden)) * 2.0
+    ref = brute_force_block(x, W, d, g)
+    orig_forward, orig_norm = O.forward, O.rms_norm
+    if mistake == "no_residual":
+        monkeypatch.setattr(O, "block_forward", lambda xx, c, Ww, gg, eps=1e-6, **kw:
+                            (orig_forward(O.rms_norm(xx, gg, eps), c, Ww, eps=eps, **kw)[0], None))
+    elif mistake == "norm_after":
+        monkeypatch.setattr(O, "block_forward", lambda xx, c, Ww, gg, eps=1e-6, **kw:
+                            (O.rms_norm(xx + orig_forward(xx, c, Ww, eps=eps, **kw)[0], gg, eps),
+                             None))
+    elif mistake == "no_gain":
+        calls = {"n": 0}
+        def norm(v, gg, eps=1e-6):
+            calls["n"] += 1
+            return orig_norm(v, np.ones_like(gg) if calls["n"] == 1 else gg, eps)
+        monkeypatch.setattr(O, "rms_norm", norm)
+    y, _ = O.block_forward(x, None, W, g, d=d)
+    assert not np.allclose(y, ref, rtol=1e-6, atol=1e-9)
