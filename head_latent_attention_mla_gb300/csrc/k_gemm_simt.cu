@@ -102,10 +102,14 @@ __global__ void __launch_bounds__(128) gemv_f8w_kernel(const __nv_bfloat16* __re
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     if (lane == 0) {
-      if (P.y_fp32)
+      if (P.y_fp32) {
         reinterpret_cast<float*>(P.Y)[(size_t)m * P.ldy + n] = v;
-      else
+      } else {
+        if (P.R)  // residual: bf16(R + bf16(product))
+          v = __bfloat162float(__float2bfloat16_rn(v)) +
+              __bfloat162float(P.R[(size_t)m * P.ldy + n]);
         reinterpret_cast<__nv_bfloat16*>(P.Y)[(size_t)m * P.ldy + n] = __float2bfloat16_rn(v);
+      }
     }
   }
 }

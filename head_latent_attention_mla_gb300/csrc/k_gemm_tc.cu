@@ -89,6 +89,7 @@ struct GemmTcArgs {
   void* Y[2];
   int ldy[2];
   int y_fp32[2];
+  const __nv_bfloat16* R[2];  // bf16 outputs: residual added after rounding (or nullptr)
   const float* sx;       // per-token activation scales [M], or [M][K/128] (SXB kernels)
   int splits;            // k-block ranges per (n tile, m tile)
   float* partial;        // [splits][M][ldp] fp32 when splits > 1
@@ -384,14 +385,30 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
           } else {
             __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(args.Y[U.prob]) +
                                (size_t)m * args.ldy[U.prob] + nb;
+            const __nv_bfloat16* res = args.R[U.prob];
 #pragma unroll
             for (int j = 0; j < CW; j += 8)
               if (nb + j < nend) {
+                float o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = acc[j + e] * sxm;
+                if (res) {  // residual: bf16(R + bf16(product))
+                  const uint4 r = *reinterpret_cast<const uint4*>(
+                      res + (size_t)m * args.ldy[U.prob] + nb + j);
+                  const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    o[2 * e] = __bfloat162float(__float2bfloat16_rn(o[2 * e])) +
+                               __uint_as_float(rw[e] << 16);
+                    o[2 * e + 1] = __bfloat162float(__float2bfloat16_rn(o[2 * e + 1])) +
+                                   __uint_as_float(rw[e] & 0xFFFF0000u);
+                  }
+                }
                 uint4 v;
-                v.x = pack_bf16x2(acc[j] * sxm, acc[j + 1] * sxm);
-                v.y = pack_bf16x2(acc[j + 2] * sxm, acc[j + 3] * sxm);
-                v.z = pack_bf16x2(acc[j + 4] * sxm, acc[j + 5] * sxm);
-                v.w = pack_bf16x2(acc[j + 6] * sxm, acc[j + 7] * sxm);
+                v.x = pack_bf16x2(o[0], o[1]);
+                v.y = pack_bf16x2(o[2], o[3]);
+                v.z = pack_bf16x2(o[4], o[5]);
+                v.w = pack_bf16x2(o[6], o[7]);
                 *reinterpret_cast<uint4*>(y + j) = v;
               }
           }
@@ -426,9 +443,16 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
             if (j < mend) y[(size_t)j * ldy] = acc[j];
         } else {
           __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(args.Y[U.prob]) + (size_t)m0 * ldy + n;
+          const __nv_bfloat16* res = args.R[U.prob];
 #pragma unroll
           for (int j = 0; j < CW; ++j)
-            if (j < mend) y[(size_t)j * ldy] = __float2bfloat16_rn(acc[j]);
+            if (j < mend) {
+              float o = acc[j];
+              if (res)  // residual: bf16(R + bf16(product))
+                o = __bfloat162float(__float2bfloat16_rn(o)) +
+                    __bfloat162float(res[(size_t)(m0 + j) * ldy + n]);
+              y[(size_t)j * ldy] = __float2bfloat16_rn(o);
+            }
         }
       }
     }
@@ -444,16 +468,20 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
 
 // Y = sum over splits of the fp32 partials, in split order (deterministic).
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int M, int ldp,
-                                     int n_off, int N, void* Y, int ldy, int y_fp32) {
+                                     int n_off, int N, void* Y, int ldy, int y_fp32,
+                                     const __nv_bfloat16* __restrict__ R) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (size_t)M * N) return;
   const int m = (int)(i / N), n = (int)(i % N);
   float s = 0.f;
   for (int k = 0; k < splits; ++k) s += part[((size_t)k * M + m) * ldp + n_off + n];
-  if (y_fp32)
+  if (y_fp32) {
     reinterpret_cast<float*>(Y)[(size_t)m * ldy + n] = s;
-  else
+  } else {
+    if (R)  // residual: bf16(R + bf16(product))
+      s = __bfloat162float(__float2bfloat16_rn(s)) + __bfloat162float(R[(size_t)m * ldy + n]);
     reinterpret_cast<__nv_bfloat16*>(Y)[(size_t)m * ldy + n] = __float2bfloat16_rn(s);
+  }
 }
 
 template <int BN, int WT, bool SXB>
@@ -538,6 +566,7 @@ cudaError_t gemm_tc_core(const uint8_t* hi, const uint8_t* lo, const float* sx, 
       a.Y[i] = P.Y;
       a.ldy[i] = P.ldy;
       a.y_fp32[i] = P.y_fp32;
+      a.R[i] = P.R;
       n_total += P.N;
     }
   }
@@ -568,7 +597,8 @@ cudaError_t gemm_tc_core(const uint8_t* hi, const uint8_t* lo, const float* sx, 
   for (int i = 0; i < np; ++i) {
     const size_t cnt = (size_t)M * p[i].N;
     splitk_reduce_kernel<<<(unsigned)((cnt + 255) / 256), 256, 0, st>>>(
-        partial, a.splits, M, n_total, i ? p[0].N : 0, p[i].N, p[i].Y, p[i].ldy, p[i].y_fp32);
+        partial, a.splits, M, n_total, i ? p[0].N : 0, p[i].N, p[i].Y, p[i].ldy, p[i].y_fp32,
+        p[i].R);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

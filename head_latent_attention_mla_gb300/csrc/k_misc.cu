@@ -185,6 +185,58 @@ __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
   }
 }
 
+// The decoder block's input RMSNorm ("rmsnorm" excerpt over the hidden size): one CTA of 224
+// threads per token, each with four 16-byte runs of 8 values.
+constexpr int IN_THREADS = HIDDEN / 32;
+__global__ void __launch_bounds__(IN_THREADS) input_norm_kernel(const __nv_bfloat16* __restrict__ x,
+                                                                const __nv_bfloat16* __restrict__ g,
+                                                                float eps,
+                                                                __nv_bfloat16* __restrict__ xn) {
+  __shared__ float red[IN_THREADS / 32];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int m = blockIdx.x, tid = threadIdx.x;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)m * HIDDEN);
+  uint4 v[4];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[i] = src[tid + IN_THREADS * i];
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float a = __uint_as_float(w[e] << 16), b = __uint_as_float(w[e] & 0xFFFF0000u);
+      ss += a * a + b * b;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < IN_THREADS / 32; ++w) tot += red[w];
+  const float rs = rsqrtf(tot / HIDDEN + eps);
+  uint4* dst = reinterpret_cast<uint4*>(xn + (size_t)m * HIDDEN);
+  const uint4* gs = reinterpret_cast<const uint4*>(g);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 gv = gs[tid + IN_THREADS * i];
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat16 y0 = __float2bfloat16_rn(__uint_as_float(gw[e] << 16) *
+                                                   bf16_round(__uint_as_float(w[e] << 16) * rs));
+      const __nv_bfloat16 y1 = __float2bfloat16_rn(
+          __uint_as_float(gw[e] & 0xFFFF0000u) * bf16_round(__uint_as_float(w[e] & 0xFFFF0000u) * rs));
+      o[e] = (uint32_t)__bfloat16_as_ushort(y0) | ((uint32_t)__bfloat16_as_ushort(y1) << 16);
+    }
+    dst[tid + IN_THREADS * i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // Row t of sequence b's latents (its first KV_LORA cache values) to row r0(b) + t of out, with
 // r0(b) = sum over b' < b of (seq_lens[b'] + T): one CTA (64 threads, 16 bytes each) per row.
 __global__ void __launch_bounds__(KV_LORA / 8) gather_latent_kernel(
@@ -454,6 +506,12 @@ cudaError_t launch_norm_rope_cache(const float* g1, int B, int T, const __nv_bfl
   return launch_kernel(norm_rope_cache_kernel, dim3(B * T), dim3(256), 0, st, pdl, g1, T, gq, gkv,
                        eps, rope_tab, rope_pairing, seq_lens, cache, limit, cq_out, ckv_out,
                        err, q_split ? *q_split : none, kv_split ? *kv_split : none);
+}
+
+cudaError_t launch_input_norm(const __nv_bfloat16* x, int M, const __nv_bfloat16* g, float eps,
+                              __nv_bfloat16* xn, cudaStream_t st, bool pdl) {
+  if (M <= 0) return cudaSuccess;
+  return launch_kernel(input_norm_kernel, dim3(M), dim3(IN_THREADS), 0, st, pdl, x, g, eps, xn);
 }
 
 cudaError_t launch_gather_latent(const CacheRef& cache, const int* seq_lens, int B, int T,

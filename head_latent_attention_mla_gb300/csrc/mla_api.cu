@@ -15,7 +15,7 @@ namespace {
 
 const int kRows[5] = {Q_LORA, QB_N, KVA_N, KVB_N, HIDDEN};
 const int kCols[5] = {HIDDEN, Q_LORA, HIDDEN, KV_LORA, O_IN};
-const int kNorm[2] = {Q_LORA, KV_LORA};
+const int kNorm[3] = {Q_LORA, KV_LORA, HIDDEN};
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -23,13 +23,13 @@ inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 bool ready(const mla_ctx* c) {
   for (int i = 0; i < 5; ++i)
     if (!c->W[i] || !c->S[i]) return false;
-  return c->gain[0] && c->gain[1];
+  return c->gain[0] && c->gain[1] && (!c->cfg.block || c->gain[2]);
 }
 
 // Workspace regions (byte offsets into the caller's buffer).
 struct Layout {
   size_t g1 = 0, cq = 0, cq_sx = 0, ckv = 0, ckv_sx = 0, q = 0, kv = 0, attn = 0, attn_sx = 0,
-         qfull = 0, opart = 0, ml = 0, olat = 0, gpart = 0, gather = 0, total = 0;
+         qfull = 0, opart = 0, ml = 0, olat = 0, gpart = 0, gather = 0, xn = 0, total = 0;
 };
 
 // Largest split-K partial buffer of the projections of one call with M token rows.
@@ -50,11 +50,12 @@ int items_max(const mla_ctx* c, int B) { return 2 * c->num_sms + B; }
 // per-sequence kv_b_proj over cache rows (0 when the cache is empty).  With cached positions
 // the layout also holds the latents of all kv_rows gathered from a paged cache (and the
 // GEMM scratch of one kv_b_proj over all of them).
-Layout prefill_layout(long M, int num_sms, long kv_rows = -1, long kvb_M = 0) {
+Layout prefill_layout(long M, int num_sms, long kv_rows = -1, long kvb_M = 0, bool block = false) {
   Layout L;
   if (kv_rows < 0) kv_rows = M;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off += up256(bytes); return o; };
+  if (block) L.xn = take((size_t)M * HIDDEN * 2);  // the block's normalised input
   L.g1 = take((size_t)M * G1_N * 4);
   L.cq = take((size_t)M * Q_LORA * 2);    // bf16, or its two e4m3 terms
   L.cq_sx = take((size_t)M * 4);
@@ -82,6 +83,7 @@ Layout decode_layout(const mla_ctx* c, int B) {
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off += up256(bytes); return o; };
   const size_t items = (size_t)items_max(c, B);
+  if (c->cfg.block) L.xn = take((size_t)B * HIDDEN * 2);  // the block's normalised input
   L.g1 = take((size_t)B * G1_N * 4);
   L.cq = take((size_t)B * Q_LORA * 2);
   L.q = take((size_t)B * QB_N * 2);
@@ -197,19 +199,35 @@ mla_status paged_ref(const mla_paged_cache* pc, CacheRef* out) {
   return MLA_OK;
 }
 
+// The layer's input: x itself, or with block = 1 its input RMSNorm, written to the workspace by
+// a first kernel (recorded in the call's launch log).  nullptr if that launch fails.
+const __nv_bfloat16* block_input(mla_ctx* c, const void* x, int M, void* ws, const Layout& L,
+                                 cudaStream_t s) {
+  const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(x);
+  if (!c->cfg.block) return X;
+  __nv_bfloat16* xn = at<__nv_bfloat16>(ws, L.xn);
+  auto launch = [&]() -> mla_status {
+    MLA_LAUNCH("input_norm", launch_input_norm(X, M, c->gain[2], c->cfg.eps, xn, s));
+    return MLA_OK;
+  };
+  return launch() == MLA_OK ? xn : nullptr;
+}
+
 mla_status cache_append_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef& CR,
                              int* lens_dev, const int* lens_host, void* ws, size_t ws_bytes,
                              void* stream) {
-  const Layout L = prefill_layout((long)B * T, c ? c->num_sms : 0);
+  const Layout L = prefill_layout((long)B * T, c ? c->num_sms : 0, -1, 0, c && c->cfg.block);
   mla_status st = check_tokens(c, x, B, T, CR.base, CR.capacity(), lens_dev, lens_host, ws,
                                ws_bytes, L.total);
   if (st != MLA_OK || B == 0 || T == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   log_reset(c);
   const int M = B * T, limit = limit_of(c, CR);
+  const __nv_bfloat16* X = block_input(c, x, M, ws, L, s);
+  if (!X) return MLA_ERR_CUDA;
   float* g1 = at<float>(ws, L.g1);
   Proj p{c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1};
-  MLA_LAUNCH("gemm_kv_a", launch_gemm(static_cast<const __nv_bfloat16*>(x), HIDDEN, M, HIDDEN, &p, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+  MLA_LAUNCH("gemm_kv_a", launch_gemm(X, HIDDEN, M, HIDDEN, &p, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s, nullptr, 0, 0, c->cfg.block != 0));
   MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
                                     c->cfg.rope_pairing, lens_dev, CR, limit, nullptr,
                                     nullptr, c->d_err, s));
@@ -231,7 +249,7 @@ mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef&
     chunked = chunked || lens_host[b] != 0;
   }
   const Layout L = prefill_layout((long)B * T, c ? c->num_sms : 0, chunked ? kv_rows : -1,
-                                  chunked ? kvb_M : 0);
+                                  chunked ? kvb_M : 0, c && c->cfg.block);
   mla_status st = check_tokens(c, x, B, T, CR.base, CR.capacity(), lens_dev, lens_host, ws,
                                ws_bytes, L.total);
   if (st != MLA_OK || B == 0 || T == 0) return st;
@@ -239,7 +257,9 @@ mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef&
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   log_reset(c);
   const int M = B * T, limit = limit_of(c, CR);
-  const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(x);
+  const __nv_bfloat16* X = block_input(c, x, M, ws, L, s);
+  if (!X) return MLA_ERR_CUDA;
+  const __nv_bfloat16* residual = c->cfg.block ? static_cast<const __nv_bfloat16*>(x) : nullptr;
   float* g1 = at<float>(ws, L.g1);
   __nv_bfloat16* cq = at<__nv_bfloat16>(ws, L.cq);
   __nv_bfloat16* ckv = at<__nv_bfloat16>(ws, L.ckv);
@@ -304,7 +324,7 @@ mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef&
     MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
     MLA_LAUNCH("gemm_kv_b", launch_gemm(ckv, KV_LORA, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
   }
-  Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
+  Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0, residual};
   if (gemm_takes_split_blocks(M)) {
     // The attention writes o_proj's e4m3 input itself (one scale per token and head).
     uint8_t* a_hi = at<uint8_t>(ws, L.attn);
@@ -341,7 +361,9 @@ mla_status decode_impl(mla_ctx* c, const void* x, int B, const CacheRef& CR, int
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   log_reset(c);
   const int limit = limit_of(c, CR);
-  const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(x);
+  const __nv_bfloat16* X = block_input(c, x, B, ws, L, s);
+  if (!X) return MLA_ERR_CUDA;
+  const __nv_bfloat16* residual = c->cfg.block ? static_cast<const __nv_bfloat16*>(x) : nullptr;
 
   // Every kernel after the first is launched with programmatic dependent launch: it may start
   // (and fetch its weights) while its predecessor finishes, and waits for the predecessor's
@@ -362,7 +384,7 @@ mla_status decode_impl(mla_ctx* c, const void* x, int B, const CacheRef& CR, int
 
   Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
                 {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
-  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s, nullptr, 0, 0, c->cfg.block != 0));
   if (B <= 2) {
     // One or two sequences: six kernels.  q_b_proj normalises the q latent itself (and one of
     // its CTAs appends the cache rows); the combine is fused with the W_UV absorption; the
@@ -380,7 +402,7 @@ mla_status decode_impl(mla_ctx* c, const void* x, int B, const CacheRef& CR, int
     MLA_LAUNCH("combine_absorb_out",
                launch_combine_absorb_out(lens_dev, lens_host, plan, opart, ml, c->W[MLA_W_KV_B],
                                          c->S[MLA_W_KV_B], attn, c->d_err, s, true));
-    Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
+    Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0, residual};
     MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
                                      c->num_sms, c->d_err, s, lens_dev, B, 1, true));
     return MLA_OK;
@@ -400,7 +422,7 @@ mla_status decode_impl(mla_ctx* c, const void* x, int B, const CacheRef& CR, int
                                                          true));
   MLA_LAUNCH("absorb_out", launch_absorb_out(olat, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], attn, s,
                                                  true));
-  Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0};
+  Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0, residual};
   if (gemm_can_advance(B)) {  // the length update rides on the last kernel
     MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
                                      c->num_sms, c->d_err, s, lens_dev, B, 1, true));
@@ -437,6 +459,7 @@ void mla_default_config(mla_config* cfg) {
   cfg->yarn_beta_slow = 1.0f;
   cfg->yarn_mscale = 1.0f;
   cfg->yarn_mscale_all_dim = 1.0f;
+  cfg->block = 0;
 }
 
 mla_status mla_create(const mla_config* cfg, mla_ctx** out) {
@@ -451,6 +474,7 @@ mla_status mla_create(const mla_config* cfg, mla_ctx** out) {
     return MLA_ERR_INVALID_ARG;
   if (cfg->rope_scaling != MLA_ROPE_PLAIN && cfg->rope_scaling != MLA_ROPE_YARN)
     return MLA_ERR_INVALID_ARG;
+  if (cfg->block != 0 && cfg->block != 1) return MLA_ERR_INVALID_ARG;
   if (cfg->rope_scaling == MLA_ROPE_YARN &&
       (!(cfg->yarn_factor >= 1.f) || cfg->yarn_original_max_positions <= 0 ||
        !(cfg->yarn_beta_fast > 0.f) || !(cfg->yarn_beta_slow > 0.f) ||
@@ -552,7 +576,7 @@ mla_status mla_upload_weights(mla_ctx* c, int which, const void* q, const float*
 }
 
 mla_status mla_upload_norm(mla_ctx* c, int which, const void* g, int n) {
-  if (!c || which < 0 || which > 1 || !g || !aligned16(g)) return MLA_ERR_INVALID_ARG;
+  if (!c || which < 0 || which > 2 || !g || !aligned16(g)) return MLA_ERR_INVALID_ARG;
   if (n != kNorm[which]) return MLA_ERR_SHAPE;
   c->gain[which] = static_cast<const __nv_bfloat16*>(g);
   return MLA_OK;
@@ -561,7 +585,7 @@ mla_status mla_upload_norm(mla_ctx* c, int which, const void* g, int n) {
 size_t mla_workspace_bytes_len(const mla_ctx* c, int B, int T, int max_len) {
   if (!c || B < 0 || T < 0 || max_len < T) return 0;
   const size_t p = prefill_layout((long)B * T, c->num_sms, (long)B * max_len,
-                                  max_len > T ? max_len : 0).total;
+                                  max_len > T ? max_len : 0, c->cfg.block != 0).total;
   const size_t d = decode_layout(c, B).total;
   return p > d ? p : d;
 }

@@ -103,6 +103,9 @@ struct Proj {
   void* Y;           // fp32 or bf16 output, row stride ldy elements
   int ldy;
   int y_fp32;        // 1: float32 output, 0: bf16 output
+  // bf16 output only: a residual [M, ldy] added to the bf16-rounded product,
+  // Y = bf16(R + bf16(XW^T)) (the decoder block's residual connection); nullptr: none.
+  const __nv_bfloat16* R = nullptr;
 };
 
 // Two-term e4m3 split of two values already divided by their scale: hi = e4m3(f),
@@ -321,6 +324,11 @@ cudaError_t launch_gather_latent(const CacheRef& cache, const int* seq_lens, int
                                  int max_len, long kv_rows, __nv_bfloat16* out, int* err,
                                  cudaStream_t st);
 
+// The decoder block's input RMSNorm: xn[m] = bf16(g * bf16(x[m] * rsqrt(mean(x[m]^2) + eps)))
+// for M rows of HIDDEN bf16 values.
+cudaError_t launch_input_norm(const __nv_bfloat16* x, int M, const __nv_bfloat16* g, float eps,
+                              __nv_bfloat16* xn, cudaStream_t st, bool pdl = false);
+
 // seq_lens[b] += T.
 cudaError_t launch_advance_lens(int* seq_lens, int B, int T, cudaStream_t st);
 
@@ -337,7 +345,7 @@ struct mla_ctx {
   int num_sms = 0;
   const uint8_t* W[5] = {};
   const float* S[5] = {};
-  const __nv_bfloat16* gain[2] = {};
+  const __nv_bfloat16* gain[3] = {};  // q_a_layernorm, kv_a_layernorm, input_layernorm
   float2* rope_tab = nullptr;  // [max_positions][32] (cos, sin)
   int* d_err = nullptr;
   // Device address, on this context's device, of the static scratch array that

@@ -93,6 +93,7 @@ extern "C" mla_status mla_decode_noalloc(mla_ctx* c, const void* x, int B, void*
   if (!c || B < 0 || cap < 0) return MLA_ERR_INVALID_ARG;
   if (B == 0) return MLA_OK;
   if (B > kMaxBatch) return MLA_ERR_CAPACITY;  // beyond the static scratch
+  if (c->cfg.block) return MLA_ERR_UNSUPPORTED;  // no room for the block's normalised input
   if (!x || !cache || !lens_dev || !lens_host || !out || out == x) return MLA_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(cache) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
   for (int i = 0; i < 5; ++i)

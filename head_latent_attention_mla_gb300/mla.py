@@ -17,12 +17,12 @@ LIB_PATH = os.path.join(_HERE, "_build", "libmla.so")
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_SHAPE, MLA_ERR_UNSUPPORTED = 0, 1, 2, 3
 MLA_ERR_CAPACITY, MLA_ERR_CUDA, MLA_ERR_TIMEOUT, MLA_ERR_STATE = 4, 5, 6, 7
 MLA_W_Q_A, MLA_W_Q_B, MLA_W_KV_A, MLA_W_KV_B, MLA_W_O = 0, 1, 2, 3, 4
-MLA_NORM_Q, MLA_NORM_KV = 0, 1
+MLA_NORM_Q, MLA_NORM_KV, MLA_NORM_INPUT = 0, 1, 2
 MLA_ROPE_ADJACENT, MLA_ROPE_HALF = 0, 1
 MLA_ROPE_PLAIN, MLA_ROPE_YARN = 0, 1
 WEIGHT_IDS = {"q_a": MLA_W_Q_A, "q_b": MLA_W_Q_B, "kv_a": MLA_W_KV_A, "kv_b": MLA_W_KV_B,
               "o": MLA_W_O}
-NORM_IDS = {"q_norm": MLA_NORM_Q, "kv_norm": MLA_NORM_KV}
+NORM_IDS = {"q_norm": MLA_NORM_Q, "kv_norm": MLA_NORM_KV, "input_norm": MLA_NORM_INPUT}
 
 
 class mla_config(ctypes.Structure):
@@ -33,7 +33,8 @@ class mla_config(ctypes.Structure):
                 ("rope_pairing", ctypes.c_int), ("rope_scaling", ctypes.c_int),
                 ("yarn_factor", ctypes.c_float), ("yarn_original_max_positions", ctypes.c_int),
                 ("yarn_beta_fast", ctypes.c_float), ("yarn_beta_slow", ctypes.c_float),
-                ("yarn_mscale", ctypes.c_float), ("yarn_mscale_all_dim", ctypes.c_float)]
+                ("yarn_mscale", ctypes.c_float), ("yarn_mscale_all_dim", ctypes.c_float),
+                ("block", ctypes.c_int)]
 
 
 class mla_paged_cache(ctypes.Structure):

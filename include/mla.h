@@ -50,8 +50,9 @@ typedef struct mla_ctx mla_ctx; /* opaque, host-side */
 
 /* Projection ids for mla_upload_weights (names of the pages' nn.Linear modules). */
 enum { MLA_W_Q_A = 0, MLA_W_Q_B = 1, MLA_W_KV_A = 2, MLA_W_KV_B = 3, MLA_W_O = 4 };
-/* RMSNorm gain ids for mla_upload_norm: q_a_layernorm and kv_a_layernorm. */
-enum { MLA_NORM_Q = 0, MLA_NORM_KV = 1 };
+/* RMSNorm gain ids for mla_upload_norm: q_a_layernorm, kv_a_layernorm, and (with
+ * mla_config.block = 1) the decoder block's input_layernorm. */
+enum { MLA_NORM_Q = 0, MLA_NORM_KV = 1, MLA_NORM_INPUT = 2 };
 /* RoPE pairing of the 64-wide rotary slice: pair j = (2j, 2j+1) or (j, j+32). */
 enum { MLA_ROPE_ADJACENT = 0, MLA_ROPE_HALF = 1 };
 /* RoPE frequencies: plain theta^(-2j/64), or YaRN (config.json rope_scaling, "KV cache" page). */
@@ -69,6 +70,8 @@ typedef struct {
   int yarn_original_max_positions; /* rope_scaling.original_max_position_embeddings (4096) */
   float yarn_beta_fast, yarn_beta_slow;     /* rope_scaling.beta_fast / beta_slow (1, 1) */
   float yarn_mscale, yarn_mscale_all_dim;   /* rope_scaling.mscale / mscale_all_dim (1, 1) */
+  int block;           /* 0: the layer alone (default); 1: the attention half of a decoder
+                          block around it (see below)                                   */
 } mla_config;
 
 /* Fills *cfg with Kimi-K2's dimensions (config.json on the "KV cache" page), eps 1e-6,
@@ -83,6 +86,17 @@ typedef struct {
  * m(factor, mscale_all_dim) and the score scale by m(factor, mscale_all_dim)^2, where
  * m(s, mu) = 0.1 mu ln s + 1 for s > 1, else 1. */
 void mla_default_config(mla_config* cfg);
+
+/* The attention half of a decoder block (block = 1).  The "Attention input" page's `block`
+ * excerpt keeps the block's input as the residual, normalises it with input_layernorm (the
+ * `rmsnorm` excerpt over the hidden size, gain uploaded as MLA_NORM_INPUT, 7168 bf16 values),
+ * runs the attention layer on the normalised input and adds the layer's output back to the
+ * residual.  With block = 1 every token call (mla_cache_append, mla_prefill, mla_decode and
+ * their paged forms) takes the block's input x: the cache rows are those of the normalised
+ * input, and the output is out = bf16(x + bf16(layer(bf16(RMSNorm_in(x))))), the rounding of
+ * the module's bf16 arithmetic.  The post-attention norm and the FFN that complete the block
+ * are not part of this library.  mla_decode_noalloc does not take block = 1
+ * (MLA_ERR_UNSUPPORTED). */
 
 /* Creates a context on the current CUDA device.  Checks the dimensions (anything but
  * Kimi-K2's gives MLA_ERR_UNSUPPORTED), builds the RoPE cos/sin table on the host in double
@@ -101,8 +115,9 @@ void mla_destroy(mla_ctx* ctx); /* NULL is ignored; synchronises the device befo
 mla_status mla_upload_weights(mla_ctx* ctx, int which, const void* e4m3_dev,
                               const float* scale_dev, int rows, int cols);
 
-/* Registers an RMSNorm gain ("rmsnorm" excerpt): bf16 device vector of n = 1536 (MLA_NORM_Q)
- * or 512 (MLA_NORM_KV) values, 16-byte aligned.  Only the pointer is recorded. */
+/* Registers an RMSNorm gain ("rmsnorm" excerpt): bf16 device vector of n = 1536 (MLA_NORM_Q),
+ * 512 (MLA_NORM_KV) or 7168 (MLA_NORM_INPUT, needed when block = 1) values, 16-byte aligned.
+ * Only the pointer is recorded. */
 mla_status mla_upload_norm(mla_ctx* ctx, int which, const void* bf16_gain_dev, int n);
 
 /* Bytes of caller-provided device workspace that mla_prefill / mla_decode /

@@ -49,6 +49,7 @@ def test_default_config_is_kimi_k2(lib):
     assert c.rope_scaling == mla.MLA_ROPE_PLAIN          # YaRN is off unless asked for
     assert (c.yarn_factor, c.yarn_original_max_positions, c.yarn_beta_fast, c.yarn_beta_slow,
             c.yarn_mscale, c.yarn_mscale_all_dim) == (32.0, 4096, 1.0, 1.0, 1.0, 1.0)
+    assert c.block == 0                                  # the layer alone unless asked for
 
 
 def test_host_argument_checks(lib):
@@ -66,6 +67,9 @@ def test_host_argument_checks(lib):
     assert lib.mla_create(ctypes.byref(c), ctypes.byref(ctx)) == mla.MLA_ERR_INVALID_ARG
     c = mla.mla_default_config()
     c.rope_scaling, c.yarn_factor = mla.MLA_ROPE_YARN, 0.5
+    assert lib.mla_create(ctypes.byref(c), ctypes.byref(ctx)) == mla.MLA_ERR_INVALID_ARG
+    c = mla.mla_default_config()
+    c.block = 2
     assert lib.mla_create(ctypes.byref(c), ctypes.byref(ctx)) == mla.MLA_ERR_INVALID_ARG
     assert lib.mla_workspace_bytes(None, 1, 1) == 0
     assert lib.mla_workspace_bytes_len(None, 1, 4, 8) == 0
