@@ -3,9 +3,10 @@ one and against the fp64 oracle.
 
 The pool is filled with NaN before use and its pages are handed out in a shuffled order, so a
 row read from the wrong page, or a row past a sequence's end that reaches the arithmetic,
-shows.  The paged calls run the same kernels on the same values as the dense ones (the rows
-only live elsewhere), so outputs and cache rows must agree bit for bit; every element is also
-checked against the oracle."""
+shows.  The paged calls write the same cache rows as the dense ones, bit for bit.  Prefill
+outputs are bitwise equal too; decode outputs agree within the bar (a paged decode reads its
+shares in page-aligned tiles, a dense one from each share's first position, so the sums run
+in a different order).  Every element is also checked against the oracle."""
 import math
 
 import numpy as np
@@ -69,8 +70,9 @@ def build_both(layer, lengths, page, capacity, seed=0):
                                           ([1, 63, 64, 65, 200, 333, 600, 127, 5], 64)])
 def test_paged_decode_bitwise_equals_dense_and_oracle(layer, lengths, page):
     """One decode step: one sequence (fused six-kernel chain), three (CUDA-core projections) and
-    nine (the B > 8 combine and tiled W_UV).  Outputs and appended rows equal the dense
-    cache's bit for bit; every output and appended row is within the bar of the oracle."""
+    nine (the B > 8 combine and tiled W_UV).  Appended rows equal the dense cache's bit for
+    bit and outputs are within the bar of the dense call's; every output and appended row is
+    within the bar of the oracle."""
     W = oracle_weights(0)
     B, capacity = len(lengths), max(lengths) + 70
     dense, dl, pool, table, pl = build_both(layer, lengths, page, capacity)
@@ -83,7 +85,7 @@ def test_paged_decode_bitwise_equals_dense_and_oracle(layer, lengths, page):
     torch.cuda.synchronize()
     assert layer.status() == mla.MLA_OK
     assert pl.tolist() == [n + 1 for n in lengths]
-    assert torch.equal(yp, yd)
+    assert_close(yp.float().cpu().numpy(), yd.float().cpu().numpy(), f"paged vs dense, page {page}")
     for b, n in enumerate(lengths):
         assert torch.equal(logical_rows(pool, table, b, n + 1), dense[b, :n + 1])
     y = yp.float().cpu().numpy()
