@@ -68,7 +68,7 @@ def build_both(layer, lengths, page, capacity, seed=0):
 
 @pytest.mark.parametrize("lengths,page", [([1000], 64), ([130, 64, 700], 128),
                                           ([1, 63, 64, 65, 200, 333, 600, 127, 5], 64)])
-def test_paged_decode_bitwise_equals_dense_and_oracle(layer, lengths, page):
+def test_paged_decode_matches_dense_and_oracle(layer, lengths, page):
     """One decode step: one sequence (fused six-kernel chain), three (CUDA-core projections) and
     nine (the B > 8 combine and tiled W_UV).  Appended rows equal the dense cache's bit for
     bit and outputs are within the bar of the dense call's; every output and appended row is
