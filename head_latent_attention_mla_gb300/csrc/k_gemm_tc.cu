@@ -51,14 +51,17 @@ constexpr int GT_RING = 192 * 1024;
 // lane = token, column = feature, so each epilogue thread ends a unit holding a run of one
 // output row and writes it as 16-byte vectors.  With fewer tokens (BN = 32, 64) the weight
 // tile is the A operand (M = 128 features, N = BN tokens): lane = feature, column = token.
-template <int BN, int WT>
+// ONE: the activations are a single e4m3 term (the FP8-activation option) instead of the
+// hi/lo pair: one MMA per k step, and a stage holds one token tile.
+template <int BN, int WT, bool ONE = false>
 struct GemmSmem {
   static constexpr bool TR = BN == 128;          // lane = token (else lane = feature)
   static constexpr int NACC = WT == 2 ? 2 : 4;   // tensor-memory accumulators
   static constexpr int ACC_COLS = WT * BN;       // columns of one accumulator (WT halves)
   static constexpr int X_TILE = BN * 128;        // e4m3 token tile [BN x 128]
   static constexpr int W_BYTES = WT * W_TILE;
-  static constexpr int STAGE = W_BYTES + 2 * X_TILE;
+  static constexpr int NX = ONE ? 1 : 2;         // activation terms per stage
+  static constexpr int STAGE = W_BYTES + NX * X_TILE;
   static constexpr int STAGES = GT_RING / STAGE;
   static constexpr int OFF_IN = 0;
   static constexpr int OFF_BAR = OFF_IN + STAGES * STAGE;
@@ -168,6 +171,41 @@ __global__ void __launch_bounds__(256) split_e4m3_kernel(const __nv_bfloat16* __
   }
 }
 
+// The FP8-activation option's input quantisation ("linear" excerpt: activation_scheme dynamic):
+// one e4m3 term per value with one scale per (token, 128-wide group), s = amax / 448 (1 for an
+// all-zero group), q = e4m3(x / s) rounded to nearest even with saturation.  One CTA per token,
+// K/8 threads of eight values; the sixteen threads of a group find its maximum by shuffles.
+__global__ void __launch_bounds__(1024) quant_e4m3_groups_kernel(const __nv_bfloat16* __restrict__ X,
+                                                                 int ldx, int K,
+                                                                 uint8_t* __restrict__ q,
+                                                                 float* __restrict__ sx) {
+  const int m = blockIdx.x, tid = threadIdx.x, k = 8 * tid;
+  const uint4 v = *reinterpret_cast<const uint4*>(X + (size_t)m * ldx + k);
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  float f[8];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(u[i] << 16);
+    f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+    amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+  }
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float s = amax > 0.f ? amax / E4M3_MAX : 1.f;
+  const float inv = 1.f / s;
+  uint32_t h[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_fp8x2_storage_t p =
+        __nv_cvt_float2_to_fp8x2(make_float2(f[2 * i] * inv, f[2 * i + 1] * inv), __NV_SATFINITE,
+                                 __NV_E4M3);
+    h[i >> 1] |= (uint32_t)p << (16 * (i & 1));
+  }
+  *reinterpret_cast<uint2*>(q + (size_t)m * K + k) = make_uint2(h[0], h[1]);
+  if ((tid & 15) == 0) sx[(size_t)m * (K / BLK) + k / BLK] = s;
+}
+
 // Two floats as bf16 (round to nearest even), the first in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -176,13 +214,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 // SXB: the activations carry one scale per (token, 128-wide k block), sx[m][kb], applied with
 // the weight's block scale to each k block's partial product (token-lane orientation only).
-template <int BN, int WT, bool SXB>
+// ONE: the activations are one e4m3 term (map_lo is not read).
+template <int BN, int WT, bool SXB, bool ONE = false>
 __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
     const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
     const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo,
     const __grid_constant__ GemmTcArgs args) {
-  using L = GemmSmem<BN, WT>;
+  using L = GemmSmem<BN, WT, ONE>;
   static_assert(!SXB || L::TR, "block-scaled activations need the token-lane orientation");
+  static_assert(!ONE || SXB, "single-term activations come with per-block scales");
   constexpr int GT_STAGES = L::STAGES;
   constexpr int GT_NACC = L::NACC;
   extern __shared__ uint8_t smem_raw[];
@@ -250,7 +290,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
           for (int h = 0; h < wt; ++h)
             tma_load_2d(stg + h * W_TILE, map_w, &in_full[st], k0, U.n0 + 128 * h);
           tma_load_2d(stg + L::W_BYTES, &map_hi, &in_full[st], k0, U.m0);
-          tma_load_2d(stg + L::W_BYTES + L::X_TILE, &map_lo, &in_full[st], k0, U.m0);
+          if constexpr (!ONE) tma_load_2d(stg + L::W_BYTES + L::X_TILE, &map_lo, &in_full[st], k0, U.m0);
         }
       }
       // Never leave the CTA with copies in flight: wait (bounded) for the last ones.
@@ -287,7 +327,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
 #pragma unroll
             for (int k = 0; k < 4; ++k) {  // descriptor address field counts 16-byte units
               mma_e4m3(d, h0 + 2 * k, b0 + 2 * k, id, k > 0);
-              mma_e4m3(d, l0 + 2 * k, b0 + 2 * k, id, true);
+              if constexpr (!ONE) mma_e4m3(d, l0 + 2 * k, b0 + 2 * k, id, true);
             }
           } else {
             // D[feature, token]: A = the weight tile, B = token tile (hi, then lo).
@@ -484,20 +524,20 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
   }
 }
 
-template <int BN, int WT, bool SXB>
+template <int BN, int WT, bool SXB, bool ONE = false>
 cudaError_t launch_bn(const CUtensorMap* w, const CUtensorMap& hi, const CUtensorMap& lo,
                       const GemmTcArgs& a, int num_sms, cudaStream_t st) {
   const int grid = a.units < num_sms ? a.units : num_sms;
-  gemm_f8w_tc_kernel<BN, WT, SXB><<<grid, GT_THREADS, GemmSmem<BN, WT>::BYTES, st>>>(
+  gemm_f8w_tc_kernel<BN, WT, SXB, ONE><<<grid, GT_THREADS, GemmSmem<BN, WT, ONE>::BYTES, st>>>(
       w[0], w[1], hi, lo, a);
   return cudaGetLastError();
 }
 
-template <int BN, int WT, bool SXB>
+template <int BN, int WT, bool SXB, bool ONE = false>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_f8w_tc_kernel<BN, WT, SXB>,
+  return cudaFuncSetAttribute(gemm_f8w_tc_kernel<BN, WT, SXB, ONE>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              GemmSmem<BN, WT>::BYTES);
+                              GemmSmem<BN, WT, ONE>::BYTES);
 }
 
 constexpr size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -533,6 +573,8 @@ cudaError_t init_gemm_tc_kernels() {
   if (e == cudaSuccess) e = set_smem_attr<128, 2, false>();
   if (e == cudaSuccess) e = set_smem_attr<128, 1, true>();
   if (e == cudaSuccess) e = set_smem_attr<128, 2, true>();
+  if (e == cudaSuccess) e = set_smem_attr<128, 1, true, true>();
+  if (e == cudaSuccess) e = set_smem_attr<128, 2, true, true>();
   return e;
 }
 
@@ -542,9 +584,11 @@ namespace {
 // k block) (sxb = true) scales; split-K partials in `partial`.
 cudaError_t gemm_tc_core(const uint8_t* hi, const uint8_t* lo, const float* sx, bool sxb, int M,
                          int K, const Proj* p, int np, float* partial, int num_sms, int* err,
-                         cudaStream_t st, int* adv, int adv_n, int adv_by) {
+                         cudaStream_t st, int* adv, int adv_n, int adv_by, bool one = false) {
   const int bn = gemm_bn(M);
   if (sxb && bn != 128) return cudaErrorInvalidValue;
+  if (one && !sxb) return cudaErrorInvalidValue;
+  if (one) lo = hi;  // not read; the tensor map only needs a valid address
   cudaError_t e = cudaSuccess;
   GemmTcArgs a{};
   a.M = M;
@@ -585,7 +629,10 @@ cudaError_t gemm_tc_core(const uint8_t* hi, const uint8_t* lo, const float* sx, 
     case 32: e = launch_bn<32, 1, false>(mw, mh, ml, a, num_sms, st); break;
     case 64: e = launch_bn<64, 1, false>(mw, mh, ml, a, num_sms, st); break;
     default:
-      if (sxb)
+      if (one)
+        e = wt == 2 ? launch_bn<128, 2, true, true>(mw, mh, ml, a, num_sms, st)
+                    : launch_bn<128, 1, true, true>(mw, mh, ml, a, num_sms, st);
+      else if (sxb)
         e = wt == 2 ? launch_bn<128, 2, true>(mw, mh, ml, a, num_sms, st)
                     : launch_bn<128, 1, true>(mw, mh, ml, a, num_sms, st);
       else
@@ -628,12 +675,20 @@ bool gemm_takes_split_blocks(int M) { return gemm_bn(M) == 128; }
 cudaError_t launch_gemm_tc_split(const uint8_t* hi, const uint8_t* lo, const float* sx,
                                  bool block_scales, int M, int K, const Proj* p, int np,
                                  float* scratch, int num_sms, int* err, cudaStream_t st, int* adv,
-                                 int adv_n, int adv_by) {
-  if (!scratch || !hi || !lo || !sx || M <= kGemvMaxM ||
-      (block_scales && !gemm_takes_split_blocks(M)))
+                                 int adv_n, int adv_by, bool one_term) {
+  if (!scratch || !hi || (!lo && !one_term) || !sx || M <= kGemvMaxM ||
+      (block_scales && !gemm_takes_split_blocks(M)) || (one_term && !block_scales))
     return cudaErrorInvalidValue;
   return gemm_tc_core(hi, lo, sx, block_scales, M, K, p, np, scratch, num_sms, err, st, adv,
-                      adv_n, adv_by);
+                      adv_n, adv_by, one_term);
+}
+
+cudaError_t launch_quant_e4m3_groups(const __nv_bfloat16* X, int ldx, int M, int K, uint8_t* q,
+                                     float* sx, cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  if (K % BLK != 0 || K > 8192) return cudaErrorInvalidValue;
+  quant_e4m3_groups_kernel<<<M, K / 8, 0, st>>>(X, ldx, K, q, sx);
+  return cudaGetLastError();
 }
 
 }  // namespace mla

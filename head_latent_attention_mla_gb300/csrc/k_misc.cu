@@ -153,7 +153,27 @@ __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
       if (ckv_out) *reinterpret_cast<uint4*>(ckv_out + (size_t)token * KV_LORA + c0) = o4;
     }
   }
-  if (q_split.hi != nullptr || kv_split.hi != nullptr) {  // the same for every CTA
+  const bool grouped = q_split.hi != nullptr ? q_split.groups != 0 : kv_split.groups != 0;
+  if ((q_split.hi != nullptr || kv_split.hi != nullptr) && grouped) {  // the same for every CTA
+    // Single e4m3 term with one scale per 128-wide group: the group is 16 consecutive threads.
+    float g = am;
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, off));
+    const E4m3Split& o = is_q ? q_split : kv_split;
+    if ((!is_q || do_q) && o.hi != nullptr) {
+      const float sg = g > 0.f ? g / 448.f : 1.f, inv = 1.f / sg;
+      const int n = is_q ? Q_LORA : KV_LORA;
+      uint32_t h[2] = {0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_fp8x2_storage_t pk = __nv_cvt_float2_to_fp8x2(
+            make_float2(y[2 * i] * inv, y[2 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+        h[i >> 1] |= (uint32_t)pk << (16 * (i & 1));
+      }
+      *reinterpret_cast<uint2*>(o.hi + (size_t)token * n + c0) = make_uint2(h[0], h[1]);
+      if ((tid & 15) == 0) o.sx[(size_t)token * (n / BLK) + c0 / BLK] = sg;
+    }
+  } else if (q_split.hi != nullptr || kv_split.hi != nullptr) {  // the same for every CTA
     const float2 m2 = block_max2(is_q ? am : 0.f, is_q ? 0.f : am, red2);
     if (is_q && do_q && q_split.hi != nullptr) {
       store_e4m3_split8(y, m2.x, (size_t)token * Q_LORA + c0, q_split);
@@ -502,7 +522,7 @@ cudaError_t launch_norm_rope_cache(const float* g1, int B, int T, const __nv_bfl
                                    __nv_bfloat16* ckv_out, int* err, cudaStream_t st, bool pdl,
                                    const E4m3Split* q_split, const E4m3Split* kv_split) {
   if (B * T == 0) return cudaSuccess;
-  const E4m3Split none{nullptr, nullptr, nullptr};
+  const E4m3Split none{nullptr, nullptr, nullptr, 0};
   return launch_kernel(norm_rope_cache_kernel, dim3(B * T), dim3(256), 0, st, pdl, g1, T, gq, gkv,
                        eps, rope_tab, rope_pairing, seq_lens, cache, limit, cq_out, ckv_out,
                        err, q_split ? *q_split : none, kv_split ? *kv_split : none);

@@ -199,6 +199,37 @@ mla_status paged_ref(const mla_paged_cache* pc, CacheRef* out) {
   return MLA_OK;
 }
 
+// Whether a projection of M token rows takes the FP8-activation option's single-term path.
+bool fp8_path(const mla_ctx* c, long M) { return c->cfg.fp8_activations && gemm_takes_split_blocks((int)M); }
+
+// Y = X W^T of bf16 activations X [M, K] (row stride ldx): launch_gemm, or with the
+// FP8-activation option the group quantisation of X into the scratch (q, then its scales
+// where the second activation term would go) and the single-term GEMM.
+cudaError_t proj_bf16(const mla_ctx* c, const __nv_bfloat16* X, int ldx, int M, int K,
+                      const Proj* p, int np, float* scratch, cudaStream_t s, int* adv = nullptr,
+                      int adv_n = 0, int adv_by = 0, bool pdl = false) {
+  if (!fp8_path(c, M))
+    return launch_gemm(X, ldx, M, K, p, np, scratch, c->num_sms, c->d_err, s, adv, adv_n, adv_by,
+                       pdl);
+  uint8_t* q = reinterpret_cast<uint8_t*>(scratch);
+  float* sx = reinterpret_cast<float*>(q + up256((size_t)M * K));
+  float* partial = reinterpret_cast<float*>(q + 2 * up256((size_t)M * K) + up256((size_t)M * 4));
+  cudaError_t e = launch_quant_e4m3_groups(X, ldx, M, K, q, sx, s);
+  if (e != cudaSuccess) return e;
+  return launch_gemm_tc_split(q, nullptr, sx, true, M, K, p, np, partial, c->num_sms, c->d_err, s,
+                              adv, adv_n, adv_by, true);
+}
+
+// The norm kernel's e4m3 output for q_b / kv_b over M token rows of n values, in the
+// workspace region at `off` (sized for bf16): hi, then lo (the default pair, with one scale per
+// token at sx_off), or with the FP8-activation option hi alone, its per-(token, 128-group)
+// scales taking lo's place.
+E4m3Split latent_split(const mla_ctx* c, void* ws, size_t off, size_t sx_off, long M, int n) {
+  uint8_t* hi = at<uint8_t>(ws, off);
+  if (fp8_path(c, M)) return E4m3Split{hi, nullptr, reinterpret_cast<float*>(hi + (size_t)M * n), 1};
+  return E4m3Split{hi, hi + (size_t)M * n, at<float>(ws, sx_off), 0};
+}
+
 // The layer's input: x itself, or with block = 1 its input RMSNorm, written to the workspace by
 // a first kernel (recorded in the call's launch log).  nullptr if that launch fails.
 const __nv_bfloat16* block_input(mla_ctx* c, const void* x, int M, void* ws, const Layout& L,
@@ -227,7 +258,7 @@ mla_status cache_append_impl(mla_ctx* c, const void* x, int B, int T, const Cach
   if (!X) return MLA_ERR_CUDA;
   float* g1 = at<float>(ws, L.g1);
   Proj p{c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1};
-  MLA_LAUNCH("gemm_kv_a", launch_gemm(X, HIDDEN, M, HIDDEN, &p, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s, nullptr, 0, 0, c->cfg.block != 0));
+  MLA_LAUNCH("gemm_kv_a", proj_bf16(c, X, HIDDEN, M, HIDDEN, &p, 1, at<float>(ws, L.gpart), s, nullptr, 0, 0, c->cfg.block != 0));
   MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
                                     c->cfg.rope_pairing, lens_dev, CR, limit, nullptr,
                                     nullptr, c->d_err, s));
@@ -269,20 +300,20 @@ mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef&
 
   Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
                 {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
-  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, M, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+  MLA_LAUNCH("gemm_q_a_kv_a", proj_bf16(c, X, HIDDEN, M, HIDDEN, p1, 2, at<float>(ws, L.gpart), s));
   Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
   Proj p3{c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], KVB_N, kv, KVB_N, 0};
   if (chunked) {
     // Keys and values of the cached and the new positions: kv_b_proj over each sequence's
     // cache rows 0 .. L_b + T - 1 (the first 512 values of a row are its normalised latent),
     // after the norm kernel has appended the new rows.
-    const E4m3Split qsp{at<uint8_t>(ws, L.cq), at<uint8_t>(ws, L.cq) + (size_t)M * Q_LORA,
-                        at<float>(ws, L.cq_sx)};
+    const E4m3Split qsp = latent_split(c, ws, L.cq, L.cq_sx, M, Q_LORA);
     MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
                                       c->cfg.rope_pairing, lens_dev, CR, limit, M > kGemvMaxM ? nullptr : cq,
                                       nullptr, c->d_err, s, false, M > kGemvMaxM ? &qsp : nullptr, nullptr));
     if (M > kGemvMaxM) {
-      MLA_LAUNCH("gemm_q_b", launch_gemm_tc_split(qsp.hi, qsp.lo, qsp.sx, false, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+      MLA_LAUNCH("gemm_q_b", launch_gemm_tc_split(qsp.hi, qsp.lo, qsp.sx, qsp.groups != 0, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
+                                                  nullptr, 0, 0, qsp.groups != 0));
     } else {
       MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
     }
@@ -293,29 +324,30 @@ mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef&
       __nv_bfloat16* lat = at<__nv_bfloat16>(ws, L.gather);
       MLA_LAUNCH("gather_latent", launch_gather_latent(CR, lens_dev, B, T, (int)kvb_M, kv_rows, lat,
                                                        c->d_err, s));
-      MLA_LAUNCH("gemm_kv_b", launch_gemm(lat, KV_LORA, (int)kv_rows, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+      MLA_LAUNCH("gemm_kv_b", proj_bf16(c, lat, KV_LORA, (int)kv_rows, KV_LORA, &p3, 1, at<float>(ws, L.gpart), s));
     } else {
       long r0 = 0;
       for (int b = 0; b < B; ++b) {
         const int Mb = lens_host[b] + T;
         const Proj pb{c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], KVB_N, kv + (size_t)r0 * KVB_N, KVB_N, 0};
-        MLA_LAUNCH("gemm_kv_b", launch_gemm(CR.base + (size_t)b * CR.page * LAT, LAT, Mb, KV_LORA, &pb, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+        MLA_LAUNCH("gemm_kv_b", proj_bf16(c, CR.base + (size_t)b * CR.page * LAT, LAT, Mb, KV_LORA, &pb, 1, at<float>(ws, L.gpart), s));
         r0 += Mb;
       }
     }
   } else if (M > kGemvMaxM) {
     // Tensor-core projections: the norm kernel writes q_b's and kv_b's e4m3 inputs itself (the
     // two terms share the bf16 latents' regions; one scale per token).
-    const E4m3Split qsp{at<uint8_t>(ws, L.cq), at<uint8_t>(ws, L.cq) + (size_t)M * Q_LORA,
-                        at<float>(ws, L.cq_sx)};
-    const E4m3Split kvsp{at<uint8_t>(ws, L.ckv), at<uint8_t>(ws, L.ckv) + (size_t)M * KV_LORA,
-                         at<float>(ws, L.ckv_sx)};
+    const E4m3Split qsp = latent_split(c, ws, L.cq, L.cq_sx, M, Q_LORA);
+    const E4m3Split kvsp = latent_split(c, ws, L.ckv, L.ckv_sx, M, KV_LORA);
+    const bool one = qsp.groups != 0;
     MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
                                       c->cfg.rope_pairing, lens_dev, CR, limit, nullptr, nullptr,
                                       c->d_err, s, false, &qsp, &kvsp));
-    MLA_LAUNCH("gemm_q_b", launch_gemm_tc_split(qsp.hi, qsp.lo, qsp.sx, false, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+    MLA_LAUNCH("gemm_q_b", launch_gemm_tc_split(qsp.hi, qsp.lo, qsp.sx, one, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
+                                                nullptr, 0, 0, one));
     MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
-    MLA_LAUNCH("gemm_kv_b", launch_gemm_tc_split(kvsp.hi, kvsp.lo, kvsp.sx, false, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+    MLA_LAUNCH("gemm_kv_b", launch_gemm_tc_split(kvsp.hi, kvsp.lo, kvsp.sx, one, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
+                                                 nullptr, 0, 0, one));
   } else {
     MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
                                       c->cfg.rope_pairing, lens_dev, CR, limit, cq, ckv,
@@ -333,8 +365,10 @@ mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef&
     MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, CR, B, T, chunked ? lens_dev : nullptr,
                                                               chunked ? kv_rows : M, c->cfg.softmax_scale, nullptr,
                                                               a_hi, a_lo, a_sx, c->d_err, s));
+    // With the FP8-activation option o_proj multiplies the high term alone: e4m3 of the
+    // attention output over its own per-(token, head) scale, a head being one 128-wide group.
     MLA_LAUNCH("gemm_o", launch_gemm_tc_split(a_hi, a_lo, a_sx, true, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
-                                              lens_dev, B, T));
+                                              lens_dev, B, T, fp8_path(c, M)));
   } else {
     MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, CR, B, T, chunked ? lens_dev : nullptr,
                                                               chunked ? kv_rows : M, c->cfg.softmax_scale, attn,
@@ -460,6 +494,7 @@ void mla_default_config(mla_config* cfg) {
   cfg->yarn_mscale = 1.0f;
   cfg->yarn_mscale_all_dim = 1.0f;
   cfg->block = 0;
+  cfg->fp8_activations = 0;
 }
 
 mla_status mla_create(const mla_config* cfg, mla_ctx** out) {
@@ -475,6 +510,7 @@ mla_status mla_create(const mla_config* cfg, mla_ctx** out) {
   if (cfg->rope_scaling != MLA_ROPE_PLAIN && cfg->rope_scaling != MLA_ROPE_YARN)
     return MLA_ERR_INVALID_ARG;
   if (cfg->block != 0 && cfg->block != 1) return MLA_ERR_INVALID_ARG;
+  if (cfg->fp8_activations != 0 && cfg->fp8_activations != 1) return MLA_ERR_INVALID_ARG;
   if (cfg->rope_scaling == MLA_ROPE_YARN &&
       (!(cfg->yarn_factor >= 1.f) || cfg->yarn_original_max_positions <= 0 ||
        !(cfg->yarn_beta_fast > 0.f) || !(cfg->yarn_beta_slow > 0.f) ||

@@ -180,10 +180,17 @@ cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const 
 // (token, 128-wide k block), sx [M, K/128] (X[m, k] ~ sx[m][k/128] (hi + lo)); block scales
 // are accepted when gemm_takes_split_blocks(M).  `partial` as for launch_gemm_tc.
 bool gemm_takes_split_blocks(int M);
+// one_term (the FP8-activation option, with block_scales): the activations are the single
+// e4m3 term hi (lo is not read), X[m, k] ~ sx[m][k/128] hi[m, k]: one MMA per k step.
 cudaError_t launch_gemm_tc_split(const uint8_t* hi, const uint8_t* lo, const float* sx,
                                  bool block_scales, int M, int K, const Proj* p, int np,
                                  float* partial, int num_sms, int* err, cudaStream_t st,
-                                 int* adv = nullptr, int adv_n = 0, int adv_by = 0);
+                                 int* adv = nullptr, int adv_n = 0, int adv_by = 0,
+                                 bool one_term = false);
+// The FP8-activation option's input quantisation: q [M, K] = e4m3(X / sx) with one scale per
+// (token, 128-wide group), sx [M, K/128] = amax / 448 (K a multiple of 128, at most 8192).
+cudaError_t launch_quant_e4m3_groups(const __nv_bfloat16* X, int ldx, int M, int K, uint8_t* q,
+                                     float* sx, cudaStream_t st);
 cudaError_t init_gemm_tc_kernels();
 
 // RMSNorm of the q latent and kv latent, RoPE of k_pe, cache row store.  Positions at or
@@ -198,6 +205,9 @@ struct E4m3Split {
   uint8_t* hi;  // [M, n]
   uint8_t* lo;  // [M, n]
   float* sx;    // [M]
+  // 1: the FP8-activation option's single term instead: hi = e4m3(v / s) with one scale per
+  // (token, 128-wide group), sx [M, n/128]; lo is not written.
+  int groups = 0;
 };
 cudaError_t launch_norm_rope_cache(const float* g1, int B, int T, const __nv_bfloat16* gq,
                                    const __nv_bfloat16* gkv, float eps, const float2* rope_tab,

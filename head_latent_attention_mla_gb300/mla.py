@@ -34,7 +34,7 @@ class mla_config(ctypes.Structure):
                 ("yarn_factor", ctypes.c_float), ("yarn_original_max_positions", ctypes.c_int),
                 ("yarn_beta_fast", ctypes.c_float), ("yarn_beta_slow", ctypes.c_float),
                 ("yarn_mscale", ctypes.c_float), ("yarn_mscale_all_dim", ctypes.c_float),
-                ("block", ctypes.c_int)]
+                ("block", ctypes.c_int), ("fp8_activations", ctypes.c_int)]
 
 
 class mla_paged_cache(ctypes.Structure):

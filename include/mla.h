@@ -72,6 +72,7 @@ typedef struct {
   float yarn_mscale, yarn_mscale_all_dim;   /* rope_scaling.mscale / mscale_all_dim (1, 1) */
   int block;           /* 0: the layer alone (default); 1: the attention half of a decoder
                           block around it (see below)                                   */
+  int fp8_activations; /* 0 (default) or 1: FP8 activations in the large projections      */
 } mla_config;
 
 /* Fills *cfg with Kimi-K2's dimensions (config.json on the "KV cache" page), eps 1e-6,
@@ -86,6 +87,16 @@ typedef struct {
  * m(factor, mscale_all_dim) and the score scale by m(factor, mscale_all_dim)^2, where
  * m(s, mu) = 0.1 mu ln s + 1 for s > 1, else 1. */
 void mla_default_config(mla_config* cfg);
+
+/* FP8 activations (fp8_activations = 1; the "linear" excerpt's quantization_config:
+ * activation_scheme dynamic).  Projections of more than 64 token rows in mla_prefill,
+ * mla_cache_append and their paged forms quantise their input to one e4m3 term per value
+ * with one scale per (token, 128-wide group), s = amax / 448, and run one FP8 tensor-core
+ * product per 128-wide k block instead of the two of the default, which multiplies the
+ * bf16 input as an exact-to-2^-8 pair of e4m3 terms.  This is lossy: e4m3 keeps 3 mantissa
+ * bits, and the layer output then misses the default bar of relative Frobenius error 1e-2
+ * against the exact layer (measured values are in the design notes).  Decode and
+ * projections of at most 64 rows are unchanged. */
 
 /* The attention half of a decoder block (block = 1).  The "Attention input" page's `block`
  * excerpt keeps the block's input as the residual, normalises it with input_layernorm (the
