@@ -19,7 +19,7 @@ from tests.mla_cases import (MARGINS, build_caches_gpu, errors, oracle_cache, or
                              oracle_weights, to_dev, weights_and_gains)
 
 pytestmark = pytest.mark.gpu
-FP8_REL, FP8_ABS = 0.2, 0.5
+FP8_REL, FP8_ABS = 0.1, 0.3     # measured at most 5.9e-2 and 1.95e-1
 
 
 @pytest.fixture(scope="module")
