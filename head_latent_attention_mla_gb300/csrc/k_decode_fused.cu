@@ -16,7 +16,7 @@
 //      the kv-latent RMSNorm, RoPE of the shared rotary key and the cache row append
 //   3  W_UK absorption and RoPE of q_pe -> qfull [M, 64, 576] bf16
 //   4  attention over the latent cache on the CUDA cores: unit (sequence, 8 heads, position
-//      chunk) with an online softmax over 32-position sub-tiles -> fp32 partials (O, m, l)
+//      chunk) with an online softmax over 64-position sub-tiles -> fp32 partials (O, m, l)
 //   5  combine of the partials (per head) and W_UV -> attn [M, 8192] bf16
 //   6  o_proj -> out [M, 7168] bf16; CTA 0 advances the lengths
 // The projections (stages 1, 2, 6) give each warp a fixed 512-wide k-slice of the input held in
@@ -36,7 +36,7 @@ constexpr int FD_THREADS = 512;
 constexpr int FD_WARPS = FD_THREADS / 32;
 constexpr int FD_QB_ROWS = 96;          // q_b rows a CTA holds: needs at least 128 CTAs
 constexpr int FD_HG = 8;                // heads of one attention unit
-constexpr int FD_TP = 32;               // positions of one attention sub-tile
+constexpr int FD_TP = 64;               // positions of one attention sub-tile
 constexpr int FD_RED = 56 * 16 * 2;     // floats of the k-slice partials (rows x slices x M)
 // Region B (floats): the partials, then 1/rms per token, per-warp sums, an abort flag and the kv
 // cache row being built (576 bf16).
@@ -158,7 +158,7 @@ __device__ void gemv_rows(int r0, int r1, const float (&xr)[M][16], RowPtr row_p
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slice = warp % KS, grp = warp / KS;
   const int k0 = slice * 512 + lane * 16;
-  constexpr int RB = 4;  // rows in flight per warp
+  constexpr int RB = 8;  // rows in flight per warp
   if (grp < NG) {
     for (int rb = r0 + grp; rb < r1; rb += NG * RB) {
       uint4 w[RB];
@@ -265,8 +265,9 @@ __global__ void __launch_bounds__(FD_THREADS, 1) decode_fused_kernel(const __gri
     for (uint32_t o = 0; o < bytes; o += 32768u)
       bulk_load(sA + o, src + o, bytes - o < 32768u ? bytes - o : 32768u, qb_bar);
   } else if (warp == 1) {
-    // W_UK of this CTA's stage-3 heads (rows 256h .. 256h+127 of kv_b, 64 KB each), W_UV of its
-    // stage-5 units (32 rows, 16 KB each), then its o_proj rows, in 64 KB prefetches.
+    // W_UK of this CTA's stage-3 heads (rows 256h .. 256h+127 of kv_b, 64 KB each) and W_UV of
+    // its stage-5 units (32 rows, 16 KB each).  (The o_proj rows follow after stage 1, whose
+    // own reads would otherwise queue behind them.)
     const uint8_t* kvb = a.W[MLA_W_KV_B];
     for (int u = u3a + lane; u < u3b; u += 32)
       if (u == u3a || u % 4 == 0) prefetch_l2_bulk(kvb + (size_t)(u / 4) * KVB_PER_HEAD * KV_LORA, 65536u);
@@ -274,10 +275,6 @@ __global__ void __launch_bounds__(FD_THREADS, 1) decode_fused_kernel(const __gri
       const int h = (u / 4) % HEADS, vb = u % 4;
       prefetch_l2_bulk(kvb + ((size_t)h * KVB_PER_HEAD + NOPE + 32 * vb) * KV_LORA, 16384u);
     }
-    const uint8_t* wo = a.W[MLA_W_O] + (size_t)r6a * O_IN;
-    const size_t ob = (size_t)(r6b - r6a) * O_IN;
-    for (size_t o = (size_t)lane * 65536u; o < ob; o += 32 * 65536u)
-      prefetch_l2_bulk(wo + o, (uint32_t)(ob - o < 65536u ? ob - o : 65536u));
   }
 
   // ---- stage 1: q_a_proj | kv_a_proj_with_mqa -> g1 -------------------------------------------
@@ -301,6 +298,12 @@ __global__ void __launch_bounds__(FD_THREADS, 1) decode_fused_kernel(const __gri
   }
 
   // ---- stage 2: q-latent norm, q_b_proj; kv-latent norm, RoPE(k_pe), cache row --------------
+  if (warp == 1) {  // this CTA's o_proj rows, into L2 while stages 2-5 run
+    const uint8_t* wo = a.W[MLA_W_O] + (size_t)r6a * O_IN;
+    const size_t ob = (size_t)(r6b - r6a) * O_IN;
+    for (size_t o = (size_t)lane * 65536u; o < ob; o += 32 * 65536u)
+      prefetch_l2_bulk(wo + o, (uint32_t)(ob - o < 65536u ? ob - o : 65536u));
+  }
   {
     float* rs = sB + B_RS;  // [M] 1 / rms of the q latent
     {
@@ -443,8 +446,8 @@ __global__ void __launch_bounds__(FD_THREADS, 1) decode_fused_kernel(const __gri
       const int m = u / ((HEADS / FD_HG) * a.npc);
       const int hg = (u / a.npc) % (HEADS / FD_HG), pc = u % a.npc;
       float* q8 = reinterpret_cast<float*>(sA);                        // [8][576]
-      __nv_bfloat16* ct = reinterpret_cast<__nv_bfloat16*>(sA + FD_HG * LAT * 4);  // [32][576]
-      float* sp = reinterpret_cast<float*>(sA + FD_HG * LAT * 4 + FD_TP * LAT * 2);  // [8][32]
+      __nv_bfloat16* ct = reinterpret_cast<__nv_bfloat16*>(sA + FD_HG * LAT * 4);  // [64][576]
+      float* sp = reinterpret_cast<float*>(sA + FD_HG * LAT * 4 + FD_TP * LAT * 2);  // [8][64]
       float* alpha = sp + FD_HG * FD_TP;                               // [8]
       const int S = a.seq_lens[m] + 1;
       const int cs = (S + a.npc - 1) / a.npc;
@@ -486,21 +489,24 @@ __global__ void __launch_bounds__(FD_THREADS, 1) decode_fused_kernel(const __gri
           if (lane == 0) sp[hh * FD_TP + j] = j < nt ? s * a.scale_log2 : -INFINITY;
         }
         __syncthreads();
-        // Online softmax: warp hh < 8 owns head hh's statistics, lane j its position j.
+        // Online softmax: warp hh < 8 owns head hh's statistics, lane j positions j and j + 32.
+        static_assert(FD_TP == 64, "two positions per lane");
         if (warp < FD_HG) {
-          const float s = sp[warp * FD_TP + lane];
-          float mx = s;
+          const float s0 = sp[warp * FD_TP + lane], s1 = sp[warp * FD_TP + lane + 32];
+          float mx = fmaxf(s0, s1);
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
           const float mnew = fmaxf(mrun, mx);
-          const float p = lane < nt ? exp2f(s - mnew) : 0.f;
-          float ps = p;
+          const float p0 = lane < nt ? exp2f(s0 - mnew) : 0.f;
+          const float p1 = lane + 32 < nt ? exp2f(s1 - mnew) : 0.f;
+          float ps = p0 + p1;
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
           const float al = mrun == -INFINITY ? 0.f : exp2f(mrun - mnew);
           lrun = lrun * al + ps;
           mrun = mnew;
-          sp[warp * FD_TP + lane] = p;
+          sp[warp * FD_TP + lane] = p0;
+          sp[warp * FD_TP + lane + 32] = p1;
           if (lane == 0) alpha[warp] = al;
         }
         __syncthreads();
