@@ -150,10 +150,6 @@ def algorithmic_bytes(kernel, B, lengths):
         # few sequences: the split combine fused with the W_UV absorption
         "combine_absorb_out": 64 * 128 * 512 + 64 * 4 * 4 + B * 64 * 512 * 2 + B * 8192 * 2,
         "advance_lens": B * 8,
-        # one or two short sequences: the whole step in one kernel (every weight once, the
-        # cache, the appended rows and the activations)
-        "decode_fused": (sum(wbytes(n) for n in WEIGHT_SHAPES) + S * LAT_BYTES
-                         + B * (7168 * 2 * 2 + LAT_BYTES)),
     }.get(kernel, 0)
 
 

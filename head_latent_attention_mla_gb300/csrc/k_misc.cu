@@ -655,7 +655,6 @@ cudaError_t init_kernels() {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ABT_SMEM);
   if (e == cudaSuccess) e = init_decode_tc_kernel();
   if (e == cudaSuccess) e = init_prefill_tc_kernel();
-  if (e == cudaSuccess) e = init_decode_fused_kernel();
   return e != cudaSuccess ? e : init_gemm_tc_kernels();
 }
 

@@ -416,39 +416,6 @@ mla_status decode_impl(mla_ctx* c, const void* x, int B, const CacheRef& CR, int
   __nv_bfloat16* olat = at<__nv_bfloat16>(ws, L.olat);
   __nv_bfloat16* attn = at<__nv_bfloat16>(ws, L.attn);
 
-  int max_len = 0;
-  for (int b = 0; b < B; ++b) max_len = lens_host[b] > max_len ? lens_host[b] : max_len;
-  if (!c->cfg.block && decode_fused_supports(B, max_len, c->num_sms)) {
-    // One or two sequences with a short cache: the whole step as one persistent kernel.
-    FusedDecode d{};
-    d.B = B;
-    d.num_sms = c->num_sms;
-    for (int i = 0; i < 5; ++i) {
-      d.W[i] = c->W[i];
-      d.S[i] = c->S[i];
-    }
-    d.gq = c->gain[0];
-    d.gkv = c->gain[1];
-    d.eps = c->cfg.eps;
-    d.rope_tab = c->rope_tab;
-    d.pairing = c->cfg.rope_pairing;
-    d.x = X;
-    d.cache = CR;
-    d.limit = limit;
-    d.seq_lens = lens_dev;
-    d.scale = c->cfg.softmax_scale;
-    d.g1 = g1;
-    d.q = q;
-    d.qfull = qfull;
-    d.opart = at<float>(ws, L.opart);
-    d.ml = ml;
-    d.attn = attn;
-    d.out = static_cast<__nv_bfloat16*>(out);
-    d.bar = reinterpret_cast<unsigned*>(c->d_err + 2);
-    d.err = c->d_err;
-    MLA_LAUNCH("decode_fused", launch_decode_fused(d, s));
-    return MLA_OK;
-  }
   Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
                 {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
   MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s, nullptr, 0, 0, c->cfg.block != 0));
@@ -583,9 +550,9 @@ mla_status mla_create(const mla_config* cfg, mla_ctx** out) {
     delete c;
     return MLA_ERR_CUDA;
   }
-  if (cudaMalloc(&c->d_err, 4 * sizeof(int)) != cudaSuccess ||
+  if (cudaMalloc(&c->d_err, sizeof(int)) != cudaSuccess ||
       cudaMemcpy(c->rope_tab, tab.data(), n * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemset(c->d_err, 0, 4 * sizeof(int)) != cudaSuccess) {
+      cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess) {
     cudaFree(c->rope_tab);
     if (c->d_err) cudaFree(c->d_err);
     delete c;
@@ -725,8 +692,6 @@ mla_status mla_get_device_status(mla_ctx* c, void* stream) {
     return MLA_ERR_CUDA;
   if (cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess) return MLA_ERR_CUDA;
   if (h == DEV_ERR_NONE) return MLA_OK;
-  // A kernel that gave up may have left the fused decode's grid barrier mid-count.
-  if (cudaMemset(c->d_err + 2, 0, 2 * sizeof(int)) != cudaSuccess) return MLA_ERR_CUDA;
   return h == DEV_ERR_TIMEOUT ? MLA_ERR_TIMEOUT : MLA_ERR_STATE;
 }
 

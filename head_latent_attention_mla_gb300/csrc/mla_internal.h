@@ -291,37 +291,6 @@ cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const CacheRe
                                        cudaStream_t st, bool pdl = false);
 cudaError_t init_decode_tc_kernel();
 
-// One decode step for one or two sequences as a single persistent cooperative kernel (one CTA
-// per SM, grid barriers between its six stages), for caches of at most kFusedMaxPositions
-// positions after the step and at least 128 SMs.  Workspace as for the decode chain: g1, q,
-// qfull, the partials (opart [B, chunks, 64, 512] fp32 and ml [B, chunks, 64, 2] fp32, within
-// the chain's partial regions) and attn; bar: two zeroed words of the context.
-constexpr int kFusedMaxPositions = 8192;
-struct FusedDecode {
-  int B, num_sms;
-  const uint8_t* W[5];
-  const float* S[5];
-  const __nv_bfloat16 *gq, *gkv;
-  float eps;
-  const float2* rope_tab;
-  int pairing;
-  const __nv_bfloat16* x;
-  CacheRef cache;
-  int limit;
-  int* seq_lens;
-  float scale;
-  float* g1;
-  __nv_bfloat16 *q, *qfull;
-  float *opart, *ml;
-  __nv_bfloat16 *attn, *out;
-  unsigned* bar;
-  int* err;
-};
-bool decode_fused_supports(int B, int max_len, int num_sms);
-int decode_fused_chunks(int B, int num_sms);
-cudaError_t launch_decode_fused(const FusedDecode& d, cudaStream_t st);
-cudaError_t init_decode_fused_kernel();
-
 // Device address of mla_decode_noalloc's static scratch array on the current device.
 cudaError_t noalloc_scratch_address(void** out);
 
@@ -388,8 +357,7 @@ struct mla_ctx {
   const float* S[5] = {};
   const __nv_bfloat16* gain[3] = {};  // q_a_layernorm, kv_a_layernorm, input_layernorm
   float2* rope_tab = nullptr;  // [max_positions][32] (cos, sin)
-  int* d_err = nullptr;       // [4]: the error word, a pad, and the fused decode's grid
-                              // barrier (count, generation), all zero at rest
+  int* d_err = nullptr;
   // Device address, on this context's device, of the static scratch array that
   // mla_decode_noalloc uses (looked up by mla_create, with the device current).
   void* noalloc_scratch = nullptr;

@@ -103,7 +103,7 @@ def test_injected_launch_failure_never_advances_lengths(layer, B, p):
     x = to_dev(xb[:, p])
     ref = layer.decode(x, cache.clone(), lens.clone(), [p] * B)
     n_launch = len(mla.mla_last_launches(layer.ctx))
-    assert n_launch >= 1   # one fused kernel for a single short sequence, a chain for five
+    assert n_launch >= 5
     before = cache[:, :p].clone()
     for n in range(n_launch):
         bad = _injected_layer(n)
