@@ -28,7 +28,8 @@
 //               maximum m and the sum l of every head.
 // A tile's MMA2 does not wait for the previous tile's: only a rescale of O^T needs the previous
 // MMA2 to be complete, and it is rare once a head's maximum has settled.
-// Partial outputs: o_part[slot][dim][head] = O / l (fp16), ml_part[slot][head] = (m, l).
+// Partial outputs: o_part[slot][dim][head] = O / l (fp16), or [slot][head][dim] when
+// head_major is set; ml_part[slot][head] = (m, l).
 // Tensor memory: O^T in columns [0, 256) (lane = latent dim, column = head within each of the
 // four 128-dim blocks), S in [256, 320) and [320, 384) (double buffer).
 #include "tc_common.cuh"
@@ -72,7 +73,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
     const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_c,
     const int* __restrict__ seq_lens, int B, const CacheRef cache, int G, long long P, int K,
     float scale_log2,
-    __half* __restrict__ o_part, float* __restrict__ ml_part, int* err) {
+    __half* __restrict__ o_part, float* __restrict__ ml_part, int* err, int head_major) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
@@ -421,8 +422,10 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
           break;
         // Segment epilogue: O / l, m and l of every head into slot b + cta.  The partial is
         // divided by its own sum, so its values are bounded by those of the cache rows, and
-        // stored as fp16 (11-bit mantissa), head-minor ([dim][head]): a thread writes the 64
-        // heads of its latent dimension (its TMEM lane) as four 32-byte vectors.
+        // stored as fp16 (11-bit mantissa).  Head-minor ([dim][head]): a thread writes the 64
+        // heads of its latent dimension (its TMEM lane) as four 32-byte vectors.  Head-major
+        // ([head][dim]): lanes 2i and 2i+1 (consecutive dims) swap one value per head pair, so
+        // each stores two dims of one head as a 4-byte pair.
         const float lrow = l + __shfl_xor_sync(0xffffffffu, l, 2);
         if (par == 0) {
           s_invl[h] = 1.f / lrow;
@@ -440,18 +443,32 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_tc_kernel(
           tmem_ld32(tmem + lane_off + TM_O + 64 * d, o[0]);
           tmem_ld32(tmem + lane_off + TM_O + 64 * d + 32, o[1]);
           tmem_wait_ld();
-          uint32_t pk[32];
+          if (head_major) {
+            const int odd = lane & 1;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int hh = 2 * e;
-            __half2 v = __floats2half2_rn(__uint_as_float(o[hh >> 5][hh & 31]) * s_invl[hh],
-                                          __uint_as_float(o[(hh + 1) >> 5][(hh + 1) & 31]) *
-                                              s_invl[hh + 1]);
-            pk[e] = *reinterpret_cast<uint32_t*>(&v);
+            for (int e = 0; e < 32; ++e) {
+              const int hh = 2 * e;
+              const float x0 = __uint_as_float(o[hh >> 5][hh & 31]) * s_invl[hh];
+              const float x1 = __uint_as_float(o[(hh + 1) >> 5][(hh + 1) & 31]) * s_invl[hh + 1];
+              // the even lane keeps head hh, the odd lane head hh + 1
+              const float got = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
+              const __half2 v = odd ? __floats2half2_rn(got, x1) : __floats2half2_rn(x0, got);
+              *reinterpret_cast<__half2*>(op + (size_t)(hh + odd) * KV_LORA + (dim - odd)) = v;
+            }
+          } else {
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int hh = 2 * e;
+              __half2 v = __floats2half2_rn(__uint_as_float(o[hh >> 5][hh & 31]) * s_invl[hh],
+                                            __uint_as_float(o[(hh + 1) >> 5][(hh + 1) & 31]) *
+                                                s_invl[hh + 1]);
+              pk[e] = *reinterpret_cast<uint32_t*>(&v);
+            }
+            __half* dst = op + (size_t)dim * HEADS;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) st_global_v8(dst + 16 * v, &pk[8 * v]);
           }
-          __half* dst = op + (size_t)dim * HEADS;
-#pragma unroll
-          for (int v = 0; v < 4; ++v) st_global_v8(dst + 16 * v, &pk[8 * v]);
         }
         fence_before();
         mbar_arrive(o_free);
@@ -507,7 +524,7 @@ cudaError_t init_decode_tc_kernel() {
 cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const CacheRef& cache,
                                        const int* seq_lens, DecodePlan plan,
                                        float scale, __half* o_part, float* ml_part, int* err,
-                                       cudaStream_t st, bool pdl) {
+                                       cudaStream_t st, bool pdl, bool head_major) {
   if (plan.B == 0) return cudaSuccess;
   const long long rows = cache.rows(plan.B);
   if (rows <= 0 || rows + DA_TILE > 0x7FFFFFFFll) return cudaErrorInvalidValue;
@@ -517,7 +534,7 @@ cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const CacheRe
     return cudaErrorInvalidValue;
   return launch_kernel(decode_attn_tc_kernel, dim3(plan.G), dim3(DA_THREADS), DA_SMEM, st, pdl,
                        mq, mc, seq_lens, plan.B, cache, plan.G, plan.P, plan.K,
-                       scale * 1.4426950408889634f, o_part, ml_part, err);
+                       scale * 1.4426950408889634f, o_part, ml_part, err, head_major ? 1 : 0);
 }
 
 }  // namespace mla

@@ -8,6 +8,12 @@ namespace mla {
 namespace {
 
 constexpr int kMaxSplits = kMaxDecodeShares;  // shares one sequence can span
+
+// A half2 partial written by the attention kernel, as two floats.
+__device__ __forceinline__ float2 half2_dep(const __half2* p) {
+  const uint32_t u = ld_dep_u32(p);
+  return __half22float2(*reinterpret_cast<const __half2*>(&u));
+}
 constexpr int kDims = 32;                       // latent dims per CTA
 constexpr int kThreads = 256;
 
@@ -20,7 +26,7 @@ constexpr int kThreads = 256;
 // a thread then owns two heads and four dims, so a warp reads 128 contiguous bytes per dim.
 __global__ void __launch_bounds__(kThreads) decode_combine_kernel(
     const int* __restrict__ seq_lens, int B, int G, long long P, int K,
-    const __half* __restrict__ o_part, const float* __restrict__ ml_part,
+    const __half* o_part, const float* ml_part,
     __nv_bfloat16* __restrict__ o_lat, int* err) {
   const int b = blockIdx.x, tid = threadIdx.x;
   __shared__ int s_first, s_n;
@@ -50,7 +56,7 @@ __global__ void __launch_bounds__(kThreads) decode_combine_kernel(
   {
     const int h = tid & (HEADS - 1), g = tid >> 6;
     float M = -INFINITY;
-    for (int i = g; i < n; i += 4) M = fmaxf(M, ml_part[((size_t)(first + i) * HEADS + h) * 2]);
+    for (int i = g; i < n; i += 4) M = fmaxf(M, ld_dep_f32(ml_part + ((size_t)(first + i) * HEADS + h) * 2));
     s_red[g][h] = M;
     __syncthreads();
     M = fmaxf(fmaxf(s_red[0][h], s_red[1][h]), fmaxf(s_red[2][h], s_red[3][h]));
@@ -58,7 +64,8 @@ __global__ void __launch_bounds__(kThreads) decode_combine_kernel(
     float L = 0.f;
     for (int i = g; i < n; i += 4) {
       const size_t it = (size_t)(first + i) * HEADS + h;
-      const float wl = exp2f(ml_part[it * 2] - M) * ml_part[it * 2 + 1];
+      const float2 v = ld_dep_f32x2(ml_part + it * 2);
+      const float wl = exp2f(v.x - M) * v.y;
       s_w[i * HEADS + h] = wl;
       L += wl;
     }
@@ -80,7 +87,8 @@ __global__ void __launch_bounds__(kThreads) decode_combine_kernel(
     const __half2* oi = op + i * step;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float2 v = __half22float2(oi[e * (HEADS / 2)]);
+      const uint32_t u = ld_dep_u32(oi + e * (HEADS / 2));
+      const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&u));
       acc[0][e] = fmaf(w0, v.x, acc[0][e]);
       acc[1][e] = fmaf(w1, v.y, acc[1][e]);
     }
@@ -96,34 +104,40 @@ __global__ void __launch_bounds__(kThreads) decode_combine_kernel(
   }
 }
 
-// Combine and output absorption of one (head h, sequence b) for a few decode sequences:
+// Combine and output absorption for a few decode sequences, CTA (h, vb, b) for head h, rows
+// 32 vb .. 32 vb + 31 of W_UV,h and sequence b:
 //   o_lat = sum_i v_i o_i as in decode_combine_kernel (rounded to bf16), then
 //   attn[b][128 h + v] = sum_c s[2h+1][c/128] * e4m3(W_kvb[256 h + 128 + v][c]) * o_lat[c]
-// ("Key content up-projection" page, W_UV,h = rows 128..255 of head h's 256).  Each warp owns 16
-// rows of W_UV,h, loaded into registers before the wait on the attention; one CTA per (h, b).
-// The share ranges come from the host's plan (and the device length is checked against it),
-// and every load after the wait is issued at once: the work after the attention is one memory
-// round trip.
+// ("Key content up-projection" page, W_UV,h = rows 128..255 of head h's 256).  The partials
+// are head-major ([slot][head][dim], fp16), so the 1 KB of head h in each share is one
+// contiguous read; each of the four CTAs of a head merges them again (from L2) rather than
+// wait for one another.  Each warp owns 4 rows of W_UV,h, loaded into registers before the
+// wait on the attention.  The share ranges come from the host's plan (and the device length is
+// checked against it), and every load after the wait is issued at once: the work after the
+// attention is one memory round trip.
 struct ShareRanges {
   int first[8], n[8], len[8];  // slot of the first share, number of shares, length (host)
 };
 constexpr int CAO_BATCH = 16;  // shares per round of loads
+constexpr int CAO_SPLIT = 4;   // CTAs per (head, sequence)
+constexpr int CAO_ROWS = VDIM / CAO_SPLIT / 8;  // rows of W_UV,h per warp
 
 __global__ void __launch_bounds__(256) combine_absorb_out_kernel(
     const int* __restrict__ seq_lens, const __grid_constant__ ShareRanges sr,
-    const __half* __restrict__ o_part, const float* __restrict__ ml_part,
+    const __half* o_part, const float* ml_part,
     const uint8_t* __restrict__ Wkvb, const float* __restrict__ Skvb,
     __nv_bfloat16* __restrict__ attn, int* err) {
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int h = blockIdx.x, vb = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  const int v0 = VDIM / CAO_SPLIT * vb + CAO_ROWS * warp;  // this warp's first row
   __shared__ float s_w[kMaxSplits];
   __shared__ float s_red[8];
   __shared__ __align__(16) float ol[KV_LORA];
-  uint4 wv[16];
+  uint4 wv[CAO_ROWS];
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
+  for (int r = 0; r < CAO_ROWS; ++r) {
     const uint8_t* src =
-        Wkvb + ((size_t)h * KVB_PER_HEAD + NOPE + 16 * warp + r) * KV_LORA + lane * 16;
+        Wkvb + ((size_t)h * KVB_PER_HEAD + NOPE + v0 + r) * KV_LORA + lane * 16;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(wv[r].x), "=r"(wv[r].y), "=r"(wv[r].z), "=r"(wv[r].w)
                  : "l"(src));
@@ -132,23 +146,22 @@ __global__ void __launch_bounds__(256) combine_absorb_out_kernel(
   const int first = sr.first[b], n = sr.n[b];
   pdl_launch_dependents();
   pdl_wait();  // the attention's partials are complete
-  // Loads first: (m, l) of share tid, and this thread's two dims of the first shares.
+  // Loads first: (m, l) of share tid, and this thread's dims 2 tid, 2 tid + 1 of the first
+  // shares.
   const bool own = tid < n;
   float mi = -INFINITY, li = 0.f;
   if (own) {
-    const float2 v = *reinterpret_cast<const float2*>(ml_part + ((size_t)(first + tid) * HEADS + h) * 2);
+    const float2 v = ld_dep_f32x2(ml_part + ((size_t)(first + tid) * HEADS + h) * 2);
     mi = v.x;
     li = v.y;
   }
-  const __half* op0 = o_part + ((size_t)first * KV_LORA + tid) * HEADS + h;
-  const __half* op1 = op0 + (size_t)256 * HEADS;
-  float v0[CAO_BATCH], v1[CAO_BATCH];
+  const __half2* op = reinterpret_cast<const __half2*>(o_part + ((size_t)first * HEADS + h) * KV_LORA) + tid;
+  constexpr size_t kSlot = (size_t)HEADS * KV_LORA / 2;  // one slot, in half2
+  float2 pv[CAO_BATCH];
 #pragma unroll
-  for (int k = 0; k < CAO_BATCH; ++k) {
-    v0[k] = k < n ? __half2float(op0[(size_t)k * KV_LORA * HEADS]) : 0.f;
-    v1[k] = k < n ? __half2float(op1[(size_t)k * KV_LORA * HEADS]) : 0.f;
-  }
-  if (tid == 0 && h == 0 && seq_lens[b] != sr.len[b])  // lengths disagree with the host plan
+  for (int k = 0; k < CAO_BATCH; ++k)
+    pv[k] = k < n ? half2_dep(op + k * kSlot) : make_float2(0.f, 0.f);
+  if (tid == 0 && h == 0 && vb == 0 && seq_lens[b] != sr.len[b])  // lengths disagree with the plan
     atomicExch(err, DEV_ERR_PLAN);
   // v_i = 2^(m_i - M) l_i / sum_j 2^(m_j - M) l_j  (n <= 256: one share per thread)
   float M = mi;
@@ -175,30 +188,28 @@ __global__ void __launch_bounds__(256) combine_absorb_out_kernel(
 #pragma unroll
   for (int k = 0; k < CAO_BATCH; ++k)
     if (k < n) {
-      a0 = fmaf(s_w[k], v0[k], a0);
-      a1 = fmaf(s_w[k], v1[k], a1);
+      a0 = fmaf(s_w[k], pv[k].x, a0);
+      a1 = fmaf(s_w[k], pv[k].y, a1);
     }
   for (int i0 = CAO_BATCH; i0 < n; i0 += CAO_BATCH) {  // long contexts: more rounds
 #pragma unroll
-    for (int k = 0; k < CAO_BATCH; ++k) {
-      v0[k] = i0 + k < n ? __half2float(op0[(size_t)(i0 + k) * KV_LORA * HEADS]) : 0.f;
-      v1[k] = i0 + k < n ? __half2float(op1[(size_t)(i0 + k) * KV_LORA * HEADS]) : 0.f;
-    }
+    for (int k = 0; k < CAO_BATCH; ++k)
+      pv[k] = i0 + k < n ? half2_dep(op + (i0 + k) * kSlot) : make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < CAO_BATCH; ++k)
       if (i0 + k < n) {
-        a0 = fmaf(s_w[i0 + k], v0[k], a0);
-        a1 = fmaf(s_w[i0 + k], v1[k], a1);
+        a0 = fmaf(s_w[i0 + k], pv[k].x, a0);
+        a1 = fmaf(s_w[i0 + k], pv[k].y, a1);
       }
   }
-  ol[tid] = __bfloat162float(__float2bfloat16_rn(a0));
-  ol[tid + 256] = __bfloat162float(__float2bfloat16_rn(a1));
+  ol[2 * tid] = __bfloat162float(__float2bfloat16_rn(a0));
+  ol[2 * tid + 1] = __bfloat162float(__float2bfloat16_rn(a1));
   __syncthreads();
   float x[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) x[i] = ol[lane * 16 + i];
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
+  for (int r = 0; r < CAO_ROWS; ++r) {
     const uint32_t u[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
     float p = 0.f;
 #pragma unroll
@@ -215,7 +226,7 @@ __global__ void __launch_bounds__(256) combine_absorb_out_kernel(
     float t = sc * p;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-    if (lane == 0) attn[(size_t)b * O_IN + h * VDIM + 16 * warp + r] = __float2bfloat16_rn(t);
+    if (lane == 0) attn[(size_t)b * O_IN + h * VDIM + v0 + r] = __float2bfloat16_rn(t);
   }
 }
 
@@ -239,7 +250,7 @@ cudaError_t launch_combine_absorb_out(const int* seq_lens, const int* lens_host,
     if (sr.n[b] < 1 || sr.n[b] > kMaxSplits) return cudaErrorInvalidValue;
     start = end + plan.K;
   }
-  return launch_kernel(combine_absorb_out_kernel, dim3(HEADS, plan.B), dim3(256), 0, st, pdl,
+  return launch_kernel(combine_absorb_out_kernel, dim3(HEADS, CAO_SPLIT, plan.B), dim3(256), 0, st, pdl,
                        seq_lens, sr, o_part, ml_part, Wkvb, Skvb, attn, err);
 }
 

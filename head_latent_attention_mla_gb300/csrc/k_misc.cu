@@ -99,7 +99,7 @@ __device__ __forceinline__ int2 pair_idx(int j, int pairing) {
 constexpr int NRC_QT = Q_LORA / 8;  // q threads
 static_assert(NRC_QT + KV_LORA / 8 == 256, "one 8-value run per thread");
 __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
-    const float* __restrict__ g1, int T, const __nv_bfloat16* __restrict__ gq,
+    const float* g1, int T, const __nv_bfloat16* __restrict__ gq,
     const __nv_bfloat16* __restrict__ gkv, float eps, const float2* __restrict__ rope_tab,
     int pairing, const int* __restrict__ seq_lens, const CacheRef cache, int limit, __nv_bfloat16* __restrict__ cq_out, __nv_bfloat16* __restrict__ ckv_out, int* err,
     E4m3Split q_split, E4m3Split kv_split) {
@@ -117,10 +117,12 @@ __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
   float x[8] = {};
   float sq = 0.f, sk = 0.f;
   if (!is_q || do_q) {
-    const float4* src = reinterpret_cast<const float4*>(in + (is_q ? 0 : Q_LORA) + c0);
-    const float4 a = src[0], b4 = src[1];
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b4.x; x[5] = b4.y; x[6] = b4.z; x[7] = b4.w;
+    const float* src = in + (is_q ? 0 : Q_LORA) + c0;
+    const uint4 a = ld_dep_v4(src), b4 = ld_dep_v4(src + 4);
+    x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+    x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+    x[4] = __uint_as_float(b4.x); x[5] = __uint_as_float(b4.y);
+    x[6] = __uint_as_float(b4.z); x[7] = __uint_as_float(b4.w);
     float s2 = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) s2 += x[i] * x[i];
@@ -194,7 +196,8 @@ __global__ void __launch_bounds__(256) norm_rope_cache_kernel(
   if (tid < ROPE / 2) {
     const int2 ij = pair_idx(tid, pairing);
     const float* kr = in + Q_LORA + KV_LORA;
-    const float2 r = rotate(kr[ij.x], kr[ij.y], rope_tab[(size_t)pos * (ROPE / 2) + tid]);
+    const float2 r = rotate(ld_dep_f32(kr + ij.x), ld_dep_f32(kr + ij.y),
+                            rope_tab[(size_t)pos * (ROPE / 2) + tid]);
     row[KV_LORA + ij.x] = __float2bfloat16_rn(r.x);
     row[KV_LORA + ij.y] = __float2bfloat16_rn(r.y);
   }
@@ -363,7 +366,7 @@ __device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float* f) {
 // [512, 576).
 constexpr int ABQ_B = 8;
 __global__ void __launch_bounds__(128) absorb_q_kernel(
-    const __nv_bfloat16* __restrict__ q, int B, const uint8_t* __restrict__ Wkvb,
+    const __nv_bfloat16* q, int B, const uint8_t* __restrict__ Wkvb,
     const float* __restrict__ Skvb, const float2* __restrict__ rope_tab, int pairing,
     const int* __restrict__ seq_lens, int limit, __nv_bfloat16* __restrict__ qfull) {
   __shared__ float qn[ABQ_B][NOPE];
@@ -386,7 +389,7 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(
     const int nb = min(ABQ_B, B - b0);
     for (int e = threadIdx.x; e < nb * NOPE; e += blockDim.x) {
       const int bb = e / NOPE, i = e % NOPE;
-      qn[bb][i] = __bfloat162float(q[((size_t)(b0 + bb) * HEADS + h) * QHEAD + i]);
+      qn[bb][i] = ld_dep_bf16(q + ((size_t)(b0 + bb) * HEADS + h) * QHEAD + i);
     }
     __syncthreads();
     for (int bb = 0; bb < nb; ++bb) {
@@ -426,7 +429,7 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(
       if (pos < 0 || pos >= limit) continue;
       const int2 ij = pair_idx(j, pairing);
       const __nv_bfloat16* qp = q + ((size_t)bb * HEADS + h) * QHEAD + NOPE;
-      const float2 r = rotate(__bfloat162float(qp[ij.x]), __bfloat162float(qp[ij.y]),
+      const float2 r = rotate(ld_dep_bf16(qp + ij.x), ld_dep_bf16(qp + ij.y),
                               rope_tab[(size_t)pos * (ROPE / 2) + j]);
       __nv_bfloat16* dst = qfull + ((size_t)bb * HEADS + h) * LAT + KV_LORA;
       dst[ij.x] = __float2bfloat16_rn(r.x);
@@ -443,7 +446,7 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(
 constexpr int ABO_B = 8;
 constexpr int ABO_CH = 32;  // sequences staged in shared memory at a time (32 KB)
 __global__ void __launch_bounds__(256) absorb_out_kernel(
-    const __nv_bfloat16* __restrict__ o_lat, int B, const uint8_t* __restrict__ Wkvb,
+    const __nv_bfloat16* o_lat, int B, const uint8_t* __restrict__ Wkvb,
     const float* __restrict__ Skvb, __nv_bfloat16* __restrict__ out) {
   __shared__ __align__(16) __nv_bfloat16 xs[ABO_CH][KV_LORA];  // o_lat of this head
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;   // h * 128 + v
@@ -465,8 +468,8 @@ __global__ void __launch_bounds__(256) absorb_out_kernel(
     __syncthreads();
     for (int e = threadIdx.x; e < nc * (KV_LORA / 8); e += blockDim.x) {
       const int bb = e / (KV_LORA / 8), k = e % (KV_LORA / 8);
-      reinterpret_cast<uint4*>(xs[bb])[k] = __ldg(
-          reinterpret_cast<const uint4*>(o_lat + ((size_t)(c0 + bb) * HEADS + h) * KV_LORA) + k);
+      reinterpret_cast<uint4*>(xs[bb])[k] =
+          ld_dep_v4(o_lat + ((size_t)(c0 + bb) * HEADS + h) * KV_LORA + 8 * k);
     }
     __syncthreads();
     for (int b0 = 0; b0 < nc; b0 += ABO_B) {
@@ -563,7 +566,7 @@ constexpr int ABT_S = 64;    // sequences per staged chunk
 constexpr int ABT_THREADS = (ABT_V / 4) * (ABT_S / 2);  // 256
 constexpr size_t ABT_SMEM = (size_t)KV_LORA * ABT_V * 4 + (size_t)KV_LORA * ABT_S * 2;
 __global__ void __launch_bounds__(ABT_THREADS) absorb_out_tiled_kernel(
-    const __nv_bfloat16* __restrict__ o_lat, int B, const uint8_t* __restrict__ Wkvb,
+    const __nv_bfloat16* o_lat, int B, const uint8_t* __restrict__ Wkvb,
     const float* __restrict__ Skvb, __nv_bfloat16* __restrict__ out) {
   extern __shared__ __align__(16) uint8_t abt_smem[];
   float* ws = reinterpret_cast<float*>(abt_smem);                              // [512][32]
@@ -594,8 +597,7 @@ __global__ void __launch_bounds__(ABT_THREADS) absorb_out_tiled_kernel(
     // o_lat rows of this head: 8 columns per 16-byte load, written transposed.
     for (int e = threadIdx.x; e < nb * (KV_LORA / 8); e += ABT_THREADS) {
       const int sb = e % nb, c0 = (e / nb) * 8;
-      const uint4 x = __ldg(reinterpret_cast<const uint4*>(
-          o_lat + ((size_t)(b0 + sb) * HEADS + h) * KV_LORA + c0));
+      const uint4 x = ld_dep_v4(o_lat + ((size_t)(b0 + sb) * HEADS + h) * KV_LORA + c0);
       const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x);
 #pragma unroll
       for (int i = 0; i < 8; ++i) xs[(c0 + i) * ABT_S + sb] = xb[i];
@@ -655,6 +657,7 @@ cudaError_t init_kernels() {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ABT_SMEM);
   if (e == cudaSuccess) e = init_decode_tc_kernel();
   if (e == cudaSuccess) e = init_prefill_tc_kernel();
+  if (e == cudaSuccess) e = init_gemv_kernels();
   return e != cudaSuccess ? e : init_gemm_tc_kernels();
 }
 

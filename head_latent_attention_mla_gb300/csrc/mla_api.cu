@@ -427,12 +427,12 @@ mla_status decode_impl(mla_ctx* c, const void* x, int B, const CacheRef& CR, int
     Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
     MLA_LAUNCH("gemm_q_b_norm", launch_qb_norm(g1, B, p2, c->gain[0], c->gain[1], c->cfg.eps,
                                                c->rope_tab, c->cfg.rope_pairing, lens_dev, CR,
-                                               limit, c->d_err, s, true));
+                                               limit, c->d_err, c->num_sms, s, true));
     MLA_LAUNCH("absorb_q", launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
                                            c->cfg.rope_pairing, lens_dev, limit, qfull, s, true));
     MLA_LAUNCH("decode_attention", launch_decode_attention_tc(qfull, CR, lens_dev, plan,
                                                               c->cfg.softmax_scale, opart, ml,
-                                                              c->d_err, s, true));
+                                                              c->d_err, s, true, true));
     MLA_LAUNCH("combine_absorb_out",
                launch_combine_absorb_out(lens_dev, lens_host, plan, opart, ml, c->W[MLA_W_KV_B],
                                          c->S[MLA_W_KV_B], attn, c->d_err, s, true));

@@ -38,6 +38,41 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// Loads of data that an earlier kernel of the stream writes, in kernels launched with pdl=true.
+// They are coherent loads (never ld.global.nc: a non-coherent load promises that the data stay
+// unchanged for the whole life of the kernel, which is not so before pdl_wait() returns, and
+// lets the compiler hoist it above the wait), issued as volatile asm so that they stay after
+// pdl_wait() in program order.  `p` must be aligned to the access size.
+__device__ __forceinline__ uint4 ld_dep_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_dep_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_dep_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint16_t ld_dep_u16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_dep_f32(const float* p) { return __uint_as_float(ld_dep_u32(p)); }
+__device__ __forceinline__ float2 ld_dep_f32x2(const float* p) {
+  const uint2 v = ld_dep_v2(p);
+  return make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+}
+__device__ __forceinline__ float ld_dep_bf16(const __nv_bfloat16* p) {
+  return __uint_as_float((uint32_t)ld_dep_u16(p) << 16);
+}
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
@@ -121,11 +156,11 @@ __device__ __forceinline__ uint32_t e4m3_split2(float2 f) {
   return (uint32_t)hp | ((uint32_t)lp << 16);
 }
 
-// Projections of at most kGemvMaxM token rows stream the weights through the CUDA cores
-// (GEMV); larger ones run on the tensor cores.  Measured decode steps (8,192 cached positions
-// per sequence): GEMV 105.5 / 118.4 / 184.0 us against the tensor cores' 109.9 / 108.5 /
-// 111.9 us for 3 / 4 / 8 sequences (the GEMV re-reads every activation row per 4 weight rows).
-constexpr int kGemvMaxM = 3;
+// Projections of at most kGemvMaxM token rows run as weight-streaming GEMVs (k_gemv.cu: the
+// CUDA cores for one or two tokens, mma.sync for three or four); larger ones run on the tcgen05
+// GEMM.  Measured decode steps with 1,000 cached positions per sequence: 80.5 / 84.0 / 103.5 us
+// with the GEMVs against 79.8 / 91.7 / 99.2 us with the tcgen05 GEMM for 3 / 4 / 8 sequences.
+constexpr int kGemvMaxM = 4;
 
 // Token-tile width of the tensor-core GEMM for M token rows.
 constexpr int gemm_bn(int M) { return M <= 32 ? 32 : (M <= 64 ? 64 : 128); }
@@ -152,7 +187,7 @@ constexpr int gemm_splits(int M, int N_total, int K, int num_sms) {
 }
 
 // Scratch of one tensor-core GEMM: hi and lo e4m3 copies of X [M, K], sx [M], and the split-K
-// partials (none for M <= kGemvMaxM, which runs on the CUDA cores).
+// partials (none for M <= kGemvMaxM, which runs as a GEMV).
 constexpr size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms) {
   if (M <= kGemvMaxM) return 0;
   const int s = gemm_splits(M, N_total, K, num_sms);
@@ -164,7 +199,7 @@ constexpr size_t gemm_partial_bytes(int M, int N_total, int K, int num_sms) {
 // ---- launchers (each returns the launch's cudaError_t) ----------------------------------
 
 // Y = X W^T for up to two projections sharing X [M, K] (row stride ldx elements).
-// M <= kGemvMaxM streams the weights through the CUDA cores; larger M runs on the tensor
+// M <= kGemvMaxM runs as a weight-streaming GEMV; larger M runs on the tcgen05 tensor
 // cores, split over K when the grid would be small, with fp32 partials in `partial`
 // (gemm_partial_bytes bytes).  Block 0 of the launch also adds adv_by to adv[0..adv_n) (the
 // call's length bookkeeping, riding on its last kernel; adv_n <= 128 with M <= kGemvMaxM).
@@ -192,6 +227,7 @@ cudaError_t launch_gemm_tc_split(const uint8_t* hi, const uint8_t* lo, const flo
 cudaError_t launch_quant_e4m3_groups(const __nv_bfloat16* X, int ldx, int M, int K, uint8_t* q,
                                      float* sx, cudaStream_t st);
 cudaError_t init_gemm_tc_kernels();
+cudaError_t init_gemv_kernels();
 
 // RMSNorm of the q latent and kv latent, RoPE of k_pe, cache row store.  Positions at or
 // past `limit` (min of cache capacity and RoPE table rows) are skipped and flagged in *err.
@@ -273,7 +309,7 @@ cudaError_t launch_decode_combine(const int* seq_lens, DecodePlan plan, const __
 cudaError_t launch_qb_norm(const float* g1, int M, const Proj& p, const __nv_bfloat16* gq,
                            const __nv_bfloat16* gkv, float eps, const float2* rope_tab,
                            int rope_pairing, const int* seq_lens, const CacheRef& cache,
-                           int limit, int* err, cudaStream_t st, bool pdl = false);
+                           int limit, int* err, int num_sms, cudaStream_t st, bool pdl = false);
 cudaError_t launch_combine_absorb_out(const int* seq_lens, const int* lens_host,
                                       DecodePlan plan, const __half* o_part,
                                       const float* ml_part, const uint8_t* Wkvb,
@@ -285,10 +321,12 @@ cudaError_t launch_combine_absorb_out(const int* seq_lens, const int* lens_host,
 // Each sequence's share is read in 64-position tiles from the share's first position; with a
 // paged cache the tiles start at multiples of 64 within the sequence instead (positions
 // before the share's start are masked), so a tile never crosses a page.
+// head_major: partials laid out [slot][head][dim] (read by the combine fused with W_UV)
+// instead of [slot][dim][head] (read by the stand-alone combine).
 cudaError_t launch_decode_attention_tc(const __nv_bfloat16* qfull, const CacheRef& cache,
                                        const int* seq_lens, DecodePlan plan,
                                        float scale, __half* o_part, float* ml_part, int* err,
-                                       cudaStream_t st, bool pdl = false);
+                                       cudaStream_t st, bool pdl = false, bool head_major = false);
 cudaError_t init_decode_tc_kernel();
 
 // Device address of mla_decode_noalloc's static scratch array on the current device.
