@@ -100,15 +100,28 @@ struct GemmTcArgs {
   int* err;
   int* adv;              // CTA 0 adds adv_by to adv[0..adv_n) (the call's length update)
   int adv_n, adv_by;
+  // Batched GEMMs (batches > 1; one problem, no split-K): batch b multiplies weight rows
+  // w_row_base + b w_row_step + [0, N), token rows b x_row_step + [0, M) of the hi/lo maps and
+  // sx, block scales S[0] + b s_step, and writes Y[0] + b y_step (elements).
+  int batches;
+  int w_row_base, w_row_step, x_row_step, s_step;
+  long long y_step;
 };
 
 // Unit u: split fastest, then m tile, then n tile (CTAs running at the same time share weight
 // tiles through L2).
 struct Unit {
-  int prob, n0, m0, split, kb_begin, kb_end;
+  int prob, n0, m0, split, kb_begin, kb_end, batch;
 };
+template <bool BATCH>
 __device__ __forceinline__ Unit unit_of(const GemmTcArgs& a, int u, int BN, int WT) {
   Unit r;
+  r.batch = 0;
+  if constexpr (BATCH) {
+    const int per_batch = a.units / a.batches;
+    r.batch = u / per_batch;
+    u -= r.batch * per_batch;
+  }
   r.split = u % a.splits;
   const int t = u / a.splits;
   const int mt = t % a.m_tiles;
@@ -171,6 +184,68 @@ __global__ void __launch_bounds__(256) split_e4m3_kernel(const __nv_bfloat16* __
   }
 }
 
+// The two-term split of per-(sequence, head) rows for the batched absorption GEMMs, written
+// head-major: CTA (b, h) splits X[b * sb + h * sh + 0 .. K) (as split_e4m3_kernel does) into row
+// h * B + b of hi / lo / sx, so that head h's B token rows are contiguous.  With rope_out set
+// (the query absorption), it also writes RoPE of the head's rotary slice X[.. + K .. + K + 64)
+// at position seq_lens[b] into rope_out[(b * H + h) * rope_ld + 0 .. 64), as a plain rotation
+// of pairs (pairing 0: (2j, 2j+1); 1: (j, j+32)).  max(32, K / 8) threads, eight values each
+// (K <= 512); launched under programmatic dependent launch (X comes from an earlier kernel).
+__global__ void __launch_bounds__(64) split_heads_e4m3_kernel(
+    const __nv_bfloat16* X, int B, int H, long long sb, int sh, int K, uint8_t* __restrict__ hi,
+    uint8_t* __restrict__ lo, float* __restrict__ sx, __nv_bfloat16* rope_out, int rope_ld,
+    const float2* __restrict__ rope_tab, int pairing, const int* __restrict__ seq_lens,
+    int limit) {
+  __shared__ float red[2];
+  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const __nv_bfloat16* row = X + (size_t)b * sb + (size_t)h * sh;
+  const size_t r = (size_t)h * B + b;
+  pdl_launch_dependents();
+  pdl_wait();
+  const bool act = 8 * tid < K;
+  const uint4 v = act ? ld_dep_v4(row + 8 * tid) : make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  float f[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(u[i] << 16);
+    f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((tid & 31) == 0) red[tid >> 5] = amax;
+  __syncthreads();
+  amax = blockDim.x > 32 ? fmaxf(red[0], red[1]) : red[0];
+  const float sc = amax > 0.f ? amax / E4M3_MAX : 1.f;
+  const float inv = 1.f / sc;
+  if (tid == 0) sx[r] = sc;
+  uint32_t hw[2] = {0u, 0u}, lw[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t hl = e4m3_split2(make_float2(f[2 * i] * inv, f[2 * i + 1] * inv));
+    hw[i >> 1] |= (hl & 0xFFFFu) << (16 * (i & 1));
+    lw[i >> 1] |= (hl >> 16) << (16 * (i & 1));
+  }
+  if (act) {
+    *reinterpret_cast<uint2*>(hi + r * K + 8 * tid) = make_uint2(hw[0], hw[1]);
+    *reinterpret_cast<uint2*>(lo + r * K + 8 * tid) = make_uint2(lw[0], lw[1]);
+  }
+  if (rope_out && tid < ROPE / 2) {
+    const int pos = seq_lens[b];
+    if (pos >= 0 && pos < limit) {
+      const int2 ij = pairing == 0 ? make_int2(2 * tid, 2 * tid + 1) : make_int2(tid, tid + ROPE / 2);
+      const float x0 = ld_dep_bf16(row + K + ij.x), x1 = ld_dep_bf16(row + K + ij.y);
+      const float2 cs = rope_tab[(size_t)pos * (ROPE / 2) + tid];
+      __nv_bfloat16* dst = rope_out + ((size_t)b * H + h) * rope_ld;
+      dst[ij.x] = __float2bfloat16_rn(x0 * cs.x - x1 * cs.y);
+      dst[ij.y] = __float2bfloat16_rn(x1 * cs.x + x0 * cs.y);
+    }
+  }
+}
+
 // The FP8-activation option's input quantisation ("linear" excerpt: activation_scheme dynamic):
 // one e4m3 term per value with one scale per (token, 128-wide group), s = amax / 448 (1 for an
 // all-zero group), q = e4m3(x / s) rounded to nearest even with saturation.  One CTA per token,
@@ -215,7 +290,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 // SXB: the activations carry one scale per (token, 128-wide k block), sx[m][kb], applied with
 // the weight's block scale to each k block's partial product (token-lane orientation only).
 // ONE: the activations are one e4m3 term (map_lo is not read).
-template <int BN, int WT, bool SXB, bool ONE = false>
+template <int BN, int WT, bool SXB, bool ONE = false, bool BATCH = false>
 __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
     const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
     const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo,
@@ -275,7 +350,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
       int i = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-        const Unit U = unit_of(args, u, BN, WT);
+        const Unit U = unit_of<BATCH>(args, u, BN, WT);
         const CUtensorMap* map_w = U.prob ? &map_w1 : &map_w0;
         for (int kb = U.kb_begin; ok && kb < U.kb_end; ++kb, ++i) {
           const int st = i % GT_STAGES;
@@ -287,10 +362,12 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
           // A weight half that lies wholly past N is neither loaded nor multiplied.
           const int wt = (WT == 2 && U.n0 + 128 >= args.N[U.prob]) ? 1 : WT;
           mbar_expect_tx(&in_full[st], L::STAGE - (WT - wt) * W_TILE);
+          const int wrow = args.w_row_base + U.batch * args.w_row_step + U.n0;
+          const int xrow = U.batch * args.x_row_step + U.m0;
           for (int h = 0; h < wt; ++h)
-            tma_load_2d(stg + h * W_TILE, map_w, &in_full[st], k0, U.n0 + 128 * h);
-          tma_load_2d(stg + L::W_BYTES, &map_hi, &in_full[st], k0, U.m0);
-          if constexpr (!ONE) tma_load_2d(stg + L::W_BYTES + L::X_TILE, &map_lo, &in_full[st], k0, U.m0);
+            tma_load_2d(stg + h * W_TILE, map_w, &in_full[st], k0, wrow + 128 * h);
+          tma_load_2d(stg + L::W_BYTES, &map_hi, &in_full[st], k0, xrow);
+          if constexpr (!ONE) tma_load_2d(stg + L::W_BYTES + L::X_TILE, &map_lo, &in_full[st], k0, xrow);
         }
       }
       // Never leave the CTA with copies in flight: wait (bounded) for the last ones.
@@ -306,7 +383,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
       int i = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-        const Unit U = unit_of(args, u, BN, WT);
+        const Unit U = unit_of<BATCH>(args, u, BN, WT);
         const int wt = (WT == 2 && U.n0 + 128 >= args.N[U.prob]) ? 1 : WT;
         for (int kb = U.kb_begin; ok && kb < U.kb_end; ++kb, ++i) {
           const int st = i % GT_STAGES, ab = i % GT_NACC;
@@ -357,15 +434,22 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
     int i = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-      const Unit U = unit_of(args, u, BN, WT);
+      const Unit U = unit_of<BATCH>(args, u, BN, WT);
       const int nh = U.n0 + 128 * half;       // first feature of this warpgroup's half
       const bool live = nh < args.N[U.prob];  // a half wholly past N was not multiplied
-      const float* scales = args.S[U.prob] + (size_t)(nh / BLK) * nkb_all;
+      const float* scales = args.S[U.prob] + (size_t)U.batch * args.s_step + (size_t)(nh / BLK) * nkb_all;
+      // This batch's token scales and output (evaluated where used, so that unbatched
+      // instantiations keep reading them from the parameter space).
+#define GT_SXP (BATCH ? args.sx + (size_t)U.batch * args.x_row_step : args.sx)
+#define GT_YBASE                                                                          \
+  (BATCH ? reinterpret_cast<char*>(args.Y[U.prob]) +                                      \
+               (size_t)U.batch * args.y_step * (args.y_fp32[U.prob] ? 4 : 2)               \
+         : reinterpret_cast<char*>(args.Y[U.prob]))
       // SXB: this thread's token (lane = token) and its block scales, one k block ahead.
       const int mt = U.m0 + 32 * q + lane;
       const int sxoff = (mt < args.M ? mt : -1) * nkb_all;  // < 0: token past M
       float sx_next = 0.f;
-      if constexpr (SXB) sx_next = sxoff >= 0 ? __ldg(args.sx + sxoff + U.kb_begin) : 0.f;
+      if constexpr (SXB) sx_next = sxoff >= 0 ? __ldg(GT_SXP + sxoff + U.kb_begin) : 0.f;
       float acc[CW];
 #pragma unroll
       for (int j = 0; j < CW; ++j) acc[j] = 0.f;
@@ -380,7 +464,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
         float sc = live ? __ldg(scales + kb) : 0.f;
         if constexpr (SXB) {
           sc *= sx_next;
-          sx_next = (sxoff >= 0 && kb + 1 < U.kb_end) ? __ldg(args.sx + sxoff + kb + 1) : 0.f;
+          sx_next = (sxoff >= 0 && kb + 1 < U.kb_end) ? __ldg(GT_SXP + sxoff + kb + 1) : 0.f;
         }
         const uint32_t t0 = tmem + lane_off + ab * L::ACC_COLS + half * BN + col0;
 #pragma unroll
@@ -410,20 +494,19 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
         const int nend = args.N[U.prob];
         if (m < args.M) {
           // Token scale, applied as each vector is formed (SXB: already in the block scales).
-          const float sxm = SXB ? 1.f : __ldg(args.sx + m);
+          const float sxm = SXB ? 1.f : __ldg(GT_SXP + m);
           if (args.splits > 1 || args.y_fp32[U.prob]) {
             float* y = args.splits > 1
                            ? args.partial + ((size_t)U.split * args.M + m) * args.ldp +
                                  (U.prob ? args.N[0] : 0) + nb
-                           : reinterpret_cast<float*>(args.Y[U.prob]) +
-                                 (size_t)m * args.ldy[U.prob] + nb;
+                           : reinterpret_cast<float*>(GT_YBASE) + (size_t)m * args.ldy[U.prob] + nb;
 #pragma unroll
             for (int j = 0; j < CW; j += 4)
               if (nb + j < nend)
                 *reinterpret_cast<float4*>(y + j) = make_float4(
                     acc[j] * sxm, acc[j + 1] * sxm, acc[j + 2] * sxm, acc[j + 3] * sxm);
           } else {
-            __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(args.Y[U.prob]) +
+            __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(GT_YBASE) +
                                (size_t)m * args.ldy[U.prob] + nb;
             const __nv_bfloat16* res = args.R[U.prob];
 #pragma unroll
@@ -462,7 +545,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
 #pragma unroll
       for (int c = 0; c < CW / 32; ++c) {
         const int m = m0 + 32 * c + lane;
-        sxr[c] = m < args.M ? __ldg(args.sx + m) : 0.f;
+        sxr[c] = m < args.M ? __ldg(GT_SXP + m) : 0.f;
       }
 #pragma unroll
       for (int j = 0; j < CW; ++j) acc[j] *= __shfl_sync(0xffffffffu, sxr[j >> 5], j & 31);
@@ -477,12 +560,12 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
           for (int j = 0; j < CW; ++j)
             if (j < mend) p[(size_t)j * args.ldp] = acc[j];
         } else if (args.y_fp32[U.prob]) {
-          float* y = reinterpret_cast<float*>(args.Y[U.prob]) + (size_t)m0 * ldy + n;
+          float* y = reinterpret_cast<float*>(GT_YBASE) + (size_t)m0 * ldy + n;
 #pragma unroll
           for (int j = 0; j < CW; ++j)
             if (j < mend) y[(size_t)j * ldy] = acc[j];
         } else {
-          __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(args.Y[U.prob]) + (size_t)m0 * ldy + n;
+          __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(GT_YBASE) + (size_t)m0 * ldy + n;
           const __nv_bfloat16* res = args.R[U.prob];
 #pragma unroll
           for (int j = 0; j < CW; ++j)
@@ -505,6 +588,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
     tmem_dealloc(tmem, L::TMEM_COLS);
   }
 }
+#undef GT_SXP
+#undef GT_YBASE
 
 // Y = sum over splits of the fp32 partials, in split order (deterministic).
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int M, int ldp,
@@ -524,18 +609,18 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
   }
 }
 
-template <int BN, int WT, bool SXB, bool ONE = false>
+template <int BN, int WT, bool SXB, bool ONE = false, bool BATCH = false>
 cudaError_t launch_bn(const CUtensorMap* w, const CUtensorMap& hi, const CUtensorMap& lo,
                       const GemmTcArgs& a, int num_sms, cudaStream_t st) {
   const int grid = a.units < num_sms ? a.units : num_sms;
-  gemm_f8w_tc_kernel<BN, WT, SXB, ONE><<<grid, GT_THREADS, GemmSmem<BN, WT, ONE>::BYTES, st>>>(
+  gemm_f8w_tc_kernel<BN, WT, SXB, ONE, BATCH><<<grid, GT_THREADS, GemmSmem<BN, WT, ONE>::BYTES, st>>>(
       w[0], w[1], hi, lo, a);
   return cudaGetLastError();
 }
 
-template <int BN, int WT, bool SXB, bool ONE = false>
+template <int BN, int WT, bool SXB, bool ONE = false, bool BATCH = false>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_f8w_tc_kernel<BN, WT, SXB, ONE>,
+  return cudaFuncSetAttribute(gemm_f8w_tc_kernel<BN, WT, SXB, ONE, BATCH>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               GemmSmem<BN, WT, ONE>::BYTES);
 }
@@ -575,6 +660,9 @@ cudaError_t init_gemm_tc_kernels() {
   if (e == cudaSuccess) e = set_smem_attr<128, 2, true>();
   if (e == cudaSuccess) e = set_smem_attr<128, 1, true, true>();
   if (e == cudaSuccess) e = set_smem_attr<128, 2, true, true>();
+  if (e == cudaSuccess) e = set_smem_attr<32, 1, false, false, true>();
+  if (e == cudaSuccess) e = set_smem_attr<64, 1, false, false, true>();
+  if (e == cudaSuccess) e = set_smem_attr<128, 1, false, false, true>();
   return e;
 }
 
@@ -593,6 +681,7 @@ cudaError_t gemm_tc_core(const uint8_t* hi, const uint8_t* lo, const float* sx, 
   GemmTcArgs a{};
   a.M = M;
   a.K = K;
+  a.batches = 1;
   a.err = err;
   a.sx = sx;
   a.adv = adv;
@@ -681,6 +770,61 @@ cudaError_t launch_gemm_tc_split(const uint8_t* hi, const uint8_t* lo, const flo
     return cudaErrorInvalidValue;
   return gemm_tc_core(hi, lo, sx, block_scales, M, K, p, np, scratch, num_sms, err, st, adv,
                       adv_n, adv_by, one_term);
+}
+
+size_t absorb_split_bytes(int B, int K) {
+  return 2 * up256((size_t)B * HEADS * K) + up256((size_t)B * HEADS * 4);
+}
+
+cudaError_t launch_absorb_tc(const __nv_bfloat16* X, long long sb, int sh, int B, int K,
+                             const uint8_t* W, long long w_rows, int w_row_base, int w_row_step,
+                             const float* S, int s_step, int N, __nv_bfloat16* Y, int ldy,
+                             long long y_step, __nv_bfloat16* rope_out, const float2* rope_tab,
+                             int pairing, const int* seq_lens, int limit, void* scratch,
+                             int num_sms, int* err, cudaStream_t st) {
+  if (B <= 0) return cudaSuccess;
+  if ((K != NOPE && K != KV_LORA) || N % 128 != 0 || !scratch) return cudaErrorInvalidValue;
+  uint8_t* hi = reinterpret_cast<uint8_t*>(scratch);
+  uint8_t* lo = hi + up256((size_t)B * HEADS * K);
+  float* sx = reinterpret_cast<float*>(lo + up256((size_t)B * HEADS * K));
+  cudaError_t e = launch_kernel(split_heads_e4m3_kernel, dim3(B, HEADS), dim3(K / 8 < 32 ? 32 : K / 8), 0, st, true,
+                                X, B, HEADS, sb, sh, K, hi, lo, sx, rope_out, LAT, rope_tab,
+                                pairing, seq_lens, limit);
+  if (e != cudaSuccess) return e;
+  const int bn = gemm_bn(B);
+  CUtensorMap mw[2], mh, ml;
+  if (!make_tmap_2d(&mw[0], false, W, (uint64_t)K, (uint64_t)w_rows, (uint64_t)K, 128, 128) ||
+      !make_tmap_2d(&mh, false, hi, (uint64_t)K, (uint64_t)B * HEADS, (uint64_t)K, 128, bn) ||
+      !make_tmap_2d(&ml, false, lo, (uint64_t)K, (uint64_t)B * HEADS, (uint64_t)K, 128, bn))
+    return cudaErrorInvalidValue;
+  mw[1] = mw[0];
+  GemmTcArgs a{};
+  a.M = B;
+  a.K = K;
+  a.N[0] = N;
+  a.S[0] = S;
+  a.Y[0] = Y;
+  a.ldy[0] = ldy;
+  a.y_fp32[0] = 0;
+  a.R[0] = nullptr;
+  a.sx = sx;
+  a.splits = 1;
+  a.ldp = N;
+  a.err = err;
+  a.m_tiles = (B + bn - 1) / bn;
+  a.n_tiles0 = a.n_tiles = N / 128;
+  a.batches = HEADS;
+  a.units = HEADS * a.n_tiles * a.m_tiles;
+  a.w_row_base = w_row_base;
+  a.w_row_step = w_row_step;
+  a.x_row_step = B;
+  a.s_step = s_step;
+  a.y_step = y_step;
+  switch (bn) {
+    case 32: return launch_bn<32, 1, false, false, true>(mw, mh, ml, a, num_sms, st);
+    case 64: return launch_bn<64, 1, false, false, true>(mw, mh, ml, a, num_sms, st);
+    default: return launch_bn<128, 1, false, false, true>(mw, mh, ml, a, num_sms, st);
+  }
 }
 
 cudaError_t launch_quant_e4m3_groups(const __nv_bfloat16* X, int ldx, int M, int K, uint8_t* q,

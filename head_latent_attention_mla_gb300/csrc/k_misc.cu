@@ -633,6 +633,29 @@ __global__ void __launch_bounds__(ABT_THREADS) absorb_out_tiled_kernel(
   }
 }
 
+namespace {
+// out[h][c][i] = W[256 h + i][c]: a 64 x 64-byte tile per CTA through shared memory.
+__global__ void __launch_bounds__(256) transpose_wuk_kernel(const uint8_t* __restrict__ W,
+                                                            uint8_t* __restrict__ out) {
+  __shared__ uint8_t t[64][65];
+  const int h = blockIdx.z, i0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+  for (int e = threadIdx.x; e < 64 * 64; e += 256) {
+    const int i = e / 64, c = e % 64;
+    t[i][c] = W[((size_t)h * KVB_PER_HEAD + i0 + i) * KV_LORA + c0 + c];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < 64 * 64; e += 256) {
+    const int c = e / 64, i = e % 64;
+    out[((size_t)h * KV_LORA + c0 + c) * NOPE + i0 + i] = t[i][c];
+  }
+}
+}  // namespace
+
+cudaError_t launch_transpose_wuk(const uint8_t* Wkvb, uint8_t* out, cudaStream_t st) {
+  transpose_wuk_kernel<<<dim3(KV_LORA / 64, NOPE / 64, HEADS), 256, 0, st>>>(Wkvb, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_absorb_q(const __nv_bfloat16* q, int B, const uint8_t* Wkvb,
                             const float* Skvb, const float2* rope_tab, int rope_pairing,
                             const int* seq_lens, int limit, __nv_bfloat16* qfull,

@@ -92,7 +92,12 @@ Layout decode_layout(const mla_ctx* c, int B) {
   L.ml = take(items * HEADS * 2 * 4);
   L.olat = take((size_t)B * HEADS * KV_LORA * 2);
   L.attn = take((size_t)B * O_IN * 2);
-  L.gpart = take(gemm_partials(B, c->num_sms));
+  size_t gp = gemm_partials(B, c->num_sms);
+  if (B >= kAbsorbTcMinB) {  // the batched absorptions' e4m3 split of o_lat (the larger one)
+    const size_t ab = absorb_split_bytes(B, KV_LORA);
+    gp = ab > gp ? ab : gp;
+  }
+  L.gpart = take(gp);
   L.total = off;
   return L;
 }
@@ -447,15 +452,41 @@ mla_status decode_impl(mla_ctx* c, const void* x, int B, const CacheRef& CR, int
   Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
   MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, B, Q_LORA, &p2, 1, at<float>(ws, L.gpart),
                                      c->num_sms, c->d_err, s, nullptr, 0, 0, true));
-  MLA_LAUNCH("absorb_q", launch_absorb_q(q, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], c->rope_tab,
-                             c->cfg.rope_pairing, lens_dev, limit, qfull, s, true));
+  // Many sequences: both absorptions as batched tcgen05 GEMMs over the heads (W_UK through its
+  // transposed copy, K-major; W_UV as stored), each after a head-major e4m3 split of its input
+  // (the query's split also writes RoPE(q_pe)).  Fewer: the CUDA-core kernels.
+  const bool absorb_tc = B >= kAbsorbTcMinB;
+  const float* skvb = c->S[MLA_W_KV_B];
+  if (absorb_tc) {
+    if (c->wuk_t_stale) {
+      MLA_LAUNCH("transpose_w_uk", launch_transpose_wuk(c->W[MLA_W_KV_B], c->wuk_t, s));
+      c->wuk_t_stale = false;
+    }
+    MLA_LAUNCH("absorb_q", launch_absorb_tc(q, QB_N, QHEAD, B, NOPE, c->wuk_t,
+                                            (long long)HEADS * KV_LORA, 0, KV_LORA, skvb,
+                                            2 * (KV_LORA / BLK), KV_LORA, qfull, HEADS * LAT, LAT,
+                                            qfull + KV_LORA, c->rope_tab, c->cfg.rope_pairing,
+                                            lens_dev, limit, at<void>(ws, L.gpart), c->num_sms,
+                                            c->d_err, s));
+  } else {
+    MLA_LAUNCH("absorb_q", launch_absorb_q(q, B, c->W[MLA_W_KV_B], skvb, c->rope_tab,
+                                           c->cfg.rope_pairing, lens_dev, limit, qfull, s, true));
+  }
   MLA_LAUNCH("decode_attention", launch_decode_attention_tc(qfull, CR, lens_dev, plan,
                                                             c->cfg.softmax_scale, opart, ml,
                                                             c->d_err, s, true));
   MLA_LAUNCH("decode_combine", launch_decode_combine(lens_dev, plan, opart, ml, olat, c->d_err, s,
                                                          true));
-  MLA_LAUNCH("absorb_out", launch_absorb_out(olat, B, c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], attn, s,
-                                                 true));
+  if (absorb_tc) {
+    MLA_LAUNCH("absorb_out", launch_absorb_tc(olat, (long long)HEADS * KV_LORA, KV_LORA, B,
+                                              KV_LORA, c->W[MLA_W_KV_B], KVB_N, NOPE,
+                                              KVB_PER_HEAD, skvb + KV_LORA / BLK,
+                                              2 * (KV_LORA / BLK), VDIM, attn, O_IN, VDIM,
+                                              nullptr, nullptr, 0, nullptr, 0,
+                                              at<void>(ws, L.gpart), c->num_sms, c->d_err, s));
+  } else {
+    MLA_LAUNCH("absorb_out", launch_absorb_out(olat, B, c->W[MLA_W_KV_B], skvb, attn, s, true));
+  }
   Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0, residual};
   if (gemm_can_advance(B)) {  // the length update rides on the last kernel
     MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, B, O_IN, &p4, 1, at<float>(ws, L.gpart),
@@ -567,6 +598,7 @@ void mla_destroy(mla_ctx* c) {
   cudaDeviceSynchronize();
   cudaFree(c->rope_tab);
   cudaFree(c->d_err);
+  if (c->wuk_t) cudaFree(c->wuk_t);
   for (cudaEvent_t e : c->ev)
     if (e) cudaEventDestroy(e);
   delete c;
@@ -606,6 +638,13 @@ mla_status mla_upload_weights(mla_ctx* c, int which, const void* q, const float*
   if (!c || which < 0 || which > 4 || !q || !s) return MLA_ERR_INVALID_ARG;
   if (!aligned16(q) || (reinterpret_cast<uintptr_t>(s) & 3u)) return MLA_ERR_INVALID_ARG;
   if (rows != kRows[which] || cols != kCols[which]) return MLA_ERR_SHAPE;
+  if (which == MLA_W_KV_B) {
+    if (!c->wuk_t && cudaMalloc(&c->wuk_t, (size_t)HEADS * KV_LORA * NOPE) != cudaSuccess) {
+      c->wuk_t = nullptr;
+      return MLA_ERR_CUDA;
+    }
+    c->wuk_t_stale = true;
+  }
   c->W[which] = static_cast<const uint8_t*>(q);
   c->S[which] = s;
   return MLA_OK;

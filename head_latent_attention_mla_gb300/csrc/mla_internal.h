@@ -224,6 +224,23 @@ cudaError_t launch_gemm_tc_split(const uint8_t* hi, const uint8_t* lo, const flo
                                  bool one_term = false);
 // The FP8-activation option's input quantisation: q [M, K] = e4m3(X / sx) with one scale per
 // (token, 128-wide group), sx [M, K/128] = amax / 448 (K a multiple of 128, at most 8192).
+// The decode absorptions for many sequences as one batched tcgen05 GEMM over the 64 heads
+// ("Key content up-projection" page; W_UK / W_UV are the two 128-row halves of each head's
+// 256 rows of kv_b_proj): for head h and sequence b,
+//   Y[b, h-th output block] = sum_k X[b, h, k] * W[w_row_base + h w_row_step + n, k] * scale,
+// with X[b, h, 0 .. K) at X + b sb + h sh (bf16, written by the previous kernel), the weight's
+// block scales at S + h s_step (row block of the head's rows, K / 128 columns), and output row
+// b of head h at Y + h y_step + b ldy (bf16, N values).  The activations are split into two
+// e4m3 terms per (sequence, head) row first (as launch_gemm_tc does per token).  With
+// rope_out set, the split launch also writes RoPE of X[b, h, K .. K + 64) at position
+// seq_lens[b] to rope_out[(b H + h) 576 .. + 64).  scratch: absorb_split_bytes(B, K) bytes.
+size_t absorb_split_bytes(int B, int K);
+cudaError_t launch_absorb_tc(const __nv_bfloat16* X, long long sb, int sh, int B, int K,
+                             const uint8_t* W, long long w_rows, int w_row_base, int w_row_step,
+                             const float* S, int s_step, int N, __nv_bfloat16* Y, int ldy,
+                             long long y_step, __nv_bfloat16* rope_out, const float2* rope_tab,
+                             int pairing, const int* seq_lens, int limit, void* scratch,
+                             int num_sms, int* err, cudaStream_t st);
 cudaError_t launch_quant_e4m3_groups(const __nv_bfloat16* X, int ldx, int M, int K, uint8_t* q,
                                      float* sx, cudaStream_t st);
 cudaError_t init_gemm_tc_kernels();
@@ -341,6 +358,11 @@ cudaError_t launch_wait_selftest(int* err, unsigned long long limit_ns, cudaStre
 cudaError_t init_kernels();
 
 // Decode output absorption: out[b, h*VDIM + v] = sum_c W_UV,h[v, c] o_lat[b, h, c].
+// W_UK^T: out[h][c][i] = Wkvb[256 h + i][c] (e4m3 bytes) for the batched query absorption.
+cudaError_t launch_transpose_wuk(const uint8_t* Wkvb, uint8_t* out, cudaStream_t st);
+// Decode with at least kAbsorbTcMinB sequences runs both absorptions as batched tcgen05 GEMMs
+// (launch_absorb_tc); fewer keep the CUDA-core kernels.
+constexpr int kAbsorbTcMinB = 9;
 cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* Wkvb,
                               const float* Skvb, __nv_bfloat16* out, cudaStream_t st,
                               bool pdl = false);
@@ -396,6 +418,11 @@ struct mla_ctx {
   const __nv_bfloat16* gain[3] = {};  // q_a_layernorm, kv_a_layernorm, input_layernorm
   float2* rope_tab = nullptr;  // [max_positions][32] (cos, sin)
   int* d_err = nullptr;
+  // W_UK of every head transposed, [64][512][128] e4m3 (the batched query absorption's weight
+  // operand, K-major), allocated when kv_b_proj is registered and rebuilt on the stream of the
+  // first call that needs it after each registration.
+  uint8_t* wuk_t = nullptr;
+  bool wuk_t_stale = true;
   // Device address, on this context's device, of the static scratch array that
   // mla_decode_noalloc uses (looked up by mla_create, with the device current).
   void* noalloc_scratch = nullptr;

@@ -280,10 +280,13 @@ def test_decode_config5_long_b8_every_sequence(layer):
 
 
 # One sequence and two take the six-kernel decode (fused q-latent norm and cache append, fused
-# combine and W_UV); three the separate kernels with GEMV projections; four to eight the
-# separate kernels with tensor-core projections.
-@pytest.mark.parametrize("lengths", [[0], [65, 300], [5, 64, 129],
-                                     [1, 63, 64, 65, 127, 128, 129, 200]])
+# combine and W_UV, row GEMVs); three and four the separate kernels with the mma.sync GEMV;
+# five to eight the tcgen05 projections; nine and more also the batched tcgen05 absorptions
+# (nine: one 32-token tile with 23 empty rows; seventeen: a 64-token tile).
+@pytest.mark.parametrize("lengths", [[0], [65, 300], [5, 64, 129], [3, 0, 70, 64],
+                                     [1, 63, 64, 65, 127, 128, 129, 200],
+                                     [1, 63, 64, 65, 127, 128, 129, 200, 0],
+                                     [int(v) for v in np.arange(17) * 37 % 300]])
 def test_decode_tile_edges_every_sequence(layer, lengths):
     """Empty cache (p=0) and lengths around the 64-position tile edges, all sequences checked,
     with the cache row each decode appends."""
