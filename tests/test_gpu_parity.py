@@ -47,9 +47,11 @@ def test_dequant_bit_exact(layer, name):
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
-@pytest.mark.parametrize("T", [1, 16, 100, 130, 1200])
+@pytest.mark.parametrize("T", [1, 3, 4, 16, 100, 130, 1200])
 def test_prefill_small_every_element(layer, T):
     """Config-1 size (T=16) and tile edge cases (T=1, T=130 = two tiles and a ragged tail).
+    T=1 runs the projections as row GEMVs, T=3 and T=4 as mma.sync GEMVs (kv_b among them,
+    K = 512 with four tiles per CTA).
     T=100 runs the projections as split-K over one partly filled 128-token tile.
     T=1200 runs the q_a/kv_a and o projections with 256-feature units over ten token tiles
     (the last one ragged), including the kv_a unit whose second weight half lies wholly past
