@@ -43,10 +43,11 @@ using namespace tc;
 constexpr int DA_TILE = 64;                     // positions per tile
 constexpr int DA_STAGES = 2;                    // tiles in flight
 constexpr int DA_QBOX = 64 * 128;               // one [64 heads x 64 bf16] query box, bytes
-constexpr int DA_BOX = DA_TILE * 128;           // one [32 rows x 64 bf16] cache box, bytes
+constexpr int DA_BOX = DA_TILE * 128;           // one [64 rows x 64 bf16] cache box, bytes
 constexpr int DA_NBOX = LAT / 64;               // 9 boxes per 576-wide row block
 constexpr int DA_Q_BYTES = DA_NBOX * DA_QBOX;    // 73728
-constexpr int DA_TILE_BYTES = DA_NBOX * DA_BOX;  // 36864
+// 73728 per tile: two stages and the query block (221 KB) fill shared memory.
+constexpr int DA_TILE_BYTES = DA_NBOX * DA_BOX;
 constexpr int DA_THREADS = 224;
 constexpr int OFF_Q = 0;
 constexpr int OFF_C = OFF_Q + DA_Q_BYTES;

@@ -137,17 +137,21 @@ __device__ __forceinline__ Unit unit_of(const GemmTcArgs& a, int u, int BN, int 
 }
 
 // One CTA per token row: sx = amax/448 (1 for an all-zero row), hi = e4m3(x/sx),
-// lo = e4m3(x/sx - hi), both rounded to nearest even with saturation.
-__global__ void __launch_bounds__(256) split_e4m3_kernel(const __nv_bfloat16* __restrict__ X,
-                                                         int ldx, int K, uint8_t* __restrict__ hi,
+// lo = e4m3(x/sx - hi), both rounded to nearest even with saturation.  Safe under
+// programmatic dependent launch (X comes from the previous kernel; hi, lo and sx may still be
+// read by an earlier GEMM until the wait returns).
+__global__ void __launch_bounds__(256) split_e4m3_kernel(const __nv_bfloat16* X, int ldx, int K,
+                                                         uint8_t* __restrict__ hi,
                                                          uint8_t* __restrict__ lo,
                                                          float* __restrict__ sx) {
   __shared__ float red[8];
   const int m = blockIdx.x, tid = threadIdx.x;
   const __nv_bfloat16* row = X + (size_t)m * ldx;
+  pdl_launch_dependents();
+  pdl_wait();
   float amax = 0.f;
   for (int k = tid * 8; k < K; k += 256 * 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(row + k);
+    const uint4 v = ld_dep_v4(row + k);
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(256) split_e4m3_kernel(const __nv_bfloat16* __
   const float inv = 1.f / s;
   if (tid == 0) sx[m] = s;
   for (int k = tid * 8; k < K; k += 256 * 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(row + k);
+    const uint4 v = ld_dep_v4(row + k);
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
     uint32_t h[2] = {0u, 0u}, l[2] = {0u, 0u};
 #pragma unroll
@@ -337,9 +341,10 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (blockIdx.x == 0 && args.adv != nullptr)  // every earlier kernel of the stream is done
-    for (int j = threadIdx.x; j < args.adv_n; j += GT_THREADS) args.adv[j] += args.adv_by;
-
+  // Under programmatic dependent launch this kernel may start while the previous one runs:
+  // the weight tiles of the first stages are requested before the wait (the weights do not
+  // depend on it); everything that reads or writes the previous kernels' data comes after.
+  pdl_launch_dependents();
   if (warp == 0) {
     // -------------------------------------------------------------------- TMA producer
     if (lane == 0) {
@@ -347,6 +352,20 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
       tma_prefetch_desc(&map_w1);
       tma_prefetch_desc(&map_hi);
       tma_prefetch_desc(&map_lo);
+      int npre = 0;  // stages whose weight tiles are issued before the wait
+      for (int u = blockIdx.x; npre < GT_STAGES && u < args.units; u += gridDim.x) {
+        const Unit U = unit_of<BATCH>(args, u, BN, WT);
+        const CUtensorMap* map_w = U.prob ? &map_w1 : &map_w0;
+        const int wt = (WT == 2 && U.n0 + 128 >= args.N[U.prob]) ? 1 : WT;
+        const int wrow = args.w_row_base + U.batch * args.w_row_step + U.n0;
+        for (int kb = U.kb_begin; npre < GT_STAGES && kb < U.kb_end; ++kb, ++npre) {
+          uint8_t* stg = smem + L::OFF_IN + npre * L::STAGE;
+          mbar_expect_tx(&in_full[npre], L::STAGE - (WT - wt) * W_TILE);
+          for (int h = 0; h < wt; ++h)
+            tma_load_2d(stg + h * W_TILE, map_w, &in_full[npre], kb * BLK, wrow + 128 * h);
+        }
+      }
+      pdl_wait();
       int i = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
@@ -361,11 +380,13 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
           const int k0 = kb * BLK;
           // A weight half that lies wholly past N is neither loaded nor multiplied.
           const int wt = (WT == 2 && U.n0 + 128 >= args.N[U.prob]) ? 1 : WT;
-          mbar_expect_tx(&in_full[st], L::STAGE - (WT - wt) * W_TILE);
           const int wrow = args.w_row_base + U.batch * args.w_row_step + U.n0;
           const int xrow = U.batch * args.x_row_step + U.m0;
-          for (int h = 0; h < wt; ++h)
-            tma_load_2d(stg + h * W_TILE, map_w, &in_full[st], k0, wrow + 128 * h);
+          if (i >= npre) {  // (the first npre stages' weight tiles are already on their way)
+            mbar_expect_tx(&in_full[st], L::STAGE - (WT - wt) * W_TILE);
+            for (int h = 0; h < wt; ++h)
+              tma_load_2d(stg + h * W_TILE, map_w, &in_full[st], k0, wrow + 128 * h);
+          }
           tma_load_2d(stg + L::W_BYTES, &map_hi, &in_full[st], k0, xrow);
           if constexpr (!ONE) tma_load_2d(stg + L::W_BYTES + L::X_TILE, &map_lo, &in_full[st], k0, xrow);
         }
@@ -427,6 +448,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
   } else if ((warp - 2) / 4 < L::NGRP) {
     // -------------------------------------------------------------------- epilogue
     constexpr int CW = L::CW, CH = L::CH;
+    pdl_wait();  // the token scales and outputs belong to the previous kernels' data
+    if (blockIdx.x == 0 && args.adv != nullptr && warp == 2)  // every earlier kernel is done
+      for (int j = lane; j < args.adv_n; j += 32) args.adv[j] += args.adv_by;
     const int grp = (warp - 2) / 4, q = warp & 3;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     const int half = WT == 2 ? grp : 0;       // weight half (128 features) of this warpgroup
@@ -449,7 +473,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
       const int mt = U.m0 + 32 * q + lane;
       const int sxoff = (mt < args.M ? mt : -1) * nkb_all;  // < 0: token past M
       float sx_next = 0.f;
-      if constexpr (SXB) sx_next = sxoff >= 0 ? __ldg(GT_SXP + sxoff + U.kb_begin) : 0.f;
+      if constexpr (SXB) sx_next = sxoff >= 0 ? ld_dep_f32(GT_SXP + sxoff + U.kb_begin) : 0.f;
       float acc[CW];
 #pragma unroll
       for (int j = 0; j < CW; ++j) acc[j] = 0.f;
@@ -464,7 +488,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
         float sc = live ? __ldg(scales + kb) : 0.f;
         if constexpr (SXB) {
           sc *= sx_next;
-          sx_next = (sxoff >= 0 && kb + 1 < U.kb_end) ? __ldg(GT_SXP + sxoff + kb + 1) : 0.f;
+          sx_next = (sxoff >= 0 && kb + 1 < U.kb_end) ? ld_dep_f32(GT_SXP + sxoff + kb + 1) : 0.f;
         }
         const uint32_t t0 = tmem + lane_off + ab * L::ACC_COLS + half * BN + col0;
 #pragma unroll
@@ -494,7 +518,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
         const int nend = args.N[U.prob];
         if (m < args.M) {
           // Token scale, applied as each vector is formed (SXB: already in the block scales).
-          const float sxm = SXB ? 1.f : __ldg(GT_SXP + m);
+          const float sxm = SXB ? 1.f : ld_dep_f32(GT_SXP + m);
           if (args.splits > 1 || args.y_fp32[U.prob]) {
             float* y = args.splits > 1
                            ? args.partial + ((size_t)U.split * args.M + m) * args.ldp +
@@ -545,7 +569,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
 #pragma unroll
       for (int c = 0; c < CW / 32; ++c) {
         const int m = m0 + 32 * c + lane;
-        sxr[c] = m < args.M ? __ldg(GT_SXP + m) : 0.f;
+        sxr[c] = m < args.M ? ld_dep_f32(GT_SXP + m) : 0.f;
       }
 #pragma unroll
       for (int j = 0; j < CW; ++j) acc[j] *= __shfl_sync(0xffffffffu, sxr[j >> 5], j & 31);
@@ -591,15 +615,18 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
 #undef GT_SXP
 #undef GT_YBASE
 
-// Y = sum over splits of the fp32 partials, in split order (deterministic).
-__global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int M, int ldp,
-                                     int n_off, int N, void* Y, int ldy, int y_fp32,
+// Y = sum over splits of the fp32 partials, in split order (deterministic).  Safe under
+// programmatic dependent launch.
+__global__ void splitk_reduce_kernel(const float* part, int splits, int M, int ldp, int n_off,
+                                     int N, void* Y, int ldy, int y_fp32,
                                      const __nv_bfloat16* __restrict__ R) {
+  pdl_launch_dependents();
+  pdl_wait();
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (size_t)M * N) return;
   const int m = (int)(i / N), n = (int)(i % N);
   float s = 0.f;
-  for (int k = 0; k < splits; ++k) s += part[((size_t)k * M + m) * ldp + n_off + n];
+  for (int k = 0; k < splits; ++k) s += ld_dep_f32(part + ((size_t)k * M + m) * ldp + n_off + n);
   if (y_fp32) {
     reinterpret_cast<float*>(Y)[(size_t)m * ldy + n] = s;
   } else {
@@ -611,11 +638,10 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
 
 template <int BN, int WT, bool SXB, bool ONE = false, bool BATCH = false>
 cudaError_t launch_bn(const CUtensorMap* w, const CUtensorMap& hi, const CUtensorMap& lo,
-                      const GemmTcArgs& a, int num_sms, cudaStream_t st) {
+                      const GemmTcArgs& a, int num_sms, cudaStream_t st, bool pdl) {
   const int grid = a.units < num_sms ? a.units : num_sms;
-  gemm_f8w_tc_kernel<BN, WT, SXB, ONE, BATCH><<<grid, GT_THREADS, GemmSmem<BN, WT, ONE>::BYTES, st>>>(
-      w[0], w[1], hi, lo, a);
-  return cudaGetLastError();
+  return launch_kernel(gemm_f8w_tc_kernel<BN, WT, SXB, ONE, BATCH>, dim3(grid), dim3(GT_THREADS),
+                       GemmSmem<BN, WT, ONE>::BYTES, st, pdl, w[0], w[1], hi, lo, a);
 }
 
 template <int BN, int WT, bool SXB, bool ONE = false, bool BATCH = false>
@@ -672,7 +698,7 @@ namespace {
 // k block) (sxb = true) scales; split-K partials in `partial`.
 cudaError_t gemm_tc_core(const uint8_t* hi, const uint8_t* lo, const float* sx, bool sxb, int M,
                          int K, const Proj* p, int np, float* partial, int num_sms, int* err,
-                         cudaStream_t st, int* adv, int adv_n, int adv_by, bool one = false) {
+                         cudaStream_t st, int* adv, int adv_n, int adv_by, bool one, bool pdl) {
   const int bn = gemm_bn(M);
   if (sxb && bn != 128) return cudaErrorInvalidValue;
   if (one && !sxb) return cudaErrorInvalidValue;
@@ -715,27 +741,26 @@ cudaError_t gemm_tc_core(const uint8_t* hi, const uint8_t* lo, const float* sx, 
   a.partial = partial;
   a.ldp = n_total;
   switch (bn) {
-    case 32: e = launch_bn<32, 1, false>(mw, mh, ml, a, num_sms, st); break;
-    case 64: e = launch_bn<64, 1, false>(mw, mh, ml, a, num_sms, st); break;
+    case 32: e = launch_bn<32, 1, false>(mw, mh, ml, a, num_sms, st, pdl); break;
+    case 64: e = launch_bn<64, 1, false>(mw, mh, ml, a, num_sms, st, pdl); break;
     default:
       if (one)
-        e = wt == 2 ? launch_bn<128, 2, true, true>(mw, mh, ml, a, num_sms, st)
-                    : launch_bn<128, 1, true, true>(mw, mh, ml, a, num_sms, st);
+        e = wt == 2 ? launch_bn<128, 2, true, true>(mw, mh, ml, a, num_sms, st, pdl)
+                    : launch_bn<128, 1, true, true>(mw, mh, ml, a, num_sms, st, pdl);
       else if (sxb)
-        e = wt == 2 ? launch_bn<128, 2, true>(mw, mh, ml, a, num_sms, st)
-                    : launch_bn<128, 1, true>(mw, mh, ml, a, num_sms, st);
+        e = wt == 2 ? launch_bn<128, 2, true>(mw, mh, ml, a, num_sms, st, pdl)
+                    : launch_bn<128, 1, true>(mw, mh, ml, a, num_sms, st, pdl);
       else
-        e = wt == 2 ? launch_bn<128, 2, false>(mw, mh, ml, a, num_sms, st)
-                    : launch_bn<128, 1, false>(mw, mh, ml, a, num_sms, st);
+        e = wt == 2 ? launch_bn<128, 2, false>(mw, mh, ml, a, num_sms, st, pdl)
+                    : launch_bn<128, 1, false>(mw, mh, ml, a, num_sms, st, pdl);
       break;
   }
   if (e != cudaSuccess || a.splits == 1) return e;
   for (int i = 0; i < np; ++i) {
     const size_t cnt = (size_t)M * p[i].N;
-    splitk_reduce_kernel<<<(unsigned)((cnt + 255) / 256), 256, 0, st>>>(
-        partial, a.splits, M, n_total, i ? p[0].N : 0, p[i].N, p[i].Y, p[i].ldy, p[i].y_fp32,
-        p[i].R);
-    e = cudaGetLastError();
+    e = launch_kernel(splitk_reduce_kernel, dim3((unsigned)((cnt + 255) / 256)), dim3(256), 0, st,
+                      pdl, partial, a.splits, M, n_total, i ? p[0].N : 0, p[i].N, p[i].Y,
+                      p[i].ldy, p[i].y_fp32, p[i].R);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -745,18 +770,18 @@ cudaError_t gemm_tc_core(const uint8_t* hi, const uint8_t* lo, const float* sx, 
 
 cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
                            float* scratch, int num_sms, int* err, cudaStream_t st, int* adv,
-                           int adv_n, int adv_by) {
+                           int adv_n, int adv_by, bool pdl) {
   if (!scratch) return cudaErrorInvalidValue;
   uint8_t* base = reinterpret_cast<uint8_t*>(scratch);
   uint8_t* hi = base;
   uint8_t* lo = hi + up256((size_t)M * K);
   float* sx = reinterpret_cast<float*>(lo + up256((size_t)M * K));
   float* partial = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sx) + up256((size_t)M * 4));
-  split_e4m3_kernel<<<M, 256, 0, st>>>(X, ldx, K, hi, lo, sx);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e =
+      launch_kernel(split_e4m3_kernel, dim3(M), dim3(256), 0, st, pdl, X, ldx, K, hi, lo, sx);
   if (e != cudaSuccess) return e;
   return gemm_tc_core(hi, lo, sx, false, M, K, p, np, partial, num_sms, err, st, adv, adv_n,
-                      adv_by);
+                      adv_by, false, pdl);
 }
 
 bool gemm_takes_split_blocks(int M) { return gemm_bn(M) == 128; }
@@ -764,12 +789,12 @@ bool gemm_takes_split_blocks(int M) { return gemm_bn(M) == 128; }
 cudaError_t launch_gemm_tc_split(const uint8_t* hi, const uint8_t* lo, const float* sx,
                                  bool block_scales, int M, int K, const Proj* p, int np,
                                  float* scratch, int num_sms, int* err, cudaStream_t st, int* adv,
-                                 int adv_n, int adv_by, bool one_term) {
+                                 int adv_n, int adv_by, bool one_term, bool pdl) {
   if (!scratch || !hi || (!lo && !one_term) || !sx || M <= kGemvMaxM ||
       (block_scales && !gemm_takes_split_blocks(M)) || (one_term && !block_scales))
     return cudaErrorInvalidValue;
   return gemm_tc_core(hi, lo, sx, block_scales, M, K, p, np, scratch, num_sms, err, st, adv,
-                      adv_n, adv_by, one_term);
+                      adv_n, adv_by, one_term, pdl);
 }
 
 size_t absorb_split_bytes(int B, int K) {
@@ -821,9 +846,9 @@ cudaError_t launch_absorb_tc(const __nv_bfloat16* X, long long sb, int sh, int B
   a.s_step = s_step;
   a.y_step = y_step;
   switch (bn) {
-    case 32: return launch_bn<32, 1, false, false, true>(mw, mh, ml, a, num_sms, st);
-    case 64: return launch_bn<64, 1, false, false, true>(mw, mh, ml, a, num_sms, st);
-    default: return launch_bn<128, 1, false, false, true>(mw, mh, ml, a, num_sms, st);
+    case 32: return launch_bn<32, 1, false, false, true>(mw, mh, ml, a, num_sms, st, true);
+    case 64: return launch_bn<64, 1, false, false, true>(mw, mh, ml, a, num_sms, st, true);
+    default: return launch_bn<128, 1, false, false, true>(mw, mh, ml, a, num_sms, st, true);
   }
 }
 

@@ -588,7 +588,7 @@ cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Pro
                         int adv_n, int adv_by, bool pdl) {
   if (M <= 0) return cudaSuccess;
   if (M > kGemvMaxM)
-    return launch_gemm_tc(X, ldx, M, K, p, np, partial, num_sms, err, st, adv, adv_n, adv_by);
+    return launch_gemm_tc(X, ldx, M, K, p, np, partial, num_sms, err, st, adv, adv_n, adv_by, pdl);
   if (p[0].N % 16 != 0 || (np > 1 && p[1].N % 16 != 0)) return cudaErrorInvalidValue;
   ProjSet ps{};
   ps.np = np;

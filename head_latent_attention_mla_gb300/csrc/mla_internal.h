@@ -207,9 +207,12 @@ cudaError_t launch_gemm(const __nv_bfloat16* X, int ldx, int M, int K, const Pro
                         float* partial, int num_sms, int* err, cudaStream_t st,
                         int* adv = nullptr, int adv_n = 0, int adv_by = 0, bool pdl = false);
 bool gemm_can_advance(int M);  // whether launch_gemm honours adv for this M
+// pdl: launch the split, GEMM and reduce kernels with programmatic dependent launch (each
+// waits for its predecessor before touching its data; the GEMM requests its first weight
+// tiles before that wait).
 cudaError_t launch_gemm_tc(const __nv_bfloat16* X, int ldx, int M, int K, const Proj* p, int np,
                            float* partial, int num_sms, int* err, cudaStream_t st,
-                           int* adv = nullptr, int adv_n = 0, int adv_by = 0);
+                           int* adv = nullptr, int adv_n = 0, int adv_by = 0, bool pdl = false);
 // The same GEMM (M > kGemvMaxM) on activations already split into two e4m3 terms, hi and
 // lo [M, K], with one scale per token, sx [M] (X[m, k] ~ sx[m] (hi + lo)), or with block_scales one per
 // (token, 128-wide k block), sx [M, K/128] (X[m, k] ~ sx[m][k/128] (hi + lo)); block scales
@@ -221,7 +224,7 @@ cudaError_t launch_gemm_tc_split(const uint8_t* hi, const uint8_t* lo, const flo
                                  bool block_scales, int M, int K, const Proj* p, int np,
                                  float* partial, int num_sms, int* err, cudaStream_t st,
                                  int* adv = nullptr, int adv_n = 0, int adv_by = 0,
-                                 bool one_term = false);
+                                 bool one_term = false, bool pdl = false);
 // The FP8-activation option's input quantisation: q [M, K] = e4m3(X / sx) with one scale per
 // (token, 128-wide group), sx [M, K/128] = amax / 448 (K a multiple of 128, at most 8192).
 // The decode absorptions for many sequences as one batched tcgen05 GEMM over the 64 heads
