@@ -95,6 +95,10 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Under programmatic dependent launch: let the next kernel be scheduled, then wait for the
+  // previous one (q, kv and the cache rows are its outputs).
+  pdl_launch_dependents();
+  pdl_wait();
   const int nq = (T + PA_TILE - 1) / PA_TILE;
   // Heads vary fastest in launch order, so all heads of the heaviest (latest) query tiles start
   // first and the light tiles fill the tail.
@@ -493,7 +497,7 @@ cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloa
                                         const CacheRef& cache, int B, int T,
                                         const int* seq_lens, long kv_rows, float scale,
                                         __nv_bfloat16* attn_out, uint8_t* o_hi, uint8_t* o_lo,
-                                        float* o_sx, int* err, cudaStream_t st) {
+                                        float* o_sx, int* err, cudaStream_t st, bool pdl) {
   if ((o_hi == nullptr) != (o_lo == nullptr) || (o_hi == nullptr) != (o_sx == nullptr) ||
       (o_hi == nullptr && attn_out == nullptr))
     return cudaErrorInvalidValue;
@@ -508,10 +512,9 @@ cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloa
     return cudaErrorInvalidValue;
   if (cache.rows(B) + PA_TILE > 0x7FFFFFFFll) return cudaErrorInvalidValue;
   const dim3 grid(HEADS, (T + PA_TILE - 1) / PA_TILE, B);
-  prefill_attn_tc_kernel<<<grid, PA_THREADS, PA_SMEM, st>>>(mq, mkv, mc, T, cache, seq_lens,
-                                                            scale * 1.4426950408889634f, attn_out,
-                                                            o_hi, o_lo, o_sx, kv_rows, err);
-  return cudaGetLastError();
+  return launch_kernel(prefill_attn_tc_kernel, grid, dim3(PA_THREADS), PA_SMEM, st, pdl, mq, mkv,
+                       mc, T, cache, seq_lens, scale * 1.4426950408889634f, attn_out, o_hi, o_lo,
+                       o_sx, kv_rows, err);
 }
 
 }  // namespace mla

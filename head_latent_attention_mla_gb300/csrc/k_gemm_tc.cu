@@ -254,12 +254,14 @@ __global__ void __launch_bounds__(64) split_heads_e4m3_kernel(
 // one e4m3 term per value with one scale per (token, 128-wide group), s = amax / 448 (1 for an
 // all-zero group), q = e4m3(x / s) rounded to nearest even with saturation.  One CTA per token,
 // K/8 threads of eight values; the sixteen threads of a group find its maximum by shuffles.
-__global__ void __launch_bounds__(1024) quant_e4m3_groups_kernel(const __nv_bfloat16* __restrict__ X,
+__global__ void __launch_bounds__(1024) quant_e4m3_groups_kernel(const __nv_bfloat16* X,
                                                                  int ldx, int K,
                                                                  uint8_t* __restrict__ q,
                                                                  float* __restrict__ sx) {
+  pdl_launch_dependents();
+  pdl_wait();  // X may come from the previous kernel
   const int m = blockIdx.x, tid = threadIdx.x, k = 8 * tid;
-  const uint4 v = *reinterpret_cast<const uint4*>(X + (size_t)m * ldx + k);
+  const uint4 v = ld_dep_v4(X + (size_t)m * ldx + k);
   const uint32_t u[4] = {v.x, v.y, v.z, v.w};
   float f[8];
   float amax = 0.f;
@@ -853,11 +855,11 @@ cudaError_t launch_absorb_tc(const __nv_bfloat16* X, long long sb, int sh, int B
 }
 
 cudaError_t launch_quant_e4m3_groups(const __nv_bfloat16* X, int ldx, int M, int K, uint8_t* q,
-                                     float* sx, cudaStream_t st) {
+                                     float* sx, cudaStream_t st, bool pdl) {
   if (M <= 0) return cudaSuccess;
   if (K % BLK != 0 || K > 8192) return cudaErrorInvalidValue;
-  quant_e4m3_groups_kernel<<<M, K / 8, 0, st>>>(X, ldx, K, q, sx);
-  return cudaGetLastError();
+  return launch_kernel(quant_e4m3_groups_kernel, dim3(M), dim3(K / 8), 0, st, pdl, X, ldx, K, q,
+                       sx);
 }
 
 }  // namespace mla

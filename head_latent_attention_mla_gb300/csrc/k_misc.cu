@@ -265,6 +265,8 @@ __global__ void __launch_bounds__(IN_THREADS) input_norm_kernel(const __nv_bfloa
 __global__ void __launch_bounds__(KV_LORA / 8) gather_latent_kernel(
     const CacheRef cache, const int* __restrict__ seq_lens, int T, long kv_rows,
     __nv_bfloat16* __restrict__ out, int* err) {
+  pdl_launch_dependents();
+  pdl_wait();  // the cache rows of this call come from the norm kernel
   const int t = blockIdx.x, b = blockIdx.y;
   const int n = seq_lens[b] + T;
   if (t >= n) return;
@@ -275,7 +277,7 @@ __global__ void __launch_bounds__(KV_LORA / 8) gather_latent_kernel(
     if (threadIdx.x == 0) atomicExch(err, crow < 0 ? DEV_ERR_RANGE : DEV_ERR_PLAN);
     return;
   }
-  const uint4 v = reinterpret_cast<const uint4*>(cache.base + (size_t)crow * LAT)[threadIdx.x];
+  const uint4 v = ld_dep_v4(cache.base + (size_t)crow * LAT + 8 * threadIdx.x);
   reinterpret_cast<uint4*>(out + (size_t)(r0 + t) * KV_LORA)[threadIdx.x] = v;
 }
 
@@ -294,6 +296,8 @@ __global__ void __launch_bounds__(HEADS * 8) rope_q_kernel(__nv_bfloat16* __rest
                                                            int limit) {
   __shared__ float2 cs[RQ_TOK][ROPE / 2];
   __shared__ int live[RQ_TOK];
+  pdl_launch_dependents();
+  pdl_wait();  // q comes from the q_b projection
   const int tok0 = blockIdx.x * RQ_TOK;
   if (threadIdx.x < RQ_TOK * (ROPE / 2)) {
     const int k = threadIdx.x / (ROPE / 2), j = threadIdx.x % (ROPE / 2), token = tok0 + k;
@@ -503,6 +507,8 @@ __global__ void __launch_bounds__(256) absorb_out_kernel(
 }
 
 __global__ void advance_lens_kernel(int* seq_lens, int B, int T) {
+  pdl_launch_dependents();
+  pdl_wait();  // every reader of the lengths in this call is done
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b < B) seq_lens[b] += T;
 }
@@ -539,20 +545,19 @@ cudaError_t launch_input_norm(const __nv_bfloat16* x, int M, const __nv_bfloat16
 
 cudaError_t launch_gather_latent(const CacheRef& cache, const int* seq_lens, int B, int T,
                                  int max_len, long kv_rows, __nv_bfloat16* out, int* err,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, bool pdl) {
   if (B * T == 0 || max_len <= 0) return cudaSuccess;
-  gather_latent_kernel<<<dim3(max_len, B), KV_LORA / 8, 0, st>>>(cache, seq_lens, T, kv_rows,
-                                                                 out, err);
-  return cudaGetLastError();
+  return launch_kernel(gather_latent_kernel, dim3(max_len, B), dim3(KV_LORA / 8), 0, st, pdl,
+                       cache, seq_lens, T, kv_rows, out, err);
 }
 
 cudaError_t launch_rope_q(__nv_bfloat16* q, int B, int T, const float2* rope_tab,
-                          int rope_pairing, const int* seq_lens, int limit, cudaStream_t st) {
+                          int rope_pairing, const int* seq_lens, int limit, cudaStream_t st,
+                          bool pdl) {
   if (B * T == 0) return cudaSuccess;
   const int M = B * T;
-  rope_q_kernel<<<(M + RQ_TOK - 1) / RQ_TOK, HEADS * 8, 0, st>>>(q, M, T, rope_tab, rope_pairing,
-                                                                 seq_lens, limit);
-  return cudaGetLastError();
+  return launch_kernel(rope_q_kernel, dim3((M + RQ_TOK - 1) / RQ_TOK), dim3(HEADS * 8), 0, st, pdl,
+                       q, M, T, rope_tab, rope_pairing, seq_lens, limit);
 }
 
 // The same output absorption for many sequences (B > 8) as a small tiled product per head:
@@ -684,9 +689,9 @@ cudaError_t init_kernels() {
   return e != cudaSuccess ? e : init_gemm_tc_kernels();
 }
 
-cudaError_t launch_advance_lens(int* seq_lens, int B, int T, cudaStream_t st) {
-  advance_lens_kernel<<<(B + 255) / 256, 256, 0, st>>>(seq_lens, B, T);
-  return cudaGetLastError();
+cudaError_t launch_advance_lens(int* seq_lens, int B, int T, cudaStream_t st, bool pdl) {
+  return launch_kernel(advance_lens_kernel, dim3((B + 255) / 256), dim3(256), 0, st, pdl, seq_lens,
+                       B, T);
 }
 
 cudaError_t launch_dequant(const uint8_t* W, const float* S, int rows, int cols, float* out,

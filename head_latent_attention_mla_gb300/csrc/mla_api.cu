@@ -219,10 +219,10 @@ cudaError_t proj_bf16(const mla_ctx* c, const __nv_bfloat16* X, int ldx, int M, 
   uint8_t* q = reinterpret_cast<uint8_t*>(scratch);
   float* sx = reinterpret_cast<float*>(q + up256((size_t)M * K));
   float* partial = reinterpret_cast<float*>(q + 2 * up256((size_t)M * K) + up256((size_t)M * 4));
-  cudaError_t e = launch_quant_e4m3_groups(X, ldx, M, K, q, sx, s);
+  cudaError_t e = launch_quant_e4m3_groups(X, ldx, M, K, q, sx, s, pdl);
   if (e != cudaSuccess) return e;
   return launch_gemm_tc_split(q, nullptr, sx, true, M, K, p, np, partial, c->num_sms, c->d_err, s,
-                              adv, adv_n, adv_by, true);
+                              adv, adv_n, adv_by, true, pdl);
 }
 
 // The norm kernel's e4m3 output for q_b / kv_b over M token rows of n values, in the
@@ -296,6 +296,10 @@ mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef&
   const __nv_bfloat16* X = block_input(c, x, M, ws, L, s);
   if (!X) return MLA_ERR_CUDA;
   const __nv_bfloat16* residual = c->cfg.block ? static_cast<const __nv_bfloat16*>(x) : nullptr;
+  // Every kernel after the first is launched with programmatic dependent launch for few
+  // tokens (the projections then stream their weights while the small kernels before them
+  // run); with many tokens the early GEMM CTAs would only take SMs from their predecessors.
+  const bool pdl = M <= kPrefillPdlMaxM;
   float* g1 = at<float>(ws, L.g1);
   __nv_bfloat16* cq = at<__nv_bfloat16>(ws, L.cq);
   __nv_bfloat16* ckv = at<__nv_bfloat16>(ws, L.ckv);
@@ -305,7 +309,7 @@ mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef&
 
   Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
                 {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
-  MLA_LAUNCH("gemm_q_a_kv_a", proj_bf16(c, X, HIDDEN, M, HIDDEN, p1, 2, at<float>(ws, L.gpart), s));
+  MLA_LAUNCH("gemm_q_a_kv_a", proj_bf16(c, X, HIDDEN, M, HIDDEN, p1, 2, at<float>(ws, L.gpart), s, nullptr, 0, 0, pdl && c->cfg.block != 0));
   Proj p2{c->W[MLA_W_Q_B], c->S[MLA_W_Q_B], QB_N, q, QB_N, 0};
   Proj p3{c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], KVB_N, kv, KVB_N, 0};
   if (chunked) {
@@ -315,27 +319,27 @@ mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef&
     const E4m3Split qsp = latent_split(c, ws, L.cq, L.cq_sx, M, Q_LORA);
     MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
                                       c->cfg.rope_pairing, lens_dev, CR, limit, M > kGemvMaxM ? nullptr : cq,
-                                      nullptr, c->d_err, s, false, M > kGemvMaxM ? &qsp : nullptr, nullptr));
+                                      nullptr, c->d_err, s, pdl, M > kGemvMaxM ? &qsp : nullptr, nullptr));
     if (M > kGemvMaxM) {
       MLA_LAUNCH("gemm_q_b", launch_gemm_tc_split(qsp.hi, qsp.lo, qsp.sx, qsp.groups != 0, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
-                                                  nullptr, 0, 0, qsp.groups != 0));
+                                                  nullptr, 0, 0, qsp.groups != 0, pdl));
     } else {
-      MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+      MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s, nullptr, 0, 0, pdl));
     }
-    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
+    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s, pdl));
     if (CR.paged()) {
       // The cached latents are scattered over pages: gather all sequences' rows 0..L_b+T-1
       // back to back, then one kv_b_proj over them.
       __nv_bfloat16* lat = at<__nv_bfloat16>(ws, L.gather);
       MLA_LAUNCH("gather_latent", launch_gather_latent(CR, lens_dev, B, T, (int)kvb_M, kv_rows, lat,
-                                                       c->d_err, s));
-      MLA_LAUNCH("gemm_kv_b", proj_bf16(c, lat, KV_LORA, (int)kv_rows, KV_LORA, &p3, 1, at<float>(ws, L.gpart), s));
+                                                       c->d_err, s, pdl));
+      MLA_LAUNCH("gemm_kv_b", proj_bf16(c, lat, KV_LORA, (int)kv_rows, KV_LORA, &p3, 1, at<float>(ws, L.gpart), s, nullptr, 0, 0, pdl));
     } else {
       long r0 = 0;
       for (int b = 0; b < B; ++b) {
         const int Mb = lens_host[b] + T;
         const Proj pb{c->W[MLA_W_KV_B], c->S[MLA_W_KV_B], KVB_N, kv + (size_t)r0 * KVB_N, KVB_N, 0};
-        MLA_LAUNCH("gemm_kv_b", proj_bf16(c, CR.base + (size_t)b * CR.page * LAT, LAT, Mb, KV_LORA, &pb, 1, at<float>(ws, L.gpart), s));
+        MLA_LAUNCH("gemm_kv_b", proj_bf16(c, CR.base + (size_t)b * CR.page * LAT, LAT, Mb, KV_LORA, &pb, 1, at<float>(ws, L.gpart), s, nullptr, 0, 0, pdl));
         r0 += Mb;
       }
     }
@@ -347,19 +351,19 @@ mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef&
     const bool one = qsp.groups != 0;
     MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
                                       c->cfg.rope_pairing, lens_dev, CR, limit, nullptr, nullptr,
-                                      c->d_err, s, false, &qsp, &kvsp));
+                                      c->d_err, s, pdl, &qsp, &kvsp));
     MLA_LAUNCH("gemm_q_b", launch_gemm_tc_split(qsp.hi, qsp.lo, qsp.sx, one, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
-                                                nullptr, 0, 0, one));
-    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
+                                                nullptr, 0, 0, one, pdl));
+    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s, pdl));
     MLA_LAUNCH("gemm_kv_b", launch_gemm_tc_split(kvsp.hi, kvsp.lo, kvsp.sx, one, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
-                                                 nullptr, 0, 0, one));
+                                                 nullptr, 0, 0, one, pdl));
   } else {
     MLA_LAUNCH("norm_rope_cache", launch_norm_rope_cache(g1, B, T, c->gain[0], c->gain[1], c->cfg.eps, c->rope_tab,
                                       c->cfg.rope_pairing, lens_dev, CR, limit, cq, ckv,
-                                      c->d_err, s));
-    MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s));
-    MLA_LAUNCH("gemm_kv_b", launch_gemm(ckv, KV_LORA, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
+                                      c->d_err, s, pdl));
+    MLA_LAUNCH("gemm_q_b", launch_gemm(cq, Q_LORA, M, Q_LORA, &p2, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s, nullptr, 0, 0, pdl));
+    MLA_LAUNCH("rope_q", launch_rope_q(q, B, T, c->rope_tab, c->cfg.rope_pairing, lens_dev, limit, s, pdl));
+    MLA_LAUNCH("gemm_kv_b", launch_gemm(ckv, KV_LORA, M, KV_LORA, &p3, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s, nullptr, 0, 0, pdl));
   }
   Proj p4{c->W[MLA_W_O], c->S[MLA_W_O], HIDDEN, out, HIDDEN, 0, residual};
   if (gemm_takes_split_blocks(M)) {
@@ -369,21 +373,21 @@ mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef&
     float* a_sx = at<float>(ws, L.attn_sx);
     MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, CR, B, T, chunked ? lens_dev : nullptr,
                                                               chunked ? kv_rows : M, c->cfg.softmax_scale, nullptr,
-                                                              a_hi, a_lo, a_sx, c->d_err, s));
+                                                              a_hi, a_lo, a_sx, c->d_err, s, pdl));
     // With the FP8-activation option o_proj multiplies the high term alone: e4m3 of the
     // attention output over its own per-(token, head) scale, a head being one 128-wide group.
     MLA_LAUNCH("gemm_o", launch_gemm_tc_split(a_hi, a_lo, a_sx, true, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
-                                              lens_dev, B, T, fp8_path(c, M)));
+                                              lens_dev, B, T, fp8_path(c, M), pdl));
   } else {
     MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, CR, B, T, chunked ? lens_dev : nullptr,
                                                               chunked ? kv_rows : M, c->cfg.softmax_scale, attn,
-                                                              nullptr, nullptr, nullptr, c->d_err, s));
+                                                              nullptr, nullptr, nullptr, c->d_err, s, pdl));
     if (gemm_can_advance(M) && B <= 128) {  // the length update rides on o_proj
       MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
-                                       lens_dev, B, T));
+                                       lens_dev, B, T, pdl));
     } else {
-      MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s));
-      MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, T, s));
+      MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s, nullptr, 0, 0, pdl));
+      MLA_LAUNCH("advance_lens", launch_advance_lens(lens_dev, B, T, s, pdl));
     }
   }
   return MLA_OK;

@@ -245,7 +245,7 @@ cudaError_t launch_absorb_tc(const __nv_bfloat16* X, long long sb, int sh, int B
                              int pairing, const int* seq_lens, int limit, void* scratch,
                              int num_sms, int* err, cudaStream_t st);
 cudaError_t launch_quant_e4m3_groups(const __nv_bfloat16* X, int ldx, int M, int K, uint8_t* q,
-                                     float* sx, cudaStream_t st);
+                                     float* sx, cudaStream_t st, bool pdl = false);
 cudaError_t init_gemm_tc_kernels();
 cudaError_t init_gemv_kernels();
 
@@ -275,7 +275,8 @@ cudaError_t launch_norm_rope_cache(const float* g1, int B, int T, const __nv_bfl
 
 // In-place RoPE of the rotary slice of q [M, HEADS, QHEAD] (prefill).
 cudaError_t launch_rope_q(__nv_bfloat16* q, int B, int T, const float2* rope_tab,
-                          int rope_pairing, const int* seq_lens, int limit, cudaStream_t st);
+                          int rope_pairing, const int* seq_lens, int limit, cudaStream_t st,
+                          bool pdl = false);
 
 // Decode query absorption: qfull[b, h] = [W_UK,h^T q_nope | RoPE(q_pe)] as bf16 [B, HEADS, LAT].
 cudaError_t launch_absorb_q(const __nv_bfloat16* q, int B, const uint8_t* Wkvb,
@@ -366,6 +367,11 @@ cudaError_t launch_transpose_wuk(const uint8_t* Wkvb, uint8_t* out, cudaStream_t
 // Decode with at least kAbsorbTcMinB sequences runs both absorptions as batched tcgen05 GEMMs
 // (launch_absorb_tc); fewer keep the CUDA-core kernels.
 constexpr int kAbsorbTcMinB = 9;
+// Prefill calls with at most this many tokens launch every kernel after the first with
+// programmatic dependent launch.  Measured: T=16 78.6 -> 74.3 us, a 16-token chunk after 300
+// positions 92.8 -> 85.2 us, a 1024-token chunk after 4096 0.503 -> 0.497 ms; T=4096 1.033 ->
+// 1.038 ms (slower: the early GEMM CTAs take SMs from the large kernels before them).
+constexpr int kPrefillPdlMaxM = 2048;
 cudaError_t launch_absorb_out(const __nv_bfloat16* o_lat, int B, const uint8_t* Wkvb,
                               const float* Skvb, __nv_bfloat16* out, cudaStream_t st,
                               bool pdl = false);
@@ -385,7 +391,8 @@ cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloa
                                         const CacheRef& cache, int B, int T,
                                         const int* seq_lens, long kv_rows, float scale,
                                         __nv_bfloat16* attn_out, uint8_t* o_hi, uint8_t* o_lo,
-                                        float* o_sx, int* err, cudaStream_t st);
+                                        float* o_sx, int* err, cudaStream_t st,
+                                        bool pdl = false);
 cudaError_t init_prefill_tc_kernel();
 
 // Chunked prefill over a paged cache: the normalised latents (the first KV_LORA values) of
@@ -395,7 +402,7 @@ cudaError_t init_prefill_tc_kernel();
 // fit kv_rows, or an invalid page, is flagged in *err and its rows are skipped.
 cudaError_t launch_gather_latent(const CacheRef& cache, const int* seq_lens, int B, int T,
                                  int max_len, long kv_rows, __nv_bfloat16* out, int* err,
-                                 cudaStream_t st);
+                                 cudaStream_t st, bool pdl = false);
 
 // The decoder block's input RMSNorm: xn[m] = bf16(g * bf16(x[m] * rsqrt(mean(x[m]^2) + eps)))
 // for M rows of HIDDEN bf16 values.
@@ -403,7 +410,7 @@ cudaError_t launch_input_norm(const __nv_bfloat16* x, int M, const __nv_bfloat16
                               __nv_bfloat16* xn, cudaStream_t st, bool pdl = false);
 
 // seq_lens[b] += T.
-cudaError_t launch_advance_lens(int* seq_lens, int B, int T, cudaStream_t st);
+cudaError_t launch_advance_lens(int* seq_lens, int B, int T, cudaStream_t st, bool pdl = false);
 
 // out[r][c] = float(e4m3(W[r][c])) * S[r/128][c/128].
 cudaError_t launch_dequant(const uint8_t* W, const float* S, int rows, int cols, float* out,
