@@ -617,24 +617,33 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
 #undef GT_SXP
 #undef GT_YBASE
 
-// Y = sum over splits of the fp32 partials, in split order (deterministic).  Safe under
-// programmatic dependent launch.
-__global__ void splitk_reduce_kernel(const float* part, int splits, int M, int ldp, int n_off,
-                                     int N, void* Y, int ldy, int y_fp32,
-                                     const __nv_bfloat16* __restrict__ R) {
+// Y = sum over splits of the fp32 partials, in split order (deterministic), for both
+// problems of the GEMM in one launch (partial columns [0, N[0]) and [N[0], N[0] + N[1])).
+// Safe under programmatic dependent launch.
+struct ReduceArgs {
+  const float* part;
+  int splits, M, ldp;  // ldp = N[0] + N[1]
+  int N0;
+  void* Y[2];
+  int ldy[2], y_fp32[2];
+  const __nv_bfloat16* R[2];
+};
+__global__ void splitk_reduce_kernel(const __grid_constant__ ReduceArgs a) {
   pdl_launch_dependents();
   pdl_wait();
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (size_t)M * N) return;
-  const int m = (int)(i / N), n = (int)(i % N);
+  if (i >= (size_t)a.M * a.ldp) return;
+  const int m = (int)(i / a.ldp), c = (int)(i % a.ldp);
+  const int pb = c < a.N0 ? 0 : 1, n = pb ? c - a.N0 : c;
   float s = 0.f;
-  for (int k = 0; k < splits; ++k) s += ld_dep_f32(part + ((size_t)k * M + m) * ldp + n_off + n);
-  if (y_fp32) {
-    reinterpret_cast<float*>(Y)[(size_t)m * ldy + n] = s;
+  for (int k = 0; k < a.splits; ++k) s += ld_dep_f32(a.part + ((size_t)k * a.M + m) * a.ldp + c);
+  if (a.y_fp32[pb]) {
+    reinterpret_cast<float*>(a.Y[pb])[(size_t)m * a.ldy[pb] + n] = s;
   } else {
-    if (R)  // residual: bf16(R + bf16(product))
-      s = __bfloat162float(__float2bfloat16_rn(s)) + __bfloat162float(R[(size_t)m * ldy + n]);
-    reinterpret_cast<__nv_bfloat16*>(Y)[(size_t)m * ldy + n] = __float2bfloat16_rn(s);
+    if (a.R[pb])  // residual: bf16(R + bf16(product))
+      s = __bfloat162float(__float2bfloat16_rn(s)) +
+          __bfloat162float(a.R[pb][(size_t)m * a.ldy[pb] + n]);
+    reinterpret_cast<__nv_bfloat16*>(a.Y[pb])[(size_t)m * a.ldy[pb] + n] = __float2bfloat16_rn(s);
   }
 }
 
@@ -758,14 +767,21 @@ cudaError_t gemm_tc_core(const uint8_t* hi, const uint8_t* lo, const float* sx, 
       break;
   }
   if (e != cudaSuccess || a.splits == 1) return e;
+  ReduceArgs r{};
+  r.part = partial;
+  r.splits = a.splits;
+  r.M = M;
+  r.ldp = n_total;
+  r.N0 = p[0].N;
   for (int i = 0; i < np; ++i) {
-    const size_t cnt = (size_t)M * p[i].N;
-    e = launch_kernel(splitk_reduce_kernel, dim3((unsigned)((cnt + 255) / 256)), dim3(256), 0, st,
-                      pdl, partial, a.splits, M, n_total, i ? p[0].N : 0, p[i].N, p[i].Y,
-                      p[i].ldy, p[i].y_fp32, p[i].R);
-    if (e != cudaSuccess) return e;
+    r.Y[i] = p[i].Y;
+    r.ldy[i] = p[i].ldy;
+    r.y_fp32[i] = p[i].y_fp32;
+    r.R[i] = p[i].R;
   }
-  return cudaSuccess;
+  const size_t cnt = (size_t)M * n_total;
+  return launch_kernel(splitk_reduce_kernel, dim3((unsigned)((cnt + 255) / 256)), dim3(256), 0, st,
+                       pdl, r);
 }
 
 }  // namespace
