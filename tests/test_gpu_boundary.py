@@ -67,17 +67,25 @@ def test_device_range_check_flags_instead_of_faulting(layer):
     assert layer.status() == mla.MLA_OK                              # the word was cleared
 
 
-def test_repeat_runs_are_bitwise_identical(layer):
-    xb = synth.hidden_states(0, 2, 0, 300)
+@pytest.mark.parametrize("B,T", [(1, 299), (8, 16), (1, 16)])
+def test_repeat_runs_are_bitwise_identical(layer, B, T):
+    """Prefill of T tokens then one decode step, twice on fresh caches: every output and cache
+    row bit for bit the same.  B=8 decodes through the tcgen05 projections with split-K, and
+    T=16 prefills through the split-K GEMMs, all under programmatic dependent launch (a kernel
+    that read its predecessor's data too early would show here)."""
+    xb = np.stack([synth.hidden_states(0, 2 + b, 0, T + 1) for b in range(B)])
     outs = []
     for _ in range(2):
-        cache = torch.zeros(1, 300, 576, dtype=torch.bfloat16, device="cuda")
-        lens = torch.zeros(1, dtype=torch.int32, device="cuda")
-        y = layer.prefill(to_dev(xb[None, :299]), cache, lens, [0])
-        yd = layer.decode(to_dev(xb[299:300]), cache, lens, [299])
+        cache = torch.zeros(B, T + 1, 576, dtype=torch.bfloat16, device="cuda")
+        lens = torch.zeros(B, dtype=torch.int32, device="cuda")
+        y = layer.prefill(to_dev(xb[:, :T]), cache, lens, [0] * B)
+        yd = layer.decode(to_dev(xb[:, T]), cache, lens, [T] * B)
+        torch.cuda.synchronize()
+        assert layer.status() == mla.MLA_OK
         outs.append((y.clone(), yd.clone(), cache.clone()))
     for a, b in zip(outs[0], outs[1]):
         assert torch.equal(a, b)
+    assert not torch.isnan(outs[0][1].float()).any()
 
 
 def _injected_layer(n):
