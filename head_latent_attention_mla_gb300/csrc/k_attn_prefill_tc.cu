@@ -47,8 +47,12 @@ constexpr int OFF_K = OFF_Q + PA_Q_BYTES;          // two k stages
 constexpr int OFF_V = OFF_K + 2 * PA_K_BYTES;      // two v stages
 constexpr int OFF_BAR = OFF_V + 2 * PA_V_BYTES;
 constexpr int OFF_MISC = OFF_BAR + 16 * 8;
-constexpr int OFF_XCH = OFF_MISC + 16;            // [2 tile parities][PA_NG groups][128 rows]
-constexpr int PA_SMEM = OFF_XCH + 2 * PA_NG * 128 * 4 + 1024;
+constexpr int OFF_QFAIL = OFF_MISC + 16;          // [4] failure flags, one per lane quarter
+constexpr int OFF_XCH = OFF_QFAIL + 16;           // [2 tile parities][PA_NG groups][128 rows]
+// [PA_NG groups][128 rows] row sums: apart from xch, which a slower warp of the quarter may
+// still be reading for the last tile when a faster one stores its sum.
+constexpr int OFF_LX = OFF_XCH + 2 * PA_NG * 128 * 4;
+constexpr int PA_SMEM = OFF_LX + PA_NG * 128 * 4 + 1024;
 constexpr uint32_t TM_O = 0, TM_S = 128, TM_P = 384;
 constexpr float RESCALE_LOG2 = 8.f;
 
@@ -133,6 +137,7 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
     }
     *abort_flag = 0;
     reinterpret_cast<volatile int*>(smem + OFF_MISC)[2] = 0;  // softmax failure flag
+    for (int qq = 0; qq < 4; ++qq) reinterpret_cast<volatile int*>(smem + OFF_QFAIL)[qq] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -255,9 +260,11 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
   } else if ((warp >= 2 && warp <= 5) || warp >= 8) {
     static_assert(PA_GC == 32, "one 32-column chunk per softmax thread");
     // -------------------------------------------------------------------- softmax warps
-    // Every softmax thread reaches the same named barriers in every tile it starts; a failed
-    // wait is published in s_fail before the tile's second barrier, and all threads leave
-    // together after it, so no barrier is left waiting for a thread that has gone.
+    // The four threads of a row sit in the four softmax warps of one tensor-memory lane
+    // quarter; they trade their maxima through shared memory at one barrier of those 128
+    // threads per tile.  Every thread of a quarter reaches that barrier in every tile it
+    // starts; a failed wait is published in the quarter's flag before it, and all four warps
+    // leave together after it.
     const int qw = warp & 3;
     const int grp = warp < 8 ? 0 : (warp - 4) / 4;  // columns [32 grp, 32 grp + 32)
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
@@ -265,42 +272,44 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
     const int qi = q0 + row;                      // query position of this thread's row
     float* xch = reinterpret_cast<float*>(smem + OFF_XCH);
     volatile int* s_fail = reinterpret_cast<volatile int*>(smem + OFF_MISC) + 2;
+    volatile int* q_fail = reinterpret_cast<volatile int*>(smem + OFF_QFAIL) + qw;
     float m = -INFINITY, l = 0.f;                 // running maximum; this group's sum
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       const int st = j & 1;
-      ok = mbar_wait(&s_full[st], (j >> 1) & 1, err, abort_flag);
+      if (ok) ok = mbar_wait(&s_full[st], (j >> 1) & 1, err, abort_flag);
       fence_after();
-      // The thread's 32 columns are read from tensor memory twice (the code stays small: a
-      // fully unrolled row overflows the instruction cache).
       const uint32_t s_addr = tmem + lane_off + TM_S + 128 * st + PA_GC * grp;
       const int kbase = j * PA_TILE + PA_GC * grp;
       const int vis = min(L + qi - kbase + 1, L + T - kbase);  // columns [0, vis) visible
       // Tiles wholly at or before the tile's first query position are visible to every row: no
       // mask there.
       const bool full = (j + 1) * PA_TILE <= L + q0 + 1;
-      float tmax = -INFINITY;  // pass 1: maximum of the visible scores
+      // The thread's 32 scores, read once; masked ones become -inf.
+      uint32_t r[32];
+      float tmax = -INFINITY;
       if (ok) {
-#pragma unroll 1
-        for (int c = 0; c < PA_GC / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(s_addr + 32 * c, r);
-          tmem_wait_ld();
-          if (full) {
+        tmem_ld32(s_addr, r);
+        tmem_wait_ld();
+        if (!full) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) tmax = fmaxf(tmax, __uint_as_float(r[i]));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              tmax = fmaxf(tmax, (32 * c + i < vis) ? __uint_as_float(r[i]) : -INFINITY);
-          }
+          for (int i = 0; i < 32; ++i)
+            if (i >= vis) r[i] = __float_as_uint(-INFINITY);
         }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) tmax = fmaxf(tmax, __uint_as_float(r[i]));
       }
       xch[(PA_NG * st + grp) * 128 + row] = tmax;
-      named_bar(1, PA_SM_THREADS);
+      if (!ok) *q_fail = 1;
+      named_bar(2 + qw, 128);
+      if (*q_fail) {
+        ok = false;
+        break;
+      }
 #pragma unroll
       for (int g = 0; g < PA_NG; ++g) tmax = fmaxf(tmax, xch[(PA_NG * st + g) * 128 + row]);
       tmax *= scale_log2;  // scale > 0
+      // The row's maximum, and so this decision, is the same in all four threads of the row.
       float alpha = 1.f;
       bool need = false;
       if (tmax > m + RESCALE_LOG2) {
@@ -312,68 +321,35 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
         m = tmax;
       }
       const float mu = (m == -INFINITY) ? 0.f : m;   // rows past T see no key at all
-      // P's buffer was last read by MMA2 of tile j-2, and O may only be rescaled once MMA2 of
-      // tile j-1 is done; their commits on the v stages say so.  (Neither stage barrier can run
-      // a phase ahead: its next phase needs this warpgroup's P of tile j or j+1.)
-      if (ok && j >= 2) ok = mbar_wait(&v_empty[st], ((j - 2) >> 1) & 1, err, abort_flag);
-      // Pass 2: p = 2^(s * scale - m), rounded to bf16, into P (16 packed columns per chunk);
-      // l sums the unrounded p.
-      const uint32_t p_addr = tmem + lane_off + TM_P + 64 * st + (PA_GC / 2) * grp;
-      float lsum = 0.f;
+      // P's buffer was last read by MMA2 of tile j-2 (its commit on the v stage says so).
+      if (j >= 2) ok = mbar_wait(&v_empty[st], ((j - 2) >> 1) & 1, err, abort_flag);
+      // p = 2^(s * scale - m) (masked scores give 0), rounded to bf16 into P (16 packed
+      // columns); l sums the unrounded p.
       if (ok) {
-#pragma unroll 1
-        for (int c = 0; c < PA_GC / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(s_addr + 32 * c, r);
-          tmem_wait_ld();
-          uint32_t pk[16];
-          float ls0 = 0.f, ls1 = 0.f;
-          if (full) {
+        uint32_t pk[16];
+        float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float e0 = fast_exp2(fmaf(__uint_as_float(r[i]), scale_log2, -mu));
-              const float e1 = fast_exp2(fmaf(__uint_as_float(r[i + 1]), scale_log2, -mu));
-              ls0 += e0;
-              ls1 += e1;
-              __nv_bfloat162 pr = __floats2bfloat162_rn(e0, e1);
-              pk[i >> 1] = *reinterpret_cast<uint32_t*>(&pr);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const int col = 32 * c + i;
-              const float e0 =
-                  col < vis ? fast_exp2(fmaf(__uint_as_float(r[i]), scale_log2, -mu)) : 0.f;
-              const float e1 =
-                  col + 1 < vis ? fast_exp2(fmaf(__uint_as_float(r[i + 1]), scale_log2, -mu)) : 0.f;
-              ls0 += e0;
-              ls1 += e1;
-              __nv_bfloat162 pr = __floats2bfloat162_rn(e0, e1);
-              pk[i >> 1] = *reinterpret_cast<uint32_t*>(&pr);
-            }
-          }
-          lsum += ls0 + ls1;
-          tmem_st16(p_addr + 16 * c, pk);
+        for (int i = 0; i < 32; i += 2) {
+          const float e0 = fast_exp2(fmaf(__uint_as_float(r[i]), scale_log2, -mu));
+          const float e1 = fast_exp2(fmaf(__uint_as_float(r[i + 1]), scale_log2, -mu));
+          ls0 += e0;
+          ls1 += e1;
+          __nv_bfloat162 pr = __floats2bfloat162_rn(e0, e1);
+          pk[i >> 1] = *reinterpret_cast<uint32_t*>(&pr);
         }
+        l += ls0 + ls1;
+        tmem_st16(tmem + lane_off + TM_P + 64 * st + (PA_GC / 2) * grp, pk);
         fence_before();
         mbar_arrive(&s_free[st]);  // S of this buffer has been read
       }
-      l += lsum;
-      if (ok && need) ok = mbar_wait(&v_empty[st ^ 1], ((j - 1) >> 1) & 1, err, abort_flag);
-      if (!ok) *s_fail = 1;
-      const bool any_need = named_bar_or(1, PA_SM_THREADS, need);
-      if (*s_fail) {
-        ok = false;
-        break;
-      }
-      if (any_need) {  // MMA2 of tile j-1 is done for every thread that needed it: for all
-        if (!need) ok = mbar_wait(&v_empty[st ^ 1], ((j - 1) >> 1) & 1, err, abort_flag);
-        if (!ok) break;  // cannot happen once another thread's identical wait succeeded
-        fence_after();
-#pragma unroll 1
-        for (int c = 0; c < PA_GC / 32; ++c) {
+      // O may only be rescaled once MMA2 of tile j-1 is done (its commit on the other v
+      // stage); each thread rescales its own 32 columns of its row.
+      if (ok && need) {
+        ok = mbar_wait(&v_empty[st ^ 1], ((j - 1) >> 1) & 1, err, abort_flag);
+        if (ok) {
+          fence_after();
           uint32_t o[32];
-          const uint32_t ta = tmem + lane_off + TM_O + PA_GC * grp + 32 * c;
+          const uint32_t ta = tmem + lane_off + TM_O + PA_GC * grp;
           tmem_ld32(ta, o);
           tmem_wait_ld();
 #pragma unroll
@@ -381,20 +357,24 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
           tmem_st32(ta, o);
         }
       }
-      tmem_wait_st();
-      fence_before();
-      mbar_arrive(&p_full[st]);
+      if (ok) {
+        tmem_wait_st();
+        fence_before();
+        mbar_arrive(&p_full[st]);
+      }
     }
+    if (!ok) *s_fail = 1;
     // Epilogue: the row's sum from all groups, O / l as bf16, this group's 32 value dims.
     if (ok) ok = mbar_wait(&v_empty[(nt - 1) & 1], ((nt - 1) >> 1) & 1, err, abort_flag);
     if (!ok) *s_fail = 1;
-    xch[grp * 128 + row] = l;
+    float* lx = reinterpret_cast<float*>(smem + OFF_LX);
+    lx[grp * 128 + row] = l;
     named_bar(1, PA_SM_THREADS);
     if (!*s_fail) {
       fence_after();
       float lrow = 0.f;
 #pragma unroll
-      for (int g = 0; g < PA_NG; ++g) lrow += xch[g * 128 + row];
+      for (int g = 0; g < PA_NG; ++g) lrow += lx[g * 128 + row];
       const float inv = (lrow > 0.f) ? 1.f / lrow : 0.f;
       static_assert(PA_GC == 32, "one 32-column load per thread");
       uint32_t o[32];
