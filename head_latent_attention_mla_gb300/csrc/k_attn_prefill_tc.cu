@@ -46,7 +46,9 @@ constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + PA_Q_BYTES;          // two k stages
 constexpr int OFF_V = OFF_K + 2 * PA_K_BYTES;      // two v stages
 constexpr int OFF_BAR = OFF_V + 2 * PA_V_BYTES;
-constexpr int OFF_MISC = OFF_BAR + 16 * 8;
+constexpr int PA_NBAR = 17;                        // mbarriers (bars[0..16])
+constexpr int OFF_MISC = OFF_BAR + 24 * 8;
+static_assert(PA_NBAR * 8 <= OFF_MISC - OFF_BAR, "the barriers must not reach the misc words");
 constexpr int OFF_QFAIL = OFF_MISC + 16;          // [4] failure flags, one per lane quarter
 constexpr int OFF_XCH = OFF_QFAIL + 16;           // [2 tile parities][PA_NG groups][128 rows]
 // [PA_NG groups][128 rows] row sums: apart from xch, which a slower warp of the quarter may
