@@ -373,7 +373,7 @@ mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef&
     float* a_sx = at<float>(ws, L.attn_sx);
     MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, CR, B, T, chunked ? lens_dev : nullptr,
                                                               chunked ? kv_rows : M, c->cfg.softmax_scale, nullptr,
-                                                              a_hi, a_lo, a_sx, c->d_err, s, pdl));
+                                                              a_hi, a_lo, a_sx, c->num_sms, c->d_err, s, pdl));
     // With the FP8-activation option o_proj multiplies the high term alone: e4m3 of the
     // attention output over its own per-(token, head) scale, a head being one 128-wide group.
     MLA_LAUNCH("gemm_o", launch_gemm_tc_split(a_hi, a_lo, a_sx, true, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
@@ -381,7 +381,7 @@ mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef&
   } else {
     MLA_LAUNCH("prefill_attention", launch_prefill_attention_tc(q, kv, CR, B, T, chunked ? lens_dev : nullptr,
                                                               chunked ? kv_rows : M, c->cfg.softmax_scale, attn,
-                                                              nullptr, nullptr, nullptr, c->d_err, s, pdl));
+                                                              nullptr, nullptr, nullptr, c->num_sms, c->d_err, s, pdl));
     if (gemm_can_advance(M) && B <= 128) {  // the length update rides on o_proj
       MLA_LAUNCH("gemm_o", launch_gemm(attn, O_IN, M, O_IN, &p4, 1, at<float>(ws, L.gpart), c->num_sms, c->d_err, s,
                                        lens_dev, B, T, pdl));

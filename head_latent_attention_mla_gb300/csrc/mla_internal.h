@@ -391,7 +391,7 @@ cudaError_t launch_prefill_attention_tc(const __nv_bfloat16* q, const __nv_bfloa
                                         const CacheRef& cache, int B, int T,
                                         const int* seq_lens, long kv_rows, float scale,
                                         __nv_bfloat16* attn_out, uint8_t* o_hi, uint8_t* o_lo,
-                                        float* o_sx, int* err, cudaStream_t st,
+                                        float* o_sx, int num_sms, int* err, cudaStream_t st,
                                         bool pdl = false);
 cudaError_t init_prefill_tc_kernel();
 
