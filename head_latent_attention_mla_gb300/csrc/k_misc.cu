@@ -513,6 +513,18 @@ __global__ void advance_lens_kernel(int* seq_lens, int B, int T) {
   if (b < B) seq_lens[b] += T;
 }
 
+// n 16-byte words from src to dst, one of them page-locked host memory that the device
+// addresses directly (the input and output copies of a decode call with host buffers).  The
+// next kernel may start at once; with wait_prev the source is the previous kernel's output,
+// read after it has finished.
+__global__ void copy16_kernel(const uint4* src, uint4* dst, size_t n, int wait_prev) {
+  pdl_launch_dependents();
+  if (wait_prev) pdl_wait();
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = ld_dep_v4(src + i);
+}
+
 __global__ void dequant_kernel(const uint8_t* __restrict__ W, const float* __restrict__ S,
                                int rows, int cols, float* __restrict__ out) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -692,6 +704,19 @@ cudaError_t init_kernels() {
 cudaError_t launch_advance_lens(int* seq_lens, int B, int T, cudaStream_t st, bool pdl) {
   return launch_kernel(advance_lens_kernel, dim3((B + 255) / 256), dim3(256), 0, st, pdl, seq_lens,
                        B, T);
+}
+
+cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, bool wait_prev,
+                          cudaStream_t st, bool pdl) {
+  if (bytes == 0) return cudaSuccess;
+  if (bytes % 16 != 0 || (reinterpret_cast<uintptr_t>(src) & 15) != 0 ||
+      (reinterpret_cast<uintptr_t>(dst) & 15) != 0)
+    return cudaErrorInvalidValue;
+  const size_t n = bytes / 16;
+  const size_t blocks = (n + 255) / 256;
+  return launch_kernel(copy16_kernel, dim3((unsigned)(blocks < 1024 ? blocks : 1024)), dim3(256),
+                       0, st, pdl, static_cast<const uint4*>(src), static_cast<uint4*>(dst), n,
+                       wait_prev ? 1 : 0);
 }
 
 cudaError_t launch_dequant(const uint8_t* W, const float* S, int rows, int cols, float* out,

@@ -393,8 +393,11 @@ mla_status prefill_impl(mla_ctx* c, const void* x, int B, int T, const CacheRef&
   return MLA_OK;
 }
 
+// input_chained: the caller has already launched (and logged) a kernel that writes x, so the
+// first projection is launched under programmatic dependent launch behind it.
 mla_status decode_impl(mla_ctx* c, const void* x, int B, const CacheRef& CR, int* lens_dev,
-                       const int* lens_host, void* out, void* ws, size_t ws_bytes, void* stream) {
+                       const int* lens_host, void* out, void* ws, size_t ws_bytes, void* stream,
+                       bool input_chained = false) {
   if (!c) return MLA_ERR_INVALID_ARG;
   const Layout L = decode_layout(c, B < 0 ? 0 : B);
   mla_status st = check_tokens(c, x, B, 1, CR.base, CR.capacity(), lens_dev, lens_host, ws,
@@ -402,7 +405,7 @@ mla_status decode_impl(mla_ctx* c, const void* x, int B, const CacheRef& CR, int
   if (st != MLA_OK || B == 0) return st;
   if (!out || !aligned16(out) || out == x) return MLA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  log_reset(c);
+  if (!input_chained) log_reset(c);
   const int limit = limit_of(c, CR);
   const __nv_bfloat16* X = block_input(c, x, B, ws, L, s);
   if (!X) return MLA_ERR_CUDA;
@@ -427,7 +430,7 @@ mla_status decode_impl(mla_ctx* c, const void* x, int B, const CacheRef& CR, int
 
   Proj p1[2] = {{c->W[MLA_W_Q_A], c->S[MLA_W_Q_A], Q_LORA, g1, G1_N, 1},
                 {c->W[MLA_W_KV_A], c->S[MLA_W_KV_A], KVA_N, g1 + Q_LORA, G1_N, 1}};
-  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s, nullptr, 0, 0, c->cfg.block != 0));
+  MLA_LAUNCH("gemm_q_a_kv_a", launch_gemm(X, HIDDEN, B, HIDDEN, p1, 2, at<float>(ws, L.gpart), c->num_sms, c->d_err, s, nullptr, 0, 0, c->cfg.block != 0 || input_chained));
   if (B <= 2) {
     // One or two sequences: six kernels.  q_b_proj normalises the q latent itself (and one of
     // its CTAs appends the cache rows); the combine is fused with the W_UV absorption; the
@@ -691,6 +694,62 @@ mla_status mla_decode(mla_ctx* c, const void* x, int B, void* cache, int cap, in
                       const int* lens_host, void* out, void* ws, size_t ws_bytes, void* stream) {
   return decode_impl(c, x, B, dense_cache(cache, cap), lens_dev, lens_host, out, ws, ws_bytes,
                      stream);
+}
+
+namespace {
+// The device address of page-locked host memory that the device can address directly (16-byte
+// aligned), else null.
+void* mapped_host(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer || !aligned16(a.devicePointer))
+    return nullptr;
+  return a.devicePointer;
+}
+}  // namespace
+
+size_t mla_decode_host_workspace_bytes(const mla_ctx* c, int B) {
+  if (!c || B <= 0) return 0;
+  return up256(mla_workspace_bytes(c, B, 1)) + 2 * up256((size_t)B * HIDDEN * 2);
+}
+
+mla_status mla_decode_host(mla_ctx* c, const void* x_host, int B, void* cache, int cap,
+                           int* lens_dev, const int* lens_host, void* out_host, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (!c || B < 0) return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (!x_host || !out_host || x_host == out_host) return MLA_ERR_INVALID_ARG;
+  const size_t base = up256(mla_workspace_bytes(c, B, 1));
+  const size_t io = up256((size_t)B * HIDDEN * 2);
+  if (!ws || ws_bytes < base + 2 * io) return MLA_ERR_INVALID_ARG;
+  const CacheRef CR = dense_cache(cache, cap);
+  // Everything the step checks, before anything is enqueued.
+  mla_status st = check_tokens(c, ws, B, 1, CR.base, CR.capacity(), lens_dev, lens_host, ws,
+                               base, decode_layout(c, B).total);
+  if (st != MLA_OK) return st;
+  uint8_t* x_dev = static_cast<uint8_t*>(ws) + base;  // staged input, then output
+  uint8_t* out_dev = x_dev + io;
+  const size_t bytes = (size_t)B * HIDDEN * 2;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* xm = mapped_host(x_host);
+  void* om = mapped_host(out_host);
+  log_reset(c);
+  if (xm) {
+    MLA_LAUNCH("copy_in", launch_copy16(xm, x_dev, bytes, false, s, false));
+  } else if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyDefault, s) != cudaSuccess) {
+    return MLA_ERR_CUDA;
+  }
+  st = decode_impl(c, x_dev, B, CR, lens_dev, lens_host, out_dev, ws, base, stream, xm != nullptr);
+  if (st != MLA_OK) return st;
+  if (om) {
+    MLA_LAUNCH("copy_out", launch_copy16(out_dev, om, bytes, true, s, true));
+  } else if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDefault, s) != cudaSuccess) {
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
 }
 
 mla_status mla_cache_append_paged(mla_ctx* c, const void* x, int B, int T,

@@ -411,6 +411,11 @@ cudaError_t launch_input_norm(const __nv_bfloat16* x, int M, const __nv_bfloat16
 
 // seq_lens[b] += T.
 cudaError_t launch_advance_lens(int* seq_lens, int B, int T, cudaStream_t st, bool pdl = false);
+// bytes (a multiple of 16, both addresses 16-byte aligned) from src to dst by a kernel, for
+// copies to or from page-locked host memory that the device addresses directly.  wait_prev:
+// the source is the previous kernel's output (read after programmatic launch's wait).
+cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, bool wait_prev,
+                          cudaStream_t st, bool pdl);
 
 // out[r][c] = float(e4m3(W[r][c])) * S[r/128][c/128].
 cudaError_t launch_dequant(const uint8_t* W, const float* S, int rows, int cols, float* out,

@@ -57,6 +57,8 @@ _SIGS = {
     "mla_cache_append": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_prefill": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_decode": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "mla_decode_host_workspace_bytes": (ctypes.c_size_t, [_P, _I]),
+    "mla_decode_host": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_cache_append_paged": (_I, [_P, _P, _I, _I, _PC, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_prefill_paged": (_I, [_P, _P, _I, _I, _PC, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_decode_paged": (_I, [_P, _P, _I, _PC, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -107,6 +109,12 @@ def _ptr(t: torch.Tensor | None) -> int | None:
         return None
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError("expected a contiguous CUDA tensor")
+    return t.data_ptr()
+
+
+def _host_ptr(t: torch.Tensor) -> int:
+    if t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+        raise ValueError("expected a contiguous bf16 host tensor")
     return t.data_ptr()
 
 
@@ -176,6 +184,22 @@ def mla_decode(ctx, x, cache, seq_lens_dev, seq_lens_host, out, ws, stream=None)
     _check(load().mla_decode(ctx, _ptr(x), B, _ptr(cache), cache.shape[1], _ptr(seq_lens_dev),
                              _host_i32(seq_lens_host), _ptr(out), _ptr(ws),
                              ws.numel() * ws.element_size(), _stream(stream)), "mla_decode")
+
+
+def mla_decode_host_workspace_bytes(ctx: int, B: int) -> int:
+    return int(load().mla_decode_host_workspace_bytes(ctx, B))
+
+
+def mla_decode_host(ctx, x_host, cache, seq_lens_dev, seq_lens_host, out_host, ws,
+                    stream=None) -> None:
+    """mla_decode with x_host and out_host [B, 7168] bf16 in host memory (page-locked for the
+    fast path); the copies are enqueued on the stream with the step."""
+    B = x_host.shape[0]
+    _check(load().mla_decode_host(ctx, _host_ptr(x_host), B, _ptr(cache), cache.shape[1],
+                                  _ptr(seq_lens_dev), _host_i32(seq_lens_host),
+                                  _host_ptr(out_host),
+                                  _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "mla_decode_host")
 
 
 def mla_decode_noalloc(ctx, x, cache, seq_lens_dev, seq_lens_host, out, stream=None) -> None:
@@ -296,6 +320,20 @@ class MlaLayer:
         mla_decode(self.ctx, x, cache, seq_lens_dev, seq_lens_host, out,
                    self.workspace(x.shape[0], 1))
         return out
+
+    def workspace_host(self, B: int) -> torch.Tensor:
+        need = mla_decode_host_workspace_bytes(self.ctx, B)
+        if self.ws.numel() < need:
+            self.ws = torch.empty(need, dtype=torch.uint8, device=self.ws.device)
+        return self.ws
+
+    def decode_host(self, x_host, cache, seq_lens_dev, seq_lens_host, out_host=None, stream=None):
+        """One decode step from and to host memory; synchronise `stream` before reading the
+        result."""
+        out_host = torch.empty_like(x_host) if out_host is None else out_host
+        mla_decode_host(self.ctx, x_host, cache, seq_lens_dev, seq_lens_host, out_host,
+                        self.workspace_host(x_host.shape[0]), stream=stream)
+        return out_host
 
     def cache_append(self, x, cache, seq_lens_dev, seq_lens_host):
         mla_cache_append(self.ctx, x, cache, seq_lens_dev, seq_lens_host,

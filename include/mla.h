@@ -183,6 +183,21 @@ mla_status mla_decode(mla_ctx* ctx, const void* x_bf16, int B, void* cache_bf16,
                       int* seq_lens_dev, const int* seq_lens_host, void* out_bf16, void* ws,
                       size_t ws_bytes, void* stream);
 
+/* mla_decode with the hidden states and the output in host memory: one call enqueues the copy
+ * of x_host [B, 7168] bf16 to the device, the decode step of mla_decode, and the copy of the
+ * step's output to out_host [B, 7168] bf16, all on `stream`; it returns before they finish
+ * (synchronise the stream before reading out_host or reusing x_host).  When a buffer is
+ * page-locked host memory that the device addresses directly (cudaHostAlloc /
+ * cudaMallocHost under unified addressing), its copy is a kernel of the decode chain; any other
+ * host or device buffer is copied by cudaMemcpyAsync.  The input and output are staged in the
+ * workspace, which must hold mla_decode_host_workspace_bytes(ctx, B) bytes.  The other
+ * arguments, the step and the errors are those of mla_decode; x_host and out_host must differ
+ * (MLA_ERR_INVALID_ARG otherwise). */
+size_t mla_decode_host_workspace_bytes(const mla_ctx* ctx, int B);
+mla_status mla_decode_host(mla_ctx* ctx, const void* x_host, int B, void* cache_bf16, int cap,
+                           int* seq_lens_dev, const int* seq_lens_host, void* out_host, void* ws,
+                           size_t ws_bytes, void* stream);
+
 /* A paged latent cache.  The "KV cache" page describes a cache with no fixed size that grows
  * call by call (the cache's get_usable_length / update in the excerpt); here it is a pool of
  * fixed-size pages and a block table per sequence, so sequences can grow without reserving

@@ -185,3 +185,57 @@ def test_ragged_b64_decode_is_bitwise_repeatable(layer):
     assert layer.status() == mla.MLA_OK
     for y, rows in outs[1:]:
         assert torch.equal(y, outs[0][0]) and torch.equal(rows, outs[0][1])
+
+
+@pytest.mark.parametrize("B", [1, 3, 9])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_decode_host_equals_decode(layer, B, pinned):
+    """mla_decode_host (input and output in host memory, the copies enqueued by the call: as
+    kernels of the chain for page-locked buffers, by cudaMemcpyAsync otherwise) gives the same
+    output, cache rows and lengths as mla_decode on device buffers, bit for bit.  B = 1, 3, 9
+    cover the row GEMV, the mma.sync GEMV and the tcgen05 projections as the first kernel
+    behind the input copy."""
+    T = 40
+    xb = np.stack([synth.hidden_states(0, 5 + b, 0, T + 1) for b in range(B)])
+    res = []
+    for host in (False, True):
+        cache = torch.zeros(B, T + 1, 576, dtype=torch.bfloat16, device="cuda")
+        lens = torch.zeros(B, dtype=torch.int32, device="cuda")
+        layer.prefill(to_dev(xb[:, :T]), cache, lens, [0] * B)
+        xd = to_dev(xb[:, T])
+        if host:
+            xh = torch.empty(xd.shape, dtype=xd.dtype, pin_memory=pinned)
+            xh.copy_(xd.cpu())
+            oh = torch.empty(xd.shape, dtype=xd.dtype, pin_memory=pinned)
+            layer.decode_host(xh, cache, lens, [T] * B, oh)
+            torch.cuda.synchronize()
+            names = [n for n, _ in mla.mla_last_launches(layer.ctx)]
+            assert ("copy_in" in names and "copy_out" in names) == pinned, names
+            y = oh.clone()
+        else:
+            y = layer.decode(xd, cache, lens, [T] * B).cpu()
+        torch.cuda.synchronize()
+        assert layer.status() == mla.MLA_OK
+        res.append((y, cache.cpu(), lens.cpu()))
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
+    assert not torch.isnan(res[0][0].float()).any()
+
+
+def test_decode_host_argument_errors(layer):
+    """Host-side checks before anything is enqueued: a short workspace, the same buffer for
+    input and output."""
+    x = torch.zeros(1, 7168, dtype=torch.bfloat16, pin_memory=True)
+    o = torch.zeros_like(x)
+    cache = torch.zeros(1, 8, 576, dtype=torch.bfloat16, device="cuda")
+    lens = torch.zeros(1, dtype=torch.int32, device="cuda")
+    small = torch.empty(mla.mla_decode_host_workspace_bytes(layer.ctx, 1) - 256,
+                        dtype=torch.uint8, device="cuda")
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode_host(layer.ctx, x, cache, lens, [0], o, small)
+    assert e.value.status == mla.MLA_ERR_INVALID_ARG
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode_host(layer.ctx, x, cache, lens, [0], x, layer.workspace_host(1))
+    assert e.value.status == mla.MLA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert lens.item() == 0
