@@ -476,6 +476,12 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
       const int sxoff = (mt < args.M ? mt : -1) * nkb_all;  // < 0: token past M
       float sx_next = 0.f;
       if constexpr (SXB) sx_next = sxoff >= 0 ? ld_dep_f32(GT_SXP + sxoff + U.kb_begin) : 0.f;
+      // The unit's first block scale and (token-lane orientation, per-token scales) this
+      // thread's token scale are requested now, not when first needed: a unit of a few k
+      // blocks would otherwise wait an L2 round trip for each.
+      float sc_next = live ? __ldg(scales + U.kb_begin) : 0.f;
+      float sxm_pre = 1.f;
+      if constexpr (L::TR && !SXB) sxm_pre = mt < args.M ? ld_dep_f32(GT_SXP + mt) : 0.f;
       float acc[CW];
 #pragma unroll
       for (int j = 0; j < CW; ++j) acc[j] = 0.f;
@@ -487,7 +493,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
           break;
         }
         fence_after();
-        float sc = live ? __ldg(scales + kb) : 0.f;
+        float sc = sc_next;
+        if (kb + 1 < U.kb_end) sc_next = live ? __ldg(scales + kb + 1) : 0.f;
         if constexpr (SXB) {
           sc *= sx_next;
           sx_next = (sxoff >= 0 && kb + 1 < U.kb_end) ? ld_dep_f32(GT_SXP + sxoff + kb + 1) : 0.f;
@@ -520,7 +527,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_f8w_tc_kernel(
         const int nend = args.N[U.prob];
         if (m < args.M) {
           // Token scale, applied as each vector is formed (SXB: already in the block scales).
-          const float sxm = SXB ? 1.f : ld_dep_f32(GT_SXP + m);
+          const float sxm = sxm_pre;
           if (args.splits > 1 || args.y_fp32[U.prob]) {
             float* y = args.splits > 1
                            ? args.partial + ((size_t)U.split * args.M + m) * args.ldp +
