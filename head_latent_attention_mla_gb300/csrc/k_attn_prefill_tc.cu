@@ -120,9 +120,9 @@ __device__ __forceinline__ PaItem pa_item(int i, int T, int nq, const int* seq_l
 // The r-th work item of this CTA, or -1: rounds of gridDim.x items, taken in alternating
 // directions so that each CTA's share of heavy and light items evens out.
 __device__ __forceinline__ int pa_item_index(int r, int n_items) {
-  const int G = gridDim.x;
-  const int i = r * G + ((r & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
-  return i < n_items ? i : -1;
+  const long long G = gridDim.x;
+  const long long i = r * G + ((r & 1) ? G - 1 - (long long)blockIdx.x : (long long)blockIdx.x);
+  return i < n_items ? (int)i : -1;
 }
 
 __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
