@@ -90,6 +90,29 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Two fp32 values in one 64-bit register (lo, hi), and the packed element-wise fused
+// multiply-add and add on them: each lane is rounded exactly as fmaf and the fp32 add round it,
+// in half the instructions.
+__device__ __forceinline__ uint64_t pack2f(float lo, float hi) {
+  return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// The largest of three values (one instruction).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // The work item (head, query tile, sequence) of a given index: heads vary fastest, then the
 // query tiles from the heaviest (latest) one, then the sequences.
 struct PaItem {
@@ -387,7 +410,8 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
               if (e >= vis) rs[e] = __float_as_uint(-INFINITY);
           }
 #pragma unroll
-          for (int e = 0; e < 32; ++e) tmax = fmaxf(tmax, __uint_as_float(rs[e]));
+          for (int e = 0; e < 32; e += 2)
+            tmax = max3f(tmax, __uint_as_float(rs[e]), __uint_as_float(rs[e + 1]));
         }
         xch[(PA_NG * st + grp) * 128 + row] = tmax;
         if (!ok) *q_fail = 1;
@@ -417,17 +441,18 @@ __global__ void __launch_bounds__(PA_THREADS, 1) prefill_attn_tc_kernel(
         // columns); l sums the unrounded p.
         if (ok) {
           uint32_t pk[16];
-          float ls0 = 0.f, ls1 = 0.f;
+          const uint64_t sc2 = pack2f(scale_log2, scale_log2), nmu2 = pack2f(-mu, -mu);
+          uint64_t ls = 0;  // the sums of the even and of the odd columns
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float e0 = fast_exp2(fmaf(__uint_as_float(rs[e]), scale_log2, -mu));
-            const float e1 = fast_exp2(fmaf(__uint_as_float(rs[e + 1]), scale_log2, -mu));
-            ls0 += e0;
-            ls1 += e1;
+            const uint64_t x = ffma2(((uint64_t)rs[e + 1] << 32) | rs[e], sc2, nmu2);
+            const float e0 = fast_exp2(__uint_as_float((uint32_t)x));
+            const float e1 = fast_exp2(__uint_as_float((uint32_t)(x >> 32)));
+            ls = fadd2(ls, pack2f(e0, e1));
             __nv_bfloat162 pr = __floats2bfloat162_rn(e0, e1);
             pk[e >> 1] = *reinterpret_cast<uint32_t*>(&pr);
           }
-          l += ls0 + ls1;
+          l += __uint_as_float((uint32_t)ls) + __uint_as_float((uint32_t)(ls >> 32));
           tmem_st16(tmem + lane_off + TM_P + 64 * st + (PA_GC / 2) * grp, pk);
           fence_before();
           mbar_arrive(&s_free[st]);  // S of this buffer has been read
