@@ -52,7 +52,9 @@ constexpr int DA_THREADS = 224;
 constexpr int OFF_Q = 0;
 constexpr int OFF_C = OFF_Q + DA_Q_BYTES;
 constexpr int OFF_BAR = OFF_C + DA_STAGES * DA_TILE_BYTES;
-constexpr int OFF_MISC = OFF_BAR + 24 * 8;  // 19 barriers used
+constexpr int DA_NBAR = 21;                     // mbarriers (bars[0..20], with gaps)
+constexpr int OFF_MISC = OFF_BAR + 24 * 8;
+static_assert(DA_NBAR * 8 <= OFF_MISC - OFF_BAR, "the barriers must not reach the misc words");
 constexpr int OFF_ALPHA = OFF_MISC + 16;   // [2][HEADS] rescale factors, by tile parity
 constexpr int OFF_INVL = OFF_ALPHA + 2 * HEADS * 4;  // [HEADS] 1 / l of the finished segment
 constexpr int MAX_SEG = 96;                     // segments one CTA can hold
