@@ -111,9 +111,10 @@ void mla_default_config(mla_config* cfg);
 
 /* Creates a context on the current CUDA device.  Checks the dimensions (anything but
  * Kimi-K2's gives MLA_ERR_UNSUPPORTED), builds the RoPE cos/sin table on the host in double
- * precision (angle = pos * theta^(-2j/64), j = 0..31) and uploads it as float32.  That table
- * and a 4-byte device error word are the only device memory the context allocates;
- * mla_destroy frees them.  *out is set only on success. */
+ * precision (angle = pos * theta^(-2j/64), j = 0..31) and uploads it as float32.  That table,
+ * a 4-byte device error word and the transposed W_UK copy described at mla_upload_weights are
+ * the only device memory the context allocates; mla_destroy frees them.  *out is set only on
+ * success. */
 mla_status mla_create(const mla_config* cfg, mla_ctx** out);
 void mla_destroy(mla_ctx* ctx); /* NULL is ignored; synchronises the device before freeing */
 
@@ -122,7 +123,11 @@ void mla_destroy(mla_ctx* ctx); /* NULL is ignored; synchronises the device befo
  * 16-byte aligned; scale_dev: device float32 [ceil(rows/128), ceil(cols/128)], one scale per
  * 128x128 block, W[o,i] = e4m3(q[o,i]) * s[o/128][i/128].  rows/cols must equal the layer's
  * shape for `which` (q_a 1536x7168, q_b 12288x1536, kv_a 576x7168, kv_b 16384x512,
- * o 7168x8192), else MLA_ERR_SHAPE.  Only the pointers are recorded: nothing is copied. */
+ * o 7168x8192), else MLA_ERR_SHAPE.  Only the pointers are recorded: the weights are not
+ * copied and must stay valid while registered.  Registering kv_b also allocates (once per
+ * context) a 4.2 MB device buffer for its W_UK rows transposed, filled by the next decode of 9
+ * or more sequences, whose absorptions read it: after changing kv_b's contents in place,
+ * register it again. */
 mla_status mla_upload_weights(mla_ctx* ctx, int which, const void* e4m3_dev,
                               const float* scale_dev, int rows, int cols);
 
