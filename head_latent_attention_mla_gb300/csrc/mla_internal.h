@@ -170,7 +170,10 @@ constexpr int gemm_bn(int M) { return M <= 32 ? 32 : (M <= 64 ? 64 : 128); }
 // the k blocks of the busiest CTA, ceil(units / SMs) * ceil(k blocks / splits), the smaller on
 // ties.
 constexpr int gemm_splits(int M, int N_total, int K, int num_sms) {
-  if (M <= kGemvMaxM || M > 128) return 1;
+  // K <= 1536 (q_b, kv_b): one split.  Their few k blocks per unit gain less from splitting
+  // than the reduce launch and the fp32 partials cost (measured: decode B=64 168.5 -> 165.0 us,
+  // prefill T=16 74.3 -> 72.3 us).
+  if (M <= kGemvMaxM || M > 128 || K <= 1536) return 1;
   const int bn = gemm_bn(M);
   const long tiles = (long)((N_total + 127) / 128) * ((M + bn - 1) / bn);
   const int nkb = K / BLK;
